@@ -1,0 +1,299 @@
+"""Python binding of libmoe_b300 (the C ABI in include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Functions carry the C entry points' names.  Importing this package
+loads the in-tree ``libmoe_b300.so``; if it is missing the import fails (there
+is no fallback path).  Build it with ``python -m expert_ffn_streaming_bit_b300.build``
+or ``__graft_entry__.build()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libmoe_b300.so is not built (run python -m expert_ffn_streaming_bit_b300.build)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_OK = 0
+MOE_FWD_RESIDUAL = 1
+MOE_PLAN_ONLY = 1
+MOE_INJECT_NONE, MOE_INJECT_H2D_FAIL, MOE_INJECT_SLOW_COPY, MOE_INJECT_PINNED_ALLOC_FAIL = 0, 1, 2, 3
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "MOE_ERR_CUDA",
+          -4: "MOE_ERR_TIMEOUT", -5: "MOE_ERR_INJECTED", -6: "MOE_ERR_STATE",
+          -7: "MOE_ERR_DEVICE"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS.get(status, status), message))
+        self.status = status
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("n_experts", ctypes.c_int),
+                ("d_expert", ctypes.c_int), ("top_k", ctypes.c_int), ("d_shared", ctypes.c_int),
+                ("group", ctypes.c_int), ("n_layers", ctypes.c_int), ("n_slots", ctypes.c_int),
+                ("max_tokens", ctypes.c_int)]
+
+
+class moe_qtensor(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("bias", ctypes.c_void_p)]
+
+
+class moe_layer_weights(ctypes.Structure):
+    _fields_ = [("router", moe_qtensor), ("router_logit_bias", ctypes.c_void_p),
+                ("shared_gate", moe_qtensor), ("shared_up", moe_qtensor),
+                ("shared_down", moe_qtensor), ("exp_gate", ctypes.POINTER(moe_qtensor)),
+                ("exp_up", ctypes.POINTER(moe_qtensor)), ("exp_down", ctypes.POINTER(moe_qtensor))]
+
+
+class moe_layer_stats(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("weights", ctypes.c_void_p), ("hits", ctypes.c_int),
+                ("misses", ctypes.c_int), ("bytes_h2d", ctypes.c_int64)]
+
+
+class moe_cache_result(ctypes.Structure):
+    _fields_ = [("hit", ctypes.c_int32 * 64), ("slot", ctypes.c_int32 * 64),
+                ("evicted", ctypes.c_int32 * 64), ("misses", ctypes.c_int)]
+
+
+class moe_info(ctypes.Structure):
+    _fields_ = [("device_weight_bytes", ctypes.c_int64), ("pinned_pool_bytes", ctypes.c_int64),
+                ("device_scratch_bytes", ctypes.c_int64), ("expert_blob_bytes", ctypes.c_int64),
+                ("num_sms", ctypes.c_int)]
+
+
+_P, _I = ctypes.c_void_p, ctypes.c_int
+_sig = {
+    "moe_create": (_I, [ctypes.POINTER(moe_config), ctypes.POINTER(moe_layer_weights),
+                        ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_destroy": (None, [_P]),
+    "moe_layer_forward": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, ctypes.POINTER(moe_layer_stats)]),
+    "moe_forward_stack": (_I, [_P, _P, _I, _P, _I, _P]),
+    "moe_forward_stack_host": (_I, [_P, _P, _I, _P, _I, _P]),
+    "moe_stack_ids": (_I, [_P, _I, _I, _P, _P]),
+    "moe_cache_step": (_I, [_P, _I, _P, _I, _I, ctypes.POINTER(moe_cache_result)]),
+    "moe_cache_reset": (_I, [_P]),
+    "moe_slot_plan_create": (_I, [_I, _I, ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_slot_plan_step": (_I, [_P, _P, _I, ctypes.POINTER(moe_cache_result)]),
+    "moe_slot_plan_destroy": (None, [_P]),
+    "moe_get_info": (_I, [_P, ctypes.POINTER(moe_info)]),
+    "moe_debug_inject": (_I, [_P, _I, _I]),
+    "moe_set_timeout_ms": (_I, [_P, _I]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_last_error": (ctypes.c_char_p, [_P]),
+}
+for _name, (_res, _args) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def moe_status_string(status: int) -> str:
+    return _lib.moe_status_string(status).decode()
+
+
+def moe_last_error(handle=None) -> str:
+    h = handle.ptr if isinstance(handle, Handle) else handle
+    return _lib.moe_last_error(h).decode()
+
+
+def _check(status: int, handle=None):
+    if status != MOE_OK:
+        raise MoEError(status, moe_last_error(handle))
+
+
+class Handle:
+    """Owns a moe_handle*; destroyed with the object or by moe_destroy."""
+
+    def __init__(self, ptr: int, cfg: moe_config):
+        self.ptr = ptr
+        self.cfg = cfg
+
+    def __del__(self):
+        if getattr(self, "ptr", None):
+            _lib.moe_destroy(self.ptr)
+            self.ptr = None
+
+
+def _host(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().contiguous()
+        if a.is_floating_point() and a.element_size() == 2:
+            import torch
+            a = a.view(torch.int16)
+        a = a.numpy()
+    return np.ascontiguousarray(a)
+
+
+def _qt(t, keep: list) -> moe_qtensor:
+    q, s, b = (_host(v) for v in ((t.q, t.scale, t.bias) if hasattr(t, "q") else t))
+    keep.extend([q, s, b])
+    return moe_qtensor(q.ctypes.data, s.ctypes.data, b.ctypes.data)
+
+
+def _layer_struct(layer: Dict[str, object], keep: list) -> moe_layer_weights:
+    w = moe_layer_weights()
+    w.router = _qt(layer["router"], keep)
+    lb = layer.get("logit_bias")
+    if lb is not None:
+        lb = _host(lb).astype(np.float32)
+        keep.append(lb)
+        w.router_logit_bias = lb.ctypes.data
+    w.shared_gate = _qt(layer["shared_gate"], keep)
+    w.shared_up = _qt(layer["shared_up"], keep)
+    w.shared_down = _qt(layer["shared_down"], keep)
+    for name, field in (("gate", "exp_gate"), ("up", "exp_up"), ("down", "exp_down")):
+        t = layer[name]
+        q, s, b = _host(t.q), _host(t.scale), _host(t.bias)
+        keep.extend([q, s, b])
+        E = q.shape[0]
+        arr = (moe_qtensor * E)()
+        for e in range(E):
+            arr[e] = moe_qtensor(q[e].ctypes.data, s[e].ctypes.data, b[e].ctypes.data)
+        keep.append(arr)
+        setattr(w, field, ctypes.cast(arr, ctypes.POINTER(moe_qtensor)))
+    return w
+
+
+def moe_create(shape, layers: Sequence[Dict[str, object]], n_slots: int = 0,
+               max_tokens: int = 1) -> Handle:
+    """shape: a synth.MoEShape-like object; layers: per-layer canonical weights."""
+    cfg = moe_config(shape.d_model, shape.n_experts, shape.d_expert, shape.top_k,
+                     shape.d_shared, shape.group, len(layers), n_slots, max_tokens)
+    keep: List[object] = []
+    arr = (moe_layer_weights * len(layers))(*[_layer_struct(l, keep) for l in layers])
+    out = ctypes.c_void_p()
+    _check(_lib.moe_create(ctypes.byref(cfg), arr, ctypes.byref(out)))
+    return Handle(out.value, cfg)
+
+
+def moe_destroy(handle: Handle):
+    if handle.ptr:
+        _lib.moe_destroy(handle.ptr)
+        handle.ptr = None
+
+
+def _dev_ptr(t) -> int:
+    assert t.is_cuda and t.is_contiguous()
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def moe_layer_forward(handle: Handle, layer: int, x, y, flags: int = 0, forced_ids=None,
+                      stream=None, want_ids: bool = False):
+    """x, y: CUDA bf16 tensors [T, D].  Returns a dict of stats (ids/weights on request)."""
+    T = x.shape[0]
+    K = handle.cfg.top_k
+    st = moe_layer_stats()
+    ids = w = None
+    if want_ids:
+        ids = np.empty((T, K), np.int32)
+        w = np.empty((T, K), np.float32)
+        st.ids, st.weights = ids.ctypes.data, w.ctypes.data
+    fptr = None
+    if forced_ids is not None:
+        forced_ids = np.ascontiguousarray(forced_ids, dtype=np.int32).reshape(T, K)
+        fptr = forced_ids.ctypes.data
+    _check(_lib.moe_layer_forward(handle.ptr, layer, _dev_ptr(x), T, _dev_ptr(y), flags, fptr,
+                                  _stream_ptr(stream), ctypes.byref(st)), handle)
+    return dict(ids=ids, weights=w, hits=st.hits, misses=st.misses, bytes_h2d=st.bytes_h2d)
+
+
+def moe_forward_stack(handle: Handle, x, y, n_layers: int, stream=None):
+    _check(_lib.moe_forward_stack(handle.ptr, _dev_ptr(x), x.shape[0], _dev_ptr(y), n_layers,
+                                  _stream_ptr(stream)), handle)
+
+
+def moe_forward_stack_host(handle: Handle, x: np.ndarray, y: np.ndarray, n_layers: int,
+                           stream=None):
+    """x, y: host uint16 (bf16 bits) arrays [T, D]; y is written."""
+    assert x.dtype == np.uint16 and y.dtype == np.uint16 and y.flags["C_CONTIGUOUS"]
+    x = np.ascontiguousarray(x)
+    _check(_lib.moe_forward_stack_host(handle.ptr, x.ctypes.data, x.shape[0], y.ctypes.data,
+                                       n_layers, _stream_ptr(stream)), handle)
+
+
+def moe_stack_ids(handle: Handle, n_layers: int, T: int):
+    K = handle.cfg.top_k
+    ids = np.empty((n_layers, T, K), np.int32)
+    w = np.empty((n_layers, T, K), np.float32)
+    _check(_lib.moe_stack_ids(handle.ptr, n_layers, T, ids.ctypes.data, w.ctypes.data), handle)
+    return ids, w
+
+
+def moe_cache_step(handle: Handle, layer: int, ids, flags: int = 0):
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    r = moe_cache_result()
+    _check(_lib.moe_cache_step(handle.ptr, layer, ids.ctypes.data, ids.shape[0], flags,
+                               ctypes.byref(r)), handle)
+    k = ids.shape[0]
+    return (np.array(r.hit[:k], np.int32), np.array(r.slot[:k], np.int32),
+            np.array(r.evicted[:k], np.int32), r.misses)
+
+
+def moe_cache_reset(handle: Handle):
+    _check(_lib.moe_cache_reset(handle.ptr), handle)
+
+
+class SlotPlan:
+    """Host-only LFU slot planner (moe_slot_plan_*)."""
+
+    def __init__(self, n_slots: int, n_experts: int):
+        out = ctypes.c_void_p()
+        _check(_lib.moe_slot_plan_create(n_slots, n_experts, ctypes.byref(out)))
+        self.ptr = out.value
+
+    def step(self, ids):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        r = moe_cache_result()
+        _check(_lib.moe_slot_plan_step(self.ptr, ids.ctypes.data, ids.shape[0], ctypes.byref(r)))
+        k = ids.shape[0]
+        return (np.array(r.hit[:k], np.int32), np.array(r.slot[:k], np.int32),
+                np.array(r.evicted[:k], np.int32))
+
+    def __del__(self):
+        if getattr(self, "ptr", None):
+            _lib.moe_slot_plan_destroy(self.ptr)
+            self.ptr = None
+
+
+def moe_slot_plan_create(n_slots: int, n_experts: int) -> SlotPlan:
+    return SlotPlan(n_slots, n_experts)
+
+
+def moe_slot_plan_step(plan: SlotPlan, ids):
+    return plan.step(ids)
+
+
+def moe_slot_plan_destroy(plan: SlotPlan):
+    plan.__del__()
+
+
+def moe_get_info(handle: Handle) -> Dict[str, int]:
+    i = moe_info()
+    _check(_lib.moe_get_info(handle.ptr, ctypes.byref(i)), handle)
+    return {f: getattr(i, f) for f, _ in moe_info._fields_}
+
+
+def moe_debug_inject(handle: Optional[Handle], what: int, arg: int = 0):
+    _check(_lib.moe_debug_inject(handle.ptr if handle else None, what, arg), handle)
+
+
+def moe_set_timeout_ms(handle: Handle, ms: int):
+    _check(_lib.moe_set_timeout_ms(handle.ptr, ms), handle)

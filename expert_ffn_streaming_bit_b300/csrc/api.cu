@@ -1,0 +1,669 @@
+// C ABI of libmoe_b300 (declared in include/moe.h): handle lifetime, weight
+// repack and upload, the resident and streaming forward paths, and the
+// per-layer expert-slot cache.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "internal.h"
+#include "repack.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_create_error;
+int g_inject_pinned_fail = 0;
+
+struct Inject {
+  int h2d_fail_in = 0;  // fail the n-th next miss copy (1 = next)
+  int slow_copy_ms = 0;
+};
+
+}  // namespace
+
+struct moe_handle {
+  moe_config cfg{};
+  Dims d{};
+  int device = 0;
+  int num_sms = 0;
+  int64_t blob = 0;
+  int64_t fixed = 0;
+  // device memory
+  uint8_t* dev_weights = nullptr;  // fixed parts of all layers + resident experts or slots
+  int64_t dev_weight_bytes = 0;
+  LayerDev* dev_layers = nullptr;
+  std::vector<LayerDev> layers;
+  uint8_t* scratch = nullptr;
+  int64_t scratch_bytes = 0;
+  uint16_t* xbuf = nullptr;
+  float* h = nullptr;
+  float* partials = nullptr;
+  int32_t* ids = nullptr;
+  float* wts = nullptr;
+  uint32_t* bar = nullptr;
+  uint16_t* io_x = nullptr;  // device copies for host-io calls
+  uint16_t* io_y = nullptr;
+  // host memory
+  uint8_t* pool = nullptr;  // pinned expert pool (streaming)
+  int64_t pool_bytes = 0;
+  uint16_t* pin_x = nullptr;
+  uint16_t* pin_y = nullptr;
+  int32_t* pin_ids = nullptr;
+  uint32_t* pin_status = nullptr;
+  // streams/events
+  cudaStream_t side = nullptr;
+  std::vector<cudaEvent_t> layer_done, copy_done;
+  cudaEvent_t ev_ids = nullptr;
+  std::vector<SlotTable> tables;
+  DecodeParams base{};
+  int grid = 0;
+  int last_T = 0, last_layers = 0;
+  Inject inj;
+  int timeout_ms = 10000;
+  std::string err;
+};
+
+struct moe_slot_plan {
+  SlotTable t;
+};
+
+namespace {
+
+moe_status fail(moe_handle* h, moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h)
+    h->err = buf;
+  else
+    g_create_error = buf;
+  return s;
+}
+
+#define CUDA_TRY(h, call)                                                                       \
+  do {                                                                                          \
+    cudaError_t e_ = (call);                                                                    \
+    if (e_ != cudaSuccess)                                                                      \
+      return fail((h), e_ == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA, "%s: %s", \
+                  #call, cudaGetErrorString(e_));                                               \
+  } while (0)
+
+bool valid_qt(const moe_qtensor& t) { return t.q && t.scale && t.bias; }
+
+void free_all(moe_handle* h) {
+  if (!h) return;
+  if (h->side) cudaStreamSynchronize(h->side);
+  if (h->dev_weights || h->scratch) cudaDeviceSynchronize();
+  for (auto e : h->layer_done) cudaEventDestroy(e);
+  for (auto e : h->copy_done) cudaEventDestroy(e);
+  if (h->ev_ids) cudaEventDestroy(h->ev_ids);
+  if (h->side) cudaStreamDestroy(h->side);
+  cudaFree(h->dev_weights);
+  cudaFree(h->dev_layers);
+  cudaFree(h->scratch);
+  cudaFreeHost(h->pool);
+  cudaFreeHost(h->pin_x);
+  cudaFreeHost(h->pin_y);
+  cudaFreeHost(h->pin_ids);
+  cudaFreeHost(h->pin_status);
+}
+
+// Host wait on an event with the handle's deadline.
+moe_status wait_event(moe_handle* h, cudaEvent_t ev) {
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return MOE_OK;
+    if (e != cudaErrorNotReady) return fail(h, MOE_ERR_CUDA, "event wait: %s", cudaGetErrorString(e));
+    const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                        std::chrono::steady_clock::now() - t0)
+                        .count();
+    if (ms > h->timeout_ms)
+      return fail(h, MOE_ERR_TIMEOUT, "device work did not finish in %d ms", h->timeout_ms);
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+}
+
+moe_status sync_stream(moe_handle* h, cudaStream_t s) {
+  cudaEvent_t ev;
+  CUDA_TRY(h, cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+  cudaError_t e = cudaEventRecord(ev, s);
+  if (e != cudaSuccess) {
+    cudaEventDestroy(ev);
+    return fail(h, MOE_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+  }
+  moe_status st = wait_event(h, ev);
+  cudaEventDestroy(ev);
+  return st;
+}
+
+// Reads the device status word (synchronising) and maps it to a status.
+moe_status check_device_status(moe_handle* h, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(h->pin_status, h->bar + 2, 4, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return fail(h, MOE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  moe_status st = sync_stream(h, s);
+  if (st != MOE_OK) return st;
+  const uint32_t v = *h->pin_status;
+  if (v == DEV_OK) return MOE_OK;
+  cudaMemsetAsync(h->bar, 0, 12, s);
+  cudaStreamSynchronize(s);
+  if (v == DEV_TIMEOUT) return fail(h, MOE_ERR_TIMEOUT, "a device-side wait timed out");
+  return fail(h, MOE_ERR_DEVICE, "a kernel reported an out-of-range expert id");
+}
+
+int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
+
+moe_status launch(moe_handle* h, const DecodeParams& p, cudaStream_t s) {
+  const int e = decode_launch(p, h->grid, s, true);
+  if (e != 0)
+    return fail(h, MOE_ERR_CUDA, "decode kernel launch: %s",
+                cudaGetErrorString(static_cast<cudaError_t>(e)));
+  return MOE_OK;
+}
+
+DecodeParams params_for(moe_handle* h, int layer0, int n_layers, const void* x, void* y, int phases,
+                        int residual) {
+  DecodeParams p = h->base;
+  p.layer0 = layer0;
+  p.n_layers = n_layers;
+  p.phases = phases;
+  p.residual = residual;
+  p.x_in = static_cast<const uint16_t*>(x);
+  p.y_out = static_cast<uint16_t*>(y);
+  return p;
+}
+
+}  // namespace
+
+#pragma GCC visibility push(default)
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_OOM: return "out of memory";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "timeout";
+    case MOE_ERR_INJECTED: return "injected fault";
+    case MOE_ERR_STATE: return "invalid state";
+    case MOE_ERR_DEVICE: return "device-reported error";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(const moe_handle* h) { return h ? h->err.c_str() : g_create_error.c_str(); }
+
+moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, moe_handle** out) {
+  if (!out) return fail(nullptr, MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg || !layers) return fail(nullptr, MOE_ERR_INVALID_ARG, "cfg or layers is NULL");
+  const moe_config& c = *cfg;
+  if (c.group != kGroup || c.d_model <= 0 || c.d_model % 256 || c.d_expert <= 0 ||
+      c.d_expert % 64 || c.d_shared <= 0 || c.d_shared % 64 || c.top_k < 1 ||
+      c.top_k > kMaxTopK || c.n_experts < c.top_k || c.n_experts > 1024 || c.n_experts % 16 ||
+      c.n_layers < 1 || c.max_tokens < 1 ||
+      (c.n_slots != 0 && (c.n_slots < c.top_k || c.n_slots > c.n_experts)))
+    return fail(nullptr, MOE_ERR_INVALID_ARG, "unsupported configuration");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const moe_layer_weights& w = layers[l];
+    if (!valid_qt(w.router) || !valid_qt(w.shared_gate) || !valid_qt(w.shared_up) ||
+        !valid_qt(w.shared_down) || !w.exp_gate || !w.exp_up || !w.exp_down)
+      return fail(nullptr, MOE_ERR_INVALID_ARG, "layer %d: missing weights", l);
+    for (int e = 0; e < c.n_experts; ++e)
+      if (!valid_qt(w.exp_gate[e]) || !valid_qt(w.exp_up[e]) || !valid_qt(w.exp_down[e]))
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "layer %d expert %d: missing weights", l, e);
+  }
+  std::unique_ptr<moe_handle> h(new moe_handle());
+  h->cfg = c;
+  h->d = Dims{c.d_model, c.n_experts, c.d_expert, c.top_k, c.d_shared};
+  const Dims& d = h->d;
+  moe_status st;
+#define CREATE_TRY(call)                                                                 \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess) {                                                            \
+      st = fail(nullptr, e_ == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA,  \
+                "%s: %s", #call, cudaGetErrorString(e_));                               \
+      free_all(h.get());                                                                \
+      return st;                                                                        \
+    }                                                                                   \
+  } while (0)
+#define CREATE_FAIL(code, msg)             \
+  do {                                     \
+    st = fail(nullptr, (code), "%s", msg); \
+    free_all(h.get());                     \
+    return st;                             \
+  } while (0)
+  CREATE_TRY(cudaGetDevice(&h->device));
+  CREATE_TRY(cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device));
+  int max_smem = 0;
+  CREATE_TRY(cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device));
+  int coop = 0;
+  CREATE_TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
+  if (!coop) CREATE_FAIL(MOE_ERR_STATE, "device does not support cooperative launches");
+  h->blob = expert_blob_bytes(d);
+  h->fixed = (layer_fixed_bytes(d) + 255) / 256 * 256;
+  const int L = c.n_layers;
+  const bool streaming = c.n_slots > 0;
+  const int64_t per_layer_experts = (streaming ? c.n_slots : c.n_experts) * h->blob;
+  h->dev_weight_bytes = L * (h->fixed + per_layer_experts);
+  CREATE_TRY(cudaMalloc(&h->dev_weights, h->dev_weight_bytes));
+  if (streaming) {
+    h->pool_bytes = static_cast<int64_t>(L) * c.n_experts * h->blob;
+    if (g_inject_pinned_fail) {
+      g_inject_pinned_fail = 0;
+      CREATE_FAIL(MOE_ERR_INJECTED, "injected pinned-pool allocation failure");
+    }
+    CREATE_TRY(cudaHostAlloc(&h->pool, h->pool_bytes, cudaHostAllocDefault));
+  }
+  // repack + upload, one layer at a time through a host staging buffer
+  {
+    std::vector<uint8_t> stage(h->fixed + (streaming ? 0 : per_layer_experts));
+    for (int l = 0; l < L; ++l) {
+      const moe_layer_weights& w = layers[l];
+      repack_layer_fixed(d, w, stage.data());
+      uint8_t* exp_dst = streaming ? h->pool + static_cast<int64_t>(l) * c.n_experts * h->blob
+                                   : stage.data() + h->fixed;
+      parallel_for(c.n_experts, [&](int64_t e) {
+        repack_expert(d, w.exp_gate[e], w.exp_up[e], w.exp_down[e], exp_dst + e * h->blob);
+      });
+      CREATE_TRY(cudaMemcpy(h->dev_weights + l * (h->fixed + per_layer_experts), stage.data(),
+                            stage.size(), cudaMemcpyHostToDevice));
+    }
+  }
+  h->layers.resize(L);
+  for (int l = 0; l < L; ++l) {
+    uint8_t* base = h->dev_weights + l * (h->fixed + per_layer_experts);
+    LayerDev& ld = h->layers[l];
+    ld.router_t = base;
+    ld.router_sb = reinterpret_cast<const uint32_t*>(base + router_t_bytes(d));
+    ld.logit_bias = layers[l].router_logit_bias
+                        ? reinterpret_cast<const float*>(base + router_t_bytes(d) + router_sb_bytes(d))
+                        : nullptr;
+    ld.shared_gu = base + router_t_bytes(d) + router_sb_bytes(d) + bias_bytes(d);
+    ld.shared_dn = ld.shared_gu + shared_gu_bytes(d);
+    ld.experts = base + h->fixed;
+    ld.slot_of = nullptr;
+  }
+  CREATE_TRY(cudaMalloc(&h->dev_layers, sizeof(LayerDev) * L));
+  CREATE_TRY(cudaMemcpy(h->dev_layers, h->layers.data(), sizeof(LayerDev) * L, cudaMemcpyHostToDevice));
+  // scratch
+  const int G = h->num_sms;
+  const int G_pad = (G + 7) / 8 * 8;
+  const int64_t T = c.max_tokens;
+  auto al = [](int64_t b) { return (b + 255) / 256 * 256; };
+  const int64_t sz_xbuf = al(2 * T * d.D * 2), sz_h = al(T * (d.K * d.I + d.S) * 4),
+                sz_part = al(d.E * G_pad * 4), sz_ids = al(int64_t(L) * T * d.K * 4), sz_bar = 256,
+                sz_io = al(T * d.D * 2);
+  h->scratch_bytes = sz_xbuf + sz_h + sz_part + 2 * sz_ids + sz_bar + 2 * sz_io;
+  CREATE_TRY(cudaMalloc(&h->scratch, h->scratch_bytes));
+  CREATE_TRY(cudaMemset(h->scratch, 0, h->scratch_bytes));
+  uint8_t* sp = h->scratch;
+  h->xbuf = reinterpret_cast<uint16_t*>(sp);
+  sp += sz_xbuf;
+  h->h = reinterpret_cast<float*>(sp);
+  sp += sz_h;
+  h->partials = reinterpret_cast<float*>(sp);
+  sp += sz_part;
+  h->ids = reinterpret_cast<int32_t*>(sp);
+  sp += sz_ids;
+  h->wts = reinterpret_cast<float*>(sp);
+  sp += sz_ids;
+  h->bar = reinterpret_cast<uint32_t*>(sp);
+  sp += sz_bar;
+  h->io_x = reinterpret_cast<uint16_t*>(sp);
+  sp += sz_io;
+  h->io_y = reinterpret_cast<uint16_t*>(sp);
+  CREATE_TRY(cudaHostAlloc(&h->pin_x, T * d.D * 2, cudaHostAllocDefault));
+  CREATE_TRY(cudaHostAlloc(&h->pin_y, T * d.D * 2, cudaHostAllocDefault));
+  CREATE_TRY(cudaHostAlloc(&h->pin_ids, T * d.K * 4 + 64, cudaHostAllocDefault));
+  CREATE_TRY(cudaHostAlloc(&h->pin_status, 64, cudaHostAllocDefault));
+  CREATE_TRY(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking));
+  CREATE_TRY(cudaEventCreateWithFlags(&h->ev_ids, cudaEventDisableTiming));
+  if (streaming) {
+    h->tables.resize(L);
+    h->layer_done.resize(L);
+    h->copy_done.resize(L);
+    for (int l = 0; l < L; ++l) {
+      h->tables[l].init(c.n_slots, c.n_experts);
+      CREATE_TRY(cudaEventCreateWithFlags(&h->layer_done[l], cudaEventDisableTiming));
+      CREATE_TRY(cudaEventCreateWithFlags(&h->copy_done[l], cudaEventDisableTiming));
+    }
+  }
+  // decode kernel parameters shared by every launch
+  DecodeParams& p = h->base;
+  p.layers = h->dev_layers;
+  p.D = d.D;
+  p.E = d.E;
+  p.I = d.I;
+  p.S = d.S;
+  p.K = d.K;
+  p.rbD = static_cast<int>(qrow_bytes(d.D));
+  p.rbI = static_cast<int>(qrow_bytes(d.I));
+  p.rbS = static_cast<int>(qrow_bytes(d.S));
+  p.blob_bytes = h->blob;
+  p.dn_off = d.I * 2 * qrow_bytes(d.D);
+  p.xbuf = h->xbuf;
+  p.h = h->h;
+  p.partials = h->partials;
+  p.ids = h->ids;
+  p.wts = h->wts;
+  p.bar = h->bar;
+  p.G_pad = G_pad;
+  const int nch_i = d.I / 32, nch_s = d.S / 32;
+  const int g = gcd(nch_i, nch_s);
+  int cpt = 1;
+  for (int q = 1; q <= 12; ++q)
+    if (g % q == 0) cpt = q;
+  p.cpt_c = cpt;
+  p.nsub_i = nch_i / cpt;
+  p.nsub_s = nch_s / cpt;
+  p.tasks_row = d.K * p.nsub_i + p.nsub_s;
+  if (p.tasks_row > kConsumers)
+    CREATE_FAIL(MOE_ERR_INVALID_ARG, "top_k * d_expert too large for the decode kernel");
+  p.rc_max = kConsumers / p.tasks_row;
+  p.timeout_ns = 2000000000ull;
+  if (decode_smem_plan(&p, max_smem) != 0)
+    CREATE_FAIL(MOE_ERR_INVALID_ARG, "decode kernel does not fit in shared memory");
+  // the first-layer router stage holds a whole CTA row slice
+  const int64_t r_stage = int64_t((d.D + G - 1) / G) * d.E + 2 * d.E * 4;
+  if (r_stage > p.slot_bytes) CREATE_FAIL(MOE_ERR_INVALID_ARG, "router stage too large for the SM count");
+  h->grid = G;
+  *out = h.release();
+  return MOE_OK;
+#undef CREATE_TRY
+#undef CREATE_FAIL
+}
+
+void moe_destroy(moe_handle* h) {
+  if (!h) return;
+  free_all(h);
+  delete h;
+}
+
+moe_status moe_get_info(const moe_handle* h, moe_info* out) {
+  if (!h || !out) return MOE_ERR_INVALID_ARG;
+  out->device_weight_bytes = h->dev_weight_bytes;
+  out->pinned_pool_bytes = h->pool_bytes;
+  out->device_scratch_bytes = h->scratch_bytes;
+  out->expert_blob_bytes = h->blob;
+  out->num_sms = h->grid;
+  return MOE_OK;
+}
+
+moe_status moe_set_timeout_ms(moe_handle* h, int ms) {
+  if (!h || ms <= 0) return MOE_ERR_INVALID_ARG;
+  h->timeout_ms = ms;
+  return MOE_OK;
+}
+
+moe_status moe_debug_inject(moe_handle* h, int what, int arg) {
+  switch (what) {
+    case MOE_INJECT_NONE:
+      g_inject_pinned_fail = 0;
+      if (h) h->inj = Inject{};
+      return MOE_OK;
+    case MOE_INJECT_PINNED_ALLOC_FAIL:
+      g_inject_pinned_fail = 1;
+      return MOE_OK;
+    case MOE_INJECT_H2D_FAIL:
+      if (!h || arg < 1) return MOE_ERR_INVALID_ARG;
+      h->inj.h2d_fail_in = arg;
+      return MOE_OK;
+    case MOE_INJECT_SLOW_COPY:
+      if (!h || arg < 0) return MOE_ERR_INVALID_ARG;
+      h->inj.slow_copy_ms = arg;
+      return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+moe_status moe_slot_plan_create(int n_slots, int n_experts, moe_slot_plan** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (n_slots < 1 || n_experts < 1 || n_slots > n_experts) return MOE_ERR_INVALID_ARG;
+  moe_slot_plan* p = new moe_slot_plan();
+  p->t.init(n_slots, n_experts);
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status moe_slot_plan_step(moe_slot_plan* p, const int32_t* ids, int k, moe_cache_result* out) {
+  if (!p || !ids || !out || k < 1 || k > 64) return MOE_ERR_INVALID_ARG;
+  const int m = p->t.plan(ids, k, out->hit, out->slot, out->evicted);
+  if (m < 0) return MOE_ERR_INVALID_ARG;
+  out->misses = m;
+  return MOE_OK;
+}
+
+void moe_slot_plan_destroy(moe_slot_plan* p) { delete p; }
+
+moe_status moe_cache_step(moe_handle* h, int layer, const int32_t* ids, int k, int flags,
+                          moe_cache_result* out) {
+  if (!h || !ids || !out || k < 1 || k > 64) return MOE_ERR_INVALID_ARG;
+  if (h->cfg.n_slots == 0) return fail(h, MOE_ERR_STATE, "moe_cache_step needs streaming mode");
+  if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, MOE_ERR_INVALID_ARG, "bad layer");
+  SlotTable& t = h->tables[layer];
+  const int m = t.plan(ids, k, out->hit, out->slot, out->evicted);
+  if (m < 0)
+    return fail(h, MOE_ERR_INVALID_ARG, "ids must be %d distinct values in [0, %d)", k,
+                h->cfg.n_experts);
+  out->misses = m;
+  if (flags & MOE_PLAN_ONLY) return MOE_OK;
+  // the slots being refilled may still be read by this layer's previous kernels
+  CUDA_TRY(h, cudaStreamWaitEvent(h->side, h->layer_done[layer], 0));
+  uint8_t* slots =
+      h->dev_weights + layer * (h->fixed + int64_t(h->cfg.n_slots) * h->blob) + h->fixed;
+  const uint8_t* pool = h->pool + int64_t(layer) * h->cfg.n_experts * h->blob;
+  moe_status result = MOE_OK;
+  for (int i = 0; i < k; ++i) {
+    if (out->hit[i]) continue;
+    if (h->inj.slow_copy_ms)
+      std::this_thread::sleep_for(std::chrono::milliseconds(h->inj.slow_copy_ms));
+    if (h->inj.h2d_fail_in > 0 && --h->inj.h2d_fail_in == 0) {
+      t.clear_slot(out->slot[i]);
+      result = fail(h, MOE_ERR_INJECTED, "injected failure of the host->HBM copy of expert %d", ids[i]);
+      continue;
+    }
+    cudaError_t e = cudaMemcpyAsync(slots + int64_t(out->slot[i]) * h->blob,
+                                    pool + int64_t(ids[i]) * h->blob, h->blob,
+                                    cudaMemcpyHostToDevice, h->side);
+    if (e != cudaSuccess) {
+      t.clear_slot(out->slot[i]);
+      result = fail(h, MOE_ERR_CUDA, "expert copy: %s", cudaGetErrorString(e));
+    }
+  }
+  CUDA_TRY(h, cudaEventRecord(h->copy_done[layer], h->side));
+  return result;
+}
+
+moe_status moe_cache_reset(moe_handle* h) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->cfg.n_slots == 0) return fail(h, MOE_ERR_STATE, "moe_cache_reset needs streaming mode");
+  for (auto& t : h->tables) t.reset();
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+static moe_status decode_layer_streaming(moe_handle* h, int layer, const void* x, void* y,
+                                         int flags, const int32_t* forced, cudaStream_t s,
+                                         moe_layer_stats* stats) {
+  const int K = h->cfg.top_k;
+  DecodeParams p1 = params_for(h, layer, 1, x, y, 0, flags & MOE_FWD_RESIDUAL);
+  int32_t ids[kMaxTopK];
+  moe_cache_result cr;
+  moe_status st;
+  if (forced) {
+    // ids known up front: start the copies, then route + shared expert meanwhile
+    std::memcpy(ids, forced, sizeof(int32_t) * K);
+    st = moe_cache_step(h, layer, ids, K, 0, &cr);
+    if (st != MOE_OK) return st;
+    p1.phases = PH_ROUTER | PH_BSHARED;
+    p1.forced = 1;
+    std::memcpy(p1.forced_ids, ids, sizeof(int32_t) * K);
+    st = launch(h, p1, s);
+    if (st != MOE_OK) return st;
+  } else {
+    p1.phases = PH_ROUTER;
+    st = launch(h, p1, s);
+    if (st != MOE_OK) return st;
+    CUDA_TRY(h, cudaMemcpyAsync(h->pin_ids, h->ids, sizeof(int32_t) * K, cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(h, cudaEventRecord(h->ev_ids, s));
+    p1.phases = PH_BSHARED;  // shared expert runs while the host plans and copies
+    st = launch(h, p1, s);
+    if (st != MOE_OK) return st;
+    st = wait_event(h, h->ev_ids);
+    if (st != MOE_OK) return st;
+    std::memcpy(ids, h->pin_ids, sizeof(int32_t) * K);
+    st = moe_cache_step(h, layer, ids, K, 0, &cr);
+    if (st != MOE_OK) return st;
+  }
+  CUDA_TRY(h, cudaStreamWaitEvent(s, h->copy_done[layer], 0));
+  DecodeParams p2 = params_for(h, layer, 1, x, y, PH_BROUTED | PH_C, flags & MOE_FWD_RESIDUAL);
+  p2.use_slots = 1;
+  for (int i = 0; i < K; ++i) p2.slots[i] = cr.slot[i];
+  st = launch(h, p2, s);
+  if (st != MOE_OK) return st;
+  CUDA_TRY(h, cudaEventRecord(h->layer_done[layer], s));
+  if (stats) {
+    stats->hits = K - cr.misses;
+    stats->misses = cr.misses;
+    stats->bytes_h2d = int64_t(cr.misses) * h->blob;
+  }
+  return MOE_OK;
+}
+
+extern "C" {
+
+moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, void* y, int flags,
+                             const int32_t* forced_ids, void* stream, moe_layer_stats* stats) {
+  if (!h || !x || !y || x == y) return MOE_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, MOE_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (T < 1 || T > h->cfg.max_tokens) return fail(h, MOE_ERR_INVALID_ARG, "T=%d out of range", T);
+  const int K = h->cfg.top_k, D = h->cfg.d_model;
+  if (forced_ids) {
+    for (int t = 0; t < T; ++t)
+      for (int i = 0; i < K; ++i) {
+        const int v = forced_ids[t * K + i];
+        if (v < 0 || v >= h->cfg.n_experts) return fail(h, MOE_ERR_INVALID_ARG, "forced id out of range");
+        for (int j = 0; j < i; ++j)
+          if (forced_ids[t * K + j] == v) return fail(h, MOE_ERR_INVALID_ARG, "forced ids repeat");
+      }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (stats) {
+    stats->hits = stats->misses = 0;
+    stats->bytes_h2d = 0;
+  }
+  const int residual = flags & MOE_FWD_RESIDUAL;
+  if (h->cfg.n_slots > 0) {
+    if (T != 1) return fail(h, MOE_ERR_STATE, "streaming mode runs one token per call");
+    moe_status st = decode_layer_streaming(h, layer, x, y, flags, forced_ids, s, stats);
+    if (st != MOE_OK) return st;
+  } else {
+    // resident: one persistent launch per token
+    for (int t = 0; t < T; ++t) {
+      DecodeParams p = params_for(h, layer, 1, static_cast<const uint16_t*>(x) + int64_t(t) * D,
+                                  static_cast<uint16_t*>(y) + int64_t(t) * D, PH_ALL, residual);
+      p.ids = h->ids + int64_t(t) * K;
+      p.wts = h->wts + int64_t(t) * K;
+      if (forced_ids) {
+        p.forced = 1;
+        std::memcpy(p.forced_ids, forced_ids + t * K, sizeof(int32_t) * K);
+      }
+      moe_status st = launch(h, p, s);
+      if (st != MOE_OK) return st;
+    }
+  }
+  h->last_T = T;
+  h->last_layers = 1;
+  if (stats && (stats->ids || stats->weights)) {
+    moe_status st = check_device_status(h, s);
+    if (st != MOE_OK) return st;
+    if (stats->ids)
+      CUDA_TRY(h, cudaMemcpy(stats->ids, h->ids, sizeof(int32_t) * T * K, cudaMemcpyDeviceToHost));
+    if (stats->weights)
+      CUDA_TRY(h, cudaMemcpy(stats->weights, h->wts, sizeof(float) * T * K, cudaMemcpyDeviceToHost));
+  }
+  return MOE_OK;
+}
+
+moe_status moe_forward_stack(moe_handle* h, const void* x, int T, void* y, int n_layers,
+                             void* stream) {
+  if (!h || !x || !y || x == y) return MOE_ERR_INVALID_ARG;
+  if (h->cfg.n_slots > 0) return fail(h, MOE_ERR_STATE, "moe_forward_stack needs resident mode");
+  if (n_layers < 1 || n_layers > h->cfg.n_layers) return fail(h, MOE_ERR_INVALID_ARG, "bad n_layers");
+  if (T < 1 || T > h->cfg.max_tokens) return fail(h, MOE_ERR_INVALID_ARG, "T=%d out of range", T);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = h->cfg.d_model, K = h->cfg.top_k;
+  for (int t = 0; t < T; ++t) {
+    DecodeParams p = params_for(h, 0, n_layers, static_cast<const uint16_t*>(x) + int64_t(t) * D,
+                                static_cast<uint16_t*>(y) + int64_t(t) * D, PH_ALL, 1);
+    // token t's ids: its own layer-major block [n_layers][K]
+    p.ids = h->ids + int64_t(t) * n_layers * K;
+    p.wts = h->wts + int64_t(t) * n_layers * K;
+    moe_status st = launch(h, p, s);
+    if (st != MOE_OK) return st;
+  }
+  h->last_T = T;
+  h->last_layers = n_layers;
+  return MOE_OK;
+}
+
+moe_status moe_forward_stack_host(moe_handle* h, const void* x, int T, void* y, int n_layers,
+                                  void* stream) {
+  if (!h || !x || !y) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > h->cfg.max_tokens) return fail(h, MOE_ERR_INVALID_ARG, "T=%d out of range", T);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = size_t(T) * h->cfg.d_model * 2;
+  std::memcpy(h->pin_x, x, bytes);
+  CUDA_TRY(h, cudaMemcpyAsync(h->io_x, h->pin_x, bytes, cudaMemcpyHostToDevice, s));
+  moe_status st = moe_forward_stack(h, h->io_x, T, h->io_y, n_layers, stream);
+  if (st != MOE_OK) return st;
+  CUDA_TRY(h, cudaMemcpyAsync(h->pin_y, h->io_y, bytes, cudaMemcpyDeviceToHost, s));
+  st = sync_stream(h, s);
+  if (st != MOE_OK) return st;
+  std::memcpy(y, h->pin_y, bytes);
+  return MOE_OK;
+}
+
+moe_status moe_stack_ids(moe_handle* h, int n_layers, int T, int32_t* ids, float* weights) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (n_layers != h->last_layers || T != h->last_T)
+    return fail(h, MOE_ERR_INVALID_ARG, "moe_stack_ids: the last call ran %d layers x %d tokens",
+                h->last_layers, h->last_T);
+  moe_status st = check_device_status(h, nullptr);
+  if (st != MOE_OK) return st;
+  const int K = h->cfg.top_k;
+  const size_t n = size_t(n_layers) * T * K;
+  std::vector<int32_t> ti(n);
+  std::vector<float> tw(n);
+  CUDA_TRY(h, cudaMemcpy(ti.data(), h->ids, n * 4, cudaMemcpyDeviceToHost));
+  CUDA_TRY(h, cudaMemcpy(tw.data(), h->wts, n * 4, cudaMemcpyDeviceToHost));
+  // device order: token-major blocks [t][layer][k]
+  for (int l = 0; l < n_layers; ++l)
+    for (int t = 0; t < T; ++t)
+      for (int i = 0; i < K; ++i) {
+        const size_t src = (size_t(t) * n_layers + l) * K + i;
+        const size_t dst = (size_t(l) * T + t) * K + i;
+        if (ids) ids[dst] = ti[src];
+        if (weights) weights[dst] = tw[src];
+      }
+  return MOE_OK;
+}
+
+}  // extern "C"
+#pragma GCC visibility pop

@@ -1,0 +1,850 @@
+// Persistent decode kernel: one token through one or more MoE layers.
+//
+// One CTA per SM (cooperative launch).  Warp 8 of each CTA is a producer: one
+// lane walks the CTA's list of weight "stages" and brings each into a ring of
+// shared-memory slots with bulk async copies (the copy engine, completion on
+// an mbarrier).  Warps 0-7 consume the stages in the same order.
+//
+// Per layer l the CTA's stages are
+//   BS  its share of the shared expert's gate/up row pairs   (weights known ahead)
+//   BR  its share of the k routed experts' gate/up pairs     (needs ids(l))
+//   C   its share of output rows: for each row the k routed down rows, the
+//       shared down row and, when a next layer follows, the next router's
+//       column block                                          (needs ids(l))
+// and the data dependences are met with two grid barriers:
+//   after BS+BR: h = gelu(W_gate x) * (W_up x) complete for all k+1 branches;
+//   after C: x_{l+1} and the next router's partial logits complete; the last
+//   CTA to arrive reduces the partials (fixed order), takes the top k and the
+//   renormalised softmax, and publishes ids(l+1) before releasing the others.
+// The producer runs ahead across barriers wherever the weights are already
+// known, so HBM keeps streaming while the grid synchronises.  Every wait is
+// bounded in time; a wait that runs out sets the status word and the CTA
+// drains its in-flight copies and exits.
+//
+// Arithmetic (shilu.ai "drumih/turbo-fieldfare", overview table row 权重 and
+// section 推理引擎的工作原理; sh.edu-sjtu.cn article, section 三件事):
+//   router: logit_e = sum_c (s q + b) x_c in fp32, + bias_e; top-k by
+//           (logit desc, index asc); w = softmax over the chosen logits;
+//   expert: h_j = gelu_tanh(g_j) u_j with g = W_gate x, u = W_up x;
+//           e = W_down h; y = sum_i w_i e_i + shared(x); optional residual.
+// Dot products: activations are held as fp16 (exact for bf16 inputs in range;
+// a power-of-two prescale keeps |v| < 2^15), codes become fp16 1024+q or
+// 1024+16q by one and-or, products accumulate in fp32 with mixed-precision
+// fma, and per 32-column chunk sum(q v) = a + b/16 - (1024 Sa + 64 Sb) is
+// recovered with the chunk's precomputed activation sums; then
+// s * sum(q v) + bias * sum(v) per group half.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+struct Part {
+  int sh_lo, sh_hi;  // shared gate/up pairs
+  int rt_lo, rt_hi;  // routed pairs, flattened k*I + j
+  int c_lo, c_hi;    // output rows
+};
+
+__device__ __forceinline__ int split_at(int n, int c, int G) {
+  return static_cast<int>(static_cast<int64_t>(n) * c / G);
+}
+
+enum : int { ST_R = 0, ST_BS = 1, ST_BR = 2, ST_C = 3 };
+
+struct Stage {
+  int kind;
+  int a;  // first pair / first row
+  int n;  // pairs / rows
+  int k;  // routed slot (ST_BR)
+};
+
+// misc[] slots in shared memory
+enum : int {
+  M_IDS = 0,   // [32] ids of the current layer
+  M_WTS = 32,  // [32] weights (float bits)
+  M_ABORT = 64,
+  M_LAST = 65,
+  M_GEN = 66,
+  M_ISSUED = 67,
+  M_RED = 72,  // [8] per-warp reduction scratch
+  M_COUNT = 96
+};
+
+struct Ctx {
+  const DecodeParams* p;
+  uint8_t* smem;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* ids_ready;
+  volatile int* misc;
+  Part part;
+  int G;
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  // round to nearest even; NaN stays a quiet NaN
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x40u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+  // tanh form of GELU (Hendrycks & Gimpel 2016)
+  const float c = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * x * (1.f + tanhf(c * (x + 0.044715f * x * x * x)));
+}
+
+__device__ __forceinline__ void csync() { named_sync(1, kConsumers); }
+
+// Contribution of 32-column chunk c of a qrow with K/2 = halfK code bytes,
+// against an fp16 vector in chunk layout: s * sum(q v) + bias * sum(v).
+__device__ __forceinline__ float chunk_dot(const uint8_t* row, int halfK, int c, const uint8_t* vec,
+                                           const float* coff, const float* vsum) {
+  const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
+  const uint32_t sb = *reinterpret_cast<const uint32_t*>(row + halfK + (c >> 1) * 4);
+  const uint4* v = reinterpret_cast<const uint4*>(vec + c * kChunkStride);
+  float a = 0.f, b = 0.f;
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 vq = v[j];
+    const uint32_t wj = words[j];
+    const uint32_t w8 = wj >> 8;
+    a = fma2_f16_f32(and_or(wj, 0x000F000Fu, 0x64006400u), vq.x, a);
+    b = fma2_f16_f32(and_or(wj, 0x00F000F0u, 0x64006400u), vq.y, b);
+    a = fma2_f16_f32(and_or(w8, 0x000F000Fu, 0x64006400u), vq.z, a);
+    b = fma2_f16_f32(and_or(w8, 0x00F000F0u, 0x64006400u), vq.w, b);
+  }
+  const float qv = fmaf(b, 0.0625f, a) - coff[c];
+  const __half2 sbh = *reinterpret_cast<const __half2*>(&sb);
+  return fmaf(__low2float(sbh), qv, __high2float(sbh) * vsum[c]);
+}
+
+// ------------------------------------------------------------ stage lists
+
+struct LayerPlan {
+  int n_r, n_bs, n_br, n_c;  // stage counts
+  int rc;                    // rows per C stage (balanced)
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ LayerPlan layer_plan(const DecodeParams& p, const Part& pt, int li) {
+  LayerPlan lp;
+  lp.n_r = (li == 0 && (p.phases & PH_ROUTER) && pt.c_hi > pt.c_lo) ? 1 : 0;
+  lp.n_bs = (p.phases & PH_BSHARED) ? ceil_div(pt.sh_hi - pt.sh_lo, kPairsPerStage) : 0;
+  lp.n_br = 0;
+  if (p.phases & PH_BROUTED) {
+    int q = pt.rt_lo;
+    while (q < pt.rt_hi) {
+      const int j = q % p.I;
+      const int n = min(kPairsPerStage, min(pt.rt_hi - q, p.I - j));
+      q += n;
+      ++lp.n_br;
+    }
+  }
+  const int rows = pt.c_hi - pt.c_lo;
+  lp.n_c = (p.phases & PH_C) ? ceil_div(rows, p.rc_max) : 0;
+  lp.rc = lp.n_c ? ceil_div(rows, lp.n_c) : 0;
+  return lp;
+}
+
+// The s-th stage of a layer (R, BS, BR, C in that order).
+__device__ Stage stage_at(const DecodeParams& p, const Part& pt, const LayerPlan& lp, int s) {
+  Stage st{0, 0, 0, 0};
+  if (s < lp.n_r) {
+    st.kind = ST_R;
+    st.a = pt.c_lo;
+    st.n = pt.c_hi - pt.c_lo;
+    return st;
+  }
+  s -= lp.n_r;
+  if (s < lp.n_bs) {
+    st.kind = ST_BS;
+    st.a = pt.sh_lo + s * kPairsPerStage;
+    st.n = min(kPairsPerStage, pt.sh_hi - st.a);
+    return st;
+  }
+  s -= lp.n_bs;
+  if (s < lp.n_br) {
+    int q = pt.rt_lo;
+    for (int t = 0;; ++t) {
+      const int j = q % p.I;
+      const int n = min(kPairsPerStage, min(pt.rt_hi - q, p.I - j));
+      if (t == s) {
+        st.kind = ST_BR;
+        st.k = q / p.I;
+        st.a = j;
+        st.n = n;
+        return st;
+      }
+      q += n;
+    }
+  }
+  s -= lp.n_br;
+  st.kind = ST_C;
+  st.a = pt.c_lo + s * lp.rc;
+  st.n = min(lp.rc, pt.c_hi - st.a);
+  return st;
+}
+
+__device__ __forceinline__ const uint8_t* expert_blob(const DecodeParams& p, const LayerDev& L,
+                                                      int slot_i, int id) {
+  int b;
+  if (p.use_slots) {
+    b = p.slots[slot_i];
+  } else {
+    b = L.slot_of ? L.slot_of[id] : id;
+  }
+  return L.experts + static_cast<int64_t>(b) * p.blob_bytes;
+}
+
+// Does layer li's C stage carry the next layer's router block?
+__device__ __forceinline__ bool c_has_router(const DecodeParams& p, int li) {
+  return (p.phases & PH_ROUTER) && (p.phases & PH_C) && li + 1 < p.n_layers;
+}
+
+__device__ __forceinline__ bool needs_ids(const DecodeParams& p) {
+  return (p.phases & (PH_BROUTED | PH_C)) != 0;
+}
+
+__device__ __forceinline__ int router_groups(int r0, int n) {
+  return (r0 + n - 1) / kGroup - r0 / kGroup + 1;
+}
+
+__device__ uint32_t stage_bytes(const DecodeParams& p, const Stage& st, int li) {
+  switch (st.kind) {
+    case ST_R:
+      return st.n * p.E + router_groups(st.a, st.n) * p.E * 4;
+    case ST_BS:
+    case ST_BR:
+      return st.n * 2 * p.rbD;
+    default: {
+      uint32_t b = st.n * (p.K * p.rbI + p.rbS);
+      if (c_has_router(p, li)) b += st.n * p.E + router_groups(st.a, st.n) * p.E * 4;
+      return b;
+    }
+  }
+}
+
+__device__ void issue_stage(const Ctx& cx, const Stage& st, int li, uint8_t* dst, uint64_t* bar) {
+  const DecodeParams& p = *cx.p;
+  const int l = p.layer0 + li;
+  const LayerDev& L = p.layers[l];
+  auto router_block = [&](const LayerDev& R, uint8_t* d) {
+    bulk_g2s(d, R.router_t + static_cast<int64_t>(st.a) * p.E, st.n * p.E, bar);
+    d += st.n * p.E;
+    const int g0 = st.a / kGroup, ng = router_groups(st.a, st.n);
+    bulk_g2s(d, R.router_sb + static_cast<int64_t>(g0) * p.E, ng * p.E * 4, bar);
+  };
+  switch (st.kind) {
+    case ST_R:
+      router_block(L, dst);
+      break;
+    case ST_BS:
+      bulk_g2s(dst, L.shared_gu + static_cast<int64_t>(st.a) * 2 * p.rbD, st.n * 2 * p.rbD, bar);
+      break;
+    case ST_BR: {
+      const int id = cx.misc[M_IDS + st.k];
+      const uint8_t* blob = expert_blob(p, L, st.k, id);
+      bulk_g2s(dst, blob + static_cast<int64_t>(st.a) * 2 * p.rbD, st.n * 2 * p.rbD, bar);
+      break;
+    }
+    default: {
+      uint8_t* d = dst;
+      for (int k = 0; k < p.K; ++k) {
+        const int id = cx.misc[M_IDS + k];
+        const uint8_t* blob = expert_blob(p, L, k, id);
+        bulk_g2s(d, blob + p.dn_off + static_cast<int64_t>(st.a) * p.rbI, st.n * p.rbI, bar);
+        d += st.n * p.rbI;
+      }
+      bulk_g2s(d, L.shared_dn + static_cast<int64_t>(st.a) * p.rbS, st.n * p.rbS, bar);
+      d += st.n * p.rbS;
+      if (c_has_router(p, li)) router_block(p.layers[l + 1], d);
+      break;
+    }
+  }
+}
+
+// ------------------------------------------------------------- producer
+
+__device__ void producer(const Ctx& cx) {
+  const DecodeParams& p = *cx.p;
+  int st_idx = 0;
+  for (int li = 0; li < p.n_layers; ++li) {
+    const LayerPlan lp = layer_plan(p, cx.part, li);
+    const int total = lp.n_r + lp.n_bs + lp.n_br + lp.n_c;
+    for (int s = 0; s <= total; ++s) {
+      if (s == lp.n_r + lp.n_bs && needs_ids(p)) {
+        // the routed stages' addresses need this layer's ids (one gate phase per layer)
+        if (!mbar_wait(cx.ids_ready, li & 1, p.timeout_ns, &cx.misc[M_ABORT])) {
+          cx.misc[M_ABORT] = 1;
+          return;
+        }
+      }
+      if (s == total) break;
+      const Stage st = stage_at(p, cx.part, lp, s);
+      const int slot = st_idx % p.nslots;
+      const uint32_t round = st_idx / p.nslots;
+      if (!mbar_wait(&cx.empty[slot], (round & 1) ^ 1, p.timeout_ns, &cx.misc[M_ABORT])) {
+        cx.misc[M_ABORT] = 1;
+        return;
+      }
+      mbar_arrive_expect_tx(&cx.full[slot], stage_bytes(p, st, li));
+      issue_stage(cx, st, li, cx.smem + static_cast<int64_t>(slot) * p.slot_bytes, &cx.full[slot]);
+      ++st_idx;
+      cx.misc[M_ISSUED] = st_idx;
+    }
+  }
+}
+
+// ------------------------------------------------------------- consumers
+
+// Max of a value over all consumer threads.
+__device__ float consumer_max(const Ctx& cx, float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5;
+  volatile float* red = reinterpret_cast<volatile float*>(cx.misc) + M_RED;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  csync();
+  float m = 0.f;
+  for (int i = 0; i < kConsumerWarps; ++i) m = fmaxf(m, red[i]);
+  csync();
+  return m;
+}
+
+// Power-of-two factor f with max|v| * f < 2^15 (1 if already in range).
+__device__ __forceinline__ float prescale_for(float m) {
+  float f = 1.f;
+  while (m * f >= 32768.f) f *= 0.5f;
+  return f;
+}
+
+// Per-chunk activation sums for chunks [c0, c1) of the vec region.
+__device__ void chunk_sums(uint8_t* vec, float* coff, float* vsum, int c0, int c1) {
+  for (int c = c0 + static_cast<int>(threadIdx.x); c < c1; c += kConsumers) {
+    const __half* hv = reinterpret_cast<const __half*>(vec + c * kChunkStride);
+    float sa = 0.f, sb = 0.f;
+    for (int e = 0; e < 32; ++e) {
+      const float v = __half2float(hv[e]);
+      if ((e & 2) == 0)
+        sa += v;  // columns 0,1,4,5 (mod 8)
+      else
+        sb += v;  // columns 2,3,6,7 (mod 8)
+    }
+    coff[c] = 1024.f * sa + 64.f * sb;
+    vsum[c] = sa + sb;
+  }
+}
+
+struct VecView {
+  uint8_t* vec;
+  float* coff;
+  float* vsum;
+  float* vscale;  // multiply a dot product by vscale[seg] to undo the prescale
+};
+
+__device__ VecView vec_view(const Ctx& cx, int nchunks) {
+  VecView v;
+  v.vec = cx.smem + cx.p->off_vec;
+  v.coff = reinterpret_cast<float*>(v.vec + nchunks * kChunkStride);
+  v.vsum = v.coff + nchunks;
+  v.vscale = v.vsum + nchunks;
+  return v;
+}
+
+// Layer input x (bf16 [D], global) -> fp16 chunks.
+__device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
+  const DecodeParams& p = *cx.p;
+  const int nc = p.D / 32;
+  VecView v = vec_view(cx, nc);
+  float m = 0.f;
+  for (int i = threadIdx.x; i < p.D / 2; i += kConsumers) {
+    const uint32_t u = ld_cg_u32(xg + 2 * i);
+    m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(u & 0xffffu)), fabsf(bf16_bits_to_f32(u >> 16))));
+  }
+  const float f = prescale_for(consumer_max(cx, m));
+  for (int i = threadIdx.x; i < p.D / 2; i += kConsumers) {
+    const uint32_t u = ld_cg_u32(xg + 2 * i);
+    const __half2 hv =
+        __floats2half2_rn(bf16_bits_to_f32(u & 0xffffu) * f, bf16_bits_to_f32(u >> 16) * f);
+    const int col = 2 * i;
+    *reinterpret_cast<__half2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) = hv;
+  }
+  if (threadIdx.x == 0) v.vscale[0] = 1.f / f;
+  csync();
+  chunk_sums(v.vec, v.coff, v.vsum, 0, nc);
+  csync();
+  return v;
+}
+
+// h (fp32 [K*I + S], global) -> fp16 chunks, one prescale per branch.
+__device__ VecView prep_h(const Ctx& cx) {
+  const DecodeParams& p = *cx.p;
+  const int nc = (p.K * p.I + p.S) / 32;
+  VecView v = vec_view(cx, nc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int seg = warp; seg <= p.K; seg += kConsumerWarps) {
+    const int base = seg * p.I;
+    const int n = seg < p.K ? p.I : p.S;
+    float m = 0.f;
+    for (int i = lane; i < n; i += 32) m = fmaxf(m, fabsf(ld_cg_f32(p.h + base + i)));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float f = prescale_for(m);
+    for (int i = lane; i < n / 2; i += 32) {
+      const int col = base + 2 * i;
+      const __half2 hv =
+          __floats2half2_rn(ld_cg_f32(p.h + col) * f, ld_cg_f32(p.h + col + 1) * f);
+      *reinterpret_cast<__half2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) = hv;
+    }
+    if (lane == 0) v.vscale[seg] = 1.f / f;
+  }
+  csync();
+  chunk_sums(v.vec, v.coff, v.vsum, 0, nc);
+  csync();
+  return v;
+}
+
+// B stage: n gate/up row pairs -> h_out[pair].
+__device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const VecView& xv,
+                          float* h_out) {
+  const DecodeParams& p = *cx.p;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int pair = warp * 2 + (lane >> 4);
+  const int row = (lane >> 3) & 1;
+  const int sub = lane & 7;
+  const int cpt = p.D / 256;
+  float acc = 0.f;
+  if (pair < n) {
+    const uint8_t* rp = buf + (pair * 2 + row) * p.rbD;
+    for (int i = 0; i < cpt; ++i)
+      acc += chunk_dot(rp, p.D / 2, sub + 8 * i, xv.vec, xv.coff, xv.vsum);
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  const float other = __shfl_xor_sync(0xffffffffu, acc, 8);
+  if (pair < n && sub == 0 && row == 0) {
+    const float g = acc * xv.vscale[0], u = other * xv.vscale[0];
+    h_out[pair] = gelu_tanh(g) * u;
+  }
+}
+
+// Router partial logits of rows [r0, r0+n) with the matching x values
+// xr[0..n), accumulated into rpart[E].
+__device__ void router_partial(const Ctx& cx, const uint8_t* blk, int r0, int n, const float* xr,
+                               float* rpart) {
+  const DecodeParams& p = *cx.p;
+  const uint8_t* q = blk;
+  const uint32_t* sb = reinterpret_cast<const uint32_t*>(blk + n * p.E);
+  const int g0 = r0 / kGroup;
+  for (int e = threadIdx.x; e < p.E; e += kConsumers) {
+    float acc = 0.f;
+    for (int r = 0; r < n; ++r) {
+      const uint32_t w = sb[((r0 + r) / kGroup - g0) * p.E + e];
+      const __half2 h2 = *reinterpret_cast<const __half2*>(&w);
+      const float wv = fmaf(__low2float(h2), static_cast<float>(q[r * p.E + e]), __high2float(h2));
+      acc = fmaf(wv, xr[r], acc);
+    }
+    rpart[e] += acc;
+  }
+}
+
+// C stage: rows [r0, r0+n) of the layer output.
+__device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int li,
+                          const VecView& hv, const uint16_t* x_l, uint16_t* x_next, float* rpart) {
+  const DecodeParams& p = *cx.p;
+  float* contrib = reinterpret_cast<float*>(cx.smem + p.off_contrib);
+  float* xnext = reinterpret_cast<float*>(cx.smem + p.off_xnext);
+  const int t = threadIdx.x;
+  const int r = t / p.tasks_row, tt = t % p.tasks_row;
+  const int nch_i = p.I / 32;
+  if (r < n) {
+    float acc = 0.f;
+    const int nrout = p.K * p.nsub_i;
+    if (tt < nrout) {
+      const int k = tt / p.nsub_i, sub = tt % p.nsub_i;
+      const uint8_t* rp = buf + static_cast<int64_t>(k) * n * p.rbI + r * p.rbI;
+      const uint8_t* vb = hv.vec + k * nch_i * kChunkStride;
+      const float* co = hv.coff + k * nch_i;
+      const float* vs = hv.vsum + k * nch_i;
+      for (int i = 0; i < p.cpt_c; ++i)
+        acc += chunk_dot(rp, p.I / 2, sub + p.nsub_i * i, vb, co, vs);
+      acc *= __int_as_float(cx.misc[M_WTS + k]) * hv.vscale[k];
+    } else {
+      const int sub = tt - nrout;
+      const uint8_t* rp = buf + static_cast<int64_t>(p.K) * n * p.rbI + r * p.rbS;
+      const int cb = p.K * nch_i;
+      const uint8_t* vb = hv.vec + cb * kChunkStride;
+      for (int i = 0; i < p.cpt_c; ++i)
+        acc += chunk_dot(rp, p.S / 2, sub + p.nsub_s * i, vb, hv.coff + cb, hv.vsum + cb);
+      acc *= hv.vscale[p.K];
+    }
+    contrib[r * p.tasks_row + tt] = acc;
+  }
+  csync();
+  if (t < n) {
+    float y = 0.f;
+    for (int j = 0; j < p.tasks_row; ++j) y += contrib[t * p.tasks_row + j];
+    const int d = r0 + t;
+    float out = y;
+    if (p.residual) out += bf16_bits_to_f32(ld_cg_u16(x_l + d));
+    const uint16_t ob = f32_to_bf16_bits(out);
+    x_next[d] = ob;
+    xnext[t] = bf16_bits_to_f32(ob);
+  }
+  csync();
+  if (c_has_router(p, li)) {
+    const uint8_t* blk = buf + static_cast<int64_t>(n) * (p.K * p.rbI + p.rbS);
+    router_partial(cx, blk, r0, n, xnext, rpart);
+  }
+}
+
+// Last CTA: reduce the partial logits, choose ids, softmax; publish to global.
+__device__ void router_finish(const Ctx& cx, int li) {
+  const DecodeParams& p = *cx.p;
+  float* logits = reinterpret_cast<float*>(cx.smem + p.off_logits);
+  const LayerDev& L = p.layers[p.layer0 + li];
+  // two threads per expert, each over half of the partials; then combine
+  for (int e2 = threadIdx.x; e2 < 2 * p.E; e2 += kConsumers) {
+    const int e = e2 >> 1, half = e2 & 1;
+    const int c0 = half ? cx.G / 2 : 0, c1 = half ? cx.G : cx.G / 2;
+    const float* src = p.partials + static_cast<int64_t>(e) * p.G_pad;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    int c = c0;
+    for (; c + 4 <= c1; c += 4) {
+      s0 += ld_cg_f32(src + c);
+      s1 += ld_cg_f32(src + c + 1);
+      s2 += ld_cg_f32(src + c + 2);
+      s3 += ld_cg_f32(src + c + 3);
+    }
+    for (; c < c1; ++c) s0 += ld_cg_f32(src + c);
+    const float s = (s0 + s1) + (s2 + s3);
+    const float o = __shfl_xor_sync(0xffffffffu, s, 1);
+    if (!half) {
+      float l = s + o;
+      if (L.logit_bias) l += L.logit_bias[e];
+      logits[e] = l;
+    }
+  }
+  csync();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int ids[kMaxTopK];
+    if (li == 0 && p.forced) {
+      for (int i = 0; i < p.K; ++i) ids[i] = p.forced_ids[i];
+    } else {
+      // k rounds of warp arg-max on (logit desc, index asc)
+      for (int i = 0; i < p.K; ++i) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int e = lane; e < p.E; e += 32) {
+          bool taken = false;
+          for (int j = 0; j < i; ++j) taken |= (ids[j] == e);
+          const float v = logits[e];
+          if (!taken && (v > bv || (v == bv && e < bi))) {
+            bv = v;
+            bi = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        ids[i] = bi;
+      }
+    }
+    if (lane == 0) {
+      float m = -INFINITY;
+      for (int i = 0; i < p.K; ++i) m = fmaxf(m, logits[ids[i]]);
+      float z = 0.f;
+      float ex[kMaxTopK];
+      for (int i = 0; i < p.K; ++i) {
+        ex[i] = expf(logits[ids[i]] - m);
+        z += ex[i];
+      }
+      for (int i = 0; i < p.K; ++i) {
+        p.ids[li * p.K + i] = ids[i];
+        p.wts[li * p.K + i] = ex[i] / z;
+      }
+    }
+  }
+}
+
+// Grid barrier among the consumer groups of all CTAs.  `last_fn` runs on the
+// last CTA to arrive before the others are released.  Returns false on
+// timeout or abort.
+template <typename F>
+__device__ bool grid_barrier(const Ctx& cx, F last_fn) {
+  const DecodeParams& p = *cx.p;
+  csync();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t g = ld_acquire_gpu(p.bar + 1);
+    const uint32_t old = atom_add_acq_rel_gpu(p.bar, 1u);
+    cx.misc[M_GEN] = static_cast<int>(g);
+    cx.misc[M_LAST] = (old == static_cast<uint32_t>(cx.G) - 1) ? 1 : 0;
+  }
+  csync();
+  const uint32_t g = static_cast<uint32_t>(cx.misc[M_GEN]);
+  if (cx.misc[M_LAST]) {
+    __threadfence();
+    last_fn();
+    csync();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      p.bar[0] = 0u;
+      st_release_gpu(p.bar + 1, g + 1u);
+    }
+  } else if (threadIdx.x == 0) {
+    bool ok = false;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      if (ld_acquire_gpu(p.bar + 1) != g) {
+        ok = true;
+        break;
+      }
+      if (ld_acquire_gpu(p.bar + 2) != DEV_OK) break;
+      if (globaltimer_ns() - t0 > p.timeout_ns) break;
+      __nanosleep(64);
+    }
+    if (!ok) {
+      atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
+      cx.misc[M_ABORT] = 1;
+    }
+    __threadfence();
+  }
+  csync();
+  return !cx.misc[M_ABORT];
+}
+
+// Load ids/weights of layer li from global into shared memory and open the
+// producer's gate for that layer's routed stages.
+__device__ void publish_ids_local(const Ctx& cx, int li) {
+  const DecodeParams& p = *cx.p;
+  if (threadIdx.x < p.K) {
+    int id = ld_cg_s32(p.ids + li * p.K + threadIdx.x);
+    if (id < 0 || id >= p.E) {
+      atomicCAS(p.bar + 2, DEV_OK, DEV_BAD_ID);
+      id = 0;
+    }
+    cx.misc[M_IDS + threadIdx.x] = id;
+    cx.misc[M_WTS + threadIdx.x] = __float_as_int(ld_cg_f32(p.wts + li * p.K + threadIdx.x));
+  }
+  csync();
+  if (threadIdx.x == 0) mbar_arrive(cx.ids_ready);
+}
+
+__device__ bool wait_full(const Ctx& cx, int st_idx) {
+  const DecodeParams& p = *cx.p;
+  const int slot = st_idx % p.nslots;
+  const uint32_t round = st_idx / p.nslots;
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&cx.full[slot], round & 1, p.timeout_ns, &cx.misc[M_ABORT]))
+      cx.misc[M_ABORT] = 1;
+  }
+  csync();
+  return !cx.misc[M_ABORT];
+}
+
+__device__ void release_slot(const Ctx& cx, int st_idx) {
+  const int slot = st_idx % cx.p->nslots;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&cx.empty[slot]);
+}
+
+__device__ void write_partials(const Ctx& cx, const float* rpart) {
+  const DecodeParams& p = *cx.p;
+  for (int e = threadIdx.x; e < p.E; e += kConsumers)
+    p.partials[static_cast<int64_t>(e) * p.G_pad + blockIdx.x] = rpart[e];
+}
+
+__device__ void consumer(const Ctx& cx) {
+  const DecodeParams& p = *cx.p;
+  float* rpart = reinterpret_cast<float*>(cx.smem + p.off_rpart);
+  float* xnext = reinterpret_cast<float*>(cx.smem + p.off_xnext);
+  int st_idx = 0;
+  for (int li = 0; li < p.n_layers; ++li) {
+    const uint16_t* x_l = li == 0 ? p.x_in : p.xbuf + ((li - 1) & 1) * p.D;
+    uint16_t* x_next = li + 1 == p.n_layers ? p.y_out : p.xbuf + (li & 1) * p.D;
+    const LayerPlan lp = layer_plan(p, cx.part, li);
+    int s = 0;
+    // ---- router of the launch's first layer (later layers: folded into C)
+    if (li == 0 && (p.phases & PH_ROUTER)) {
+      for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
+      csync();
+      if (lp.n_r) {
+        if (!wait_full(cx, st_idx)) return;
+        const Stage st = stage_at(p, cx.part, lp, s);
+        for (int i = threadIdx.x; i < st.n; i += kConsumers)
+          xnext[i] = bf16_bits_to_f32(ld_cg_u16(x_l + st.a + i));
+        csync();
+        router_partial(cx, cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes,
+                       st.a, st.n, xnext, rpart);
+        csync();
+        release_slot(cx, st_idx);
+        ++st_idx;
+        ++s;
+      }
+      write_partials(cx, rpart);
+      if (!grid_barrier(cx, [&] { router_finish(cx, li); })) return;
+    }
+    if (needs_ids(p)) publish_ids_local(cx, li);
+    // ---- gate/up (shared, then routed)
+    VecView xv{};
+    if (lp.n_bs + lp.n_br) xv = prep_x(cx, x_l);
+    for (; s < lp.n_r + lp.n_bs + lp.n_br; ++s) {
+      const Stage st = stage_at(p, cx.part, lp, s);
+      if (!wait_full(cx, st_idx)) return;
+      const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
+      float* h_out = st.kind == ST_BS ? p.h + p.K * p.I + st.a : p.h + st.k * p.I + st.a;
+      compute_b(cx, buf, st.n, xv, h_out);
+      csync();
+      release_slot(cx, st_idx);
+      ++st_idx;
+    }
+    if (!(p.phases & PH_C)) continue;
+    // ---- down + combine (+ next router's partial logits)
+    if (!grid_barrier(cx, [] {})) return;
+    const VecView hv = prep_h(cx);
+    const bool nr = c_has_router(p, li);
+    for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
+    csync();
+    for (; s < lp.n_r + lp.n_bs + lp.n_br + lp.n_c; ++s) {
+      const Stage st = stage_at(p, cx.part, lp, s);
+      if (!wait_full(cx, st_idx)) return;
+      const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
+      compute_c(cx, buf, st.a, st.n, li, hv, x_l, x_next, rpart);
+      csync();
+      release_slot(cx, st_idx);
+      ++st_idx;
+    }
+    if (nr) {
+      write_partials(cx, rpart);
+      if (!grid_barrier(cx, [&] { router_finish(cx, li + 1); })) return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  Ctx cx;
+  cx.p = &p;
+  cx.smem = smem;
+  cx.full = reinterpret_cast<uint64_t*>(smem + p.off_bars);
+  cx.empty = cx.full + kMaxSlots;
+  cx.ids_ready = cx.empty + kMaxSlots;
+  cx.misc = reinterpret_cast<volatile int*>(smem + p.off_misc);
+  cx.G = gridDim.x;
+  const int c = blockIdx.x, G = gridDim.x;
+  cx.part.sh_lo = split_at(p.S, c, G);
+  cx.part.sh_hi = split_at(p.S, c + 1, G);
+  cx.part.rt_lo = split_at(p.K * p.I, c, G);
+  cx.part.rt_hi = split_at(p.K * p.I, c + 1, G);
+  cx.part.c_lo = split_at(p.D, c, G);
+  cx.part.c_hi = split_at(p.D, c + 1, G);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.nslots; ++i) {
+      mbar_init(&cx.full[i], 1);
+      mbar_init(&cx.empty[i], kConsumerWarps);
+    }
+    mbar_init(cx.ids_ready, 1);
+    for (int i = 0; i < M_COUNT; ++i) cx.misc[i] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x >= kConsumers) {
+    if (threadIdx.x == kConsumers) producer(cx);
+  } else {
+    consumer(cx);
+    if (threadIdx.x == 0 && cx.misc[M_ABORT]) atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
+  }
+  __syncthreads();
+  // Drain: copies issued but not consumed must land before the CTA exits.
+  // Only the last stage issued on each slot can still be pending.
+  if (threadIdx.x == 0) {
+    const int issued = cx.misc[M_ISSUED];
+    for (int st = issued - p.nslots < 0 ? 0 : issued - p.nslots; st < issued; ++st)
+      mbar_wait(&cx.full[st % p.nslots], (st / p.nslots) & 1, p.timeout_ns, nullptr);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+int decode_smem_plan(DecodeParams* p, int max_smem) {
+  const int nc_x = p->D / 32;
+  const int nc_h = (p->K * p->I + p->S) / 32;
+  auto vec_bytes = [](int nc, int nscale) { return nc * kChunkStride + nc * 8 + nscale * 4; };
+  int vb = vec_bytes(nc_x, 1);
+  const int vh = vec_bytes(nc_h, p->K + 1);
+  if (vh > vb) vb = vh;
+  vb = (vb + 127) / 128 * 128;
+  const int b_stage = kPairsPerStage * 2 * p->rbD;
+  const int rsb = 2 * p->E * 4;
+  const int c_stage = p->rc_max * (p->K * p->rbI + p->rbS + p->E) + rsb;
+  int slot = b_stage > c_stage ? b_stage : c_stage;
+  slot = (slot + 127) / 128 * 128;
+  const int fixed = vb + 1024 /*contrib*/ + p->E * 4 /*rpart*/ + 256 * 4 /*xnext*/ +
+                    p->E * 4 /*logits*/ + 512 /*misc*/ + (2 * kMaxSlots + 1) * 8 + 512;
+  int ns = (max_smem - fixed) / slot;
+  if (ns > kMaxSlots) ns = kMaxSlots;
+  if (ns < 2) return -1;
+  p->slot_bytes = slot;
+  p->nslots = ns;
+  int off = ns * slot;
+  p->off_vec = off;
+  off += vb;
+  p->off_contrib = off;
+  off += 1024;
+  p->off_rpart = off;
+  off += (p->E * 4 + 127) / 128 * 128;
+  p->off_xnext = off;
+  off += 1024;
+  p->off_logits = off;
+  off += (p->E * 4 + 127) / 128 * 128;
+  p->off_misc = off;
+  off += 512;
+  p->off_bars = off;
+  off += (2 * kMaxSlots + 1) * 8;
+  p->smem_total = (off + 127) / 128 * 128;
+  return p->smem_total <= max_smem ? 0 : -1;
+}
+
+int decode_launch(const DecodeParams& p, int grid, void* stream, bool cooperative) {
+  static int attr_bytes = 0;  // largest dynamic shared memory size enabled so far
+  if (p.smem_total > attr_bytes) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_total);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    attr_bytes = p.smem_total;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = p.smem_total;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = cooperative ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, decode_kernel, p));
+}
+
+}  // namespace moe

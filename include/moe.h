@@ -1,0 +1,254 @@
+/*
+ * moe.h — C ABI of the B300 Mixture-of-Experts layer-step library
+ * (libmoe_b300.so, built for sm_103a).
+ *
+ * The library runs the data-parallel hot path of an out-of-core MoE runtime on
+ * one GPU: per layer and token, an 8-bit router scores the experts and keeps
+ * the top k, the chosen 4-bit routed experts and an always-on shared expert
+ * run as gated FFNs, and their outputs are combined.  Optionally the routed
+ * experts live in a pinned host pool and only a per-layer set of HBM slots is
+ * resident, filled on demand under an LFU policy.
+ *
+ * Passages the operations follow (page title, section):
+ *   sh.edu-sjtu.cn "TurboFieldfare：8GB Mac 本地跑 Gemma 4 26B-A4B 的 Swift +
+ *     Metal 运行时", section "TurboFieldfare 把内存压到约 2GB 的三件事": per
+ *     layer the router picks the top-8 expert ids, they are planned against the
+ *     layer's 16-slot LFU cache, misses are read into GPU-visible buffers while
+ *     the GPU computes the resident shared expert, and the two outputs are
+ *     combined; prompts are prefilled in chunks of at most 128 tokens.
+ *   shilu.ai "drumih/turbo-fieldfare", overview table (row 权重): MLX affine
+ *     4-bit weights with group 64, 8-bit router; section 推理引擎的工作原理:
+ *     the same per-layer plan/fill/overlap/combine sequence; section 状态和范围:
+ *     bounded expert cache, chunked single-prompt prefill, token-at-a-time
+ *     generation.
+ * The pages give no formulas.  The readings used: y = sum_i w_i FFN_i(x) +
+ * FFN_shared(x), FFN(x) = W_down (gelu_tanh(W_gate x) * (W_up x)), w = softmax
+ * of the chosen router logits, ties in the logits go to the lower expert index.
+ *
+ * Conventions for every call:
+ *   - Return value: MOE_OK or a negative moe_status.  No call aborts or throws
+ *     across the ABI.  On error the handle stays usable unless the status is
+ *     MOE_ERR_CUDA (the CUDA context may be lost) and moe_last_error() holds a
+ *     one-line description.
+ *   - "device" pointers are CUDA global memory on the handle's device;
+ *     "host" pointers are ordinary (pageable or pinned) host memory.
+ *   - Activations are bf16 bit patterns, row-major [T][d_model].
+ *   - A handle is used by one host thread at a time.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Kernels run asynchronously; an error a kernel reports on the device
+ *     (a bounded wait that ran out, an expert id out of range) is returned by
+ *     the next call that synchronises (moe_stack_ids, the host-I/O call, or a
+ *     forward call that asks for ids).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* bad pointer, size or configuration */
+  MOE_ERR_OOM = -2,         /* device or pinned host allocation failed */
+  MOE_ERR_CUDA = -3,        /* a CUDA runtime call failed */
+  MOE_ERR_TIMEOUT = -4,     /* a bounded wait (host or device) ran out */
+  MOE_ERR_INJECTED = -5,    /* a fault injected with moe_debug_inject() */
+  MOE_ERR_STATE = -6,       /* call not valid in this handle's mode or state */
+  MOE_ERR_DEVICE = -7       /* a kernel reported an inconsistent input (e.g. id out of range) */
+} moe_status;
+
+typedef struct moe_handle moe_handle;
+
+/* Shape of the layer stack.  Requirements: group == 64; d_model % 256 == 0;
+ * d_expert % 64 == 0; d_shared % 64 == 0; 1 <= top_k <= 32; top_k <= n_experts
+ * <= 1024; n_experts % 16 == 0; n_layers >= 1; max_tokens >= 1. */
+typedef struct {
+  int d_model;    /* D: hidden size */
+  int n_experts;  /* E: routed experts per layer */
+  int d_expert;   /* I: routed expert inner size */
+  int top_k;      /* k: experts chosen per token */
+  int d_shared;   /* S: shared expert inner size */
+  int group;      /* quantisation group along the input dimension (64) */
+  int n_layers;   /* L */
+  int n_slots;    /* 0: every expert resident in HBM.  Else per-layer HBM slot
+                     count (top_k <= n_slots <= n_experts); the full expert
+                     set then lives in a pinned host pool owned by the handle. */
+  int max_tokens; /* largest T passed to any forward call */
+} moe_config;
+
+/* One affine-quantised matrix in canonical form, HOST memory, row-major
+ * [rows][cols] with groups of `group` along cols:
+ *   value(r, c) = fp16(scale[r][c/group]) * code(r, c) + fp16(bias[r][c/group])
+ * 4-bit: q is [rows][cols/2]; column 2i is the low nibble of byte i.
+ * 8-bit: q is [rows][cols].  scale and bias hold IEEE binary16 bit patterns. */
+typedef struct {
+  const uint8_t* q;
+  const uint16_t* scale;
+  const uint16_t* bias;
+} moe_qtensor;
+
+/* Weights of one layer, HOST memory, canonical form.  Shapes:
+ *   router       8-bit [E][D]
+ *   router_logit_bias  fp32 [E], added to the logits before ranking; may be NULL
+ *   shared_gate, shared_up   4-bit [S][D];   shared_down  4-bit [D][S]
+ *   exp_gate, exp_up         arrays of E tensors, each 4-bit [I][D]
+ *   exp_down                 array of E tensors, each 4-bit [D][I]          */
+typedef struct {
+  moe_qtensor router;
+  const float* router_logit_bias;
+  moe_qtensor shared_gate, shared_up, shared_down;
+  const moe_qtensor* exp_gate;
+  const moe_qtensor* exp_up;
+  const moe_qtensor* exp_down;
+} moe_layer_weights;
+
+/*
+ * moe_create — build a handle for `cfg` on the current CUDA device.
+ * Copies and repacks all weights (`layers`: n_layers entries, host memory) into
+ * the GPU layout: into HBM when cfg->n_slots == 0, else into a pinned host
+ * pool plus n_slots HBM slots per layer.  The caller may free `layers` when
+ * the call returns.  Allocates the handle's device scratch (sized by
+ * max_tokens), a side copy stream and events.  On failure *out is NULL and
+ * nothing is leaked.
+ */
+moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, moe_handle** out);
+
+/* moe_destroy — synchronise the handle's own streams and free everything.
+ * NULL is accepted. */
+void moe_destroy(moe_handle* h);
+
+/* Flags for the forward calls. */
+#define MOE_FWD_RESIDUAL 1 /* y = bf16(x + moe(x)) instead of bf16(moe(x)) */
+
+/* Per-call statistics (all fields written by the call when non-NULL). */
+typedef struct {
+  int32_t* ids;     /* host [T][k] or NULL: chosen expert ids (a copy, synchronising) */
+  float* weights;   /* host [T][k] or NULL: routing weights (synchronising) */
+  int hits;         /* streaming mode: cache hits of this call */
+  int misses;       /* streaming mode: cache misses (experts copied host->HBM) */
+  int64_t bytes_h2d;/* streaming mode: weight bytes copied host->HBM */
+} moe_layer_stats;
+
+/*
+ * moe_layer_forward — one MoE layer step for T tokens (1 <= T <= max_tokens).
+ * x: device [T][D] bf16 input.  y: device [T][D] bf16 output; y may not alias x.
+ * forced_ids: host [T][k] or NULL.  When given, those experts are used (each
+ *   row k distinct ids in [0, E)); their weights are still the softmax of the
+ *   router logits over the forced set.
+ * Streaming mode (n_slots > 0) requires T == 1: the call routes, plans the
+ *   chosen ids against the layer's LFU slots (see moe_cache_step), copies the
+ *   misses from the pinned pool on the handle's side stream while the shared
+ *   expert runs on `stream`, then runs the routed experts and the combine.
+ *   Without forced_ids this reads the ids back to the host (synchronising).
+ * All kernels are enqueued on `stream`; the call returns without
+ * synchronising unless stats->ids / stats->weights are requested or the mode
+ * needs a host decision.
+ */
+moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, void* y, int flags,
+                             const int32_t* forced_ids, void* stream, moe_layer_stats* stats);
+
+/*
+ * moe_forward_stack — layers [0, n_layers) back to back with the residual
+ * between layers: x_{l+1} = bf16(x_l + moe_l(x_l)); y = x_{n_layers}.
+ * Resident mode only.  x, y: device [T][D] bf16, y may not alias x.
+ * For T == 1 the whole stack runs as one persistent cooperative kernel.
+ */
+moe_status moe_forward_stack(moe_handle* h, const void* x, int T, void* y, int n_layers,
+                             void* stream);
+
+/*
+ * moe_forward_stack_host — moe_forward_stack with HOST input and output:
+ * copies x (host [T][D] bf16) to the device, runs the stack, copies the result
+ * to y (host [T][D] bf16) and synchronises `stream`.  Uses the handle's
+ * pinned staging buffers; x and y may be pageable.
+ */
+moe_status moe_forward_stack_host(moe_handle* h, const void* x, int T, void* y, int n_layers,
+                                  void* stream);
+
+/*
+ * moe_stack_ids — copy the expert ids and weights chosen by the most recent
+ * forward call on this handle: ids host [n_layers][T][k] int32, weights host
+ * [n_layers][T][k] fp32 (either may be NULL).  Synchronises the device.
+ */
+moe_status moe_stack_ids(moe_handle* h, int n_layers, int T, int32_t* ids, float* weights);
+
+/* Flags for moe_cache_step. */
+#define MOE_PLAN_ONLY 1 /* update the slot table but copy no weights */
+
+/* Outcome of one cache step for k ids (k <= 64). */
+typedef struct {
+  int32_t hit[64];     /* 1 if ids[i] was resident */
+  int32_t slot[64];    /* HBM slot holding ids[i] after the step */
+  int32_t evicted[64]; /* expert evicted to make room for ids[i], or -1 */
+  int misses;
+} moe_cache_result;
+
+/*
+ * moe_cache_step — plan k distinct expert ids (host, each in [0, E)) against
+ * layer `layer`'s slots: hits first (use count + 1, last use = this step), then
+ * misses in ascending expert id take the lowest empty slot, or else evict,
+ * among slots this step has not used, the least-used slot (then the least
+ * recently used, then the lowest slot index); newcomers start at count 1.
+ * Unless MOE_PLAN_ONLY, each miss is copied from the pinned pool into its
+ * slot with one cudaMemcpyAsync on the handle's side stream; the copies are
+ * ordered before the next forward call on this layer.  Streaming mode only.
+ * If a copy cannot be enqueued the slot is left empty and the call fails.
+ */
+moe_status moe_cache_step(moe_handle* h, int layer, const int32_t* ids, int k, int flags,
+                          moe_cache_result* out);
+
+/* moe_cache_reset — empty every slot of every layer (no copies). */
+moe_status moe_cache_reset(moe_handle* h);
+
+/*
+ * Host-only slot planner: the same LFU policy as moe_cache_step, without a
+ * handle, a GPU or any copy.  For callers that plan ahead (e.g. to prefetch)
+ * and for tests.  moe_slot_plan_step fails with MOE_ERR_INVALID_ARG (state
+ * unchanged) if the ids repeat, fall outside [0, n_experts) or k > n_slots.
+ */
+typedef struct moe_slot_plan moe_slot_plan;
+moe_status moe_slot_plan_create(int n_slots, int n_experts, moe_slot_plan** out);
+moe_status moe_slot_plan_step(moe_slot_plan* p, const int32_t* ids, int k, moe_cache_result* out);
+void moe_slot_plan_destroy(moe_slot_plan* p);
+
+/* Sizes of what the handle holds. */
+typedef struct {
+  int64_t device_weight_bytes;  /* HBM bytes of repacked weights (incl. slots) */
+  int64_t pinned_pool_bytes;    /* pinned host pool (streaming mode) */
+  int64_t device_scratch_bytes; /* HBM scratch */
+  int64_t expert_blob_bytes;    /* bytes of one repacked routed expert */
+  int num_sms;                  /* SMs used by the persistent kernels */
+} moe_info;
+moe_status moe_get_info(const moe_handle* h, moe_info* out);
+
+/* Host-side fault injection for tests (never touches the GPU):
+ *   MOE_INJECT_H2D_FAIL: the n-th next miss copy is not enqueued and reported
+ *     as MOE_ERR_INJECTED; the slot it was meant for is left empty.
+ *   MOE_INJECT_SLOW_COPY: sleep `arg` milliseconds on the host before each
+ *     miss copy is enqueued (results must not change).
+ *   MOE_INJECT_PINNED_ALLOC_FAIL: the next moe_create in this process fails
+ *     its pinned-pool allocation (h may be NULL).
+ *   MOE_INJECT_NONE: clear everything. */
+#define MOE_INJECT_NONE 0
+#define MOE_INJECT_H2D_FAIL 1
+#define MOE_INJECT_SLOW_COPY 2
+#define MOE_INJECT_PINNED_ALLOC_FAIL 3
+moe_status moe_debug_inject(moe_handle* h, int what, int arg);
+
+/* Host waits on device work poll with this deadline (default 10000 ms) and
+ * return MOE_ERR_TIMEOUT when it passes. */
+moe_status moe_set_timeout_ms(moe_handle* h, int ms);
+
+const char* moe_status_string(moe_status s);
+/* Last error text of this handle ("" if none); with h == NULL, of the last
+ * failed moe_create in this process. */
+const char* moe_last_error(const moe_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

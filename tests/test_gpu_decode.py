@@ -1,0 +1,177 @@
+"""GPU parity of the decode path (T tokens, one at a time) against the oracle.
+
+Every call goes through the C ABI (libmoe_b300.so) via the thin binding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import check_ids, check_output, check_weights
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import expert_ffn_streaming_bit_b300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def tiny_layer():
+    return synth.make_layer(synth.TINY, "tiny", 0)
+
+
+def _run_layer(moe, h, x_cpu, layer=0, flags=0, forced=None):
+    x = x_cpu.cuda()
+    y = torch.empty_like(x)
+    st = moe.moe_layer_forward(h, layer, x, y, flags=flags, forced_ids=forced, want_ids=True)
+    torch.cuda.synchronize()
+    return y.cpu(), st
+
+
+def test_tiny_router_ids_weights_and_output(moe, tiny_layer):
+    sh = synth.TINY
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=64)
+    x = synth.make_tokens(sh, "tiny", 64)
+    y, st = _run_layer(moe, h, x)
+    ref = oracle.moe_layer(oracle.LayerView(sh, tiny_layer), x)
+    assert check_ids(st["ids"], ref, sh.top_k) <= 1
+    check_weights(st["weights"], ref, st["ids"])
+    check_output(y, ref["y"])
+
+
+def test_tiny_residual_output(moe, tiny_layer):
+    sh = synth.TINY
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=8)
+    x = synth.make_tokens(sh, "tiny", 8, index=1)
+    y, st = _run_layer(moe, h, x, flags=moe.MOE_FWD_RESIDUAL)
+    ref = oracle.moe_layer(oracle.LayerView(sh, tiny_layer), x)
+    check_output(y, ref["y"], x_bf16=x)
+
+
+def test_tiny_forced_ids(moe, tiny_layer):
+    sh = synth.TINY
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=4)
+    x = synth.make_tokens(sh, "tiny", 4, index=2)
+    forced = np.array([[0, 15], [7, 3], [8, 9], [14, 1]], np.int32)
+    y, st = _run_layer(moe, h, x, forced=forced)
+    ref = oracle.moe_layer(oracle.LayerView(sh, tiny_layer), x, forced)
+    assert np.array_equal(st["ids"], forced)
+    check_weights(st["weights"], ref, st["ids"])
+    check_output(y, ref["y"])
+
+
+def test_tiny_repeated_runs_are_bit_identical(moe, tiny_layer):
+    sh = synth.TINY
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=16)
+    x = synth.make_tokens(sh, "tiny", 16, index=3)
+    y1, s1 = _run_layer(moe, h, x)
+    y2, s2 = _run_layer(moe, h, x)
+    assert torch.equal(y1, y2) and np.array_equal(s1["ids"], s2["ids"])
+
+
+def test_tiny_edge_inputs(moe, tiny_layer):
+    """All-zero input: every logit is exactly 0, so the ties go to ids 0..k-1
+    and the output is exactly 0.  Inputs beyond the fp16 range (|x| ~ 1e5)
+    exercise the power-of-two prescale of the activations."""
+    sh = synth.TINY
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=2)
+    x = torch.zeros(2, sh.d_model, dtype=torch.bfloat16)
+    x[1] = synth.make_tokens(sh, "tiny", 1, index=4)[0] * 30000.0
+    y, st = _run_layer(moe, h, x)
+    ref = oracle.moe_layer(oracle.LayerView(sh, tiny_layer), x)
+    assert st["ids"][0].tolist() == list(range(sh.top_k)) == ref["ids"][0].tolist()
+    assert torch.all(y[0] == 0)
+    assert check_ids(st["ids"][1:], {k: v[1:] for k, v in ref.items()}, sh.top_k) == 0
+    check_output(y[1:], ref["y"][1:])
+
+
+def test_tiny_stack_matches_teacher_forced_oracle(moe):
+    sh = synth.MoEShape("tiny4", 256, 16, 128, 2, 256, 64, 4)
+    layers = [synth.make_layer(sh, "tiny", l) for l in range(4)]
+    h = moe.moe_create(sh, layers, max_tokens=1)
+    x0 = synth.make_tokens(sh, "tiny", 1, index=9)
+    xs = [x0]
+    for n in range(1, 5):
+        y = torch.empty_like(x0).cuda()
+        moe.moe_forward_stack(h, x0.cuda(), y, n)
+        torch.cuda.synchronize()
+        xs.append(y.cpu())
+    ids, w = moe.moe_stack_ids(h, 4, 1)
+    for l in range(4):
+        ref = oracle.moe_layer(oracle.LayerView(sh, layers[l]), xs[l])
+        check_ids(ids[l], ref, sh.top_k)
+        check_weights(w[l], ref, ids[l])
+        check_output(xs[l + 1], ref["y"], x_bf16=xs[l])
+
+
+# ---------------------------------------------------------------- full shape
+
+@pytest.fixture(scope="module")
+def gemma_layers():
+    """30 layers of the Gemma-4-26B-A4B MoE block shape, drawn on the GPU."""
+    sh = synth.GEMMA
+    out = []
+    for l in range(sh.n_layers):
+        L = synth.make_layer(sh, "decode", l, device="cuda")
+        out.append(synth.layer_to(L, "cpu"))
+        del L
+    torch.cuda.empty_cache()
+    return out
+
+
+def test_gemma_single_layer_tokens(moe, gemma_layers):
+    sh = synth.GEMMA
+    h = moe.moe_create(sh, gemma_layers[:1], max_tokens=8)
+    x = synth.make_tokens(sh, "decode", 8, index=0)
+    y, st = _run_layer(moe, h, x)
+    ref = oracle.moe_layer(oracle.LayerView(sh, gemma_layers[0]), x)
+    assert check_ids(st["ids"], ref, sh.top_k) <= 1
+    check_weights(st["weights"], ref, st["ids"])
+    check_output(y, ref["y"])
+
+
+def test_gemma_30_layer_stack_teacher_forced(moe, gemma_layers):
+    """The benchmark's launch configuration: one persistent kernel per token
+    through all 30 layers.  Sampled layers are checked against the oracle on
+    the GPU's own bf16 input to that layer (prefix runs give x_l exactly)."""
+    sh = synth.GEMMA
+    h = moe.moe_create(sh, gemma_layers, max_tokens=1)
+    x0 = synth.make_tokens(sh, "decode", 1, index=100)
+    xd = x0.cuda()
+    y = torch.empty_like(xd)
+    moe.moe_forward_stack(h, xd, y, sh.n_layers)
+    torch.cuda.synchronize()
+    ids, w = moe.moe_stack_ids(h, sh.n_layers, 1)
+    y_full = y.cpu()
+    layers_to_check = [0, 1, 2, 14, 28, 29]
+    xs = {0: x0}
+    for n in sorted(set(layers_to_check + [l + 1 for l in layers_to_check])):
+        if n == 0 or n in xs:
+            continue
+        yy = torch.empty_like(xd)
+        moe.moe_forward_stack(h, xd, yy, n)
+        torch.cuda.synchronize()
+        xs[n] = yy.cpu()
+    assert torch.equal(xs[sh.n_layers], y_full)
+    for l in layers_to_check:
+        ref = oracle.moe_layer(oracle.LayerView(sh, gemma_layers[l]), xs[l])
+        check_ids(ids[l], ref, sh.top_k)
+        check_weights(w[l], ref, ids[l])
+        check_output(xs[l + 1], ref["y"], x_bf16=xs[l])
+
+
+def test_gemma_stack_host_io_matches_device_io(moe, gemma_layers):
+    sh = synth.GEMMA
+    h = moe.moe_create(sh, gemma_layers[:4], max_tokens=1)
+    x0 = synth.make_tokens(sh, "decode", 1, index=7)
+    yd = torch.empty_like(x0).cuda()
+    moe.moe_forward_stack(h, x0.cuda(), yd, 4)
+    torch.cuda.synchronize()
+    xh = x0.view(torch.int16).numpy().view(np.uint16)
+    yh = np.empty_like(xh)
+    moe.moe_forward_stack_host(h, xh, yh, 4)
+    assert np.array_equal(yh, yd.cpu().view(torch.int16).numpy().view(np.uint16))
