@@ -380,7 +380,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   // the first-layer router stage holds a whole CTA row slice
   const int64_t r_stage = int64_t((d.D + G - 1) / G) * d.E + 2 * d.E * 4;
   if (r_stage > p.slot_bytes) CREATE_FAIL(MOE_ERR_INVALID_ARG, "router stage too large for the SM count");
-  h->grid = G;
+  h->grid = G < d.D ? G : static_cast<int>(d.D);  // every CTA owns at least one output row
   *out = h.release();
   return MOE_OK;
 #undef CREATE_TRY
