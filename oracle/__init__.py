@@ -76,7 +76,9 @@ def lib():
             L.orc_ffn.restype = None
             L.orc_ffn.argtypes = [ctypes.POINTER(QT)] * 3 + [i32, i32, i32, P, P]
             L.orc_moe_layer.restype = i32
-            L.orc_moe_layer.argtypes = [ctypes.POINTER(Layer), P, i32, P, P, P, P, P]
+            L.orc_moe_layer.argtypes = [ctypes.POINTER(Layer), P, i32, P, i32, P, P, P, P]
+            L.orc_rms_normalise.restype = None
+            L.orc_rms_normalise.argtypes = [P, i32, ctypes.c_double, P]
             L.orc_bucket.restype = i32
             L.orc_bucket.argtypes = [P, i32, i32, i32, P, P, P]
             L.orc_lfu_step.restype = i32
@@ -192,8 +194,21 @@ def router_logits(view: LayerView, x_bf16: np.ndarray) -> np.ndarray:
     return out
 
 
-def moe_layer(view: LayerView, x_bf16, forced_ids: Optional[np.ndarray] = None):
-    """Returns dict(ids [T,k] int32, w [T,k] f64, logits [T,E] f32, y [T,D] f64)."""
+RMS_EPS = 1e-6
+
+
+def rms_normalise(x: np.ndarray, eps: float = RMS_EPS) -> np.ndarray:
+    xx = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty_like(xx)
+    lib().orc_rms_normalise(_p(xx), xx.shape[0], eps, _p(out))
+    return out
+
+
+def moe_layer(view: LayerView, x_bf16, forced_ids: Optional[np.ndarray] = None,
+              prenorm: bool = False):
+    """Returns dict(ids [T,k] int32, w [T,k] f64, logits [T,E] f32, y [T,D] f64).
+
+    prenorm: the layer reads the RMS-normalised input (unit gain, eps 1e-6)."""
     sh = view.shape
     x = _np(x_bf16, np.uint16)
     T = x.shape[0]
@@ -205,7 +220,8 @@ def moe_layer(view: LayerView, x_bf16, forced_ids: Optional[np.ndarray] = None):
     if forced_ids is not None:
         forced_ids = np.ascontiguousarray(forced_ids, dtype=np.int32).reshape(T, sh.top_k)
         fptr = forced_ids.ctypes.data
-    rc = lib().orc_moe_layer(ctypes.byref(view.s), _p(x), T, fptr, _p(ids), _p(w),
+    rc = lib().orc_moe_layer(ctypes.byref(view.s), _p(x), T, fptr, 1 if prenorm else 0,
+                             _p(ids), _p(w),
                              _p(logits), _p(y))
     if rc != 0:
         raise ValueError("orc_moe_layer: bad arguments")

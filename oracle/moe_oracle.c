@@ -242,6 +242,22 @@ void orc_ffn(const orc_qt* wg, const orc_qt* wu, const orc_qt* wd, int D, int F,
 }
 
 /*
+ * Parameter-free RMS normalisation of a layer input: u = x / sqrt(mean(x^2) + eps).
+ * [P4] 状态和范围 lists normalisation kernels beside the MoE kernels, and the
+ * pages' model (Gemma 4) normalises the residual stream before each FFN block;
+ * its learned gain is a trained weight, so the reading takes unit gain.
+ */
+void orc_rms_normalise(const double* x, int D, double eps, double* u) {
+  double ss = 0.0;
+  for (int c = 0; c < D; ++c) ss += x[c] * x[c];
+  const double r = 1.0 / sqrt(ss / (double)D + eps);
+  for (int c = 0; c < D; ++c) u[c] = x[c] * r;
+}
+
+#define ORC_PRENORM 1
+#define ORC_RMS_EPS 1e-6
+
+/*
  * One MoE layer step for T tokens ([P2] 三件事, first bullet; [P4]
  * 推理引擎的工作原理): per token, route to k experts, run them and the shared
  * expert, and combine.  The pages say only that the two outputs are combined
@@ -249,10 +265,12 @@ void orc_ffn(const orc_qt* wg, const orc_qt* wu, const orc_qt* wd, int D, int F,
  *
  * x_bf16: [T][D] bf16 bits.  forced_ids: [T][k] or NULL; when given, those
  * experts are used and the weights are the softmax over their logits.
+ * flags & ORC_PRENORM: the router and the experts read orc_rms_normalise(x)
+ * (eps 1e-6) instead of x.
  * Outputs: ids [T][k], w [T][k], logits [T][E] (fp32), y [T][D] (fp64).
  */
 int orc_moe_layer(const orc_layer* L, const uint16_t* x_bf16, int T, const int32_t* forced_ids,
-                  int32_t* ids, double* w, float* logits, double* y) {
+                  int flags, int32_t* ids, double* w, float* logits, double* y) {
   const int D = L->d_model, E = L->n_experts, I = L->d_expert, k = L->top_k;
   const int S = L->d_shared, G = L->group;
   if (k < 1 || k > E || D % G || I % G || S % G) return -1;
@@ -260,6 +278,7 @@ int orc_moe_layer(const orc_layer* L, const uint16_t* x_bf16, int T, const int32
   double* e_out = (double*)malloc(sizeof(double) * (size_t)D);
   for (int t = 0; t < T; ++t) {
     for (int c = 0; c < D; ++c) x[c] = bf16_to_double(x_bf16[(int64_t)t * D + c]);
+    if (flags & ORC_PRENORM) orc_rms_normalise(x, D, ORC_RMS_EPS, x);
     float* lt = logits + (int64_t)t * E;
     int32_t* it = ids + (int64_t)t * k;
     double* wt = w + (int64_t)t * k;

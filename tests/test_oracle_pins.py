@@ -307,6 +307,49 @@ def test_forced_ids_use_router_softmax_over_the_forced_set():
         assert abs(out["w"][t, 0] - 1 / (1 + math.exp(d))) < 1e-15
 
 
+def test_prenorm_is_invariant_to_input_scale():
+    """The RMS pre-normalisation makes the layer depend on the direction of x
+    only: scaling x by a power of two (exact in bf16) changes nothing but the
+    eps term, and the expert choice is unchanged."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 7)
+    x = synth.make_tokens(sh, "tiny", 4, index=7)
+    view = oracle.LayerView(sh, L)
+    base = oracle.moe_layer(view, x, prenorm=True)
+    for c in (8.0, 0.125, 64.0):
+        out = oracle.moe_layer(view, (x.float() * c).to(torch.bfloat16), prenorm=True)
+        assert np.array_equal(out["ids"], base["ids"])
+        # eps / c^2 moves the normalised input by at most ~3e-5 relative here
+        assert np.abs(out["y"] - base["y"]).max() <= 1e-3 * np.abs(base["y"]).max()
+    raw = oracle.moe_layer(view, (x.float() * 64.0).to(torch.bfloat16))
+    assert np.abs(raw["y"] - base["y"]).max() > 10 * np.abs(base["y"]).max()
+
+
+def test_prenorm_leaves_a_unit_rms_input_nearly_unchanged():
+    """x with entries +-1 has mean square exactly 1, so the normalised input is
+    x / sqrt(1 + 1e-6): the layer output moves by about 5e-7 relative."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 8)
+    rng = np.random.default_rng(8)
+    x = torch.from_numpy(rng.choice([-1.0, 1.0], size=(3, sh.d_model)).astype(np.float32))
+    x = x.to(torch.bfloat16)
+    view = oracle.LayerView(sh, L)
+    a = oracle.moe_layer(view, x, prenorm=True)
+    b = oracle.moe_layer(view, x)
+    assert np.array_equal(a["ids"], b["ids"])
+    rel = np.abs(a["y"] - b["y"]).max() / np.abs(b["y"]).max()
+    assert 1e-8 < rel < 5e-6, rel
+
+
+def test_prenorm_of_a_zero_input_is_zero():
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 9)
+    x = torch.zeros(1, sh.d_model, dtype=torch.bfloat16)
+    out = oracle.moe_layer(oracle.LayerView(sh, L), x, prenorm=True)
+    assert out["ids"][0].tolist() == list(range(sh.top_k))
+    assert np.all(out["y"] == 0.0)
+
+
 # ------------------------------------------------------------ bucketing
 
 def _read_golden(name):
