@@ -123,7 +123,7 @@ def oracle_sample(shape, layers, x_cpu, budget_s: float):
     x = x_cpu
     import torch
     while n < len(layers):
-        ref = oracle.moe_layer(oracle.LayerView(shape, layers[n]), x)
+        ref = oracle.moe_layer(oracle.LayerView(shape, layers[n]), x, prenorm=True)
         y = torch.tensor(ref["y"], dtype=torch.float32)
         x = (x.float() + y).to(torch.bfloat16)
         n += 1
@@ -255,10 +255,10 @@ def run_reference(args):
     view = oracle.LayerView(shape, layers[0])
     xs = synth.make_tokens(shape, "decode", args.warmup + args.steps, index=4000)
     for i in range(args.warmup):
-        oracle.moe_layer(view, xs[i:i + 1])
+        oracle.moe_layer(view, xs[i:i + 1], prenorm=True)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle.moe_layer(view, xs[args.warmup + i:args.warmup + i + 1])
+        oracle.moe_layer(view, xs[args.warmup + i:args.warmup + i + 1], prenorm=True)
     dt = time.perf_counter() - t0
     per_layer = dt / args.steps
     value = 1.0 / (per_layer * shape.n_layers)

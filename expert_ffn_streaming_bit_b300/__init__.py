@@ -2,8 +2,9 @@
 
 Argument marshalling only: every step of the layer runs in the library's CUDA
 kernels.  Functions carry the C entry points' names.  Importing this package
-loads the in-tree ``libmoe_b300.so``; if it is missing the import fails (there
-is no fallback path).  Build it with ``python -m expert_ffn_streaming_bit_b300.build``
+loads the in-tree ``libmoe_b300.so``, rebuilding it first when a source is
+newer; if it cannot be built or loaded the import fails (there is no fallback
+path).  Build it with ``python -m expert_ffn_streaming_bit_b300.build``
 or ``__graft_entry__.build()``.
 """
 from __future__ import annotations
@@ -14,17 +15,23 @@ from typing import Dict, List, Optional, Sequence
 
 import numpy as np
 
-_HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+from . import build as _build
 
+LIB_PATH = _build.LIB
+
+# Rebuild in-tree when a source is newer than the library (a no-op otherwise).
+# A failed build or a missing library makes this import fail: there is no
+# fallback path.
+if _build.stale():
+    _build.build()
 if not os.path.exists(LIB_PATH):
-    raise ImportError(
-        "libmoe_b300.so is not built (run python -m expert_ffn_streaming_bit_b300.build)")
+    raise ImportError("libmoe_b300.so is not built (python -m expert_ffn_streaming_bit_b300.build)")
 
 _lib = ctypes.CDLL(LIB_PATH)
 
 MOE_OK = 0
 MOE_FWD_RESIDUAL = 1
+MOE_FWD_PRENORM = 2
 MOE_PLAN_ONLY = 1
 MOE_INJECT_NONE, MOE_INJECT_H2D_FAIL, MOE_INJECT_SLOW_COPY, MOE_INJECT_PINNED_ALLOC_FAIL = 0, 1, 2, 3
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "MOE_ERR_CUDA",

@@ -173,12 +173,13 @@ moe_status launch(moe_handle* h, const DecodeParams& p, cudaStream_t s) {
 }
 
 DecodeParams params_for(moe_handle* h, int layer0, int n_layers, const void* x, void* y, int phases,
-                        int residual) {
+                        int flags) {
   DecodeParams p = h->base;
   p.layer0 = layer0;
   p.n_layers = n_layers;
   p.phases = phases;
-  p.residual = residual;
+  p.residual = (flags & MOE_FWD_RESIDUAL) ? 1 : 0;
+  p.prenorm = (flags & MOE_FWD_PRENORM) ? 1 : 0;
   p.x_in = static_cast<const uint16_t*>(x);
   p.y_out = static_cast<uint16_t*>(y);
   return p;
@@ -305,7 +306,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   const int64_t T = c.max_tokens;
   auto al = [](int64_t b) { return (b + 255) / 256 * 256; };
   const int64_t sz_xbuf = al(2 * T * d.D * 2), sz_h = al(T * (d.K * d.I + d.S) * 4),
-                sz_part = al(d.E * G_pad * 4), sz_ids = al(int64_t(L) * T * d.K * 4), sz_bar = 256,
+                sz_part = al((d.E + 1) * G_pad * 4), sz_ids = al(int64_t(L) * T * d.K * 4), sz_bar = 256,
                 sz_io = al(T * d.D * 2);
   h->scratch_bytes = sz_xbuf + sz_h + sz_part + 2 * sz_ids + sz_bar + 2 * sz_io;
   CREATE_TRY(cudaMalloc(&h->scratch, h->scratch_bytes));
@@ -362,6 +363,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   p.wts = h->wts;
   p.bar = h->bar;
   p.G_pad = G_pad;
+  p.rms_eps = 1e-6f;
   const int nch_i = d.I / 32, nch_s = d.S / 32;
   const int g = gcd(nch_i, nch_s);
   int cpt = 1;
@@ -502,7 +504,7 @@ static moe_status decode_layer_streaming(moe_handle* h, int layer, const void* x
                                          int flags, const int32_t* forced, cudaStream_t s,
                                          moe_layer_stats* stats) {
   const int K = h->cfg.top_k;
-  DecodeParams p1 = params_for(h, layer, 1, x, y, 0, flags & MOE_FWD_RESIDUAL);
+  DecodeParams p1 = params_for(h, layer, 1, x, y, 0, flags);
   int32_t ids[kMaxTopK];
   moe_cache_result cr;
   moe_status st;
@@ -532,7 +534,7 @@ static moe_status decode_layer_streaming(moe_handle* h, int layer, const void* x
     if (st != MOE_OK) return st;
   }
   CUDA_TRY(h, cudaStreamWaitEvent(s, h->copy_done[layer], 0));
-  DecodeParams p2 = params_for(h, layer, 1, x, y, PH_BROUTED | PH_C, flags & MOE_FWD_RESIDUAL);
+  DecodeParams p2 = params_for(h, layer, 1, x, y, PH_BROUTED | PH_C, flags);
   p2.use_slots = 1;
   for (int i = 0; i < K; ++i) p2.slots[i] = cr.slot[i];
   st = launch(h, p2, s);
@@ -568,7 +570,6 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
     stats->hits = stats->misses = 0;
     stats->bytes_h2d = 0;
   }
-  const int residual = flags & MOE_FWD_RESIDUAL;
   if (h->cfg.n_slots > 0) {
     if (T != 1) return fail(h, MOE_ERR_STATE, "streaming mode runs one token per call");
     moe_status st = decode_layer_streaming(h, layer, x, y, flags, forced_ids, s, stats);
@@ -577,7 +578,7 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
     // resident: one persistent launch per token
     for (int t = 0; t < T; ++t) {
       DecodeParams p = params_for(h, layer, 1, static_cast<const uint16_t*>(x) + int64_t(t) * D,
-                                  static_cast<uint16_t*>(y) + int64_t(t) * D, PH_ALL, residual);
+                                  static_cast<uint16_t*>(y) + int64_t(t) * D, PH_ALL, flags);
       p.ids = h->ids + int64_t(t) * K;
       p.wts = h->wts + int64_t(t) * K;
       if (forced_ids) {
@@ -611,7 +612,8 @@ moe_status moe_forward_stack(moe_handle* h, const void* x, int T, void* y, int n
   const int D = h->cfg.d_model, K = h->cfg.top_k;
   for (int t = 0; t < T; ++t) {
     DecodeParams p = params_for(h, 0, n_layers, static_cast<const uint16_t*>(x) + int64_t(t) * D,
-                                static_cast<uint16_t*>(y) + int64_t(t) * D, PH_ALL, 1);
+                                static_cast<uint16_t*>(y) + int64_t(t) * D, PH_ALL,
+                                MOE_FWD_RESIDUAL | MOE_FWD_PRENORM);
     // token t's ids: its own layer-major block [n_layers][K]
     p.ids = h->ids + int64_t(t) * n_layers * K;
     p.wts = h->wts + int64_t(t) * n_layers * K;

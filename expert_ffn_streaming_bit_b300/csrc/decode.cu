@@ -321,6 +321,20 @@ __device__ float consumer_max(const Ctx& cx, float v) {
   return m;
 }
 
+// Sum of a value over all consumer threads (fixed order over warps).
+__device__ float consumer_sum(const Ctx& cx, float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5;
+  volatile float* red = reinterpret_cast<volatile float*>(cx.misc) + M_RED;
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  csync();
+  float s = 0.f;
+  for (int i = 0; i < kConsumerWarps; ++i) s += red[i];
+  csync();
+  return s;
+}
+
 // Power-of-two factor f with max|v| * f < 2^15 (1 if already in range).
 __device__ __forceinline__ float prescale_for(float m) {
   float f = 1.f;
@@ -372,14 +386,23 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
     m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(u & 0xffffu)), fabsf(bf16_bits_to_f32(u >> 16))));
   }
   const float f = prescale_for(consumer_max(cx, m));
+  float ss = 0.f;  // sum of (f x)^2, for the pre-norm
   for (int i = threadIdx.x; i < p.D / 2; i += kConsumers) {
     const uint32_t u = ld_cg_u32(xg + 2 * i);
-    const __half2 hv =
-        __floats2half2_rn(bf16_bits_to_f32(u & 0xffffu) * f, bf16_bits_to_f32(u >> 16) * f);
+    const float a = bf16_bits_to_f32(u & 0xffffu) * f, b = bf16_bits_to_f32(u >> 16) * f;
+    ss = fmaf(a, a, fmaf(b, b, ss));
     const int col = 2 * i;
-    *reinterpret_cast<__half2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) = hv;
+    *reinterpret_cast<__half2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) =
+        __floats2half2_rn(a, b);
   }
-  if (threadIdx.x == 0) v.vscale[0] = 1.f / f;
+  if (p.prenorm) {
+    // dot products of the prescaled x are multiplied by r / f, where
+    // r = 1 / sqrt(mean(x^2) + eps) = f / sqrt(mean((f x)^2) + eps f^2)
+    ss = consumer_sum(cx, ss);
+    if (threadIdx.x == 0) v.vscale[0] = rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps * f * f);
+  } else if (threadIdx.x == 0) {
+    v.vscale[0] = 1.f / f;
+  }
   csync();
   chunk_sums(v.vec, v.coff, v.vsum, 0, nc);
   csync();
@@ -506,6 +529,11 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
   if (c_has_router(p, li)) {
     const uint8_t* blk = buf + static_cast<int64_t>(n) * (p.K * p.rbI + p.rbS);
     router_partial(cx, blk, r0, n, xnext, rpart);
+    if (threadIdx.x == 0) {
+      float ss = 0.f;
+      for (int i = 0; i < n; ++i) ss = fmaf(xnext[i], xnext[i], ss);
+      rpart[p.E] += ss;
+    }
   }
 }
 
@@ -530,8 +558,24 @@ __device__ void router_finish(const Ctx& cx, int li) {
     for (; c < c1; ++c) s0 += ld_cg_f32(src + c);
     const float s = (s0 + s1) + (s2 + s3);
     const float o = __shfl_xor_sync(0xffffffffu, s, 1);
-    if (!half) {
-      float l = s + o;
+    if (!half) logits[e] = s + o;
+  }
+  if (p.prenorm && threadIdx.x < 32) {
+    // r = 1 / sqrt(mean(x^2) + eps) from the partial sums of squares (row E)
+    const float* src = p.partials + static_cast<int64_t>(p.E) * p.G_pad;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < cx.G; c += 32) ss += ld_cg_f32(src + c);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (threadIdx.x == 0)
+      reinterpret_cast<volatile float*>(cx.misc)[M_RED] =
+          rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps);
+  }
+  csync();
+  {
+    const float r = p.prenorm ? reinterpret_cast<volatile float*>(cx.misc)[M_RED] : 1.f;
+    for (int e = threadIdx.x; e < p.E; e += kConsumers) {
+      float l = logits[e] * r;
       if (L.logit_bias) l += L.logit_bias[e];
       logits[e] = l;
     }
@@ -669,7 +713,7 @@ __device__ void release_slot(const Ctx& cx, int st_idx) {
 
 __device__ void write_partials(const Ctx& cx, const float* rpart) {
   const DecodeParams& p = *cx.p;
-  for (int e = threadIdx.x; e < p.E; e += kConsumers)
+  for (int e = threadIdx.x; e <= p.E; e += kConsumers)
     p.partials[static_cast<int64_t>(e) * p.G_pad + blockIdx.x] = rpart[e];
 }
 
@@ -685,7 +729,7 @@ __device__ void consumer(const Ctx& cx) {
     int s = 0;
     // ---- router of the launch's first layer (later layers: folded into C)
     if (li == 0 && (p.phases & PH_ROUTER)) {
-      for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
+      for (int e = threadIdx.x; e <= p.E; e += kConsumers) rpart[e] = 0.f;
       csync();
       if (lp.n_r) {
         if (!wait_full(cx, st_idx)) return;
@@ -695,6 +739,11 @@ __device__ void consumer(const Ctx& cx) {
         csync();
         router_partial(cx, cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes,
                        st.a, st.n, xnext, rpart);
+        if (threadIdx.x == 0) {
+          float ss = 0.f;
+          for (int i = 0; i < st.n; ++i) ss = fmaf(xnext[i], xnext[i], ss);
+          rpart[p.E] = ss;
+        }
         csync();
         release_slot(cx, st_idx);
         ++st_idx;
@@ -722,7 +771,7 @@ __device__ void consumer(const Ctx& cx) {
     if (!grid_barrier(cx, [] {})) return;
     const VecView hv = prep_h(cx);
     const bool nr = c_has_router(p, li);
-    for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
+    for (int e = threadIdx.x; e <= p.E; e += kConsumers) rpart[e] = 0.f;
     csync();
     for (; s < lp.n_r + lp.n_bs + lp.n_br + lp.n_c; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
@@ -800,7 +849,7 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
   const int c_stage = p->rc_max * (p->K * p->rbI + p->rbS + p->E) + rsb;
   int slot = b_stage > c_stage ? b_stage : c_stage;
   slot = (slot + 127) / 128 * 128;
-  const int fixed = vb + 1024 /*contrib*/ + p->E * 4 /*rpart*/ + 256 * 4 /*xnext*/ +
+  const int fixed = vb + 1024 /*contrib*/ + (p->E + 1) * 4 + 124 /*rpart*/ + 256 * 4 /*xnext*/ +
                     p->E * 4 /*logits*/ + 512 /*misc*/ + (2 * kMaxSlots + 1) * 8 + 512;
   int ns = (max_smem - fixed) / slot;
   if (ns > kMaxSlots) ns = kMaxSlots;
@@ -813,7 +862,7 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
   p->off_contrib = off;
   off += 1024;
   p->off_rpart = off;
-  off += (p->E * 4 + 127) / 128 * 128;
+  off += ((p->E + 1) * 4 + 127) / 128 * 128;
   p->off_xnext = off;
   off += 1024;
   p->off_logits = off;

@@ -55,6 +55,8 @@ struct DecodeParams {
   int64_t blob_bytes, dn_off;
   int phases;
   int residual;
+  int prenorm;                // layer input is x / sqrt(mean(x^2) + rms_eps)
+  float rms_eps;
   int forced;                 // ids of layer0 given below (single-layer launches)
   int forced_ids[kMaxTopK];
   int use_slots;              // blob index of routed slot i = slots[i] (single-layer launches)
@@ -63,7 +65,8 @@ struct DecodeParams {
   uint16_t* y_out;         // bf16 [D], output of the last layer
   uint16_t* xbuf;          // bf16 [2][D] scratch
   float* h;                // [K*I + S] fp32 scratch
-  float* partials;         // [E][G_pad] router partial logits (transposed)
+  float* partials;         // [E + 1][G_pad] router partial logits (transposed);
+                           // row E holds partial sums of x^2 for the pre-norm
   int32_t* ids;            // [n_layers][K], relative to layer0
   float* wts;              // [n_layers][K]
   uint32_t* bar;           // [0] arrivals, [1] generation, [2] status

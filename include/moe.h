@@ -122,7 +122,11 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
 void moe_destroy(moe_handle* h);
 
 /* Flags for the forward calls. */
-#define MOE_FWD_RESIDUAL 1 /* y = bf16(x + moe(x)) instead of bf16(moe(x)) */
+#define MOE_FWD_RESIDUAL 1 /* y = bf16(x + moe(u)) instead of bf16(moe(u)) */
+#define MOE_FWD_PRENORM 2  /* u = x / sqrt(mean(x^2) + 1e-6) (unit-gain RMS norm per token);
+                              without it u = x.  shilu.ai page, section 状态和范围, lists
+                              normalisation kernels beside the MoE kernels; the pages'
+                              model normalises each FFN block's input. */
 
 /* Per-call statistics (all fields written by the call when non-NULL). */
 typedef struct {
@@ -152,8 +156,10 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
                              const int32_t* forced_ids, void* stream, moe_layer_stats* stats);
 
 /*
- * moe_forward_stack — layers [0, n_layers) back to back with the residual
- * between layers: x_{l+1} = bf16(x_l + moe_l(x_l)); y = x_{n_layers}.
+ * moe_forward_stack — layers [0, n_layers) back to back, each reading the
+ * RMS-normalised residual stream and adding its output to it:
+ * x_{l+1} = bf16(x_l + moe_l(x_l / sqrt(mean(x_l^2) + 1e-6))); y = x_{n_layers}
+ * (the flags MOE_FWD_RESIDUAL | MOE_FWD_PRENORM on every layer).
  * Resident mode only.  x, y: device [T][D] bf16, y may not alias x.
  * For T == 1 the whole stack runs as one persistent cooperative kernel.
  */

@@ -89,6 +89,22 @@ def test_tiny_edge_inputs(moe, tiny_layer):
     check_output(y[1:], ref["y"][1:])
 
 
+def test_tiny_prenorm_matches_oracle_at_any_input_scale(moe, tiny_layer):
+    """MOE_FWD_PRENORM: the layer reads x / sqrt(mean(x^2) + 1e-6); inputs far
+    outside the fp16 range give the same ids and output as unit-scale ones."""
+    sh = synth.TINY
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=8)
+    x = synth.make_tokens(sh, "tiny", 8, index=5)
+    x[4:] = (x[4:].float() * 65536.0).to(torch.bfloat16)
+    y, st = _run_layer(moe, h, x, flags=moe.MOE_FWD_PRENORM)
+    ref = oracle.moe_layer(oracle.LayerView(sh, tiny_layer), x, prenorm=True)
+    assert check_ids(st["ids"], ref, sh.top_k) == 0
+    check_weights(st["weights"], ref, st["ids"])
+    check_output(y, ref["y"])
+    y2, _ = _run_layer(moe, h, x, flags=moe.MOE_FWD_PRENORM | moe.MOE_FWD_RESIDUAL)
+    check_output(y2, ref["y"], x_bf16=x)
+
+
 def test_tiny_stack_matches_teacher_forced_oracle(moe):
     sh = synth.MoEShape("tiny4", 256, 16, 128, 2, 256, 64, 4)
     layers = [synth.make_layer(sh, "tiny", l) for l in range(4)]
@@ -102,7 +118,7 @@ def test_tiny_stack_matches_teacher_forced_oracle(moe):
         xs.append(y.cpu())
     ids, w = moe.moe_stack_ids(h, 4, 1)
     for l in range(4):
-        ref = oracle.moe_layer(oracle.LayerView(sh, layers[l]), xs[l])
+        ref = oracle.moe_layer(oracle.LayerView(sh, layers[l]), xs[l], prenorm=True)
         check_ids(ids[l], ref, sh.top_k)
         check_weights(w[l], ref, ids[l])
         check_output(xs[l + 1], ref["y"], x_bf16=xs[l])
@@ -132,6 +148,11 @@ def test_gemma_single_layer_tokens(moe, gemma_layers):
     assert check_ids(st["ids"], ref, sh.top_k) <= 1
     check_weights(st["weights"], ref, st["ids"])
     check_output(y, ref["y"])
+    y, st = _run_layer(moe, h, x, flags=moe.MOE_FWD_PRENORM)
+    ref = oracle.moe_layer(oracle.LayerView(sh, gemma_layers[0]), x, prenorm=True)
+    assert check_ids(st["ids"], ref, sh.top_k) <= 1
+    check_weights(st["weights"], ref, st["ids"])
+    check_output(y, ref["y"])
 
 
 def test_gemma_30_layer_stack_teacher_forced(moe, gemma_layers):
@@ -158,7 +179,7 @@ def test_gemma_30_layer_stack_teacher_forced(moe, gemma_layers):
         xs[n] = yy.cpu()
     assert torch.equal(xs[sh.n_layers], y_full)
     for l in layers_to_check:
-        ref = oracle.moe_layer(oracle.LayerView(sh, gemma_layers[l]), xs[l])
+        ref = oracle.moe_layer(oracle.LayerView(sh, gemma_layers[l]), xs[l], prenorm=True)
         check_ids(ids[l], ref, sh.top_k)
         check_weights(w[l], ref, ids[l])
         check_output(xs[l + 1], ref["y"], x_bf16=xs[l])
