@@ -87,6 +87,7 @@ _sig = {
     "moe_layer_forward": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, ctypes.POINTER(moe_layer_stats)]),
     "moe_forward_stack": (_I, [_P, _P, _I, _P, _I, _P]),
     "moe_forward_stack_host": (_I, [_P, _P, _I, _P, _I, _P]),
+    "moe_forward_stack_noalloc": (_I, [_P, _P, _P, _I, _P]),
     "moe_stack_ids": (_I, [_P, _I, _I, _P, _P]),
     "moe_cache_step": (_I, [_P, _I, _P, _I, _I, ctypes.POINTER(moe_cache_result)]),
     "moe_cache_reset": (_I, [_P]),
@@ -234,6 +235,14 @@ def moe_forward_stack_host(handle: Handle, x: np.ndarray, y: np.ndarray, n_layer
     x = np.ascontiguousarray(x)
     _check(_lib.moe_forward_stack_host(handle.ptr, x.ctypes.data, x.shape[0], y.ctypes.data,
                                        n_layers, _stream_ptr(stream)), handle)
+
+
+def moe_forward_stack_noalloc(handle: Handle, x, y, n_layers: int, stream=None):
+    """One token through the stack with the library's fixed scratch array
+    (no allocation of any kind).  x, y: CUDA bf16 tensors [1, D]."""
+    assert x.shape[0] == 1 and y.shape[0] == 1
+    _check(_lib.moe_forward_stack_noalloc(handle.ptr, _dev_ptr(x), _dev_ptr(y), n_layers,
+                                          _stream_ptr(stream)), handle)
 
 
 def moe_stack_ids(handle: Handle, n_layers: int, T: int):

@@ -187,6 +187,25 @@ DecodeParams params_for(moe_handle* h, int layer0, int n_layers, const void* x, 
 
 }  // namespace
 
+namespace moe {
+
+int stack_launch_params(moe_handle* h, const void* x, void* y, int n_layers, DecodeParams* p,
+                        int* grid, int* device) {
+  if (!h || !x || !y || x == y || !p || !grid || !device) return MOE_ERR_INVALID_ARG;
+  if (h->cfg.n_slots > 0) return fail(h, MOE_ERR_STATE, "the decode stack needs resident mode");
+  if (n_layers < 1 || n_layers > h->cfg.n_layers) return fail(h, MOE_ERR_INVALID_ARG, "bad n_layers");
+  *p = params_for(h, 0, n_layers, x, y, PH_ALL, MOE_FWD_RESIDUAL | MOE_FWD_PRENORM);
+  *grid = h->grid;
+  *device = h->device;
+  return MOE_OK;
+}
+
+int handle_error(moe_handle* h, int status, const char* msg) {
+  return fail(h, static_cast<moe_status>(status), "%s", msg);
+}
+
+}  // namespace moe
+
 #pragma GCC visibility push(default)
 extern "C" {
 

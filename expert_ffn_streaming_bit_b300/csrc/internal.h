@@ -84,3 +84,15 @@ int decode_smem_plan(DecodeParams* p, int max_smem);   // fills the carve-up; 0 
 int decode_launch(const DecodeParams& p, int grid, void* stream, bool cooperative);
 
 }  // namespace moe
+
+// Implemented in api.cu for the library's other translation units.
+struct moe_handle;
+namespace moe {
+// Launch parameters of a one-token resident decode stack over layers
+// [0, n_layers) with pre-norm and residual (the moe_forward_stack recipe),
+// without scratch pointers.  Fails like moe_forward_stack on bad arguments.
+int stack_launch_params(moe_handle* h, const void* x, void* y, int n_layers, DecodeParams* p,
+                        int* grid, int* device);
+// Records an error message on the handle and returns `status`.
+int handle_error(moe_handle* h, int status, const char* msg);
+}  // namespace moe

@@ -176,6 +176,32 @@ moe_status moe_forward_stack_host(moe_handle* h, const void* x, int T, void* y, 
                                   void* stream);
 
 /*
+ * moe_forward_stack_noalloc — moe_forward_stack for one token (T = 1) that
+ * allocates nothing.  The pages have no counterpart to this call: it exists
+ * for callers that may not allocate device memory while they run, such as
+ * code inside an allocator or memory-pool hook, real-time loops where
+ * cudaMalloc's implicit synchronisation is not allowed, or hosts whose
+ * allocator belongs to another framework.
+ *   x, y: device [1][D] bf16, y may not alias x (caller-owned, as for
+ *   moe_forward_stack).  Resident mode only; the handle's device must be
+ *   current.
+ * The per-call scratch (grid-barrier words, activation double buffer, h,
+ * router partials, ids, weights) lives in one statically sized device array
+ * of 1 MiB inside the library.  Every GPU that loads the library holds that
+ * array until the process exits.  A shape whose scratch does not fit is
+ * rejected with MOE_ERR_INVALID_ARG and a message giving both sizes.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it, so make that first call before any
+ * stream capture.  Every call shares the one array and overwrites what the
+ * previous call left there: calls that overlap on the GPU (other streams, or
+ * other handles on the same device) race and must be serialised by the
+ * caller.  Ids, weights and device-side error status of this call are not
+ * retrievable (moe_stack_ids reads the handle's own scratch).
+ */
+moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, void* y, int n_layers,
+                                     void* stream);
+
+/*
  * moe_stack_ids — copy the expert ids and weights chosen by the most recent
  * forward call on this handle: ids host [n_layers][T][k] int32, weights host
  * [n_layers][T][k] fp32 (either may be NULL).  Synchronises the device.
