@@ -164,6 +164,8 @@ moe_status check_device_status(moe_handle* h, cudaStream_t s) {
 
 int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 moe_status launch(moe_handle* h, const DecodeParams& p, cudaStream_t s) {
   const int e = decode_launch(p, h->grid, s, true);
   if (e != 0)
@@ -192,6 +194,7 @@ namespace moe {
 int stack_launch_params(moe_handle* h, const void* x, void* y, int n_layers, DecodeParams* p,
                         int* grid, int* device) {
   if (!h || !x || !y || x == y || !p || !grid || !device) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return fail(h, MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
   if (h->cfg.n_slots > 0) return fail(h, MOE_ERR_STATE, "the decode stack needs resident mode");
   if (n_layers < 1 || n_layers > h->cfg.n_layers) return fail(h, MOE_ERR_INVALID_ARG, "bad n_layers");
   *p = params_for(h, 0, n_layers, x, y, PH_ALL, MOE_FWD_RESIDUAL | MOE_FWD_PRENORM);
@@ -394,6 +397,10 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   p.tasks_row = d.K * p.nsub_i + p.nsub_s;
   if (p.tasks_row > kConsumers)
     CREATE_FAIL(MOE_ERR_INVALID_ARG, "top_k * d_expert too large for the decode kernel");
+  if (d.D > 8 * kConsumers * 4 || d.K * d.I + d.S > 4 * kConsumers * 8)
+    CREATE_FAIL(MOE_ERR_INVALID_ARG, "d_model or top_k * d_expert + d_shared too large for the decode kernel");
+  if ((d.D + std::min<int64_t>(G, d.D) - 1) / std::min<int64_t>(G, d.D) > 256)
+    CREATE_FAIL(MOE_ERR_INVALID_ARG, "too few SMs for d_model in the decode kernel");
   p.rc_max = kConsumers / p.tasks_row;
   p.timeout_ns = 2000000000ull;
   if (decode_smem_plan(&p, max_smem) != 0)
@@ -572,6 +579,7 @@ extern "C" {
 moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, void* y, int flags,
                              const int32_t* forced_ids, void* stream, moe_layer_stats* stats) {
   if (!h || !x || !y || x == y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return fail(h, MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
   if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, MOE_ERR_INVALID_ARG, "bad layer %d", layer);
   if (T < 1 || T > h->cfg.max_tokens) return fail(h, MOE_ERR_INVALID_ARG, "T=%d out of range", T);
   const int K = h->cfg.top_k, D = h->cfg.d_model;
@@ -624,6 +632,7 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
 moe_status moe_forward_stack(moe_handle* h, const void* x, int T, void* y, int n_layers,
                              void* stream) {
   if (!h || !x || !y || x == y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return fail(h, MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
   if (h->cfg.n_slots > 0) return fail(h, MOE_ERR_STATE, "moe_forward_stack needs resident mode");
   if (n_layers < 1 || n_layers > h->cfg.n_layers) return fail(h, MOE_ERR_INVALID_ARG, "bad n_layers");
   if (T < 1 || T > h->cfg.max_tokens) return fail(h, MOE_ERR_INVALID_ARG, "T=%d out of range", T);

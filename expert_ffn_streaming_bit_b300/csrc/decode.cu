@@ -71,7 +71,8 @@ enum : int {
   M_GEN = 66,
   M_ISSUED = 67,
   M_RED = 72,  // [8] per-warp reduction scratch
-  M_COUNT = 96
+  M_SEG = 96,  // [K+1] per-branch max |h| (float bits)
+  M_COUNT = 136
 };
 
 struct Ctx {
@@ -275,12 +276,52 @@ __device__ void issue_stage(const Ctx& cx, const Stage& st, int li, uint8_t* dst
 
 // ------------------------------------------------------------- producer
 
+// L2 prefetches of the layer's weights that this CTA will stream later, so
+// that HBM keeps working while the ring is full or the grid synchronises.
+// Fixed weights (shared down rows, the next router's block) at the start of
+// the layer; routed rows as soon as the layer's ids are known.
+__device__ void prefetch_fixed(const Ctx& cx, int li) {
+  const DecodeParams& p = *cx.p;
+  if (!(p.phases & PH_C)) return;
+  const int rows = cx.part.c_hi - cx.part.c_lo;
+  if (rows <= 0) return;
+  const int l = p.layer0 + li;
+  prefetch_l2(p.layers[l].shared_dn + static_cast<int64_t>(cx.part.c_lo) * p.rbS, rows * p.rbS);
+  if (c_has_router(p, li)) {
+    const LayerDev& R = p.layers[l + 1];
+    prefetch_l2(R.router_t + static_cast<int64_t>(cx.part.c_lo) * p.E, rows * p.E);
+  }
+}
+
+__device__ void prefetch_routed(const Ctx& cx, int li) {
+  const DecodeParams& p = *cx.p;
+  const LayerDev& L = p.layers[p.layer0 + li];
+  if (p.phases & PH_BROUTED) {
+    int q = cx.part.rt_lo;
+    while (q < cx.part.rt_hi) {
+      const int k = q / p.I, j = q % p.I;
+      const int n = min(cx.part.rt_hi - q, p.I - j);
+      const uint8_t* blob = expert_blob(p, L, k, cx.misc[M_IDS + k]);
+      prefetch_l2(blob + static_cast<int64_t>(j) * 2 * p.rbD, n * 2 * p.rbD);
+      q += n;
+    }
+  }
+  const int rows = cx.part.c_hi - cx.part.c_lo;
+  if ((p.phases & PH_C) && rows > 0) {
+    for (int k = 0; k < p.K; ++k) {
+      const uint8_t* blob = expert_blob(p, L, k, cx.misc[M_IDS + k]);
+      prefetch_l2(blob + p.dn_off + static_cast<int64_t>(cx.part.c_lo) * p.rbI, rows * p.rbI);
+    }
+  }
+}
+
 __device__ void producer(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
   int st_idx = 0;
   for (int li = 0; li < p.n_layers; ++li) {
     const LayerPlan lp = layer_plan(p, cx.part, li);
     const int total = lp.n_r + lp.n_bs + lp.n_br + lp.n_c;
+    prefetch_fixed(cx, li);
     for (int s = 0; s <= total; ++s) {
       if (s == lp.n_r + lp.n_bs && needs_ids(p)) {
         // the routed stages' addresses need this layer's ids (one gate phase per layer)
@@ -288,6 +329,7 @@ __device__ void producer(const Ctx& cx) {
           cx.misc[M_ABORT] = 1;
           return;
         }
+        prefetch_routed(cx, li);
       }
       if (s == total) break;
       const Stage st = stage_at(p, cx.part, lp, s);
@@ -375,25 +417,58 @@ __device__ VecView vec_view(const Ctx& cx, int nchunks) {
   return v;
 }
 
-// Layer input x (bf16 [D], global) -> fp16 chunks.
+// Layer input x (bf16 [D], global) -> fp16 chunks.  One batch of 16-byte
+// loads per thread (D <= 8 * kConsumers * kMaxXV); the CTA's own output rows
+// [c_lo, c_hi) are also kept as fp32 in xres for the residual.
+constexpr int kMaxXV = 4;
+
 __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
   const DecodeParams& p = *cx.p;
   const int nc = p.D / 32;
   VecView v = vec_view(cx, nc);
+  float* xres = reinterpret_cast<float*>(cx.smem + p.off_xres);
+  const int nv = p.D / 8;
+  uint4 r[kMaxXV];
   float m = 0.f;
-  for (int i = threadIdx.x; i < p.D / 2; i += kConsumers) {
-    const uint32_t u = ld_cg_u32(xg + 2 * i);
-    m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(u & 0xffffu)), fabsf(bf16_bits_to_f32(u >> 16))));
+#pragma unroll
+  for (int i = 0; i < kMaxXV; ++i) {
+    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
+    if (idx < nv) r[i] = __ldcg(reinterpret_cast<const uint4*>(xg) + idx);
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxXV; ++i) {
+    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
+    if (idx < nv) {
+      const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(w[j] & 0xffffu)), fabsf(bf16_bits_to_f32(w[j] >> 16))));
+        const int col = idx * 8 + 2 * j;
+        if (col >= cx.part.c_lo && col < cx.part.c_hi) xres[col - cx.part.c_lo] = bf16_bits_to_f32(w[j] & 0xffffu);
+        if (col + 1 >= cx.part.c_lo && col + 1 < cx.part.c_hi)
+          xres[col + 1 - cx.part.c_lo] = bf16_bits_to_f32(w[j] >> 16);
+      }
+    }
   }
   const float f = prescale_for(consumer_max(cx, m));
   float ss = 0.f;  // sum of (f x)^2, for the pre-norm
-  for (int i = threadIdx.x; i < p.D / 2; i += kConsumers) {
-    const uint32_t u = ld_cg_u32(xg + 2 * i);
-    const float a = bf16_bits_to_f32(u & 0xffffu) * f, b = bf16_bits_to_f32(u >> 16) * f;
-    ss = fmaf(a, a, fmaf(b, b, ss));
-    const int col = 2 * i;
-    *reinterpret_cast<__half2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) =
-        __floats2half2_rn(a, b);
+#pragma unroll
+  for (int i = 0; i < kMaxXV; ++i) {
+    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
+    if (idx < nv) {
+      const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+      uint32_t hv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = bf16_bits_to_f32(w[j] & 0xffffu) * f, b = bf16_bits_to_f32(w[j] >> 16) * f;
+        ss = fmaf(a, a, fmaf(b, b, ss));
+        const __half2 h2 = __floats2half2_rn(a, b);
+        hv[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      const int col = idx * 8;
+      *reinterpret_cast<uint4*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) =
+          make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    }
   }
   if (p.prenorm) {
     // dot products of the prescaled x are multiplied by r / f, where
@@ -409,28 +484,53 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
   return v;
 }
 
-// h (fp32 [K*I + S], global) -> fp16 chunks, one prescale per branch.
+// h (fp32 [K*I + S], global) -> fp16 chunks, one power-of-two prescale per
+// branch.  One batch of 16-byte loads per thread (K*I + S <= 4 * kConsumers *
+// kMaxHV); the per-branch max is an order-independent smem atomicMax on the
+// bit patterns of non-negative floats.
+constexpr int kMaxHV = 8;
+
 __device__ VecView prep_h(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
-  const int nc = (p.K * p.I + p.S) / 32;
+  const int nh = p.K * p.I + p.S;
+  const int nc = nh / 32;
   VecView v = vec_view(cx, nc);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int seg = warp; seg <= p.K; seg += kConsumerWarps) {
-    const int base = seg * p.I;
-    const int n = seg < p.K ? p.I : p.S;
-    float m = 0.f;
-    for (int i = lane; i < n; i += 32) m = fmaxf(m, fabsf(ld_cg_f32(p.h + base + i)));
+  volatile int* segmax = cx.misc + M_SEG;
+  if (threadIdx.x <= static_cast<unsigned>(p.K)) segmax[threadIdx.x] = 0;
+  const int n4 = nh / 4;
+  float4 r[kMaxHV];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float f = prescale_for(m);
-    for (int i = lane; i < n / 2; i += 32) {
-      const int col = base + 2 * i;
-      const __half2 hv =
-          __floats2half2_rn(ld_cg_f32(p.h + col) * f, ld_cg_f32(p.h + col + 1) * f);
-      *reinterpret_cast<__half2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) = hv;
-    }
-    if (lane == 0) v.vscale[seg] = 1.f / f;
+  for (int i = 0; i < kMaxHV; ++i) {
+    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
+    if (idx < n4) r[i] = __ldcg(reinterpret_cast<const float4*>(p.h) + idx);
   }
+  csync();
+  const int KI = p.K * p.I;
+#pragma unroll
+  for (int i = 0; i < kMaxHV; ++i) {
+    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
+    if (idx < n4) {
+      const int seg = idx * 4 < KI ? idx * 4 / p.I : p.K;
+      const float m = fmaxf(fmaxf(fabsf(r[i].x), fabsf(r[i].y)), fmaxf(fabsf(r[i].z), fabsf(r[i].w)));
+      atomicMax(const_cast<int*>(segmax) + seg, __float_as_int(m));
+    }
+  }
+  csync();
+#pragma unroll
+  for (int i = 0; i < kMaxHV; ++i) {
+    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
+    if (idx < n4) {
+      const int seg = idx * 4 < KI ? idx * 4 / p.I : p.K;
+      const float f = prescale_for(__int_as_float(segmax[seg]));
+      const __half2 a = __floats2half2_rn(r[i].x * f, r[i].y * f);
+      const __half2 b = __floats2half2_rn(r[i].z * f, r[i].w * f);
+      const int col = idx * 4;
+      *reinterpret_cast<uint2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+  }
+  if (threadIdx.x <= static_cast<unsigned>(p.K))
+    v.vscale[threadIdx.x] = 1.f / prescale_for(__int_as_float(segmax[threadIdx.x]));
   csync();
   chunk_sums(v.vec, v.coff, v.vsum, 0, nc);
   csync();
@@ -520,7 +620,7 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
     for (int j = 0; j < p.tasks_row; ++j) y += contrib[t * p.tasks_row + j];
     const int d = r0 + t;
     float out = y;
-    if (p.residual) out += bf16_bits_to_f32(ld_cg_u16(x_l + d));
+    if (p.residual) out += reinterpret_cast<const float*>(cx.smem + p.off_xres)[d - cx.part.c_lo];
     const uint16_t ob = f32_to_bf16_bits(out);
     x_next[d] = ob;
     xnext[t] = bf16_bits_to_f32(ob);
@@ -537,26 +637,36 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
   }
 }
 
+constexpr int kRedBatch = 5;
+
 // Last CTA: reduce the partial logits, choose ids, softmax; publish to global.
 __device__ void router_finish(const Ctx& cx, int li) {
   const DecodeParams& p = *cx.p;
   float* logits = reinterpret_cast<float*>(cx.smem + p.off_logits);
   const LayerDev& L = p.layers[p.layer0 + li];
-  // two threads per expert, each over half of the partials; then combine
+  // two threads per expert, each over half of the partials (16-byte loads,
+  // all issued before use); then combine.  Columns >= G are never written.
+  const int Gv = (cx.G + 3) / 4;
   for (int e2 = threadIdx.x; e2 < 2 * p.E; e2 += kConsumers) {
     const int e = e2 >> 1, half = e2 & 1;
-    const int c0 = half ? cx.G / 2 : 0, c1 = half ? cx.G : cx.G / 2;
-    const float* src = p.partials + static_cast<int64_t>(e) * p.G_pad;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    int c = c0;
-    for (; c + 4 <= c1; c += 4) {
-      s0 += ld_cg_f32(src + c);
-      s1 += ld_cg_f32(src + c + 1);
-      s2 += ld_cg_f32(src + c + 2);
-      s3 += ld_cg_f32(src + c + 3);
+    const int c0 = half ? Gv / 2 : 0, c1 = half ? Gv : Gv / 2;
+    const float4* src = reinterpret_cast<const float4*>(p.partials + static_cast<int64_t>(e) * p.G_pad);
+    float s = 0.f;
+    for (int cb = c0; cb < c1; cb += kRedBatch) {
+      float4 v[kRedBatch];
+#pragma unroll
+      for (int i = 0; i < kRedBatch; ++i)
+        if (cb + i < c1) v[i] = __ldcg(src + cb + i);
+#pragma unroll
+      for (int i = 0; i < kRedBatch; ++i)
+        if (cb + i < c1) {
+          const int c = 4 * (cb + i);
+          s += v[i].x;
+          if (c + 1 < cx.G) s += v[i].y;
+          if (c + 2 < cx.G) s += v[i].z;
+          if (c + 3 < cx.G) s += v[i].w;
+        }
     }
-    for (; c < c1; ++c) s0 += ld_cg_f32(src + c);
-    const float s = (s0 + s1) + (s2 + s3);
     const float o = __shfl_xor_sync(0xffffffffu, s, 1);
     if (!half) logits[e] = s + o;
   }
@@ -564,7 +674,7 @@ __device__ void router_finish(const Ctx& cx, int li) {
     // r = 1 / sqrt(mean(x^2) + eps) from the partial sums of squares (row E)
     const float* src = p.partials + static_cast<int64_t>(p.E) * p.G_pad;
     float ss = 0.f;
-    for (int c = threadIdx.x; c < cx.G; c += 32) ss += ld_cg_f32(src + c);
+    for (int c = threadIdx.x; c < cx.G; c += 32) ss += __ldcg(src + c);
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (threadIdx.x == 0)
@@ -755,7 +865,7 @@ __device__ void consumer(const Ctx& cx) {
     if (needs_ids(p)) publish_ids_local(cx, li);
     // ---- gate/up (shared, then routed)
     VecView xv{};
-    if (lp.n_bs + lp.n_br) xv = prep_x(cx, x_l);
+    if (p.phases & (PH_BSHARED | PH_BROUTED | PH_C)) xv = prep_x(cx, x_l);
     for (; s < lp.n_r + lp.n_bs + lp.n_br; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
@@ -849,29 +959,36 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
   const int c_stage = p->rc_max * (p->K * p->rbI + p->rbS + p->E) + rsb;
   int slot = b_stage > c_stage ? b_stage : c_stage;
   slot = (slot + 127) / 128 * 128;
-  const int fixed = vb + 1024 /*contrib*/ + (p->E + 1) * 4 + 124 /*rpart*/ + 256 * 4 /*xnext*/ +
-                    p->E * 4 /*logits*/ + 512 /*misc*/ + (2 * kMaxSlots + 1) * 8 + 512;
+  // fixed regions after the slot ring
+  int fixed = 0;
+  auto take = [&](int bytes) {
+    const int o = fixed;
+    fixed += (bytes + 127) / 128 * 128;
+    return o;
+  };
+  const int o_vec = take(vb);
+  const int o_contrib = take(kConsumers * 4);
+  const int o_rpart = take((p->E + 1) * 4);
+  const int o_xnext = take(256 * 4);
+  const int o_xres = take(256 * 4);
+  const int o_logits = take(p->E * 4);
+  const int o_misc = take(M_COUNT * 4);
+  const int o_bars = take((2 * kMaxSlots + 1) * 8);
   int ns = (max_smem - fixed) / slot;
   if (ns > kMaxSlots) ns = kMaxSlots;
   if (ns < 2) return -1;
   p->slot_bytes = slot;
   p->nslots = ns;
-  int off = ns * slot;
-  p->off_vec = off;
-  off += vb;
-  p->off_contrib = off;
-  off += 1024;
-  p->off_rpart = off;
-  off += ((p->E + 1) * 4 + 127) / 128 * 128;
-  p->off_xnext = off;
-  off += 1024;
-  p->off_logits = off;
-  off += (p->E * 4 + 127) / 128 * 128;
-  p->off_misc = off;
-  off += 512;
-  p->off_bars = off;
-  off += (2 * kMaxSlots + 1) * 8;
-  p->smem_total = (off + 127) / 128 * 128;
+  const int base = ns * slot;
+  p->off_vec = base + o_vec;
+  p->off_contrib = base + o_contrib;
+  p->off_rpart = base + o_rpart;
+  p->off_xnext = base + o_xnext;
+  p->off_xres = base + o_xres;
+  p->off_logits = base + o_logits;
+  p->off_misc = base + o_misc;
+  p->off_bars = base + o_bars;
+  p->smem_total = base + fixed;
   return p->smem_total <= max_smem ? 0 : -1;
 }
 

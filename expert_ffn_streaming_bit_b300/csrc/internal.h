@@ -75,7 +75,8 @@ struct DecodeParams {
   int cpt_c, nsub_i, nsub_s, tasks_row, rc_max;
   // shared memory carve-up (bytes)
   int slot_bytes, nslots;
-  int off_vec, off_contrib, off_rpart, off_xnext, off_logits, off_misc, off_bars, smem_total;
+  int off_vec, off_contrib, off_rpart, off_xnext, off_xres, off_logits, off_misc, off_bars,
+      smem_total;
   uint64_t timeout_ns;     // bound on every device-side wait
 };
 
