@@ -91,6 +91,9 @@ _sig = {
     "moe_stack_ids": (_I, [_P, _I, _I, _P, _P]),
     "moe_cache_step": (_I, [_P, _I, _P, _I, _I, ctypes.POINTER(moe_cache_result)]),
     "moe_cache_reset": (_I, [_P]),
+    "moe_trace_enable": (_I, [_P, _I]),
+    "moe_trace_read": (_I, [_P, _P, _I]),
+    "moe_last_buckets": (_I, [_P, _P, _P, _P]),
     "moe_slot_plan_create": (_I, [_I, _I, ctypes.POINTER(ctypes.c_void_p)]),
     "moe_slot_plan_step": (_I, [_P, _P, _I, ctypes.POINTER(moe_cache_result)]),
     "moe_slot_plan_destroy": (None, [_P]),
@@ -261,6 +264,32 @@ def moe_cache_step(handle: Handle, layer: int, ids, flags: int = 0):
     k = ids.shape[0]
     return (np.array(r.hit[:k], np.int32), np.array(r.slot[:k], np.int32),
             np.array(r.evicted[:k], np.int32), r.misses)
+
+
+def moe_last_buckets(handle: Handle, T: int):
+    """(counts [E], offsets [E+1], perm [T*k]) of the last multi-token call."""
+    E, K = handle.cfg.n_experts, handle.cfg.top_k
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    perm = np.empty(T * K, np.int32)
+    _check(_lib.moe_last_buckets(handle.ptr, counts.ctypes.data, offsets.ctypes.data,
+                                 perm.ctypes.data), handle)
+    return counts, offsets, perm
+
+
+MOE_TRACE_EVENTS = 9
+
+
+def moe_trace_enable(handle: Handle, on: bool = True):
+    _check(_lib.moe_trace_enable(handle.ptr, 1 if on else 0), handle)
+
+
+def moe_trace_read(handle: Handle, n_layers: int) -> np.ndarray:
+    """int64 [num_sms][n_layers][MOE_TRACE_EVENTS] %globaltimer stamps (ns)."""
+    G = moe_get_info(handle)["num_sms"]
+    out = np.zeros((G, n_layers, MOE_TRACE_EVENTS), np.int64)
+    _check(_lib.moe_trace_read(handle.ptr, out.ctypes.data, n_layers), handle)
+    return out
 
 
 def moe_cache_reset(handle: Handle):

@@ -67,6 +67,37 @@ struct moe_handle {
   DecodeParams base{};
   int grid = 0;
   int last_T = 0, last_layers = 0;
+  bool last_prefill = false;
+  uint64_t* trace = nullptr;  // [grid][kTraceMaxLayers][kTraceEvents], inside scratch
+  bool trace_on = false;
+  // prefill (T >= 2, resident mode)
+  struct LayerMaps {
+    CUtensorMap gu_code[2], gu_sb[2], dn_code[2], dn_sb[2];  // [0] routed, [1] shared
+  };
+  std::vector<LayerMaps> maps;
+  bool prefill_ok = false;
+  int mt_gu_r = 0, mt_dn = 0, mt_gu_s = 0;
+  uint8_t* pf = nullptr;  // prefill scratch (one allocation)
+  int64_t pf_bytes = 0;
+  uint16_t* pf_x16 = nullptr;
+  float* pf_sigma = nullptr;
+  float* pf_rscale = nullptr;
+  float* pf_partials = nullptr;
+  int32_t* pf_ids = nullptr;     // [L][Tmax][K]
+  float* pf_wts = nullptr;       // [L][Tmax][K]
+  int32_t* pf_forced = nullptr;  // [Tmax][K]
+  int32_t* pf_counts = nullptr;
+  int32_t* pf_offsets = nullptr;
+  int32_t* pf_perm = nullptr;
+  int32_t* pf_inv = nullptr;
+  GemmUnit* pf_units_gu = nullptr;
+  GemmUnit* pf_units_dn = nullptr;
+  int32_t* pf_nunits = nullptr;
+  uint16_t* pf_hr = nullptr;
+  uint16_t* pf_hs = nullptr;
+  uint16_t* pf_e = nullptr;
+  float* pf_s = nullptr;
+  uint16_t* pf_xs[2] = {nullptr, nullptr};  // stack double buffer
   Inject inj;
   int timeout_ms = 10000;
   std::string err;
@@ -112,6 +143,7 @@ void free_all(moe_handle* h) {
   cudaFree(h->dev_weights);
   cudaFree(h->dev_layers);
   cudaFree(h->scratch);
+  cudaFree(h->pf);
   cudaFreeHost(h->pool);
   cudaFreeHost(h->pin_x);
   cudaFreeHost(h->pin_y);
@@ -156,7 +188,7 @@ moe_status check_device_status(moe_handle* h, cudaStream_t s) {
   if (st != MOE_OK) return st;
   const uint32_t v = *h->pin_status;
   if (v == DEV_OK) return MOE_OK;
-  cudaMemsetAsync(h->bar, 0, 12, s);
+  cudaMemsetAsync(h->bar, 0, kBarWords * 4, s);
   cudaStreamSynchronize(s);
   if (v == DEV_TIMEOUT) return fail(h, MOE_ERR_TIMEOUT, "a device-side wait timed out");
   return fail(h, MOE_ERR_DEVICE, "a kernel reported an out-of-range expert id");
@@ -174,6 +206,42 @@ moe_status launch(moe_handle* h, const DecodeParams& p, cudaStream_t s) {
   return MOE_OK;
 }
 
+// cuTensorMapEncodeTiled, fetched from the driver at run time (the library
+// does not link against libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// A byte tensor of `rank` 2 or 3: rows of `row_bytes` (pitch `row_bytes`),
+// `rows` rows, and for rank 3 `planes` planes `plane_bytes` apart.
+bool make_qrow_map(CUtensorMap* m, const void* base, int rank, uint64_t row_bytes, uint64_t rows,
+                   uint64_t planes, uint64_t plane_bytes, uint32_t box_x, bool swizzle) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {row_bytes, rows, planes};
+  const cuuint64_t strides[2] = {row_bytes, plane_bytes};
+  const cuuint32_t box[3] = {box_x, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 DecodeParams params_for(moe_handle* h, int layer0, int n_layers, const void* x, void* y, int phases,
                         int flags) {
   DecodeParams p = h->base;
@@ -184,6 +252,7 @@ DecodeParams params_for(moe_handle* h, int layer0, int n_layers, const void* x, 
   p.prenorm = (flags & MOE_FWD_PRENORM) ? 1 : 0;
   p.x_in = static_cast<const uint16_t*>(x);
   p.y_out = static_cast<uint16_t*>(y);
+  p.trace = h->trace_on ? h->trace : nullptr;
   return p;
 }
 
@@ -329,8 +398,8 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   auto al = [](int64_t b) { return (b + 255) / 256 * 256; };
   const int64_t sz_xbuf = al(2 * T * d.D * 2), sz_h = al(T * (d.K * d.I + d.S) * 4),
                 sz_part = al((d.E + 1) * G_pad * 4), sz_ids = al(int64_t(L) * T * d.K * 4), sz_bar = 256,
-                sz_io = al(T * d.D * 2);
-  h->scratch_bytes = sz_xbuf + sz_h + sz_part + 2 * sz_ids + sz_bar + 2 * sz_io;
+                sz_io = al(T * d.D * 2), sz_trace = al(int64_t(G) * kTraceMaxLayers * kTraceEvents * 8);
+  h->scratch_bytes = sz_xbuf + sz_h + sz_part + 2 * sz_ids + sz_bar + 2 * sz_io + sz_trace;
   CREATE_TRY(cudaMalloc(&h->scratch, h->scratch_bytes));
   CREATE_TRY(cudaMemset(h->scratch, 0, h->scratch_bytes));
   uint8_t* sp = h->scratch;
@@ -349,6 +418,8 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   h->io_x = reinterpret_cast<uint16_t*>(sp);
   sp += sz_io;
   h->io_y = reinterpret_cast<uint16_t*>(sp);
+  sp += sz_io;
+  h->trace = reinterpret_cast<uint64_t*>(sp);
   CREATE_TRY(cudaHostAlloc(&h->pin_x, T * d.D * 2, cudaHostAllocDefault));
   CREATE_TRY(cudaHostAlloc(&h->pin_y, T * d.D * 2, cudaHostAllocDefault));
   CREATE_TRY(cudaHostAlloc(&h->pin_ids, T * d.K * 4 + 64, cudaHostAllocDefault));
@@ -409,6 +480,74 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   const int64_t r_stage = int64_t((d.D + G - 1) / G) * d.E + 2 * d.E * 4;
   if (r_stage > p.slot_bytes) CREATE_FAIL(MOE_ERR_INVALID_ARG, "router stage too large for the SM count");
   h->grid = G < d.D ? G : static_cast<int>(d.D);  // every CTA owns at least one output row
+  // ---- prefill (T >= 2): tensor maps over the resident weights and scratch
+  if (!streaming && c.max_tokens >= 2 && d.E <= kMaxPrefillExperts) {
+    h->mt_gu_r = static_cast<int>(2 * d.I / 128);
+    h->mt_dn = static_cast<int>(d.D / 128);
+    h->mt_gu_s = static_cast<int>(2 * d.S / 128);
+    h->maps.resize(L);
+    const int64_t rbD = qrow_bytes(d.D), rbI = qrow_bytes(d.I), rbS = qrow_bytes(d.S);
+    bool ok = (2 * d.I) % 128 == 0 && d.D % 128 == 0 && (2 * d.S) % 128 == 0;
+    for (int l = 0; l < L && ok; ++l) {
+      const LayerDev& ld = h->layers[l];
+      auto& mp = h->maps[l];
+      const uint8_t* dn = ld.experts + d.I * 2 * rbD;
+      ok = ok && make_qrow_map(&mp.gu_code[0], ld.experts, 3, rbD, 2 * d.I, d.E, h->blob, 128, true);
+      ok = ok && make_qrow_map(&mp.gu_sb[0], ld.experts, 3, rbD, 2 * d.I, d.E, h->blob, 16, false);
+      ok = ok && make_qrow_map(&mp.dn_code[0], dn, 3, rbI, d.D, d.E, h->blob, 128, true);
+      ok = ok && make_qrow_map(&mp.dn_sb[0], dn, 3, rbI, d.D, d.E, h->blob, 16, false);
+      ok = ok && make_qrow_map(&mp.gu_code[1], ld.shared_gu, 2, rbD, 2 * d.S, 1, 0, 128, true);
+      ok = ok && make_qrow_map(&mp.gu_sb[1], ld.shared_gu, 2, rbD, 2 * d.S, 1, 0, 16, false);
+      ok = ok && make_qrow_map(&mp.dn_code[1], ld.shared_dn, 2, rbS, d.D, 1, 0, 128, true);
+      ok = ok && make_qrow_map(&mp.dn_sb[1], ld.shared_dn, 2, rbS, d.D, 1, 0, 16, false);
+    }
+    if (!ok) CREATE_FAIL(MOE_ERR_CUDA, "could not encode the prefill tensor maps");
+    const int64_t Tm = c.max_tokens, K = d.K, E = d.E;
+    int64_t part = 0;
+    for (int64_t t = 2; t <= Tm; ++t) {
+      const int64_t v = int64_t(router_gemm_splits(int(t), int(E), int(d.D), G)) * t * E;
+      if (v > part) part = v;
+    }
+    const int64_t nt = Tm * K / kUnitTokens + E + 1, stl = (Tm + kUnitTokens - 1) / kUnitTokens;
+    const int64_t ngu = nt * h->mt_gu_r + stl * h->mt_gu_s, ndn = (nt + stl) * h->mt_dn;
+    int64_t sizes[] = {Tm * d.D * 2,      Tm * 4,          Tm * 4,        part * 4,
+                       L * Tm * K * 4,    L * Tm * K * 4,  Tm * K * 4,    E * 4,
+                       (E + 1) * 4,       Tm * K * 4,      Tm * K * 4,    ngu * int64_t(sizeof(GemmUnit)),
+                       ndn * int64_t(sizeof(GemmUnit)), 16, Tm * K * d.I * 2, Tm * d.S * 2,
+                       Tm * K * d.D * 2,  Tm * d.D * 4,    Tm * d.D * 2,  Tm * d.D * 2};
+    const int ns = sizeof(sizes) / sizeof(sizes[0]);
+    int64_t offs[32];
+    int64_t tot = 0;
+    for (int i = 0; i < ns; ++i) {
+      offs[i] = tot;
+      tot += al(sizes[i]);
+    }
+    CREATE_TRY(cudaMalloc(&h->pf, tot));
+    CREATE_TRY(cudaMemset(h->pf, 0, tot));
+    h->pf_bytes = tot;
+    int i = 0;
+    h->pf_x16 = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    h->pf_sigma = reinterpret_cast<float*>(h->pf + offs[i++]);
+    h->pf_rscale = reinterpret_cast<float*>(h->pf + offs[i++]);
+    h->pf_partials = reinterpret_cast<float*>(h->pf + offs[i++]);
+    h->pf_ids = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
+    h->pf_wts = reinterpret_cast<float*>(h->pf + offs[i++]);
+    h->pf_forced = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
+    h->pf_counts = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
+    h->pf_offsets = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
+    h->pf_perm = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
+    h->pf_inv = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
+    h->pf_units_gu = reinterpret_cast<GemmUnit*>(h->pf + offs[i++]);
+    h->pf_units_dn = reinterpret_cast<GemmUnit*>(h->pf + offs[i++]);
+    h->pf_nunits = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
+    h->pf_hr = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    h->pf_hs = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    h->pf_e = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    h->pf_s = reinterpret_cast<float*>(h->pf + offs[i++]);
+    h->pf_xs[0] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    h->pf_xs[1] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    h->prefill_ok = true;
+  }
   *out = h.release();
   return MOE_OK;
 #undef CREATE_TRY
@@ -425,7 +564,7 @@ moe_status moe_get_info(const moe_handle* h, moe_info* out) {
   if (!h || !out) return MOE_ERR_INVALID_ARG;
   out->device_weight_bytes = h->dev_weight_bytes;
   out->pinned_pool_bytes = h->pool_bytes;
-  out->device_scratch_bytes = h->scratch_bytes;
+  out->device_scratch_bytes = h->scratch_bytes + h->pf_bytes;
   out->expert_blob_bytes = h->blob;
   out->num_sms = h->grid;
   return MOE_OK;
@@ -517,6 +656,33 @@ moe_status moe_cache_step(moe_handle* h, int layer, const int32_t* ids, int k, i
   return result;
 }
 
+moe_status moe_last_buckets(moe_handle* h, int32_t* counts, int32_t* offsets, int32_t* perm) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (!h->last_prefill || h->last_T < 2)
+    return fail(h, MOE_ERR_STATE, "moe_last_buckets: the last call was not a multi-token call");
+  moe_status st = check_device_status(h, nullptr);
+  if (st != MOE_OK) return st;
+  const int64_t E = h->d.E, n = int64_t(h->last_T) * h->d.K;
+  if (counts) CUDA_TRY(h, cudaMemcpy(counts, h->pf_counts, E * 4, cudaMemcpyDeviceToHost));
+  if (offsets) CUDA_TRY(h, cudaMemcpy(offsets, h->pf_offsets, (E + 1) * 4, cudaMemcpyDeviceToHost));
+  if (perm) CUDA_TRY(h, cudaMemcpy(perm, h->pf_perm, n * 4, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+moe_status moe_trace_enable(moe_handle* h, int on) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  h->trace_on = on != 0;
+  return MOE_OK;
+}
+
+moe_status moe_trace_read(moe_handle* h, int64_t* out, int n_layers) {
+  if (!h || !out || n_layers < 1 || n_layers > kTraceMaxLayers) return MOE_ERR_INVALID_ARG;
+  CUDA_TRY(h, cudaDeviceSynchronize());
+  CUDA_TRY(h, cudaMemcpy(out, h->trace, size_t(h->grid) * n_layers * kTraceEvents * 8,
+                         cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
 moe_status moe_cache_reset(moe_handle* h) {
   if (!h) return MOE_ERR_INVALID_ARG;
   if (h->cfg.n_slots == 0) return fail(h, MOE_ERR_STATE, "moe_cache_reset needs streaming mode");
@@ -525,6 +691,118 @@ moe_status moe_cache_reset(moe_handle* h) {
 }
 
 }  // extern "C"
+
+// One layer for T >= 2 tokens, resident mode: route, bucket, grouped GEMMs on
+// the tensor cores, combine.  Everything is enqueued on s; ids and weights of
+// the layer land in pf_ids / pf_wts block `slot` ([T][K]).
+static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, void* y, int flags,
+                                const int32_t* forced, cudaStream_t s, int slot) {
+  const Dims& d = h->d;
+  const int K = static_cast<int>(d.K);
+  const int64_t Tm = h->cfg.max_tokens;
+  int32_t* ids = h->pf_ids + int64_t(slot) * Tm * K;
+  float* wts = h->pf_wts + int64_t(slot) * Tm * K;
+  if (forced)
+    CUDA_TRY(h, cudaMemcpyAsync(h->pf_forced, forced, sizeof(int32_t) * T * K,
+                                cudaMemcpyHostToDevice, s));
+  const LayerDev& ld = h->layers[layer];
+  RouteArgs ra{};
+  ra.x = static_cast<const uint16_t*>(x);
+  ra.T = T;
+  ra.D = static_cast<int>(d.D);
+  ra.E = static_cast<int>(d.E);
+  ra.K = K;
+  ra.prenorm = (flags & MOE_FWD_PRENORM) ? 1 : 0;
+  ra.rms_eps = h->base.rms_eps;
+  ra.router_t = ld.router_t;
+  ra.router_sb = ld.router_sb;
+  ra.logit_bias = ld.logit_bias;
+  ra.forced = forced ? h->pf_forced : nullptr;
+  ra.x16 = h->pf_x16;
+  ra.sigma = h->pf_sigma;
+  ra.rscale = h->pf_rscale;
+  ra.partials = h->pf_partials;
+  ra.nsplit = router_gemm_splits(T, ra.E, ra.D, h->num_sms);
+  ra.ids = ids;
+  ra.wts = wts;
+  int e = prefill_route(ra, s);
+  if (e) return fail(h, MOE_ERR_CUDA, "prefill router: %s", cudaGetErrorString(cudaError_t(e)));
+  BucketArgs ba{};
+  ba.ids = ids;
+  ba.T = T;
+  ba.K = K;
+  ba.E = ra.E;
+  ba.mt_gu_r = h->mt_gu_r;
+  ba.mt_dn = h->mt_dn;
+  ba.mt_gu_s = h->mt_gu_s;
+  ba.counts = h->pf_counts;
+  ba.offsets = h->pf_offsets;
+  ba.perm = h->pf_perm;
+  ba.inv = h->pf_inv;
+  ba.units_gu = h->pf_units_gu;
+  ba.units_dn = h->pf_units_dn;
+  ba.n_units = h->pf_nunits;
+  ba.status = h->bar + 2;
+  e = prefill_bucket(ba, s);
+  if (e) return fail(h, MOE_ERR_CUDA, "prefill bucketing: %s", cudaGetErrorString(cudaError_t(e)));
+  const auto& mp = h->maps[layer];
+  GemmParams gp{};
+  gp.perm = h->pf_perm;
+  gp.topk = K;
+  gp.sigma = h->pf_sigma;
+  gp.wts = wts;
+  gp.D = static_cast<int>(d.D);
+  gp.status = h->bar + 2;
+  gp.timeout_ns = h->base.timeout_ns;
+  // gate/up (+ GELU): routed rows in bucket order, shared rows by token
+  gp.tm_code[0] = mp.gu_code[0];
+  gp.tm_code[1] = mp.gu_code[1];
+  gp.tm_sb[0] = mp.gu_sb[0];
+  gp.tm_sb[1] = mp.gu_sb[1];
+  gp.units = h->pf_units_gu;
+  gp.n_units = h->pf_nunits;
+  gp.mode = 0;
+  gp.K[0] = gp.K[1] = static_cast<int>(d.D);
+  gp.bsrc[0] = gp.bsrc[1] = h->pf_x16;
+  gp.bld[0] = gp.bld[1] = static_cast<int>(d.D);
+  gp.hout[0] = h->pf_hr;
+  gp.hout[1] = h->pf_hs;
+  gp.hld[0] = static_cast<int>(d.I);
+  gp.hld[1] = static_cast<int>(d.S);
+  e = gemm_tc_launch(gp, h->num_sms, s);
+  if (e) return fail(h, MOE_ERR_CUDA, "gate/up GEMM launch: %s", cudaGetErrorString(cudaError_t(e)));
+  // down: routed output weighted by the routing weight (bf16), shared (fp32)
+  gp.tm_code[0] = mp.dn_code[0];
+  gp.tm_code[1] = mp.dn_code[1];
+  gp.tm_sb[0] = mp.dn_sb[0];
+  gp.tm_sb[1] = mp.dn_sb[1];
+  gp.units = h->pf_units_dn;
+  gp.n_units = h->pf_nunits + 1;
+  gp.mode = 1;
+  gp.K[0] = static_cast<int>(d.I);
+  gp.K[1] = static_cast<int>(d.S);
+  gp.bsrc[0] = h->pf_hr;
+  gp.bsrc[1] = h->pf_hs;
+  gp.bld[0] = static_cast<int>(d.I);
+  gp.bld[1] = static_cast<int>(d.S);
+  gp.eout = h->pf_e;
+  gp.sout = h->pf_s;
+  e = gemm_tc_launch(gp, h->num_sms, s);
+  if (e) return fail(h, MOE_ERR_CUDA, "down GEMM launch: %s", cudaGetErrorString(cudaError_t(e)));
+  CombineArgs ca{};
+  ca.x = static_cast<const uint16_t*>(x);
+  ca.e = h->pf_e;
+  ca.s = h->pf_s;
+  ca.inv = h->pf_inv;
+  ca.y = static_cast<uint16_t*>(y);
+  ca.T = T;
+  ca.D = static_cast<int>(d.D);
+  ca.K = K;
+  ca.residual = (flags & MOE_FWD_RESIDUAL) ? 1 : 0;
+  e = prefill_combine(ca, s);
+  if (e) return fail(h, MOE_ERR_CUDA, "combine: %s", cudaGetErrorString(cudaError_t(e)));
+  return MOE_OK;
+}
 
 static moe_status decode_layer_streaming(moe_handle* h, int layer, const void* x, void* y,
                                          int flags, const int32_t* forced, cudaStream_t s,
@@ -601,6 +879,21 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
     if (T != 1) return fail(h, MOE_ERR_STATE, "streaming mode runs one token per call");
     moe_status st = decode_layer_streaming(h, layer, x, y, flags, forced_ids, s, stats);
     if (st != MOE_OK) return st;
+  } else if (T >= 2 && h->prefill_ok) {
+    moe_status st = prefill_layer(h, layer, x, T, y, flags, forced_ids, s, 0);
+    if (st != MOE_OK) return st;
+    h->last_T = T;
+    h->last_layers = 1;
+    h->last_prefill = true;
+    if (stats && (stats->ids || stats->weights)) {
+      st = check_device_status(h, s);
+      if (st != MOE_OK) return st;
+      if (stats->ids)
+        CUDA_TRY(h, cudaMemcpy(stats->ids, h->pf_ids, sizeof(int32_t) * T * K, cudaMemcpyDeviceToHost));
+      if (stats->weights)
+        CUDA_TRY(h, cudaMemcpy(stats->weights, h->pf_wts, sizeof(float) * T * K, cudaMemcpyDeviceToHost));
+    }
+    return MOE_OK;
   } else {
     // resident: one persistent launch per token
     for (int t = 0; t < T; ++t) {
@@ -618,6 +911,7 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
   }
   h->last_T = T;
   h->last_layers = 1;
+  h->last_prefill = false;
   if (stats && (stats->ids || stats->weights)) {
     moe_status st = check_device_status(h, s);
     if (st != MOE_OK) return st;
@@ -638,6 +932,20 @@ moe_status moe_forward_stack(moe_handle* h, const void* x, int T, void* y, int n
   if (T < 1 || T > h->cfg.max_tokens) return fail(h, MOE_ERR_INVALID_ARG, "T=%d out of range", T);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = h->cfg.d_model, K = h->cfg.top_k;
+  if (T >= 2 && h->prefill_ok) {
+    // layer by layer over all T tokens through the tensor-core path
+    for (int l = 0; l < n_layers; ++l) {
+      const void* xin = l == 0 ? x : h->pf_xs[(l - 1) & 1];
+      void* yout = l + 1 == n_layers ? y : h->pf_xs[l & 1];
+      moe_status st = prefill_layer(h, l, xin, T, yout, MOE_FWD_RESIDUAL | MOE_FWD_PRENORM, nullptr,
+                                    s, l);
+      if (st != MOE_OK) return st;
+    }
+    h->last_T = T;
+    h->last_layers = n_layers;
+    h->last_prefill = true;
+    return MOE_OK;
+  }
   for (int t = 0; t < T; ++t) {
     DecodeParams p = params_for(h, 0, n_layers, static_cast<const uint16_t*>(x) + int64_t(t) * D,
                                 static_cast<uint16_t*>(y) + int64_t(t) * D, PH_ALL,
@@ -650,6 +958,7 @@ moe_status moe_forward_stack(moe_handle* h, const void* x, int T, void* y, int n
   }
   h->last_T = T;
   h->last_layers = n_layers;
+  h->last_prefill = false;
   return MOE_OK;
 }
 
@@ -679,6 +988,19 @@ moe_status moe_stack_ids(moe_handle* h, int n_layers, int T, int32_t* ids, float
   if (st != MOE_OK) return st;
   const int K = h->cfg.top_k;
   const size_t n = size_t(n_layers) * T * K;
+  if (h->last_prefill) {
+    // layer l's block starts at l * max_tokens * K
+    const size_t blk = size_t(h->cfg.max_tokens) * K;
+    for (int l = 0; l < n_layers; ++l) {
+      if (ids)
+        CUDA_TRY(h, cudaMemcpy(ids + size_t(l) * T * K, h->pf_ids + l * blk, size_t(T) * K * 4,
+                               cudaMemcpyDeviceToHost));
+      if (weights)
+        CUDA_TRY(h, cudaMemcpy(weights + size_t(l) * T * K, h->pf_wts + l * blk, size_t(T) * K * 4,
+                               cudaMemcpyDeviceToHost));
+    }
+    return MOE_OK;
+  }
   std::vector<int32_t> ti(n);
   std::vector<float> tw(n);
   CUDA_TRY(h, cudaMemcpy(ti.data(), h->ids, n * 4, cudaMemcpyDeviceToHost));

@@ -11,28 +11,31 @@
 //   C   its share of output rows: for each row the k routed down rows, the
 //       shared down row and, when a next layer follows, the next router's
 //       column block                                          (needs ids(l))
-// and the data dependences are met with two grid barriers:
-//   after BS+BR: h = gelu(W_gate x) * (W_up x) complete for all k+1 branches;
-//   after C: x_{l+1} and the next router's partial logits complete; the last
-//   CTA to arrive reduces the partials (fixed order), takes the top k and the
-//   renormalised softmax, and publishes ids(l+1) before releasing the others.
+// and the data dependences are met with two grid barriers per layer:
+//   after BS+BR: h = gelu(W_gate u) * (W_up u) complete for all k+1 branches;
+//   after C: x_{l+1} and the next router's partial logits complete.  The
+//   barrier releases at once; the last CTA to arrive then reduces the partial
+//   logits (fixed order), takes the top k and the renormalised softmax, and
+//   publishes ids(l+1) under a flag.  Meanwhile every CTA converts x_{l+1} and
+//   computes its share of the shared expert (BS), which needs no ids.
 // The producer runs ahead across barriers wherever the weights are already
-// known, so HBM keeps streaming while the grid synchronises.  Every wait is
+// known, and prefetches into L2 the routed rows it will stream once the ids
+// arrive, so HBM keeps working while the grid synchronises.  Every wait is
 // bounded in time; a wait that runs out sets the status word and the CTA
 // drains its in-flight copies and exits.
 //
 // Arithmetic (shilu.ai "drumih/turbo-fieldfare", overview table row 权重 and
 // section 推理引擎的工作原理; sh.edu-sjtu.cn article, section 三件事):
-//   router: logit_e = sum_c (s q + b) x_c in fp32, + bias_e; top-k by
-//           (logit desc, index asc); w = softmax over the chosen logits;
-//   expert: h_j = gelu_tanh(g_j) u_j with g = W_gate x, u = W_up x;
-//           e = W_down h; y = sum_i w_i e_i + shared(x); optional residual.
-// Dot products: activations are held as fp16 (exact for bf16 inputs in range;
-// a power-of-two prescale keeps |v| < 2^15), codes become fp16 1024+q or
-// 1024+16q by one and-or, products accumulate in fp32 with mixed-precision
-// fma, and per 32-column chunk sum(q v) = a + b/16 - (1024 Sa + 64 Sb) is
-// recovered with the chunk's precomputed activation sums; then
-// s * sum(q v) + bias * sum(v) per group half.
+//   router: logit_e = r * sum_c (s q + b) x_c in fp32, + bias_e (r = the
+//           pre-norm scale or 1); top-k by (logit desc, index asc); w = softmax
+//           over the chosen logits;
+//   expert: h_j = gelu_tanh(g_j) u_j with g = W_gate u, u = W_up u;
+//           e = W_down h; y = sum_i w_i e_i + shared(u); optional residual.
+// Expert dot products are integer-exact: the activation vector (x, or one
+// branch of h) is held as int16 X = rint(v / sigma), sigma = max|v| / 32767,
+// the 4-bit codes as bytes, and a 2-way integer dot product accumulates
+// sum q X exactly in int32 per 32-column chunk; the chunk contributes
+// s * sum(q X) + bias * sum(X), and the row total is multiplied by sigma.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -104,28 +107,28 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 
 __device__ __forceinline__ void csync() { named_sync(1, kConsumers); }
 
-// Contribution of 32-column chunk c of a qrow with K/2 = halfK code bytes,
-// against an fp16 vector in chunk layout: s * sum(q v) + bias * sum(v).
+// Contribution of 32-column chunk c of a qrow with K/2 = halfK code bytes
+// against an int16 activation vector in chunk layout (kChunkStride bytes per
+// chunk, chunk sums in xsum): s * sum(q X) + bias * sum(X).
 __device__ __forceinline__ float chunk_dot(const uint8_t* row, int halfK, int c, const uint8_t* vec,
-                                           const float* coff, const float* vsum) {
+                                           const float* xsum) {
   const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
   const uint32_t sb = *reinterpret_cast<const uint32_t*>(row + halfK + (c >> 1) * 4);
   const uint4* v = reinterpret_cast<const uint4*>(vec + c * kChunkStride);
-  float a = 0.f, b = 0.f;
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+  int acc = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint4 vq = v[j];
-    const uint32_t wj = words[j];
-    const uint32_t w8 = wj >> 8;
-    a = fma2_f16_f32(and_or(wj, 0x000F000Fu, 0x64006400u), vq.x, a);
-    b = fma2_f16_f32(and_or(wj, 0x00F000F0u, 0x64006400u), vq.y, b);
-    a = fma2_f16_f32(and_or(w8, 0x000F000Fu, 0x64006400u), vq.z, a);
-    b = fma2_f16_f32(and_or(w8, 0x00F000F0u, 0x64006400u), vq.w, b);
+    const uint4 xq = v[j];  // int16 pairs of columns 8j+{0,1}, {2,3}, {4,5}, {6,7}
+    const uint32_t lo = words[j] & 0x0F0F0F0Fu;          // codes of columns 8j+0..3
+    const uint32_t hi = (words[j] >> 4) & 0x0F0F0F0Fu;   // codes of columns 8j+4..7
+    acc = dp2a_lo(xq.x, lo, acc);
+    acc = dp2a_hi(xq.y, lo, acc);
+    acc = dp2a_lo(xq.z, hi, acc);
+    acc = dp2a_hi(xq.w, hi, acc);
   }
-  const float qv = fmaf(b, 0.0625f, a) - coff[c];
   const __half2 sbh = *reinterpret_cast<const __half2*>(&sb);
-  return fmaf(__low2float(sbh), qv, __high2float(sbh) * vsum[c]);
+  return fmaf(__low2float(sbh), static_cast<float>(acc), __high2float(sbh) * xsum[c]);
 }
 
 // ------------------------------------------------------------ stage lists
@@ -377,47 +380,46 @@ __device__ float consumer_sum(const Ctx& cx, float v) {
   return s;
 }
 
-// Power-of-two factor f with max|v| * f < 2^15 (1 if already in range).
-__device__ __forceinline__ float prescale_for(float m) {
-  float f = 1.f;
-  while (m * f >= 32768.f) f *= 0.5f;
-  return f;
+// int16 quantisation factor for a vector with max |v| = m: X = rint(v * q).
+__device__ __forceinline__ float quant_factor(float m) { return m > 0.f ? 32767.f / m : 0.f; }
+
+__device__ __forceinline__ uint32_t pack_s16x2(float a, float b) {
+  const int ia = __float2int_rn(a), ib = __float2int_rn(b);
+  return (static_cast<uint32_t>(ia) & 0xffffu) | (static_cast<uint32_t>(ib) << 16);
 }
 
-// Per-chunk activation sums for chunks [c0, c1) of the vec region.
-__device__ void chunk_sums(uint8_t* vec, float* coff, float* vsum, int c0, int c1) {
-  for (int c = c0 + static_cast<int>(threadIdx.x); c < c1; c += kConsumers) {
-    const __half* hv = reinterpret_cast<const __half*>(vec + c * kChunkStride);
-    float sa = 0.f, sb = 0.f;
-    for (int e = 0; e < 32; ++e) {
-      const float v = __half2float(hv[e]);
-      if ((e & 2) == 0)
-        sa += v;  // columns 0,1,4,5 (mod 8)
-      else
-        sb += v;  // columns 2,3,6,7 (mod 8)
+// Per-chunk sums of the int16 values of chunks [0, nc) (exact in fp32).
+__device__ void chunk_sums(uint8_t* vec, float* xsum, int nc) {
+  for (int c = threadIdx.x; c < nc; c += kConsumers) {
+    const uint4* v = reinterpret_cast<const uint4*>(vec + c * kChunkStride);
+    int s = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q = v[j];
+      s = dp2a_lo(q.x, 0x01010101u, s);
+      s = dp2a_lo(q.y, 0x01010101u, s);
+      s = dp2a_lo(q.z, 0x01010101u, s);
+      s = dp2a_lo(q.w, 0x01010101u, s);
     }
-    coff[c] = 1024.f * sa + 64.f * sb;
-    vsum[c] = sa + sb;
+    xsum[c] = static_cast<float>(s);
   }
 }
 
 struct VecView {
-  uint8_t* vec;
-  float* coff;
-  float* vsum;
-  float* vscale;  // multiply a dot product by vscale[seg] to undo the prescale
+  uint8_t* vec;   // int16 chunks, kChunkStride bytes each
+  float* xsum;    // per-chunk sums
+  float* vscale;  // dot products are multiplied by vscale[segment]
 };
 
 __device__ VecView vec_view(const Ctx& cx, int nchunks) {
   VecView v;
   v.vec = cx.smem + cx.p->off_vec;
-  v.coff = reinterpret_cast<float*>(v.vec + nchunks * kChunkStride);
-  v.vsum = v.coff + nchunks;
-  v.vscale = v.vsum + nchunks;
+  v.xsum = reinterpret_cast<float*>(v.vec + nchunks * kChunkStride);
+  v.vscale = v.xsum + nchunks;
   return v;
 }
 
-// Layer input x (bf16 [D], global) -> fp16 chunks.  One batch of 16-byte
+// Layer input x (bf16 [D], global) -> int16 chunks.  One batch of 16-byte
 // loads per thread (D <= 8 * kConsumers * kMaxXV); the CTA's own output rows
 // [c_lo, c_hi) are also kept as fp32 in xres for the residual.
 constexpr int kMaxXV = 4;
@@ -442,16 +444,17 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
       const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(w[j] & 0xffffu)), fabsf(bf16_bits_to_f32(w[j] >> 16))));
+        const float a = bf16_bits_to_f32(w[j] & 0xffffu), b = bf16_bits_to_f32(w[j] >> 16);
+        m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
         const int col = idx * 8 + 2 * j;
-        if (col >= cx.part.c_lo && col < cx.part.c_hi) xres[col - cx.part.c_lo] = bf16_bits_to_f32(w[j] & 0xffffu);
-        if (col + 1 >= cx.part.c_lo && col + 1 < cx.part.c_hi)
-          xres[col + 1 - cx.part.c_lo] = bf16_bits_to_f32(w[j] >> 16);
+        if (col >= cx.part.c_lo && col < cx.part.c_hi) xres[col - cx.part.c_lo] = a;
+        if (col + 1 >= cx.part.c_lo && col + 1 < cx.part.c_hi) xres[col + 1 - cx.part.c_lo] = b;
       }
     }
   }
-  const float f = prescale_for(consumer_max(cx, m));
-  float ss = 0.f;  // sum of (f x)^2, for the pre-norm
+  const float m_all = consumer_max(cx, m);
+  const float q = quant_factor(m_all);
+  float ss = 0.f;  // sum of (q x)^2, for the pre-norm
 #pragma unroll
   for (int i = 0; i < kMaxXV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
@@ -460,10 +463,9 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
       uint32_t hv[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float a = bf16_bits_to_f32(w[j] & 0xffffu) * f, b = bf16_bits_to_f32(w[j] >> 16) * f;
+        const float a = bf16_bits_to_f32(w[j] & 0xffffu) * q, b = bf16_bits_to_f32(w[j] >> 16) * q;
         ss = fmaf(a, a, fmaf(b, b, ss));
-        const __half2 h2 = __floats2half2_rn(a, b);
-        hv[j] = *reinterpret_cast<const uint32_t*>(&h2);
+        hv[j] = pack_s16x2(a, b);
       }
       const int col = idx * 8;
       *reinterpret_cast<uint4*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) =
@@ -471,20 +473,21 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
     }
   }
   if (p.prenorm) {
-    // dot products of the prescaled x are multiplied by r / f, where
-    // r = 1 / sqrt(mean(x^2) + eps) = f / sqrt(mean((f x)^2) + eps f^2)
+    // sum q X ~ q * (W x); the layer wants r * (W x) with
+    // r = 1 / sqrt(mean(x^2) + eps), so the factor is r / q = 1 / sqrt(mean((q x)^2) + eps q^2)
     ss = consumer_sum(cx, ss);
-    if (threadIdx.x == 0) v.vscale[0] = rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps * f * f);
+    if (threadIdx.x == 0)
+      v.vscale[0] = q > 0.f ? rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps * q * q) : 0.f;
   } else if (threadIdx.x == 0) {
-    v.vscale[0] = 1.f / f;
+    v.vscale[0] = m_all / 32767.f;
   }
   csync();
-  chunk_sums(v.vec, v.coff, v.vsum, 0, nc);
+  chunk_sums(v.vec, v.xsum, nc);
   csync();
   return v;
 }
 
-// h (fp32 [K*I + S], global) -> fp16 chunks, one power-of-two prescale per
+// h (fp32 [K*I + S], global) -> int16 chunks, one quantisation scale per
 // branch.  One batch of 16-byte loads per thread (K*I + S <= 4 * kConsumers *
 // kMaxHV); the per-branch max is an order-independent smem atomicMax on the
 // bit patterns of non-negative floats.
@@ -521,44 +524,47 @@ __device__ VecView prep_h(const Ctx& cx) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
     if (idx < n4) {
       const int seg = idx * 4 < KI ? idx * 4 / p.I : p.K;
-      const float f = prescale_for(__int_as_float(segmax[seg]));
-      const __half2 a = __floats2half2_rn(r[i].x * f, r[i].y * f);
-      const __half2 b = __floats2half2_rn(r[i].z * f, r[i].w * f);
+      const float q = quant_factor(__int_as_float(segmax[seg]));
       const int col = idx * 4;
       *reinterpret_cast<uint2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) =
-          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+          make_uint2(pack_s16x2(r[i].x * q, r[i].y * q), pack_s16x2(r[i].z * q, r[i].w * q));
     }
   }
   if (threadIdx.x <= static_cast<unsigned>(p.K))
-    v.vscale[threadIdx.x] = 1.f / prescale_for(__int_as_float(segmax[threadIdx.x]));
+    v.vscale[threadIdx.x] = __int_as_float(segmax[threadIdx.x]) / 32767.f;
   csync();
-  chunk_sums(v.vec, v.coff, v.vsum, 0, nc);
+  chunk_sums(v.vec, v.xsum, nc);
   csync();
   return v;
 }
 
-// B stage: n gate/up row pairs -> h_out[pair].
+// B stage: n gate/up row pairs -> h_out[pair].  Each half-warp owns one pair
+// and each of its lanes both rows of a strided set of chunks, so an
+// activation chunk is read once for the two rows.
 __device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const VecView& xv,
                           float* h_out) {
   const DecodeParams& p = *cx.p;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = warp * 2 + (lane >> 4);
-  const int row = (lane >> 3) & 1;
-  const int sub = lane & 7;
-  const int cpt = p.D / 256;
-  float acc = 0.f;
+  const int sub = lane & 15;
+  const int nc = p.D / 32;
+  float g = 0.f, u = 0.f;
   if (pair < n) {
-    const uint8_t* rp = buf + (pair * 2 + row) * p.rbD;
-    for (int i = 0; i < cpt; ++i)
-      acc += chunk_dot(rp, p.D / 2, sub + 8 * i, xv.vec, xv.coff, xv.vsum);
+    const uint8_t* rg = buf + (2 * pair) * p.rbD;
+    const uint8_t* ru = rg + p.rbD;
+    for (int c = sub; c < nc; c += 16) {
+      g += chunk_dot(rg, p.D / 2, c, xv.vec, xv.xsum);
+      u += chunk_dot(ru, p.D / 2, c, xv.vec, xv.xsum);
+    }
   }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-  const float other = __shfl_xor_sync(0xffffffffu, acc, 8);
-  if (pair < n && sub == 0 && row == 0) {
-    const float g = acc * xv.vscale[0], u = other * xv.vscale[0];
-    h_out[pair] = gelu_tanh(g) * u;
+#pragma unroll
+  for (int o = 8; o; o >>= 1) {
+    g += __shfl_xor_sync(0xffffffffu, g, o);
+    u += __shfl_xor_sync(0xffffffffu, u, o);
+  }
+  if (pair < n && sub == 0) {
+    const float vs = xv.vscale[0];
+    h_out[pair] = gelu_tanh(g * vs) * (u * vs);
   }
 }
 
@@ -584,7 +590,7 @@ __device__ void router_partial(const Ctx& cx, const uint8_t* blk, int r0, int n,
 
 // C stage: rows [r0, r0+n) of the layer output.
 __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int li,
-                          const VecView& hv, const uint16_t* x_l, uint16_t* x_next, float* rpart) {
+                          const VecView& hv, uint16_t* x_next, float* rpart) {
   const DecodeParams& p = *cx.p;
   float* contrib = reinterpret_cast<float*>(cx.smem + p.off_contrib);
   float* xnext = reinterpret_cast<float*>(cx.smem + p.off_xnext);
@@ -598,10 +604,8 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
       const int k = tt / p.nsub_i, sub = tt % p.nsub_i;
       const uint8_t* rp = buf + static_cast<int64_t>(k) * n * p.rbI + r * p.rbI;
       const uint8_t* vb = hv.vec + k * nch_i * kChunkStride;
-      const float* co = hv.coff + k * nch_i;
-      const float* vs = hv.vsum + k * nch_i;
-      for (int i = 0; i < p.cpt_c; ++i)
-        acc += chunk_dot(rp, p.I / 2, sub + p.nsub_i * i, vb, co, vs);
+      const float* xs = hv.xsum + k * nch_i;
+      for (int i = 0; i < p.cpt_c; ++i) acc += chunk_dot(rp, p.I / 2, sub + p.nsub_i * i, vb, xs);
       acc *= __int_as_float(cx.misc[M_WTS + k]) * hv.vscale[k];
     } else {
       const int sub = tt - nrout;
@@ -609,7 +613,7 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
       const int cb = p.K * nch_i;
       const uint8_t* vb = hv.vec + cb * kChunkStride;
       for (int i = 0; i < p.cpt_c; ++i)
-        acc += chunk_dot(rp, p.S / 2, sub + p.nsub_s * i, vb, hv.coff + cb, hv.vsum + cb);
+        acc += chunk_dot(rp, p.S / 2, sub + p.nsub_s * i, vb, hv.xsum + cb);
       acc *= hv.vscale[p.K];
     }
     contrib[r * p.tasks_row + tt] = acc;
@@ -639,7 +643,9 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
 
 constexpr int kRedBatch = 5;
 
-// Last CTA: reduce the partial logits, choose ids, softmax; publish to global.
+// Reduce the partial logits of all CTAs (fixed order), apply the pre-norm
+// scale and the logit bias, choose ids and softmax weights; write them to
+// p.ids / p.wts for layer li.  Runs on one CTA.
 __device__ void router_finish(const Ctx& cx, int li) {
   const DecodeParams& p = *cx.p;
   float* logits = reinterpret_cast<float*>(cx.smem + p.off_logits);
@@ -739,11 +745,11 @@ __device__ void router_finish(const Ctx& cx, int li) {
   }
 }
 
-// Grid barrier among the consumer groups of all CTAs.  `last_fn` runs on the
-// last CTA to arrive before the others are released.  Returns false on
-// timeout or abort.
-template <typename F>
-__device__ bool grid_barrier(const Ctx& cx, F last_fn) {
+// Grid barrier among the consumer groups of all CTAs.  The last CTA to arrive
+// releases the others at once and records that it was last (misc[M_LAST]);
+// misc[M_GEN] holds the barrier's generation.  Returns false on timeout or
+// abort.
+__device__ bool grid_barrier(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
   csync();
   if (threadIdx.x == 0) {
@@ -751,36 +757,66 @@ __device__ bool grid_barrier(const Ctx& cx, F last_fn) {
     const uint32_t g = ld_acquire_gpu(p.bar + 1);
     const uint32_t old = atom_add_acq_rel_gpu(p.bar, 1u);
     cx.misc[M_GEN] = static_cast<int>(g);
-    cx.misc[M_LAST] = (old == static_cast<uint32_t>(cx.G) - 1) ? 1 : 0;
-  }
-  csync();
-  const uint32_t g = static_cast<uint32_t>(cx.misc[M_GEN]);
-  if (cx.misc[M_LAST]) {
-    __threadfence();
-    last_fn();
-    csync();
-    if (threadIdx.x == 0) {
-      __threadfence();
+    if (old == static_cast<uint32_t>(cx.G) - 1) {
+      cx.misc[M_LAST] = 1;
       p.bar[0] = 0u;
       st_release_gpu(p.bar + 1, g + 1u);
-    }
-  } else if (threadIdx.x == 0) {
-    bool ok = false;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-      if (ld_acquire_gpu(p.bar + 1) != g) {
-        ok = true;
-        break;
+    } else {
+      cx.misc[M_LAST] = 0;
+      bool ok = false;
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        if (ld_acquire_gpu(p.bar + 1) != g) {
+          ok = true;
+          break;
+        }
+        if (ld_acquire_gpu(p.bar + 2) != DEV_OK) break;
+        if (globaltimer_ns() - t0 > p.timeout_ns) break;
+        __nanosleep(32);
       }
-      if (ld_acquire_gpu(p.bar + 2) != DEV_OK) break;
-      if (globaltimer_ns() - t0 > p.timeout_ns) break;
-      __nanosleep(64);
+      if (!ok) {
+        atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
+        cx.misc[M_ABORT] = 1;
+      }
+    }
+  }
+  csync();
+  return !cx.misc[M_ABORT];
+}
+
+// On the CTA that arrived last at the barrier just passed: compute layer li's
+// routing and publish it (flag = the barrier's generation + 1).
+__device__ void publish_router(const Ctx& cx, int li) {
+  router_finish(cx, li);
+  csync();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    st_release_gpu(cx.p->bar + 3, static_cast<uint32_t>(cx.misc[M_GEN]) + 1u);
+  }
+}
+
+// Wait until the routing computed after the last barrier is published.
+__device__ bool wait_router(const Ctx& cx) {
+  const DecodeParams& p = *cx.p;
+  if (threadIdx.x == 0) {
+    const uint32_t target = static_cast<uint32_t>(cx.misc[M_GEN]) + 1u;
+    bool ok = ld_acquire_gpu(p.bar + 3) == target;
+    if (!ok) {
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        if (ld_acquire_gpu(p.bar + 3) == target) {
+          ok = true;
+          break;
+        }
+        if (ld_acquire_gpu(p.bar + 2) != DEV_OK) break;
+        if (globaltimer_ns() - t0 > p.timeout_ns) break;
+        __nanosleep(32);
+      }
     }
     if (!ok) {
       atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
       cx.misc[M_ABORT] = 1;
     }
-    __threadfence();
   }
   csync();
   return !cx.misc[M_ABORT];
@@ -791,13 +827,13 @@ __device__ bool grid_barrier(const Ctx& cx, F last_fn) {
 __device__ void publish_ids_local(const Ctx& cx, int li) {
   const DecodeParams& p = *cx.p;
   if (threadIdx.x < p.K) {
-    int id = ld_cg_s32(p.ids + li * p.K + threadIdx.x);
+    int id = __ldcg(p.ids + li * p.K + threadIdx.x);
     if (id < 0 || id >= p.E) {
       atomicCAS(p.bar + 2, DEV_OK, DEV_BAD_ID);
       id = 0;
     }
     cx.misc[M_IDS + threadIdx.x] = id;
-    cx.misc[M_WTS + threadIdx.x] = __float_as_int(ld_cg_f32(p.wts + li * p.K + threadIdx.x));
+    cx.misc[M_WTS + threadIdx.x] = __float_as_int(__ldcg(p.wts + li * p.K + threadIdx.x));
   }
   csync();
   if (threadIdx.x == 0) mbar_arrive(cx.ids_ready);
@@ -827,6 +863,12 @@ __device__ void write_partials(const Ctx& cx, const float* rpart) {
     p.partials[static_cast<int64_t>(e) * p.G_pad + blockIdx.x] = rpart[e];
 }
 
+__device__ __forceinline__ void trace(const Ctx& cx, int li, int ev) {
+  const DecodeParams& p = *cx.p;
+  if (p.trace && threadIdx.x == 0 && li < kTraceMaxLayers)
+    p.trace[(static_cast<int64_t>(blockIdx.x) * p.n_layers + li) * kTraceEvents + ev] = globaltimer_ns();
+}
+
 __device__ void consumer(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
   float* rpart = reinterpret_cast<float*>(cx.smem + p.off_rpart);
@@ -836,7 +878,10 @@ __device__ void consumer(const Ctx& cx) {
     const uint16_t* x_l = li == 0 ? p.x_in : p.xbuf + ((li - 1) & 1) * p.D;
     uint16_t* x_next = li + 1 == p.n_layers ? p.y_out : p.xbuf + (li & 1) * p.D;
     const LayerPlan lp = layer_plan(p, cx.part, li);
+    // was layer li's routing computed in this launch (so we wait for its flag)?
+    const bool routed_here = li > 0 || (p.phases & PH_ROUTER);
     int s = 0;
+    trace(cx, li, 0);
     // ---- router of the launch's first layer (later layers: folded into C)
     if (li == 0 && (p.phases & PH_ROUTER)) {
       for (int e = threadIdx.x; e <= p.E; e += kConsumers) rpart[e] = 0.f;
@@ -845,7 +890,7 @@ __device__ void consumer(const Ctx& cx) {
         if (!wait_full(cx, st_idx)) return;
         const Stage st = stage_at(p, cx.part, lp, s);
         for (int i = threadIdx.x; i < st.n; i += kConsumers)
-          xnext[i] = bf16_bits_to_f32(ld_cg_u16(x_l + st.a + i));
+          xnext[i] = bf16_bits_to_f32(__ldcg(x_l + st.a + i));
         csync();
         router_partial(cx, cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes,
                        st.a, st.n, xnext, rpart);
@@ -860,26 +905,45 @@ __device__ void consumer(const Ctx& cx) {
         ++s;
       }
       write_partials(cx, rpart);
-      if (!grid_barrier(cx, [&] { router_finish(cx, li); })) return;
+      if (!grid_barrier(cx)) return;
+      if (cx.misc[M_LAST]) publish_router(cx, 0);
     }
-    if (needs_ids(p)) publish_ids_local(cx, li);
-    // ---- gate/up (shared, then routed)
+    // ---- layer input, then the shared expert's gate/up (needs no ids)
     VecView xv{};
     if (p.phases & (PH_BSHARED | PH_BROUTED | PH_C)) xv = prep_x(cx, x_l);
-    for (; s < lp.n_r + lp.n_bs + lp.n_br; ++s) {
+    trace(cx, li, 1);
+    for (; s < lp.n_r + lp.n_bs; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
-      float* h_out = st.kind == ST_BS ? p.h + p.K * p.I + st.a : p.h + st.k * p.I + st.a;
-      compute_b(cx, buf, st.n, xv, h_out);
+      compute_b(cx, buf, st.n, xv, p.h + p.K * p.I + st.a);
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
     }
+    trace(cx, li, 2);
+    if (needs_ids(p)) {
+      if (routed_here && !wait_router(cx)) return;
+      publish_ids_local(cx, li);
+    }
+    trace(cx, li, 3);
+    // ---- routed gate/up
+    for (; s < lp.n_r + lp.n_bs + lp.n_br; ++s) {
+      const Stage st = stage_at(p, cx.part, lp, s);
+      if (!wait_full(cx, st_idx)) return;
+      const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
+      compute_b(cx, buf, st.n, xv, p.h + st.k * p.I + st.a);
+      csync();
+      release_slot(cx, st_idx);
+      ++st_idx;
+    }
+    trace(cx, li, 4);
     if (!(p.phases & PH_C)) continue;
     // ---- down + combine (+ next router's partial logits)
-    if (!grid_barrier(cx, [] {})) return;
+    if (!grid_barrier(cx)) return;
+    trace(cx, li, 5);
     const VecView hv = prep_h(cx);
+    trace(cx, li, 6);
     const bool nr = c_has_router(p, li);
     for (int e = threadIdx.x; e <= p.E; e += kConsumers) rpart[e] = 0.f;
     csync();
@@ -887,15 +951,18 @@ __device__ void consumer(const Ctx& cx) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
-      compute_c(cx, buf, st.a, st.n, li, hv, x_l, x_next, rpart);
+      compute_c(cx, buf, st.a, st.n, li, hv, x_next, rpart);
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
     }
+    trace(cx, li, 7);
     if (nr) {
       write_partials(cx, rpart);
-      if (!grid_barrier(cx, [&] { router_finish(cx, li + 1); })) return;
+      if (!grid_barrier(cx)) return;
+      if (cx.misc[M_LAST]) publish_router(cx, li + 1);
     }
+    trace(cx, li, 8);
   }
 }
 

@@ -4,10 +4,12 @@
 // the GPU: K/2 bytes of codes, then K/64 32-bit words (fp16 scale in the low
 // half, fp16 bias in the high half), padded to a multiple of 16 bytes so that
 // any run of rows is a legal bulk-copy source.  Inside each 32-bit word of
-// codes (columns 8w..8w+7) the nibble at bit 4s holds column 8w+2s and the
-// nibble at bit 16+4s holds column 8w+2s+1 (s = 0..3), so one and-or with a
-// mask yields two fp16 values 1024+q (or 1024+16q) that pair with one fp16x2
-// word of activations.
+// codes (columns 8w..8w+7), byte i holds column 8w+i in its low nibble and
+// column 8w+4+i in its high nibble (i = 0..3).  So word & 0x0F0F0F0F gives
+// the codes of columns 0..3 as bytes and (word >> 4) & 0x0F0F0F0F those of
+// columns 4..7, which pair with int16 activation pairs in a 2-way integer dot
+// product (decode), or with one byte permute become fp16 1024+q pairs
+// (prefill dequantisation).
 //
 // Per layer (device):
 //   router_t   [D][E] uint8 codes, transposed so a run of input rows is contiguous
@@ -17,6 +19,8 @@
 //   expert blob (one per routed expert, contiguous, `blob_bytes`):
 //              [I][2] qrows of K=D (gate/up interleaved), then [D] qrows of K=I
 #pragma once
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
+
 #include <cstdint>
 
 namespace moe {
@@ -26,7 +30,7 @@ constexpr int kMaxTopK = 32;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;   // threads that compute
 constexpr int kThreads = kConsumers + 32;         // + one producer warp
-constexpr int kChunkStride = 80;  // smem bytes per 32-element fp16 chunk (64 data + 16 pad)
+constexpr int kChunkStride = 80;  // smem bytes per 32-element int16 chunk (64 data + 16 pad)
 constexpr int kPairsPerStage = 16;  // gate/up row pairs per B stage (8 warps x 2)
 constexpr int kMaxSlots = 6;
 
@@ -46,6 +50,14 @@ enum : int { PH_ROUTER = 1, PH_BSHARED = 2, PH_BROUTED = 4, PH_C = 8, PH_ALL = 1
 
 // Device status word codes (bar[2]).
 enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_ID = 2 };
+// Grid synchronisation words (bar[]): [0] arrivals, [1] barrier generation,
+// [2] status, [3] generation whose routing (ids, weights) has been published.
+constexpr int kBarWords = 4;
+// Decode trace events per layer (thread 0 of each CTA, %globaltimer ns):
+// layer start, x converted, shared gate/up done, ids known, routed gate/up
+// done, h complete (barrier), h converted, down done, next-layer barrier passed.
+constexpr int kTraceEvents = 9;
+constexpr int kTraceMaxLayers = 64;
 
 struct DecodeParams {
   const LayerDev* layers;  // device array, indexed by absolute layer
@@ -69,7 +81,7 @@ struct DecodeParams {
                            // row E holds partial sums of x^2 for the pre-norm
   int32_t* ids;            // [n_layers][K], relative to layer0
   float* wts;              // [n_layers][K]
-  uint32_t* bar;           // [0] arrivals, [1] generation, [2] status
+  uint32_t* bar;           // kBarWords grid synchronisation words
   int G_pad;               // partial stride (grid size rounded up to 8)
   // C-phase task mapping
   int cpt_c, nsub_i, nsub_s, tasks_row, rc_max;
@@ -78,7 +90,106 @@ struct DecodeParams {
   int off_vec, off_contrib, off_rpart, off_xnext, off_xres, off_logits, off_misc, off_bars,
       smem_total;
   uint64_t timeout_ns;     // bound on every device-side wait
+  uint64_t* trace;         // optional: [grid][n_layers][kTraceEvents] %globaltimer stamps
 };
+
+// ------------------------------------------------------------------ prefill
+//
+// Multi-token layer step (T >= 2): token prep, SIMT router GEMM + top-k,
+// bucketing of the T*k assignments by expert (which also emits the grouped
+// GEMM's work units), two grouped GEMMs on the tensor cores (gate/up with the
+// GELU epilogue, then down), and a gather combine.
+
+constexpr int kUnitTokens = 256;   // max B rows (tokens) of one GEMM work unit
+constexpr int kMaxPrefillExperts = 256;
+
+// One work unit of the grouped GEMM: a 128-row tile of one weight matrix
+// against up to kUnitTokens activation rows.
+struct GemmUnit {
+  int kind;    // 0 routed expert, 1 shared expert
+  int mt;      // weight row tile (rows mt*128 .. mt*128+127)
+  int expert;  // routed: blob index of the expert
+  int row0;    // routed: first bucket position; shared: first token
+  int n;       // activation rows in the unit (1 .. kUnitTokens)
+  int pad[3];
+};
+
+struct PrefillDims {
+  int T, D, E, I, K, S;
+  int mt_gu_r, mt_dn, mt_gu_s;  // 128-row tiles: routed gate/up, down, shared gate/up
+};
+
+// Router GEMM: logits partials [nsplit][T][E].
+int router_gemm_splits(int T, int E, int D, int num_sms);
+
+struct RouteArgs {
+  const uint16_t* x;  // bf16 [T][D]
+  int T, D, E, K;
+  int prenorm;
+  float rms_eps;
+  const uint8_t* router_t;    // [D][E] codes
+  const uint32_t* router_sb;  // [D/64][E]
+  const float* logit_bias;    // [E] or nullptr
+  const int32_t* forced;      // device [T][K] or nullptr
+  uint16_t* x16;              // fp16 [T][D] out: x * f_t
+  float* sigma;               // [T] out: (r_t / f_t), the scale of dot products with x16
+  float* rscale;              // [T] out: r_t (pre-norm factor, 1 without)
+  float* partials;            // [nsplit][T][E]
+  int nsplit;
+  int32_t* ids;               // [T][K] out
+  float* wts;                 // [T][K] out
+};
+int prefill_route(const RouteArgs& a, void* stream);
+
+struct BucketArgs {
+  const int32_t* ids;  // [T][K]
+  int T, K, E;
+  int mt_gu_r, mt_dn, mt_gu_s;
+  int32_t* counts;     // [E]
+  int32_t* offsets;    // [E+1]
+  int32_t* perm;       // [T*K] bucket position -> assignment t*K + j
+  int32_t* inv;        // [T*K] assignment -> bucket position
+  GemmUnit* units_gu;  // gate/up units
+  GemmUnit* units_dn;  // down units
+  int32_t* n_units;    // [2] gate/up, down
+  uint32_t* status;
+};
+int prefill_bucket(const BucketArgs& a, void* stream);
+
+struct CombineArgs {
+  const uint16_t* x;   // bf16 [T][D] (residual input)
+  const uint16_t* e;   // bf16 [T*K][D] weighted routed outputs, bucket order
+  const float* s;      // fp32 [T][D] shared expert output
+  const int32_t* inv;  // [T*K]
+  uint16_t* y;         // bf16 [T][D]
+  int T, D, K, residual;
+};
+int prefill_combine(const CombineArgs& a, void* stream);
+
+// Grouped GEMM on the tensor cores (gemm_tc.cu).  Index [kind]: 0 routed, 1 shared.
+struct GemmParams {
+  CUtensorMap tm_code[2];  // 4-bit codes: box 128 B x 128 rows, 128-byte swizzle
+  CUtensorMap tm_sb[2];    // scale/bias words: box 16 B x 128 rows
+  const GemmUnit* units;
+  const int32_t* n_units;  // device: number of units
+  int mode;                // 0: gate/up (+ GELU epilogue), 1: down
+  int K[2];                // reduction length (D for gate/up; I or S for down)
+  const void* bsrc[2];     // fp16 activation rows (x16, or h)
+  int bld[2];              // row pitch of bsrc in elements
+  const int32_t* perm;     // bucket position -> assignment
+  int topk;
+  const float* sigma;      // per-token scale of dot products with x16 (gate/up)
+  void* hout[2];           // gate/up: fp16 h rows (routed: bucket order; shared: tokens)
+  int hld[2];
+  void* eout;              // down, routed: bf16 [T*K][D], weighted by the routing weight
+  float* sout;             // down, shared: fp32 [T][D]
+  const float* wts;        // [T*K] routing weights by assignment
+  int D;
+  uint32_t* status;
+  unsigned long long timeout_ns;
+};
+int gemm_tc_smem_bytes();
+int gemm_tc_launch(const GemmParams& p, int grid, void* stream);
 
 // Host entry points implemented in decode.cu.
 int decode_smem_plan(DecodeParams* p, int max_smem);   // fills the carve-up; 0 if it fits

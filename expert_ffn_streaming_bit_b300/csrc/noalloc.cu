@@ -100,6 +100,7 @@ extern "C" moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, vo
   p.partials = reinterpret_cast<float*>(base + bar + xbuf + hb);
   p.ids = reinterpret_cast<int32_t*>(base + bar + xbuf + hb + part);
   p.wts = reinterpret_cast<float*>(base + bar + xbuf + hb + part + ids);
+  p.trace = nullptr;  // the trace buffer belongs to the handle's own scratch
   // The array keeps the previous call's contents; the grid-barrier counters
   // and the status word must start at zero.  Everything else is written before
   // it is read.

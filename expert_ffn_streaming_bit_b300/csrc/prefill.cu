@@ -1,0 +1,471 @@
+// Multi-token (prefill) layer step, SIMT parts: token preparation, the 8-bit
+// router GEMM with top-k and softmax, bucketing of the T*k (token, expert)
+// assignments by expert together with the grouped GEMM's work units, and the
+// gather combine.  The grouped GEMMs themselves are in gemm_tc.cu.
+//
+// Passages (sh.edu-sjtu.cn article, section 三件事, third bullet; shilu.ai
+// "drumih/turbo-fieldfare", section 推理引擎的工作原理): prompts are prefilled in
+// chunks so that each expert brought in serves every row routed to it; the
+// bucketing below is that grouping, done on the device.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ float bf16f(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x40u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------ token prep
+// Per token (one warp): a power-of-two factor f with max|x| f in [2^14, 2^15)
+// (1 for a zero row), x16 = fp16(f x) (exact for bf16 inputs in range), and
+// the scales that turn dot products with x16 into dot products with the
+// layer input u = r x (r = 1 / sqrt(mean(x^2) + eps) with the pre-norm, else 1).
+__global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restrict__ x, int T, int D,
+                                                       int prenorm, float eps,
+                                                       __half* __restrict__ x16,
+                                                       float* __restrict__ sigma,
+                                                       float* __restrict__ rscale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const uint4* row = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * D);
+  const int nv = D / 8;
+  float m = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16f(w[j] & 0xffffu)), fabsf(bf16f(w[j] >> 16))));
+  }
+  m = warp_max(m);
+  int e = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xffu) - 127 : 14;
+  e = max(-100, min(100, e));
+  const float f = ldexpf(1.f, 14 - e);
+  uint4* out = reinterpret_cast<uint4*>(x16 + static_cast<size_t>(t) * D);
+  float ss = 0.f;
+  for (int i = lane; i < nv; i += 32) {
+    const uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16f(w[j] & 0xffffu) * f, b = bf16f(w[j] >> 16) * f;
+      ss = fmaf(a, a, fmaf(b, b, ss));
+      const __half2 h = __floats2half2_rn(a, b);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) {
+    double r = 1.0;
+    if (prenorm) {
+      const double fd = static_cast<double>(f);
+      r = fd / sqrt(static_cast<double>(ss) / D + static_cast<double>(eps) * fd * fd);
+    }
+    sigma[t] = static_cast<float>(r / static_cast<double>(f));
+    rscale[t] = static_cast<float>(r);
+  }
+}
+
+// ------------------------------------------------------------ router GEMM
+// partial[split][t][e] = sum over the split's groups g of sum_{c in g}
+// (s[e,g] q[c,e] + b[e,g]) x[t,c], fp32, fixed order.  Tile: 32 tokens x 64
+// experts per CTA, 4 x 4 outputs per thread.
+constexpr int kRtTok = 32, kRtExp = 64;
+
+__global__ void __launch_bounds__(128) router_gemm_kernel(const uint16_t* __restrict__ x, int T,
+                                                          int D, int E,
+                                                          const uint8_t* __restrict__ rt,
+                                                          const uint32_t* __restrict__ rsb,
+                                                          int groups_per_split,
+                                                          float* __restrict__ partial) {
+  __shared__ float xs[64][kRtTok + 1];
+  __shared__ __align__(16) float ws[64][kRtExp];
+  const int t0 = blockIdx.x * kRtTok, e0 = blockIdx.y * kRtExp, split = blockIdx.z;
+  const int ng = D / 64;
+  const int g0 = split * groups_per_split, g1 = min(ng, g0 + groups_per_split);
+  const int tid = threadIdx.x;
+  const int tg = tid >> 4, eg = tid & 15;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int g = g0; g < g1; ++g) {
+    {  // x tile: token tid/4, 16 columns at (tid%4)*16
+      const int tt = tid >> 2, c0 = (tid & 3) * 16;
+      const int t = t0 + tt;
+      uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+      if (t < T) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * D + g * 64 + c0);
+        a = __ldg(src);
+        b = __ldg(src + 1);
+      }
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        xs[c0 + 2 * j][tt] = bf16f(w[j] & 0xffffu);
+        xs[c0 + 2 * j + 1][tt] = bf16f(w[j] >> 16);
+      }
+    }
+    {  // weight tile: column k = tid/2 of the group, 32 experts at (tid%2)*32
+      const int k = tid >> 1, eo = (tid & 1) * 32;
+      const uint8_t* src = rt + static_cast<size_t>(g * 64 + k) * E + e0 + eo;
+      const uint32_t* sbp = rsb + static_cast<size_t>(g) * E + e0 + eo;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int eb = e0 + eo + 16 * h;
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (eb < E) q = __ldg(reinterpret_cast<const uint4*>(src + 16 * h));
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float wv = 0.f;
+          if (eb + i < E) {
+            const uint32_t sb = __ldg(sbp + 16 * h + i);
+            const __half2 h2 = *reinterpret_cast<const __half2*>(&sb);
+            const float code = static_cast<float>((qw[i >> 2] >> (8 * (i & 3))) & 0xffu);
+            wv = fmaf(__low2float(h2), code, __high2float(h2));
+          }
+          ws[k][eo + 16 * h + i] = wv;
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < 64; ++k) {
+      float xv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xv[i] = xs[k][tg * 4 + i];
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[k][eg * 4]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[i][0] = fmaf(xv[i], wv.x, acc[i][0]);
+        acc[i][1] = fmaf(xv[i], wv.y, acc[i][1]);
+        acc[i][2] = fmaf(xv[i], wv.z, acc[i][2]);
+        acc[i][3] = fmaf(xv[i], wv.w, acc[i][3]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + tg * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + eg * 4 + j;
+      if (e < E) partial[(static_cast<size_t>(split) * T + t) * E + e] = acc[i][j];
+    }
+  }
+}
+
+// ------------------------------------------------------------ router top-k
+// One warp per token: logits = rscale * (sum of the splits, in order) + bias;
+// top-k by (logit desc, index asc) (or the forced ids); softmax over the k.
+constexpr int kMaxEPerLane = kMaxPrefillExperts / 32;
+
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ partial,
+                                                          int nsplit, int T, int E, int K,
+                                                          const float* __restrict__ rscale,
+                                                          const float* __restrict__ bias,
+                                                          const int32_t* __restrict__ forced,
+                                                          int32_t* __restrict__ ids,
+                                                          float* __restrict__ wts) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float lv[kMaxEPerLane];
+  const float r = rscale[t];
+#pragma unroll
+  for (int i = 0; i < kMaxEPerLane; ++i) {
+    const int e = lane + 32 * i;
+    float v = -INFINITY;
+    if (e < E) {
+      float s = 0.f;
+      for (int sp = 0; sp < nsplit; ++sp) s += partial[(static_cast<size_t>(sp) * T + t) * E + e];
+      v = s * r;
+      if (bias) v += bias[e];
+    }
+    lv[i] = v;
+  }
+  int chosen[kMaxTopK];
+  float cl[kMaxTopK];
+  for (int j = 0; j < K; ++j) {
+    if (forced) {
+      const int id = forced[t * K + j];
+      chosen[j] = id;
+      float v = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxEPerLane; ++i)
+        if (lane + 32 * i == id) v = lv[i];
+      // the owner lane holds the value; others contribute 0 (one owner)
+      cl[j] = warp_sum((id & 31) == lane ? v : 0.f);
+      continue;
+    }
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxEPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && (lv[i] > bv || (lv[i] == bv && e < bi))) {
+        bv = lv[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    chosen[j] = bi;
+    cl[j] = bv;
+#pragma unroll
+    for (int i = 0; i < kMaxEPerLane; ++i)
+      if (lane + 32 * i == bi) lv[i] = -INFINITY;
+  }
+  if (lane == 0) {
+    float m = -INFINITY;
+    for (int j = 0; j < K; ++j) m = fmaxf(m, cl[j]);
+    float ex[kMaxTopK];
+    float z = 0.f;
+    for (int j = 0; j < K; ++j) {
+      ex[j] = expf(cl[j] - m);
+      z += ex[j];
+    }
+    for (int j = 0; j < K; ++j) {
+      ids[t * K + j] = chosen[j];
+      wts[t * K + j] = ex[j] / z;
+    }
+  }
+}
+
+// -------------------------------------------------------------- bucketing
+// One CTA of 1024 threads.  Stable counting sort of the n = T*K assignments
+// a = t*K + j by expert: each warp owns a contiguous segment of assignments;
+// per-(warp, expert) counts give every warp its write base, and a warp places
+// its assignments in order with a match/rank step, so the result is in
+// (expert, t, j) order.  Then the GEMM work units: each expert's rows are cut
+// into ceil(count / kUnitTokens) nearly equal token tiles, times the weight
+// row tiles of the gate/up and of the down matrix; the shared expert's units
+// (all T tokens) follow the routed ones.
+constexpr int kBucketThreads = 1024;
+constexpr int kBucketWarps = kBucketThreads / 32;
+
+__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
+  __shared__ int hist[kBucketWarps][kMaxPrefillExperts];
+  __shared__ int cnt[kMaxPrefillExperts];
+  __shared__ int off[kMaxPrefillExperts + 1];
+  __shared__ int tiles[kMaxPrefillExperts];
+  __shared__ int toff[kMaxPrefillExperts + 1];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E;
+  const int n = a.T * a.K;
+  for (int i = tid; i < kBucketWarps * kMaxPrefillExperts; i += kBucketThreads)
+    (&hist[0][0])[i] = 0;
+  __syncthreads();
+  const int seg = (n + kBucketWarps - 1) / kBucketWarps;
+  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+  for (int i = s0 + lane; i < s1; i += 32) {
+    int e = a.ids[i];
+    if (e < 0 || e >= E) {
+      atomicCAS(a.status, DEV_OK, DEV_BAD_ID);
+      e = 0;
+    }
+    atomicAdd(&hist[warp][e], 1);
+  }
+  __syncthreads();
+  if (tid < E) {
+    int c = 0;
+    for (int w = 0; w < kBucketWarps; ++w) c += hist[w][tid];
+    cnt[tid] = c;
+  }
+  __syncthreads();
+  if (tid == 0) {  // E <= 256: a serial scan is cheap
+    int acc = 0, tacc = 0;
+    for (int e = 0; e < E; ++e) {
+      off[e] = acc;
+      acc += cnt[e];
+      const int nt = (cnt[e] + kUnitTokens - 1) / kUnitTokens;
+      tiles[e] = nt;
+      toff[e] = tacc;
+      tacc += nt;
+    }
+    off[E] = acc;
+    toff[E] = tacc;
+  }
+  __syncthreads();
+  if (tid < E) {  // per-(warp, expert) write bases, in warp order
+    int base = off[tid];
+    for (int w = 0; w < kBucketWarps; ++w) {
+      const int c = hist[w][tid];
+      hist[w][tid] = base;
+      base += c;
+    }
+    a.counts[tid] = cnt[tid];
+    a.offsets[tid] = off[tid];
+  }
+  if (tid == 0) a.offsets[E] = off[E];
+  __syncthreads();
+  for (int i0 = s0; i0 < s1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool act = i < s1;
+    int e = act ? a.ids[i] : -1;
+    if (act && (e < 0 || e >= E)) e = 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (act) {
+      const unsigned lower = peers & ((1u << lane) - 1u);
+      const int pos = hist[warp][e] + __popc(lower);
+      a.perm[pos] = i;
+      a.inv[i] = pos;
+    }
+    __syncwarp();
+    if (act && (peers & ((1u << lane) - 1u)) == 0) hist[warp][e] += __popc(peers);
+    __syncwarp();
+  }
+  // ---- work units
+  const int routed_tiles = toff[E];
+  const int st = (a.T + kUnitTokens - 1) / kUnitTokens;  // shared token tiles
+  const int ngu = routed_tiles * a.mt_gu_r + st * a.mt_gu_s;
+  const int ndn = (routed_tiles + st) * a.mt_dn;
+  if (tid == 0) {
+    a.n_units[0] = ngu;
+    a.n_units[1] = ndn;
+  }
+  for (int e = warp; e < E; e += kBucketWarps) {
+    const int c = cnt[e], nt = tiles[e];
+    for (int tt = 0; tt < nt; ++tt) {
+      const int r0 = static_cast<int>(static_cast<int64_t>(c) * tt / nt);
+      const int r1 = static_cast<int>(static_cast<int64_t>(c) * (tt + 1) / nt);
+      const int tile = toff[e] + tt;
+      for (int m = lane; m < a.mt_gu_r; m += 32) {
+        GemmUnit u{0, m, e, off[e] + r0, r1 - r0, {0, 0, 0}};
+        a.units_gu[tile * a.mt_gu_r + m] = u;
+      }
+      for (int m = lane; m < a.mt_dn; m += 32) {
+        GemmUnit u{0, m, e, off[e] + r0, r1 - r0, {0, 0, 0}};
+        a.units_dn[tile * a.mt_dn + m] = u;
+      }
+    }
+  }
+  for (int tt = warp; tt < st; tt += kBucketWarps) {
+    const int r0 = static_cast<int>(static_cast<int64_t>(a.T) * tt / st);
+    const int r1 = static_cast<int>(static_cast<int64_t>(a.T) * (tt + 1) / st);
+    for (int m = lane; m < a.mt_gu_s; m += 32) {
+      GemmUnit u{1, m, 0, r0, r1 - r0, {0, 0, 0}};
+      a.units_gu[routed_tiles * a.mt_gu_r + tt * a.mt_gu_s + m] = u;
+    }
+    for (int m = lane; m < a.mt_dn; m += 32) {
+      GemmUnit u{1, m, 0, r0, r1 - r0, {0, 0, 0}};
+      a.units_dn[(routed_tiles + tt) * a.mt_dn + m] = u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- combine
+// y[t] = bf16([x[t]] + s[t] + sum_j e[inv[t*K + j]]), summed in that order in
+// fp32.  Each thread handles 8 consecutive columns.
+__global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+  const int t = blockIdx.y;
+  const int c8 = blockIdx.x * 128 + threadIdx.x;
+  if (c8 * 8 >= a.D) return;
+  const size_t base = static_cast<size_t>(t) * a.D + c8 * 8;
+  float acc[8];
+  const float4 s0 = __ldg(reinterpret_cast<const float4*>(a.s + base));
+  const float4 s1 = __ldg(reinterpret_cast<const float4*>(a.s + base) + 1);
+  acc[0] = s0.x; acc[1] = s0.y; acc[2] = s0.z; acc[3] = s0.w;
+  acc[4] = s1.x; acc[5] = s1.y; acc[6] = s1.z; acc[7] = s1.w;
+  for (int j = 0; j < a.K; ++j) {
+    const int pos = __ldg(a.inv + t * a.K + j);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.e + static_cast<size_t>(pos) * a.D + c8 * 8));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += bf16f(w[i] & 0xffffu);
+      acc[2 * i + 1] += bf16f(w[i] >> 16);
+    }
+  }
+  if (a.residual) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + base));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += bf16f(w[i] & 0xffffu);
+      acc[2 * i + 1] += bf16f(w[i] >> 16);
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = static_cast<uint32_t>(f32_to_bf16(acc[2 * i])) |
+           (static_cast<uint32_t>(f32_to_bf16(acc[2 * i + 1])) << 16);
+  *reinterpret_cast<uint4*>(a.y + base) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+}  // namespace
+
+int router_gemm_splits(int T, int E, int D, int num_sms) {
+  const int tiles = ((T + kRtTok - 1) / kRtTok) * ((E + kRtExp - 1) / kRtExp);
+  const int ng = D / 64;
+  int splits = (2 * num_sms + tiles - 1) / tiles;
+  if (splits < 1) splits = 1;
+  if (splits > ng) splits = ng;
+  const int gps = (ng + splits - 1) / splits;
+  return (ng + gps - 1) / gps;
+}
+
+int prefill_route(const RouteArgs& a, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  tok_prep_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a.x, a.T, a.D, a.prenorm, a.rms_eps,
+                                                reinterpret_cast<__half*>(a.x16), a.sigma, a.rscale);
+  const int ng = a.D / 64;
+  const int gps = (ng + a.nsplit - 1) / a.nsplit;
+  dim3 grid((a.T + kRtTok - 1) / kRtTok, (a.E + kRtExp - 1) / kRtExp, a.nsplit);
+  router_gemm_kernel<<<grid, 128, 0, s>>>(a.x, a.T, a.D, a.E, a.router_t, a.router_sb, gps,
+                                          a.partials);
+  router_topk_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a.partials, a.nsplit, a.T, a.E, a.K, a.rscale,
+                                                   a.logit_bias, a.forced, a.ids, a.wts);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int prefill_bucket(const BucketArgs& a, void* stream) {
+  bucket_kernel<<<1, kBucketThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int prefill_combine(const CombineArgs& a, void* stream) {
+  dim3 grid((a.D / 8 + 127) / 128, a.T);
+  combine_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace moe

@@ -146,6 +146,19 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc)
   return acc;
 }
 
+// c + a.lo * b.byte0 + a.hi * b.byte1 (a: two signed 16-bit, b: unsigned bytes).
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// c + a.lo * b.byte2 + a.hi * b.byte3.
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // (x & mask) | magic in one logic op.
 __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t magic) {
   uint32_t r;

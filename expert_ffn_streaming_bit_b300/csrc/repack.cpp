@@ -14,14 +14,13 @@ static void repack_row4(const uint8_t* q, const uint16_t* scale, const uint16_t*
   const int64_t words = K / 8;
   uint32_t* out = reinterpret_cast<uint32_t*>(dst);
   for (int64_t w = 0; w < words; ++w) {
-    uint32_t orig;
+    uint32_t orig;  // canonical: column 8w + c in nibble c (low nibble = even column)
     std::memcpy(&orig, q + 4 * w, 4);
     uint32_t v = 0;
-    for (int s = 0; s < 4; ++s) {
-      const uint32_t even = (orig >> (8 * s)) & 0xFu;     // column 8w + 2s
-      const uint32_t odd = (orig >> (8 * s + 4)) & 0xFu;  // column 8w + 2s + 1
-      v |= even << (4 * s);
-      v |= odd << (16 + 4 * s);
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (orig >> (4 * i)) & 0xFu;        // column 8w + i
+      const uint32_t hi = (orig >> (4 * (i + 4))) & 0xFu;  // column 8w + 4 + i
+      v |= (lo | (hi << 4)) << (8 * i);
     }
     out[w] = v;
   }

@@ -139,6 +139,13 @@ typedef struct {
 
 /*
  * moe_layer_forward — one MoE layer step for T tokens (1 <= T <= max_tokens).
+ * Resident mode: T == 1 runs the persistent decode kernel; T >= 2 runs the
+ *   prefill path: router GEMM + top-k, token-to-expert bucketing, grouped
+ *   GEMMs on the tensor cores (fp16 operands: weights dequantised to fp16 in
+ *   shared memory, activations scaled by a per-token power of two; fp32
+ *   accumulation), and a gather combine.  The prefill path holds the gated
+ *   intermediate h in fp16 (values beyond +-65504 saturate) and the routed
+ *   expert outputs in bf16 before the combine.
  * x: device [T][D] bf16 input.  y: device [T][D] bf16 output; y may not alias x.
  * forced_ids: host [T][k] or NULL.  When given, those experts are used (each
  *   row k distinct ids in [0, E)); their weights are still the softmax of the
@@ -156,7 +163,9 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
                              const int32_t* forced_ids, void* stream, moe_layer_stats* stats);
 
 /*
- * moe_forward_stack — layers [0, n_layers) back to back, each reading the
+ * moe_forward_stack — layers [0, n_layers) back to back (T == 1: one
+ * persistent kernel for the whole stack; T >= 2: the prefill path layer by
+ * layer over all T tokens), each reading the
  * RMS-normalised residual stream and adding its output to it:
  * x_{l+1} = bf16(x_l + moe_l(x_l / sqrt(mean(x_l^2) + 1e-6))); y = x_{n_layers}
  * (the flags MOE_FWD_RESIDUAL | MOE_FWD_PRENORM on every layer).
@@ -207,6 +216,21 @@ moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, void* y, int 
  * [n_layers][T][k] fp32 (either may be NULL).  Synchronises the device.
  */
 moe_status moe_stack_ids(moe_handle* h, int n_layers, int T, int32_t* ids, float* weights);
+
+/*
+ * moe_last_buckets — the token-to-expert bucketing of the most recent
+ * multi-token (T >= 2, resident mode) forward call's last layer, copied to
+ * host memory (synchronises the device).  For a prefill chunk the T*k
+ * assignments a = t*k + j are grouped by expert, stably (sh.edu-sjtu.cn
+ * article, section 三件事, third bullet; shilu.ai page, section 推理引擎的工作原理:
+ * each expert brought in serves every row routed to it):
+ *   counts  [E]     assignments per expert
+ *   offsets [E+1]   exclusive prefix sum of counts
+ *   perm    [T*k]   assignments in (expert, t, j) order
+ * Any pointer may be NULL.  MOE_ERR_STATE if the last call was not a
+ * multi-token call.
+ */
+moe_status moe_last_buckets(moe_handle* h, int32_t* counts, int32_t* offsets, int32_t* perm);
 
 /* Flags for moe_cache_step. */
 #define MOE_PLAN_ONLY 1 /* update the slot table but copy no weights */
@@ -274,6 +298,21 @@ moe_status moe_debug_inject(moe_handle* h, int what, int arg);
 /* Host waits on device work poll with this deadline (default 10000 ms) and
  * return MOE_ERR_TIMEOUT when it passes. */
 moe_status moe_set_timeout_ms(moe_handle* h, int ms);
+
+/*
+ * Decode tracing (for profiling the persistent decode kernel).
+ * moe_trace_enable(h, 1): later decode launches of this handle record, per
+ * CTA and layer, MOE_TRACE_EVENTS %globaltimer stamps (ns) taken by the CTA's
+ * first consumer thread: layer start, input converted, shared gate/up done,
+ * ids known, routed gate/up done, h complete, h converted, down done, next
+ * barrier passed.  moe_trace_enable(h, 0) stops recording.
+ * moe_trace_read(h, out, n_layers): copies the last launch's stamps to host
+ * out [num_sms][n_layers][MOE_TRACE_EVENTS] int64 (n_layers of that launch,
+ * at most 64; synchronises).
+ */
+#define MOE_TRACE_EVENTS 9
+moe_status moe_trace_enable(moe_handle* h, int on);
+moe_status moe_trace_read(moe_handle* h, int64_t* out, int n_layers);
 
 const char* moe_status_string(moe_status s);
 /* Last error text of this handle ("" if none); with h == NULL, of the last
