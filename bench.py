@@ -39,6 +39,18 @@ def peaks():
         return 6400.0, 1800.0, "fallback"
 
 
+def job_throughput(seconds: float, units_per_rank: float, world: int, device=None) -> float:
+    """Whole-job throughput of independent replicas: every rank processed
+    units_per_rank units; the job took as long as its slowest rank (max over
+    ranks with a collective when world > 1)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return units_per_rank * world / float(t.item())
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -178,12 +190,8 @@ def run_ours(args):
         dist.barrier()
     ms = t_start.elapsed_time(t_end)
     launch_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
-    t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    tokens = args.steps * world
-    value = tokens / (ms_max / 1e3)
+    value = job_throughput(ms / 1e3, args.steps, world, device="cuda")
+    ms_max = args.steps * world / value * 1e3
     # end to end through the host-I/O entry point: H2D of x, stack, D2H of y, per step
     xh = synth.make_tokens(shape, "decode", P, index=2000 + rank).view(torch.int16).numpy().view(np.uint16)
     yh = np.empty((1, shape.d_model), np.uint16)
@@ -194,10 +202,7 @@ def run_ours(args):
     for i in range(n_e2e):
         moe.moe_forward_stack_host(h, xh[i % P:i % P + 1], yh, L)
     te = time.perf_counter() - te0
-    e2e_t = torch.tensor([te], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = n_e2e * world / float(e2e_t.item())
+    e2e_value = job_throughput(te, n_e2e, world, device="cuda")
     hbm, bf16, src = peaks()
     sub = synth.MoEShape(shape.name, shape.d_model, shape.n_experts, shape.d_expert, shape.top_k,
                          shape.d_shared, shape.group, L)
@@ -240,6 +245,150 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def gemm_flops_per_layer(shape, T):
+    """Algorithmic FLOPs of the expert GEMMs of one layer for T tokens (routed
+    gate/up + down over T*k rows, shared gate/up + down over T rows)."""
+    D, I, S, k = shape.d_model, shape.d_expert, shape.d_shared, shape.top_k
+    return 2 * T * k * (2 * I * D + D * I) + 2 * T * (2 * S * D + D * S)
+
+
+def run_prefill(args):
+    """Large-batch prefill: T = 4096 tokens through one Gemma-shape layer,
+    repeated 30 times (each repetition reads the previous one's output, with
+    pre-norm and residual).  One step = 30 layer calls."""
+    import torch
+    import synth
+    import expert_ffn_streaming_bit_b300 as moe
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    shape = synth.GEMMA
+    T, R = 4096, args.layers or 30
+    layer = make_layers(shape, "prefill", 1, "cuda")[0]
+    h = moe.moe_create(shape, [layer], max_tokens=T)
+    x = synth.make_tokens(shape, "prefill", T, index=rank).cuda()
+    bufs = [torch.empty_like(x), torch.empty_like(x)]
+    flags = moe.MOE_FWD_PRENORM | moe.MOE_FWD_RESIDUAL
+
+    def step():
+        src = x
+        for r in range(R):
+            moe.moe_layer_forward(h, 0, src, bufs[r & 1], flags=flags)
+            src = bufs[r & 1]
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    moe.moe_prefill_phase_ms(h)  # clear
+    moe.moe_trace_enable(h, True)   # phase events on the launching stream
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    moe.moe_trace_enable(h, False)
+    ms = t0.elapsed_time(t1) / args.steps
+    phases, calls = moe.moe_prefill_phase_ms(h)
+    per_call = [v / max(calls, 1) for v in phases]
+    fl = gemm_flops_per_layer(shape, T)
+    gemm_ms = per_call[2] + per_call[3]
+    hbm, bf16, src = peaks()
+    value = T / (ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 x f16 -> f32 (tcgen05 kind::f16), 4-bit weights",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 tokens)",
+        "config": {"workload": "large prefill: 4096 tokens, one Gemma-shape MoE layer repeated %d "
+                               "times, router-driven uniform routing" % R,
+                   "tokens_per_step": T, "layer_calls_per_step": R,
+                   "l2": "inputs larger than L2: 439 MB of weights per layer call"},
+        "phase_ms_per_layer": dict(zip(["router", "bucket", "gemm_gate_up", "gemm_down", "combine"],
+                                       per_call)),
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (gate/up + down launches)",
+                     "achieved": fl / (gemm_ms / 1e3) / 1e12, "peak": bf16,
+                     "peak_source": src + " bf16 dense (fp16 dense has the same nominal rate)",
+                     "unit": "TFLOP/s", "frac": fl / (gemm_ms / 1e3) / 1e12 / bf16,
+                     "flops_per_layer": fl, "avg_gemm_ms_per_layer": gemm_ms, "traffic": None},
+        "layer_tflops": (fl + 2 * T * shape.n_experts * shape.d_model) / (ms / R / 1e3) / 1e12,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_chunked(args):
+    """Chunked prefill: 1024 tokens in 8 chunks of 128 through the 30-layer
+    stack, router biased so expert popularity follows Zipf(1.1).  One step =
+    8 chunks x 30 layers."""
+    import torch
+    import synth
+    import expert_ffn_streaming_bit_b300 as moe
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    shape = synth.GEMMA
+    L = args.layers or shape.n_layers
+    out = []
+    for l in range(L):
+        Lw = synth.make_layer(shape, "chunked_prefill", l, device="cuda", logit_bias=True)
+        out.append(synth.layer_to(Lw, "cpu"))
+        del Lw
+    torch.cuda.empty_cache()
+    h = moe.moe_create(shape, out, max_tokens=128)
+    x = synth.make_tokens(shape, "chunked_prefill", 1024, index=rank).cuda()
+    y = torch.empty_like(x)
+
+    def step():
+        for c in range(8):
+            moe.moe_forward_stack(h, x[c * 128:(c + 1) * 128], y[c * 128:(c + 1) * 128], L)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    # touched expert bytes: distinct experts per (chunk, layer) from the ids
+    touched = 0
+    for c in range(8):
+        moe.moe_forward_stack(h, x[c * 128:(c + 1) * 128], y[c * 128:(c + 1) * 128], L)
+        ids, _ = moe.moe_stack_ids(h, L, 128)
+        for l in range(L):
+            touched += len(np.unique(ids[l])) * shape.expert_bytes()
+    touched += 8 * L * (shape.shared_bytes() + shape.router_bytes())
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    hbm, bf16, src = peaks()
+    gbs = touched / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": 1024 / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 x f16 -> f32 (tcgen05 kind::f16), 4-bit weights",
+        "data": "synthetic (seeded; Zipf(1.1) router logit bias)",
+        "config": {"workload": "chunked prefill: 1024 tokens in 8 chunks of 128 through %d "
+                               "layers, Zipf(1.1)-biased routing" % L,
+                   "tokens_per_step": 1024},
+        "touched_weight_bytes_per_step": touched,
+        "roofline": {"bound": "hbm", "kernel": "whole chunk step (touched weight bytes)",
+                     "achieved": gbs, "peak": hbm, "peak_source": src, "unit": "GB/s",
+                     "frac": gbs / hbm, "traffic": None},
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_reference(args):
@@ -290,6 +439,9 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "chunked_prefill"],
+                    help="decode (default, the headline line), or a prefill workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -297,6 +449,10 @@ def main():
         if args.steps > 20:
             args.steps = 20   # each reference step is a whole oracle layer on the host
         run_reference(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
+    elif args.workload == "chunked_prefill":
+        run_chunked(args)
     else:
         run_ours(args)
 

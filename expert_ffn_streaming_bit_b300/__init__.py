@@ -93,6 +93,7 @@ _sig = {
     "moe_cache_reset": (_I, [_P]),
     "moe_trace_enable": (_I, [_P, _I]),
     "moe_trace_read": (_I, [_P, _P, _I]),
+    "moe_prefill_phase_ms": (_I, [_P, _P, _P]),
     "moe_last_buckets": (_I, [_P, _P, _P, _P]),
     "moe_slot_plan_create": (_I, [_I, _I, ctypes.POINTER(ctypes.c_void_p)]),
     "moe_slot_plan_step": (_I, [_P, _P, _I, ctypes.POINTER(moe_cache_result)]),
@@ -290,6 +291,15 @@ def moe_trace_read(handle: Handle, n_layers: int) -> np.ndarray:
     out = np.zeros((G, n_layers, MOE_TRACE_EVENTS), np.int64)
     _check(_lib.moe_trace_read(handle.ptr, out.ctypes.data, n_layers), handle)
     return out
+
+
+def moe_prefill_phase_ms(handle: Handle):
+    """Summed CUDA-event times (ms) of the recorded multi-token calls:
+    (router, bucketing, gate/up GEMM, down GEMM, combine), and the call count."""
+    ms = (ctypes.c_float * 5)()
+    calls = ctypes.c_int()
+    _check(_lib.moe_prefill_phase_ms(handle.ptr, ms, ctypes.byref(calls)), handle)
+    return list(ms), calls.value
 
 
 def moe_cache_reset(handle: Handle):

@@ -46,7 +46,7 @@ struct moe_handle {
   int64_t scratch_bytes = 0;
   uint16_t* xbuf = nullptr;
   float* h = nullptr;
-  float* partials = nullptr;
+  unsigned long long* lacc = nullptr;
   int32_t* ids = nullptr;
   float* wts = nullptr;
   uint32_t* bar = nullptr;
@@ -82,6 +82,7 @@ struct moe_handle {
   uint16_t* pf_x16 = nullptr;
   float* pf_sigma = nullptr;
   float* pf_rscale = nullptr;
+  float* pf_hscale = nullptr;
   float* pf_partials = nullptr;
   int32_t* pf_ids = nullptr;     // [L][Tmax][K]
   float* pf_wts = nullptr;       // [L][Tmax][K]
@@ -98,6 +99,9 @@ struct moe_handle {
   uint16_t* pf_e = nullptr;
   float* pf_s = nullptr;
   uint16_t* pf_xs[2] = {nullptr, nullptr};  // stack double buffer
+  // phase timing of multi-token calls while tracing is on: 6 events per call
+  std::vector<cudaEvent_t> pf_ev;
+  int pf_ev_calls = 0;
   Inject inj;
   int timeout_ms = 10000;
   std::string err;
@@ -138,6 +142,7 @@ void free_all(moe_handle* h) {
   if (h->dev_weights || h->scratch) cudaDeviceSynchronize();
   for (auto e : h->layer_done) cudaEventDestroy(e);
   for (auto e : h->copy_done) cudaEventDestroy(e);
+  for (auto e : h->pf_ev) cudaEventDestroy(e);
   if (h->ev_ids) cudaEventDestroy(h->ev_ids);
   if (h->side) cudaStreamDestroy(h->side);
   cudaFree(h->dev_weights);
@@ -189,12 +194,15 @@ moe_status check_device_status(moe_handle* h, cudaStream_t s) {
   const uint32_t v = *h->pin_status;
   if (v == DEV_OK) return MOE_OK;
   cudaMemsetAsync(h->bar, 0, kBarWords * 4, s);
+  cudaMemsetAsync(h->lacc, 0, 2 * h->d.E * 8, s);  // an aborted launch may leave partial sums
   cudaStreamSynchronize(s);
   if (v == DEV_TIMEOUT) return fail(h, MOE_ERR_TIMEOUT, "a device-side wait timed out");
   return fail(h, MOE_ERR_DEVICE, "a kernel reported an out-of-range expert id");
 }
 
 int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
+
+constexpr int kPhaseTimedCalls = 256;  // multi-token calls timed per moe_prefill_phase_ms read
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -393,11 +401,10 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   CREATE_TRY(cudaMemcpy(h->dev_layers, h->layers.data(), sizeof(LayerDev) * L, cudaMemcpyHostToDevice));
   // scratch
   const int G = h->num_sms;
-  const int G_pad = (G + 7) / 8 * 8;
   const int64_t T = c.max_tokens;
   auto al = [](int64_t b) { return (b + 255) / 256 * 256; };
   const int64_t sz_xbuf = al(2 * T * d.D * 2), sz_h = al(T * (d.K * d.I + d.S) * 4),
-                sz_part = al((d.E + 1) * G_pad * 4), sz_ids = al(int64_t(L) * T * d.K * 4), sz_bar = 256,
+                sz_part = al(2 * d.E * 8), sz_ids = al(int64_t(L) * T * d.K * 4), sz_bar = 256,
                 sz_io = al(T * d.D * 2), sz_trace = al(int64_t(G) * kTraceMaxLayers * kTraceEvents * 8);
   h->scratch_bytes = sz_xbuf + sz_h + sz_part + 2 * sz_ids + sz_bar + 2 * sz_io + sz_trace;
   CREATE_TRY(cudaMalloc(&h->scratch, h->scratch_bytes));
@@ -407,7 +414,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   sp += sz_xbuf;
   h->h = reinterpret_cast<float*>(sp);
   sp += sz_h;
-  h->partials = reinterpret_cast<float*>(sp);
+  h->lacc = reinterpret_cast<unsigned long long*>(sp);
   sp += sz_part;
   h->ids = reinterpret_cast<int32_t*>(sp);
   sp += sz_ids;
@@ -451,11 +458,10 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   p.dn_off = d.I * 2 * qrow_bytes(d.D);
   p.xbuf = h->xbuf;
   p.h = h->h;
-  p.partials = h->partials;
+  p.lacc = h->lacc;
   p.ids = h->ids;
   p.wts = h->wts;
   p.bar = h->bar;
-  p.G_pad = G_pad;
   p.rms_eps = 1e-6f;
   const int nch_i = d.I / 32, nch_s = d.S / 32;
   const int g = gcd(nch_i, nch_s);
@@ -510,7 +516,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     }
     const int64_t nt = Tm * K / kUnitTokens + E + 1, stl = (Tm + kUnitTokens - 1) / kUnitTokens;
     const int64_t ngu = nt * h->mt_gu_r + stl * h->mt_gu_s, ndn = (nt + stl) * h->mt_dn;
-    int64_t sizes[] = {Tm * d.D * 2,      Tm * 4,          Tm * 4,        part * 4,
+    int64_t sizes[] = {Tm * d.D * 2,      Tm * 4,          Tm * 4,        Tm * 4,        part * 4,
                        L * Tm * K * 4,    L * Tm * K * 4,  Tm * K * 4,    E * 4,
                        (E + 1) * 4,       Tm * K * 4,      Tm * K * 4,    ngu * int64_t(sizeof(GemmUnit)),
                        ndn * int64_t(sizeof(GemmUnit)), 16, Tm * K * d.I * 2, Tm * d.S * 2,
@@ -529,6 +535,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     h->pf_x16 = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
     h->pf_sigma = reinterpret_cast<float*>(h->pf + offs[i++]);
     h->pf_rscale = reinterpret_cast<float*>(h->pf + offs[i++]);
+    h->pf_hscale = reinterpret_cast<float*>(h->pf + offs[i++]);
     h->pf_partials = reinterpret_cast<float*>(h->pf + offs[i++]);
     h->pf_ids = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
     h->pf_wts = reinterpret_cast<float*>(h->pf + offs[i++]);
@@ -547,6 +554,8 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     h->pf_xs[0] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
     h->pf_xs[1] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
     h->prefill_ok = true;
+    h->pf_ev.resize(6 * kPhaseTimedCalls);
+    for (auto& ev : h->pf_ev) CREATE_TRY(cudaEventCreate(&ev));
   }
   *out = h.release();
   return MOE_OK;
@@ -683,6 +692,22 @@ moe_status moe_trace_read(moe_handle* h, int64_t* out, int n_layers) {
   return MOE_OK;
 }
 
+moe_status moe_prefill_phase_ms(moe_handle* h, float* ms, int* calls) {
+  if (!h || !ms) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i) ms[i] = 0.f;
+  if (calls) *calls = h->pf_ev_calls;
+  if (h->pf_ev_calls == 0) return MOE_OK;
+  CUDA_TRY(h, cudaEventSynchronize(h->pf_ev[6 * h->pf_ev_calls - 1]));
+  for (int c = 0; c < h->pf_ev_calls; ++c)
+    for (int i = 0; i < 5; ++i) {
+      float t = 0.f;
+      CUDA_TRY(h, cudaEventElapsedTime(&t, h->pf_ev[6 * c + i], h->pf_ev[6 * c + i + 1]));
+      ms[i] += t;
+    }
+  h->pf_ev_calls = 0;
+  return MOE_OK;
+}
+
 moe_status moe_cache_reset(moe_handle* h) {
   if (!h) return MOE_ERR_INVALID_ARG;
   if (h->cfg.n_slots == 0) return fail(h, MOE_ERR_STATE, "moe_cache_reset needs streaming mode");
@@ -705,6 +730,9 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   if (forced)
     CUDA_TRY(h, cudaMemcpyAsync(h->pf_forced, forced, sizeof(int32_t) * T * K,
                                 cudaMemcpyHostToDevice, s));
+  cudaEvent_t* ev = nullptr;  // phase events of this call (tracing only)
+  if (h->trace_on && h->pf_ev_calls < kPhaseTimedCalls) ev = &h->pf_ev[6 * h->pf_ev_calls++];
+  if (ev) CUDA_TRY(h, cudaEventRecord(ev[0], s));
   const LayerDev& ld = h->layers[layer];
   RouteArgs ra{};
   ra.x = static_cast<const uint16_t*>(x);
@@ -721,12 +749,14 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   ra.x16 = h->pf_x16;
   ra.sigma = h->pf_sigma;
   ra.rscale = h->pf_rscale;
+  ra.hscale = h->pf_hscale;
   ra.partials = h->pf_partials;
   ra.nsplit = router_gemm_splits(T, ra.E, ra.D, h->num_sms);
   ra.ids = ids;
   ra.wts = wts;
   int e = prefill_route(ra, s);
   if (e) return fail(h, MOE_ERR_CUDA, "prefill router: %s", cudaGetErrorString(cudaError_t(e)));
+  if (ev) CUDA_TRY(h, cudaEventRecord(ev[1], s));
   BucketArgs ba{};
   ba.ids = ids;
   ba.T = T;
@@ -745,11 +775,13 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   ba.status = h->bar + 2;
   e = prefill_bucket(ba, s);
   if (e) return fail(h, MOE_ERR_CUDA, "prefill bucketing: %s", cudaGetErrorString(cudaError_t(e)));
+  if (ev) CUDA_TRY(h, cudaEventRecord(ev[2], s));
   const auto& mp = h->maps[layer];
   GemmParams gp{};
   gp.perm = h->pf_perm;
   gp.topk = K;
   gp.sigma = h->pf_sigma;
+  gp.hscale = h->pf_hscale;
   gp.wts = wts;
   gp.D = static_cast<int>(d.D);
   gp.status = h->bar + 2;
@@ -771,6 +803,7 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   gp.hld[1] = static_cast<int>(d.S);
   e = gemm_tc_launch(gp, h->num_sms, s);
   if (e) return fail(h, MOE_ERR_CUDA, "gate/up GEMM launch: %s", cudaGetErrorString(cudaError_t(e)));
+  if (ev) CUDA_TRY(h, cudaEventRecord(ev[3], s));
   // down: routed output weighted by the routing weight (bf16), shared (fp32)
   gp.tm_code[0] = mp.dn_code[0];
   gp.tm_code[1] = mp.dn_code[1];
@@ -789,6 +822,7 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   gp.sout = h->pf_s;
   e = gemm_tc_launch(gp, h->num_sms, s);
   if (e) return fail(h, MOE_ERR_CUDA, "down GEMM launch: %s", cudaGetErrorString(cudaError_t(e)));
+  if (ev) CUDA_TRY(h, cudaEventRecord(ev[4], s));
   CombineArgs ca{};
   ca.x = static_cast<const uint16_t*>(x);
   ca.e = h->pf_e;
@@ -801,6 +835,7 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   ca.residual = (flags & MOE_FWD_RESIDUAL) ? 1 : 0;
   e = prefill_combine(ca, s);
   if (e) return fail(h, MOE_ERR_CUDA, "combine: %s", cudaGetErrorString(cudaError_t(e)));
+  if (ev) CUDA_TRY(h, cudaEventRecord(ev[5], s));
   return MOE_OK;
 }
 

@@ -13,11 +13,11 @@
 //       column block                                          (needs ids(l))
 // and the data dependences are met with two grid barriers per layer:
 //   after BS+BR: h = gelu(W_gate u) * (W_up u) complete for all k+1 branches;
-//   after C: x_{l+1} and the next router's partial logits complete.  The
-//   barrier releases at once; the last CTA to arrive then reduces the partial
-//   logits (fixed order), takes the top k and the renormalised softmax, and
-//   publishes ids(l+1) under a flag.  Meanwhile every CTA converts x_{l+1} and
-//   computes its share of the shared expert (BS), which needs no ids.
+//   after C: x_{l+1} and the next router's logits complete.  Each CTA adds
+//   its rows' partial logits into one accumulator per expert as 64-bit fixed
+//   point (integer addition, so the sum does not depend on arrival order);
+//   after the barrier every CTA reads the E sums, and takes the top k and the
+//   renormalised softmax itself (identical in every CTA).
 // The producer runs ahead across barriers wherever the weights are already
 // known, and prefetches into L2 the routed rows it will stream once the ids
 // arrive, so HBM keeps working while the grid synchronises.  Every wait is
@@ -73,6 +73,7 @@ enum : int {
   M_LAST = 65,
   M_GEN = 66,
   M_ISSUED = 67,
+  M_R = 68,    // pre-norm factor r of the current layer input (float bits)
   M_RED = 72,  // [8] per-warp reduction scratch
   M_SEG = 96,  // [K+1] per-branch max |h| (float bits)
   M_COUNT = 136
@@ -116,19 +117,20 @@ __device__ __forceinline__ float chunk_dot(const uint8_t* row, int halfK, int c,
   const uint32_t sb = *reinterpret_cast<const uint32_t*>(row + halfK + (c >> 1) * 4);
   const uint4* v = reinterpret_cast<const uint4*>(vec + c * kChunkStride);
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-  int acc = 0;
+  int acc[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 4; ++j) {  // four independent chains (integer sums are exact)
     const uint4 xq = v[j];  // int16 pairs of columns 8j+{0,1}, {2,3}, {4,5}, {6,7}
     const uint32_t lo = words[j] & 0x0F0F0F0Fu;          // codes of columns 8j+0..3
     const uint32_t hi = (words[j] >> 4) & 0x0F0F0F0Fu;   // codes of columns 8j+4..7
-    acc = dp2a_lo(xq.x, lo, acc);
-    acc = dp2a_hi(xq.y, lo, acc);
-    acc = dp2a_lo(xq.z, hi, acc);
-    acc = dp2a_hi(xq.w, hi, acc);
+    acc[j] = dp2a_lo(xq.x, lo, 0);
+    acc[j] = dp2a_hi(xq.y, lo, acc[j]);
+    acc[j] = dp2a_lo(xq.z, hi, acc[j]);
+    acc[j] = dp2a_hi(xq.w, hi, acc[j]);
   }
+  const int total = (acc[0] + acc[1]) + (acc[2] + acc[3]);
   const __half2 sbh = *reinterpret_cast<const __half2*>(&sb);
-  return fmaf(__low2float(sbh), static_cast<float>(acc), __high2float(sbh) * xsum[c]);
+  return fmaf(__low2float(sbh), static_cast<float>(total), __high2float(sbh) * xsum[c]);
 }
 
 // ------------------------------------------------------------ stage lists
@@ -423,8 +425,9 @@ __device__ VecView vec_view(const Ctx& cx, int nchunks) {
 // loads per thread (D <= 8 * kConsumers * kMaxXV); the CTA's own output rows
 // [c_lo, c_hi) are also kept as fp32 in xres for the residual.
 constexpr int kMaxXV = 4;
+constexpr int kMaxLogitLoads = 4;  // E <= 4 * kConsumers
 
-__device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
+__device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long long* lacc) {
   const DecodeParams& p = *cx.p;
   const int nc = p.D / 32;
   VecView v = vec_view(cx, nc);
@@ -436,6 +439,20 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
   for (int i = 0; i < kMaxXV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
     if (idx < nv) r[i] = __ldcg(reinterpret_cast<const uint4*>(xg) + idx);
+  }
+  if (lacc) {  // the layer's raw router logits, in the same round trip
+    float* logits = reinterpret_cast<float*>(cx.smem + p.off_logits);
+    long long lv[kMaxLogitLoads];
+#pragma unroll
+    for (int i = 0; i < kMaxLogitLoads; ++i) {
+      const int e = static_cast<int>(threadIdx.x) + i * kConsumers;
+      if (e < p.E) lv[i] = static_cast<long long>(__ldcg(lacc + e));
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxLogitLoads; ++i) {
+      const int e = static_cast<int>(threadIdx.x) + i * kConsumers;
+      if (e < p.E) logits[e] = static_cast<float>(static_cast<double>(lv[i]) * 0x1p-32);
+    }
   }
 #pragma unroll
   for (int i = 0; i < kMaxXV; ++i) {
@@ -476,10 +493,14 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg) {
     // sum q X ~ q * (W x); the layer wants r * (W x) with
     // r = 1 / sqrt(mean(x^2) + eps), so the factor is r / q = 1 / sqrt(mean((q x)^2) + eps q^2)
     ss = consumer_sum(cx, ss);
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
       v.vscale[0] = q > 0.f ? rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps * q * q) : 0.f;
+      const double qd = q, msq = q > 0.f ? static_cast<double>(ss) / p.D / (qd * qd) : 0.0;
+      reinterpret_cast<volatile float*>(cx.misc)[M_R] = static_cast<float>(1.0 / sqrt(msq + p.rms_eps));
+    }
   } else if (threadIdx.x == 0) {
     v.vscale[0] = m_all / 32767.f;
+    reinterpret_cast<volatile float*>(cx.misc)[M_R] = 1.f;
   }
   csync();
   chunk_sums(v.vec, v.xsum, nc);
@@ -633,72 +654,31 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
   if (c_has_router(p, li)) {
     const uint8_t* blk = buf + static_cast<int64_t>(n) * (p.K * p.rbI + p.rbS);
     router_partial(cx, blk, r0, n, xnext, rpart);
-    if (threadIdx.x == 0) {
-      float ss = 0.f;
-      for (int i = 0; i < n; ++i) ss = fmaf(xnext[i], xnext[i], ss);
-      rpart[p.E] += ss;
-    }
   }
 }
 
-constexpr int kRedBatch = 5;
-
-// Reduce the partial logits of all CTAs (fixed order), apply the pre-norm
-// scale and the logit bias, choose ids and softmax weights; write them to
-// p.ids / p.wts for layer li.  Runs on one CTA.
-__device__ void router_finish(const Ctx& cx, int li) {
+// Every CTA routes layer li itself from the raw logits that prep_x loaded
+// into shared memory (identical in every CTA): apply the pre-norm factor r
+// and the logit bias, take the top k (or the forced ids) and the softmax.  The
+// ids and weights land in shared memory (M_IDS, M_WTS); CTA 0 also writes
+// them to p.ids / p.wts for layer li.  Then the producer's gate for the
+// layer's routed stages opens.
+__device__ void route_all(const Ctx& cx, int li) {
   const DecodeParams& p = *cx.p;
   float* logits = reinterpret_cast<float*>(cx.smem + p.off_logits);
   const LayerDev& L = p.layers[p.layer0 + li];
-  // two threads per expert, each over half of the partials (16-byte loads,
-  // all issued before use); then combine.  Columns >= G are never written.
-  const int Gv = (cx.G + 3) / 4;
-  for (int e2 = threadIdx.x; e2 < 2 * p.E; e2 += kConsumers) {
-    const int e = e2 >> 1, half = e2 & 1;
-    const int c0 = half ? Gv / 2 : 0, c1 = half ? Gv : Gv / 2;
-    const float4* src = reinterpret_cast<const float4*>(p.partials + static_cast<int64_t>(e) * p.G_pad);
-    float s = 0.f;
-    for (int cb = c0; cb < c1; cb += kRedBatch) {
-      float4 v[kRedBatch];
-#pragma unroll
-      for (int i = 0; i < kRedBatch; ++i)
-        if (cb + i < c1) v[i] = __ldcg(src + cb + i);
-#pragma unroll
-      for (int i = 0; i < kRedBatch; ++i)
-        if (cb + i < c1) {
-          const int c = 4 * (cb + i);
-          s += v[i].x;
-          if (c + 1 < cx.G) s += v[i].y;
-          if (c + 2 < cx.G) s += v[i].z;
-          if (c + 3 < cx.G) s += v[i].w;
-        }
-    }
-    const float o = __shfl_xor_sync(0xffffffffu, s, 1);
-    if (!half) logits[e] = s + o;
-  }
-  if (p.prenorm && threadIdx.x < 32) {
-    // r = 1 / sqrt(mean(x^2) + eps) from the partial sums of squares (row E)
-    const float* src = p.partials + static_cast<int64_t>(p.E) * p.G_pad;
-    float ss = 0.f;
-    for (int c = threadIdx.x; c < cx.G; c += 32) ss += __ldcg(src + c);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (threadIdx.x == 0)
-      reinterpret_cast<volatile float*>(cx.misc)[M_RED] =
-          rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps);
-  }
-  csync();
+  const int t = threadIdx.x;
   {
-    const float r = p.prenorm ? reinterpret_cast<volatile float*>(cx.misc)[M_RED] : 1.f;
-    for (int e = threadIdx.x; e < p.E; e += kConsumers) {
+    const float r = reinterpret_cast<volatile float*>(cx.misc)[M_R];
+    for (int e = t; e < p.E; e += kConsumers) {
       float l = logits[e] * r;
       if (L.logit_bias) l += L.logit_bias[e];
       logits[e] = l;
     }
   }
   csync();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
+  if (t < 32) {
+    const int lane = t;
     int ids[kMaxTopK];
     if (li == 0 && p.forced) {
       for (int i = 0; i < p.K; ++i) ids[i] = p.forced_ids[i];
@@ -738,84 +718,53 @@ __device__ void router_finish(const Ctx& cx, int li) {
         z += ex[i];
       }
       for (int i = 0; i < p.K; ++i) {
-        p.ids[li * p.K + i] = ids[i];
-        p.wts[li * p.K + i] = ex[i] / z;
+        int id = ids[i];
+        if (id < 0 || id >= p.E) {
+          atomicCAS(p.bar + 2, DEV_OK, DEV_BAD_ID);
+          id = 0;
+        }
+        const float w = ex[i] / z;
+        cx.misc[M_IDS + i] = id;
+        cx.misc[M_WTS + i] = __float_as_int(w);
+        if (blockIdx.x == 0) {
+          p.ids[li * p.K + i] = ids[i];
+          p.wts[li * p.K + i] = w;
+        }
       }
     }
   }
+  csync();
+  if (t == 0) mbar_arrive(cx.ids_ready);
 }
 
-// Grid barrier among the consumer groups of all CTAs.  The last CTA to arrive
-// releases the others at once and records that it was last (misc[M_LAST]);
-// misc[M_GEN] holds the barrier's generation.  Returns false on timeout or
-// abort.
+// Grid barrier among the consumer groups of all CTAs on a monotonically
+// increasing 64-bit arrival counter (bar[0..1]): an arrival returning `old`
+// completes at the next multiple of the grid size, so the last arrival
+// releases everyone by itself.  Returns false on timeout or abort.
 __device__ bool grid_barrier(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
   csync();
   if (threadIdx.x == 0) {
+    unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.bar);
     __threadfence();
-    const uint32_t g = ld_acquire_gpu(p.bar + 1);
-    const uint32_t old = atom_add_acq_rel_gpu(p.bar, 1u);
-    cx.misc[M_GEN] = static_cast<int>(g);
-    if (old == static_cast<uint32_t>(cx.G) - 1) {
-      cx.misc[M_LAST] = 1;
-      p.bar[0] = 0u;
-      st_release_gpu(p.bar + 1, g + 1u);
-    } else {
-      cx.misc[M_LAST] = 0;
+    const unsigned long long old = atom_add_acq_rel_gpu_u64(ctr, 1ull);
+    const unsigned long long G = static_cast<unsigned long long>(cx.G);
+    const unsigned long long target = (old / G + 1ull) * G;
+    if (ld_acquire_gpu_u64(ctr) < target) {
       bool ok = false;
       const uint64_t t0 = globaltimer_ns();
       for (;;) {
-        if (ld_acquire_gpu(p.bar + 1) != g) {
+        if (ld_acquire_gpu_u64(ctr) >= target) {
           ok = true;
           break;
         }
         if (ld_acquire_gpu(p.bar + 2) != DEV_OK) break;
         if (globaltimer_ns() - t0 > p.timeout_ns) break;
-        __nanosleep(32);
       }
       if (!ok) {
         atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
         cx.misc[M_ABORT] = 1;
       }
-    }
-  }
-  csync();
-  return !cx.misc[M_ABORT];
-}
-
-// On the CTA that arrived last at the barrier just passed: compute layer li's
-// routing and publish it (flag = the barrier's generation + 1).
-__device__ void publish_router(const Ctx& cx, int li) {
-  router_finish(cx, li);
-  csync();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    st_release_gpu(cx.p->bar + 3, static_cast<uint32_t>(cx.misc[M_GEN]) + 1u);
-  }
-}
-
-// Wait until the routing computed after the last barrier is published.
-__device__ bool wait_router(const Ctx& cx) {
-  const DecodeParams& p = *cx.p;
-  if (threadIdx.x == 0) {
-    const uint32_t target = static_cast<uint32_t>(cx.misc[M_GEN]) + 1u;
-    bool ok = ld_acquire_gpu(p.bar + 3) == target;
-    if (!ok) {
-      const uint64_t t0 = globaltimer_ns();
-      for (;;) {
-        if (ld_acquire_gpu(p.bar + 3) == target) {
-          ok = true;
-          break;
-        }
-        if (ld_acquire_gpu(p.bar + 2) != DEV_OK) break;
-        if (globaltimer_ns() - t0 > p.timeout_ns) break;
-        __nanosleep(32);
-      }
-    }
-    if (!ok) {
-      atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
-      cx.misc[M_ABORT] = 1;
     }
   }
   csync();
@@ -857,10 +806,14 @@ __device__ void release_slot(const Ctx& cx, int st_idx) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(&cx.empty[slot]);
 }
 
-__device__ void write_partials(const Ctx& cx, const float* rpart) {
+// Add this CTA's partial logits into the layer's accumulators: fp32 -> 64-bit
+// fixed point in units of 2^-32 (|partial| < 2^31), integer atomic add.
+__device__ void add_partials(const Ctx& cx, const float* rpart, unsigned long long* lacc) {
   const DecodeParams& p = *cx.p;
-  for (int e = threadIdx.x; e <= p.E; e += kConsumers)
-    p.partials[static_cast<int64_t>(e) * p.G_pad + blockIdx.x] = rpart[e];
+  for (int e = threadIdx.x; e < p.E; e += kConsumers) {
+    const long long v = __float2ll_rn(rpart[e] * 0x1p32f);
+    red_add_gpu_u64(lacc + e, static_cast<unsigned long long>(v));
+  }
 }
 
 __device__ __forceinline__ void trace(const Ctx& cx, int li, int ev) {
@@ -884,7 +837,7 @@ __device__ void consumer(const Ctx& cx) {
     trace(cx, li, 0);
     // ---- router of the launch's first layer (later layers: folded into C)
     if (li == 0 && (p.phases & PH_ROUTER)) {
-      for (int e = threadIdx.x; e <= p.E; e += kConsumers) rpart[e] = 0.f;
+      for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
       csync();
       if (lp.n_r) {
         if (!wait_full(cx, st_idx)) return;
@@ -894,24 +847,23 @@ __device__ void consumer(const Ctx& cx) {
         csync();
         router_partial(cx, cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes,
                        st.a, st.n, xnext, rpart);
-        if (threadIdx.x == 0) {
-          float ss = 0.f;
-          for (int i = 0; i < st.n; ++i) ss = fmaf(xnext[i], xnext[i], ss);
-          rpart[p.E] = ss;
-        }
         csync();
         release_slot(cx, st_idx);
         ++st_idx;
         ++s;
       }
-      write_partials(cx, rpart);
+      add_partials(cx, rpart, p.lacc);
       if (!grid_barrier(cx)) return;
-      if (cx.misc[M_LAST]) publish_router(cx, 0);
     }
-    // ---- layer input, then the shared expert's gate/up (needs no ids)
+    // ---- layer input (+ its router logits), routing, then the shared
+    // expert's gate/up (which needs no ids) while the routed rows arrive
     VecView xv{};
-    if (p.phases & (PH_BSHARED | PH_BROUTED | PH_C)) xv = prep_x(cx, x_l);
+    unsigned long long* lacc_l = p.lacc + (li & 1) * p.E;
+    xv = prep_x(cx, x_l, routed_here ? lacc_l : nullptr);
     trace(cx, li, 1);
+    if (routed_here) route_all(cx, li);
+    else if (needs_ids(p)) publish_ids_local(cx, li);  // ids from an earlier launch
+    trace(cx, li, 2);
     for (; s < lp.n_r + lp.n_bs; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
@@ -920,11 +872,6 @@ __device__ void consumer(const Ctx& cx) {
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
-    }
-    trace(cx, li, 2);
-    if (needs_ids(p)) {
-      if (routed_here && !wait_router(cx)) return;
-      publish_ids_local(cx, li);
     }
     trace(cx, li, 3);
     // ---- routed gate/up
@@ -942,10 +889,14 @@ __device__ void consumer(const Ctx& cx) {
     // ---- down + combine (+ next router's partial logits)
     if (!grid_barrier(cx)) return;
     trace(cx, li, 5);
+    // every CTA has read layer li's logit accumulators: clear them for the
+    // layer after next (their next additions come after the next barrier)
+    if (blockIdx.x == 0)
+      for (int e = threadIdx.x; e < p.E; e += kConsumers) lacc_l[e] = 0ull;
     const VecView hv = prep_h(cx);
     trace(cx, li, 6);
     const bool nr = c_has_router(p, li);
-    for (int e = threadIdx.x; e <= p.E; e += kConsumers) rpart[e] = 0.f;
+    for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
     csync();
     for (; s < lp.n_r + lp.n_bs + lp.n_br + lp.n_c; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
@@ -958,11 +909,10 @@ __device__ void consumer(const Ctx& cx) {
     }
     trace(cx, li, 7);
     if (nr) {
-      write_partials(cx, rpart);
+      add_partials(cx, rpart, p.lacc + ((li + 1) & 1) * p.E);
       if (!grid_barrier(cx)) return;
-      if (cx.misc[M_LAST]) publish_router(cx, li + 1);
+      trace(cx, li, 8);
     }
-    trace(cx, li, 8);
   }
 }
 
@@ -1035,7 +985,7 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
   };
   const int o_vec = take(vb);
   const int o_contrib = take(kConsumers * 4);
-  const int o_rpart = take((p->E + 1) * 4);
+  const int o_rpart = take(p->E * 4);
   const int o_xnext = take(256 * 4);
   const int o_xres = take(256 * 4);
   const int o_logits = take(p->E * 4);

@@ -21,8 +21,9 @@
 //   warps 6-13   dequantisation: P stage -> fp16 weights w = s q + b (one
 //                rounding) in the swizzled K-major layout -> A ring (3 stages)
 //   warps 14-17  epilogue: tensor memory -> registers; gate/up units write
-//                h = gelu(g) * u (fp16), down units write the routing-weighted
-//                expert output (bf16) or the shared output (fp32)
+//                h = gelu(g) * u (fp16, times a per-token power of two that
+//                keeps it in range), down units undo that factor and write the
+//                routing-weighted expert output (bf16) or the shared output (fp32)
 // Rings are mbarrier-pipelined; every wait is bounded in time and a wait that
 // runs out sets the status word and ends the CTA's work.
 #include <cuda.h>
@@ -282,7 +283,7 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, int nU) {
             const int brow = un.row0 + col;
             const int tok = un.kind == 0 ? p.perm[brow] / p.topk : brow;
             const float sg = p.sigma[tok];
-            const float h = gelu_tanh(g * sg) * (v * sg);
+            const float h = gelu_tanh(g * sg) * (v * sg) * p.hscale[tok];
             const __half hh = __float2half_rn(fminf(fmaxf(h, -65504.f), 65504.f));
             reinterpret_cast<__half*>(p.hout[un.kind])[static_cast<int64_t>(brow) * p.hld[un.kind] + j] = hh;
           }
@@ -294,13 +295,14 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, int nU) {
           const int col = c0 + i;
           if (col < un.n) {
             const int brow = un.row0 + col;
-            const float v = __uint_as_float(r[i]);
             if (un.kind == 0) {
-              const float wv = p.wts[p.perm[brow]];
+              const int a = p.perm[brow];
+              const float v = __uint_as_float(r[i]) / p.hscale[a / p.topk];
+              const float wv = p.wts[a];
               reinterpret_cast<__nv_bfloat16*>(p.eout)[static_cast<int64_t>(brow) * p.D + d] =
                   __float2bfloat16_rn(v * wv);
             } else {
-              p.sout[static_cast<int64_t>(brow) * p.D + d] = v;
+              p.sout[static_cast<int64_t>(brow) * p.D + d] = __uint_as_float(r[i]) / p.hscale[brow];
             }
           }
         }

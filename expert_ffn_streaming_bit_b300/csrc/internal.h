@@ -77,12 +77,11 @@ struct DecodeParams {
   uint16_t* y_out;         // bf16 [D], output of the last layer
   uint16_t* xbuf;          // bf16 [2][D] scratch
   float* h;                // [K*I + S] fp32 scratch
-  float* partials;         // [E + 1][G_pad] router partial logits (transposed);
-                           // row E holds partial sums of x^2 for the pre-norm
+  unsigned long long* lacc;  // [2][E] router logit accumulators, fixed point (units of
+                             // 2^-32, two's complement), one per layer parity
   int32_t* ids;            // [n_layers][K], relative to layer0
   float* wts;              // [n_layers][K]
   uint32_t* bar;           // kBarWords grid synchronisation words
-  int G_pad;               // partial stride (grid size rounded up to 8)
   // C-phase task mapping
   int cpt_c, nsub_i, nsub_s, tasks_row, rc_max;
   // shared memory carve-up (bytes)
@@ -134,6 +133,7 @@ struct RouteArgs {
   uint16_t* x16;              // fp16 [T][D] out: x * f_t
   float* sigma;               // [T] out: (r_t / f_t), the scale of dot products with x16
   float* rscale;              // [T] out: r_t (pre-norm factor, 1 without)
+  float* hscale;              // [T] out: power-of-two scale of the fp16 intermediate h
   float* partials;            // [nsplit][T][E]
   int nsplit;
   int32_t* ids;               // [T][K] out
@@ -179,6 +179,7 @@ struct GemmParams {
   const int32_t* perm;     // bucket position -> assignment
   int topk;
   const float* sigma;      // per-token scale of dot products with x16 (gate/up)
+  const float* hscale;     // per-token scale of the fp16 h (gate/up multiplies, down divides)
   void* hout[2];           // gate/up: fp16 h rows (routed: bucket order; shared: tokens)
   int hld[2];
   void* eout;              // down, routed: bf16 [T*K][D], weighted by the routing weight

@@ -75,11 +75,11 @@ extern "C" moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, vo
     return static_cast<moe_status>(moe::handle_error(
         h, MOE_ERR_STATE, "moe_forward_stack_noalloc: the handle's device must be current"));
   // Carve-up of the fixed array: barrier words, x double buffer, h, router
-  // partials, ids, weights (the same pieces as the handle's own scratch).
+  // logit accumulators, ids, weights (the same pieces as the handle's own scratch).
   const size_t bar = 256;
   const size_t xbuf = align256(size_t(2) * p.D * 2);
   const size_t hb = align256(size_t(p.K * p.I + p.S) * 4);
-  const size_t part = align256(size_t(p.E + 1) * p.G_pad * 4);
+  const size_t part = align256(size_t(2) * p.E * 8);
   const size_t ids = align256(size_t(n_layers) * p.K * 4);
   const size_t need = bar + xbuf + hb + part + 2 * ids;
   if (need > kNoAllocScratchBytes) {
@@ -97,14 +97,15 @@ extern "C" moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, vo
   p.bar = reinterpret_cast<uint32_t*>(base);
   p.xbuf = reinterpret_cast<uint16_t*>(base + bar);
   p.h = reinterpret_cast<float*>(base + bar + xbuf);
-  p.partials = reinterpret_cast<float*>(base + bar + xbuf + hb);
+  p.lacc = reinterpret_cast<unsigned long long*>(base + bar + xbuf + hb);
   p.ids = reinterpret_cast<int32_t*>(base + bar + xbuf + hb + part);
   p.wts = reinterpret_cast<float*>(base + bar + xbuf + hb + part + ids);
   p.trace = nullptr;  // the trace buffer belongs to the handle's own scratch
-  // The array keeps the previous call's contents; the grid-barrier counters
-  // and the status word must start at zero.  Everything else is written before
-  // it is read.
+  // The array keeps the previous call's contents; the grid-barrier counters,
+  // the status word and the router logit accumulators must start at zero.
+  // Everything else is written before it is read.
   cudaError_t e = cudaMemsetAsync(base, 0, bar, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.lacc, 0, part, s);
   if (e == cudaSuccess) {
     const int le = moe::decode_launch(p, grid, s, true);
     e = static_cast<cudaError_t>(le);

@@ -44,11 +44,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 // (1 for a zero row), x16 = fp16(f x) (exact for bf16 inputs in range), and
 // the scales that turn dot products with x16 into dot products with the
 // layer input u = r x (r = 1 / sqrt(mean(x^2) + eps) with the pre-norm, else 1).
+// hscale = 2^(-2e), e = ceil(log2(max|u|)): the gated intermediate h grows
+// like |u|^2, so it is held as fp16(h * hscale), inside fp16's normal range
+// for tiny and huge inputs alike, and the down output is divided by hscale
+// again (exact powers of two).
 __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restrict__ x, int T, int D,
                                                        int prenorm, float eps,
                                                        __half* __restrict__ x16,
                                                        float* __restrict__ sigma,
-                                                       float* __restrict__ rscale) {
+                                                       float* __restrict__ rscale,
+                                                       float* __restrict__ hscale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -89,6 +94,13 @@ __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restric
     }
     sigma[t] = static_cast<float>(r / static_cast<double>(f));
     rscale[t] = static_cast<float>(r);
+    const double umax = static_cast<double>(m) * r;
+    int eu = 0;  // ceil(log2(umax)), clamped; 0 for a zero row
+    if (umax > 0.0) {
+      eu = static_cast<int>(ceil(log2(umax)));
+      eu = max(-60, min(60, eu));
+    }
+    hscale[t] = ldexpf(1.f, -2 * eu);
   }
 }
 
@@ -446,7 +458,8 @@ int router_gemm_splits(int T, int E, int D, int num_sms) {
 int prefill_route(const RouteArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   tok_prep_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a.x, a.T, a.D, a.prenorm, a.rms_eps,
-                                                reinterpret_cast<__half*>(a.x16), a.sigma, a.rscale);
+                                                reinterpret_cast<__half*>(a.x16), a.sigma, a.rscale,
+                                                a.hscale);
   const int ng = a.D / 64;
   const int gps = (ng + a.nsplit - 1) / a.nsplit;
   dim3 grid((a.T + kRtTok - 1) / kRtTok, (a.E + kRtExp - 1) / kRtExp, a.nsplit);

@@ -144,8 +144,9 @@ typedef struct {
  *   GEMMs on the tensor cores (fp16 operands: weights dequantised to fp16 in
  *   shared memory, activations scaled by a per-token power of two; fp32
  *   accumulation), and a gather combine.  The prefill path holds the gated
- *   intermediate h in fp16 (values beyond +-65504 saturate) and the routed
- *   expert outputs in bf16 before the combine.
+ *   intermediate h in fp16 scaled per token by a power of two chosen from
+ *   the token's input range, and the routed expert outputs in bf16 before
+ *   the combine.
  * x: device [T][D] bf16 input.  y: device [T][D] bf16 output; y may not alias x.
  * forced_ids: host [T][k] or NULL.  When given, those experts are used (each
  *   row k distinct ids in [0, E)); their weights are still the softmax of the
@@ -313,6 +314,16 @@ moe_status moe_set_timeout_ms(moe_handle* h, int ms);
 #define MOE_TRACE_EVENTS 9
 moe_status moe_trace_enable(moe_handle* h, int on);
 moe_status moe_trace_read(moe_handle* h, int64_t* out, int n_layers);
+
+/*
+ * While tracing is on, multi-token (prefill) layer calls also record CUDA
+ * events between their phases on the call's stream (up to 256 calls).
+ * moe_prefill_phase_ms(h, ms, calls) synchronises, writes the summed times
+ * of the recorded calls to ms[5] (router prep + GEMM + top-k, bucketing,
+ * gate/up GEMM, down GEMM, combine), the number of calls to *calls (may be
+ * NULL), and starts a new recording.
+ */
+moe_status moe_prefill_phase_ms(moe_handle* h, float* ms, int* calls);
 
 const char* moe_status_string(moe_status s);
 /* Last error text of this handle ("" if none); with h == NULL, of the last

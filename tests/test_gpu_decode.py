@@ -1,6 +1,9 @@
-"""GPU parity of the decode path (T tokens, one at a time) against the oracle.
+"""GPU parity of the decode path (one token per call) against the oracle.
 
 Every call goes through the C ABI (libmoe_b300.so) via the thin binding.
+Handles are created with max_tokens = 1 and tokens are sent one per call, so
+every call runs the persistent decode kernel (calls with T >= 2 take the
+prefill path, tested in test_gpu_prefill.py).
 """
 import numpy as np
 import pytest
@@ -25,16 +28,23 @@ def tiny_layer():
 
 
 def _run_layer(moe, h, x_cpu, layer=0, flags=0, forced=None):
+    """Token by token through the decode kernel; stacks ids and weights."""
     x = x_cpu.cuda()
     y = torch.empty_like(x)
-    st = moe.moe_layer_forward(h, layer, x, y, flags=flags, forced_ids=forced, want_ids=True)
+    ids, wts = [], []
+    for t in range(x.shape[0]):
+        f = None if forced is None else np.asarray(forced)[t:t + 1]
+        st = moe.moe_layer_forward(h, layer, x[t:t + 1], y[t:t + 1], flags=flags, forced_ids=f,
+                                   want_ids=True)
+        ids.append(st["ids"])
+        wts.append(st["weights"])
     torch.cuda.synchronize()
-    return y.cpu(), st
+    return y.cpu(), dict(ids=np.concatenate(ids), weights=np.concatenate(wts))
 
 
 def test_tiny_router_ids_weights_and_output(moe, tiny_layer):
     sh = synth.TINY
-    h = moe.moe_create(sh, [tiny_layer], max_tokens=64)
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=1)
     x = synth.make_tokens(sh, "tiny", 64)
     y, st = _run_layer(moe, h, x)
     ref = oracle.moe_layer(oracle.LayerView(sh, tiny_layer), x)
@@ -45,7 +55,7 @@ def test_tiny_router_ids_weights_and_output(moe, tiny_layer):
 
 def test_tiny_residual_output(moe, tiny_layer):
     sh = synth.TINY
-    h = moe.moe_create(sh, [tiny_layer], max_tokens=8)
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=1)
     x = synth.make_tokens(sh, "tiny", 8, index=1)
     y, st = _run_layer(moe, h, x, flags=moe.MOE_FWD_RESIDUAL)
     ref = oracle.moe_layer(oracle.LayerView(sh, tiny_layer), x)
@@ -54,7 +64,7 @@ def test_tiny_residual_output(moe, tiny_layer):
 
 def test_tiny_forced_ids(moe, tiny_layer):
     sh = synth.TINY
-    h = moe.moe_create(sh, [tiny_layer], max_tokens=4)
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=1)
     x = synth.make_tokens(sh, "tiny", 4, index=2)
     forced = np.array([[0, 15], [7, 3], [8, 9], [14, 1]], np.int32)
     y, st = _run_layer(moe, h, x, forced=forced)
@@ -66,7 +76,7 @@ def test_tiny_forced_ids(moe, tiny_layer):
 
 def test_tiny_repeated_runs_are_bit_identical(moe, tiny_layer):
     sh = synth.TINY
-    h = moe.moe_create(sh, [tiny_layer], max_tokens=16)
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=1)
     x = synth.make_tokens(sh, "tiny", 16, index=3)
     y1, s1 = _run_layer(moe, h, x)
     y2, s2 = _run_layer(moe, h, x)
@@ -78,7 +88,7 @@ def test_tiny_edge_inputs(moe, tiny_layer):
     and the output is exactly 0.  Inputs beyond the fp16 range (|x| ~ 1e5)
     exercise the power-of-two prescale of the activations."""
     sh = synth.TINY
-    h = moe.moe_create(sh, [tiny_layer], max_tokens=2)
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=1)
     x = torch.zeros(2, sh.d_model, dtype=torch.bfloat16)
     x[1] = synth.make_tokens(sh, "tiny", 1, index=4)[0] * 30000.0
     y, st = _run_layer(moe, h, x)
@@ -93,7 +103,7 @@ def test_tiny_prenorm_matches_oracle_at_any_input_scale(moe, tiny_layer):
     """MOE_FWD_PRENORM: the layer reads x / sqrt(mean(x^2) + 1e-6); inputs far
     outside the fp16 range give the same ids and output as unit-scale ones."""
     sh = synth.TINY
-    h = moe.moe_create(sh, [tiny_layer], max_tokens=8)
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=1)
     x = synth.make_tokens(sh, "tiny", 8, index=5)
     x[4:] = (x[4:].float() * 65536.0).to(torch.bfloat16)
     y, st = _run_layer(moe, h, x, flags=moe.MOE_FWD_PRENORM)
@@ -141,7 +151,7 @@ def gemma_layers():
 
 def test_gemma_single_layer_tokens(moe, gemma_layers):
     sh = synth.GEMMA
-    h = moe.moe_create(sh, gemma_layers[:1], max_tokens=8)
+    h = moe.moe_create(sh, gemma_layers[:1], max_tokens=1)
     x = synth.make_tokens(sh, "decode", 8, index=0)
     y, st = _run_layer(moe, h, x)
     ref = oracle.moe_layer(oracle.LayerView(sh, gemma_layers[0]), x)

@@ -90,6 +90,23 @@ def test_tiny_prefill_forced_ids_and_edge_inputs(moe):
     check_output(y, ref["y"])
 
 
+def test_tiny_prefill_large_unnormalised_inputs(moe):
+    """Without the pre-norm the gated intermediate grows like |x|^2; inputs
+    around 3e4 must still match (per-token power-of-two range scaling)."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 0)
+    h = moe.moe_create(sh, [L], max_tokens=4)
+    x = synth.make_tokens(sh, "tiny", 4, index=4)
+    x[1] = (x[1].float() * 30000.0).to(torch.bfloat16)
+    x[3] = (x[3].float() * 1e-4).to(torch.bfloat16)
+    y, st = _forward(moe, h, x)
+    ref = oracle.moe_layer(oracle.LayerView(sh, L), x)
+    # the 1e-4-scaled token has logit gaps below the near-tie margin
+    assert check_ids(st["ids"], ref, sh.top_k) <= 1
+    for t in range(4):  # each token against its own scale
+        check_output(y[t:t + 1], ref["y"][t:t + 1])
+
+
 def test_tiny_prefill_repeated_runs_are_bit_identical(moe):
     sh = synth.TINY
     L = synth.make_layer(sh, "tiny", 3)
