@@ -463,22 +463,37 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   p.wts = h->wts;
   p.bar = h->bar;
   p.rms_eps = 1e-6f;
+  // C-stage task split: each output row gets tasks_row tasks (k routed
+  // branches x nsub_i chunk strides + nsub_s for the shared branch); rows per
+  // stage are limited by the slot size (a C stage must fit the B stage's
+  // slot) and by tasks_row * rows <= kConsumers.  Pick the chunk stride that
+  // keeps the most consumers busy.
   const int nch_i = d.I / 32, nch_s = d.S / 32;
-  const int g = gcd(nch_i, nch_s);
-  int cpt = 1;
-  for (int q = 1; q <= 12; ++q)
-    if (g % q == 0) cpt = q;
-  p.cpt_c = cpt;
-  p.nsub_i = nch_i / cpt;
-  p.nsub_s = nch_s / cpt;
-  p.tasks_row = d.K * p.nsub_i + p.nsub_s;
-  if (p.tasks_row > kConsumers)
+  const int rc_cap = std::max<int>(
+      1, (kPairsPerStage * 2 * qrow_bytes(d.D) - 2 * d.E * 4) /
+             (d.K * qrow_bytes(d.I) + qrow_bytes(d.S) + d.E));
+  int best_busy = -1;
+  for (int cpt = 1; cpt <= nch_s; ++cpt) {
+    const int ni = (nch_i + cpt - 1) / cpt, ns = (nch_s + cpt - 1) / cpt;
+    const int tr = d.K * ni + ns;
+    if (tr > kConsumers) continue;
+    const int rc = std::min(rc_cap, kConsumers / tr);
+    const int busy = rc * tr;
+    if (busy > best_busy) {
+      best_busy = busy;
+      p.cpt_c = cpt;
+      p.nsub_i = ni;
+      p.nsub_s = ns;
+      p.tasks_row = tr;
+      p.rc_max = rc;
+    }
+  }
+  if (best_busy < 0)
     CREATE_FAIL(MOE_ERR_INVALID_ARG, "top_k * d_expert too large for the decode kernel");
-  if (d.D > 8 * kConsumers * 4 || d.K * d.I + d.S > 4 * kConsumers * 8)
+  if (d.D > 8 * kConsumers * 2 || d.K * d.I + d.S > 4 * kConsumers * 4 || d.E > 2 * kConsumers)
     CREATE_FAIL(MOE_ERR_INVALID_ARG, "d_model or top_k * d_expert + d_shared too large for the decode kernel");
   if ((d.D + std::min<int64_t>(G, d.D) - 1) / std::min<int64_t>(G, d.D) > 256)
     CREATE_FAIL(MOE_ERR_INVALID_ARG, "too few SMs for d_model in the decode kernel");
-  p.rc_max = kConsumers / p.tasks_row;
   p.timeout_ns = 2000000000ull;
   if (decode_smem_plan(&p, max_smem) != 0)
     CREATE_FAIL(MOE_ERR_INVALID_ARG, "decode kernel does not fit in shared memory");

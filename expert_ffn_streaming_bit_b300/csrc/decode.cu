@@ -74,6 +74,7 @@ enum : int {
   M_GEN = 66,
   M_ISSUED = 67,
   M_R = 68,    // pre-norm factor r of the current layer input (float bits)
+  M_TARGET = 70,  // [2] next grid-barrier target (64-bit; 0 before the first barrier)
   M_RED = 72,  // [8] per-warp reduction scratch
   M_SEG = 96,  // [K+1] per-branch max |h| (float bits)
   M_COUNT = 136
@@ -117,18 +118,19 @@ __device__ __forceinline__ float chunk_dot(const uint8_t* row, int halfK, int c,
   const uint32_t sb = *reinterpret_cast<const uint32_t*>(row + halfK + (c >> 1) * 4);
   const uint4* v = reinterpret_cast<const uint4*>(vec + c * kChunkStride);
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-  int acc[4];
+  int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};  // independent chains; integer sums are exact
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {  // four independent chains (integer sums are exact)
+  for (int j = 0; j < 4; ++j) {
     const uint4 xq = v[j];  // int16 pairs of columns 8j+{0,1}, {2,3}, {4,5}, {6,7}
-    const uint32_t lo = words[j] & 0x0F0F0F0Fu;          // codes of columns 8j+0..3
-    const uint32_t hi = (words[j] >> 4) & 0x0F0F0F0Fu;   // codes of columns 8j+4..7
-    acc[j] = dp2a_lo(xq.x, lo, 0);
-    acc[j] = dp2a_hi(xq.y, lo, acc[j]);
-    acc[j] = dp2a_lo(xq.z, hi, acc[j]);
-    acc[j] = dp2a_hi(xq.w, hi, acc[j]);
+    const uint32_t lo = words[j] & 0x0F0F0F0Fu;  // codes of columns 8j+0..3
+    const uint32_t hi = words[j] & 0xF0F0F0F0u;  // 16 x codes of columns 8j+4..7
+    lo_acc[j & 1] = dp2a_lo(xq.x, lo, lo_acc[j & 1]);
+    lo_acc[j & 1] = dp2a_hi(xq.y, lo, lo_acc[j & 1]);
+    hi_acc[j & 1] = dp2a_lo(xq.z, hi, hi_acc[j & 1]);
+    hi_acc[j & 1] = dp2a_hi(xq.w, hi, hi_acc[j & 1]);
   }
-  const int total = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  // the high-nibble sums are exact multiples of 16
+  const int total = (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
   const __half2 sbh = *reinterpret_cast<const __half2*>(&sb);
   return fmaf(__low2float(sbh), static_cast<float>(total), __high2float(sbh) * xsum[c]);
 }
@@ -424,8 +426,8 @@ __device__ VecView vec_view(const Ctx& cx, int nchunks) {
 // Layer input x (bf16 [D], global) -> int16 chunks.  One batch of 16-byte
 // loads per thread (D <= 8 * kConsumers * kMaxXV); the CTA's own output rows
 // [c_lo, c_hi) are also kept as fp32 in xres for the residual.
-constexpr int kMaxXV = 4;
-constexpr int kMaxLogitLoads = 4;  // E <= 4 * kConsumers
+constexpr int kMaxXV = 2;
+constexpr int kMaxLogitLoads = 2;  // E <= 2 * kConsumers
 
 __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long long* lacc) {
   const DecodeParams& p = *cx.p;
@@ -512,7 +514,7 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
 // branch.  One batch of 16-byte loads per thread (K*I + S <= 4 * kConsumers *
 // kMaxHV); the per-branch max is an order-independent smem atomicMax on the
 // bit patterns of non-negative floats.
-constexpr int kMaxHV = 8;
+constexpr int kMaxHV = 4;
 
 __device__ VecView prep_h(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
@@ -559,31 +561,30 @@ __device__ VecView prep_h(const Ctx& cx) {
   return v;
 }
 
-// B stage: n gate/up row pairs -> h_out[pair].  Each half-warp owns one pair
-// and each of its lanes both rows of a strided set of chunks, so an
-// activation chunk is read once for the two rows.
+// B stage: n gate/up row pairs -> h_out[pair].  Each warp owns one pair and
+// each lane both rows of a strided set of chunks, so an activation chunk is
+// read once for the two rows.
 __device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const VecView& xv,
                           float* h_out) {
   const DecodeParams& p = *cx.p;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int pair = warp * 2 + (lane >> 4);
-  const int sub = lane & 15;
+  const int pair = warp;
   const int nc = p.D / 32;
   float g = 0.f, u = 0.f;
   if (pair < n) {
     const uint8_t* rg = buf + (2 * pair) * p.rbD;
     const uint8_t* ru = rg + p.rbD;
-    for (int c = sub; c < nc; c += 16) {
+    for (int c = lane; c < nc; c += 32) {
       g += chunk_dot(rg, p.D / 2, c, xv.vec, xv.xsum);
       u += chunk_dot(ru, p.D / 2, c, xv.vec, xv.xsum);
     }
   }
 #pragma unroll
-  for (int o = 8; o; o >>= 1) {
+  for (int o = 16; o; o >>= 1) {
     g += __shfl_xor_sync(0xffffffffu, g, o);
     u += __shfl_xor_sync(0xffffffffu, u, o);
   }
-  if (pair < n && sub == 0) {
+  if (pair < n && lane == 0) {
     const float vs = xv.vscale[0];
     h_out[pair] = gelu_tanh(g * vs) * (u * vs);
   }
@@ -626,29 +627,36 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
       const uint8_t* rp = buf + static_cast<int64_t>(k) * n * p.rbI + r * p.rbI;
       const uint8_t* vb = hv.vec + k * nch_i * kChunkStride;
       const float* xs = hv.xsum + k * nch_i;
-      for (int i = 0; i < p.cpt_c; ++i) acc += chunk_dot(rp, p.I / 2, sub + p.nsub_i * i, vb, xs);
+      for (int c = sub; c < nch_i; c += p.nsub_i) acc += chunk_dot(rp, p.I / 2, c, vb, xs);
       acc *= __int_as_float(cx.misc[M_WTS + k]) * hv.vscale[k];
     } else {
       const int sub = tt - nrout;
       const uint8_t* rp = buf + static_cast<int64_t>(p.K) * n * p.rbI + r * p.rbS;
       const int cb = p.K * nch_i;
       const uint8_t* vb = hv.vec + cb * kChunkStride;
-      for (int i = 0; i < p.cpt_c; ++i)
-        acc += chunk_dot(rp, p.S / 2, sub + p.nsub_s * i, vb, hv.xsum + cb);
+      const int nch_s = p.S / 32;
+      for (int c = sub; c < nch_s; c += p.nsub_s) acc += chunk_dot(rp, p.S / 2, c, vb, hv.xsum + cb);
       acc *= hv.vscale[p.K];
     }
     contrib[r * p.tasks_row + tt] = acc;
   }
   csync();
-  if (t < n) {
-    float y = 0.f;
-    for (int j = 0; j < p.tasks_row; ++j) y += contrib[t * p.tasks_row + j];
-    const int d = r0 + t;
-    float out = y;
-    if (p.residual) out += reinterpret_cast<const float*>(cx.smem + p.off_xres)[d - cx.part.c_lo];
-    const uint16_t ob = f32_to_bf16_bits(out);
-    x_next[d] = ob;
-    xnext[t] = bf16_bits_to_f32(ob);
+  {  // one warp per row: lanes take strided tasks, then a fixed-order tree sum
+    const int warp = t >> 5, lane = t & 31;
+    for (int rr = warp; rr < n; rr += kConsumerWarps) {
+      float y = 0.f;
+      for (int j = lane; j < p.tasks_row; j += 32) y += contrib[rr * p.tasks_row + j];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+      if (lane == 0) {
+        const int d = r0 + rr;
+        float out = y;
+        if (p.residual) out += reinterpret_cast<const float*>(cx.smem + p.off_xres)[d - cx.part.c_lo];
+        const uint16_t ob = f32_to_bf16_bits(out);
+        x_next[d] = ob;
+        xnext[rr] = bf16_bits_to_f32(ob);
+      }
+    }
   }
   csync();
   if (c_has_router(p, li)) {
@@ -677,59 +685,49 @@ __device__ void route_all(const Ctx& cx, int li) {
     }
   }
   csync();
-  if (t < 32) {
-    const int lane = t;
-    int ids[kMaxTopK];
-    if (li == 0 && p.forced) {
-      for (int i = 0; i < p.K; ++i) ids[i] = p.forced_ids[i];
-    } else {
-      // k rounds of warp arg-max on (logit desc, index asc)
-      for (int i = 0; i < p.K; ++i) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int e = lane; e < p.E; e += 32) {
-          bool taken = false;
-          for (int j = 0; j < i; ++j) taken |= (ids[j] == e);
-          const float v = logits[e];
-          if (!taken && (v > bv || (v == bv && e < bi))) {
-            bv = v;
-            bi = e;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        ids[i] = bi;
+  // Top k in parallel: the rank of expert e is the number of experts before it
+  // in (logit desc, index asc) order; the experts of rank < k are the choice,
+  // in that order (or the forced ids).  Slot i's id goes to misc[M_IDS + i].
+  if (li == 0 && p.forced) {
+    if (t < p.K) cx.misc[M_IDS + t] = p.forced_ids[t];
+  } else {
+    for (int e = t; e < p.E; e += kConsumers) {
+      const float v = logits[e];
+      int rank = 0;
+      for (int f = 0; f < p.E; ++f) {
+        const float u = logits[f];
+        rank += (u > v || (u == v && f < e)) ? 1 : 0;
       }
+      if (rank < p.K) cx.misc[M_IDS + rank] = e;
     }
-    if (lane == 0) {
-      float m = -INFINITY;
-      for (int i = 0; i < p.K; ++i) m = fmaxf(m, logits[ids[i]]);
-      float z = 0.f;
-      float ex[kMaxTopK];
-      for (int i = 0; i < p.K; ++i) {
-        ex[i] = expf(logits[ids[i]] - m);
-        z += ex[i];
+  }
+  csync();
+  if (t < 32) {  // softmax over the k chosen logits (lanes 0..k-1)
+    const int lane = t;
+    int my_id = 0;
+    float my_l = -INFINITY;
+    if (lane < p.K) {
+      my_id = cx.misc[M_IDS + lane];
+      if (my_id < 0 || my_id >= p.E) {
+        atomicCAS(p.bar + 2, DEV_OK, DEV_BAD_ID);
+        my_id = 0;
       }
-      for (int i = 0; i < p.K; ++i) {
-        int id = ids[i];
-        if (id < 0 || id >= p.E) {
-          atomicCAS(p.bar + 2, DEV_OK, DEV_BAD_ID);
-          id = 0;
-        }
-        const float w = ex[i] / z;
-        cx.misc[M_IDS + i] = id;
-        cx.misc[M_WTS + i] = __float_as_int(w);
-        if (blockIdx.x == 0) {
-          p.ids[li * p.K + i] = ids[i];
-          p.wts[li * p.K + i] = w;
-        }
+      my_l = logits[my_id];
+    }
+    float m = my_l;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float ex = lane < p.K ? expf(my_l - m) : 0.f;
+    float z = ex;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane < p.K) {
+      const float w = ex / z;
+      cx.misc[M_IDS + lane] = my_id;
+      cx.misc[M_WTS + lane] = __float_as_int(w);
+      if (blockIdx.x == 0) {
+        p.ids[li * p.K + lane] = my_id;
+        p.wts[li * p.K + lane] = w;
       }
     }
   }
@@ -738,20 +736,32 @@ __device__ void route_all(const Ctx& cx, int li) {
 }
 
 // Grid barrier among the consumer groups of all CTAs on a monotonically
-// increasing 64-bit arrival counter (bar[0..1]): an arrival returning `old`
-// completes at the next multiple of the grid size, so the last arrival
-// releases everyone by itself.  Returns false on timeout or abort.
+// increasing 64-bit arrival counter (bar[0..1]) that is a multiple of the grid
+// size G between launches.  A CTA's first arrival in a launch is an atomic
+// that returns the counter, from which it learns the launch's base multiple;
+// the n-th barrier then completes when the counter reaches base + n G.  Later
+// arrivals are fire-and-forget reductions, and each CTA polls the counter
+// itself, so no arrival waits for a round trip before the others can see it.
+// Returns false on timeout or abort.
 __device__ bool grid_barrier(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
   csync();
   if (threadIdx.x == 0) {
     unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.bar);
-    __threadfence();
-    const unsigned long long old = atom_add_acq_rel_gpu_u64(ctr, 1ull);
     const unsigned long long G = static_cast<unsigned long long>(cx.G);
-    const unsigned long long target = (old / G + 1ull) * G;
-    if (ld_acquire_gpu_u64(ctr) < target) {
-      bool ok = false;
+    volatile unsigned long long* tgt = reinterpret_cast<volatile unsigned long long*>(cx.misc + M_TARGET);
+    __threadfence();
+    unsigned long long target;
+    if (*tgt == 0ull) {
+      const unsigned long long old = atom_add_acq_rel_gpu_u64(ctr, 1ull);
+      target = (old / G + 1ull) * G;
+    } else {
+      red_add_release_gpu_u64(ctr, 1ull);
+      target = *tgt + G;
+    }
+    *tgt = target;
+    bool ok = ld_acquire_gpu_u64(ctr) >= target;
+    if (!ok) {
       const uint64_t t0 = globaltimer_ns();
       for (;;) {
         if (ld_acquire_gpu_u64(ctr) >= target) {
@@ -760,11 +770,12 @@ __device__ bool grid_barrier(const Ctx& cx) {
         }
         if (ld_acquire_gpu(p.bar + 2) != DEV_OK) break;
         if (globaltimer_ns() - t0 > p.timeout_ns) break;
+        __nanosleep(16);
       }
-      if (!ok) {
-        atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
-        cx.misc[M_ABORT] = 1;
-      }
+    }
+    if (!ok) {
+      atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
+      cx.misc[M_ABORT] = 1;
     }
   }
   csync();

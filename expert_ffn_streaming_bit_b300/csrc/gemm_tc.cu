@@ -57,8 +57,10 @@ struct Bars {
   int abort;
 };
 
-constexpr int kSmemBytes = kNP * kPBytes + kNA * kABytes + kNB * kBBytes + 1024 /*Bars*/ +
-                           1024 /*alignment slack*/;
+constexpr int kStageBytes = 32 * 128 * 4;           // epilogue staging: 32 tokens x 128 fp32
+constexpr int kMetaBytes = 2 * kUnitTokens * 4;     // per-column factors
+constexpr int kSmemBytes = kNP * kPBytes + kNA * kABytes + kNB * kBBytes + kStageBytes +
+                           kMetaBytes + 1024 /*Bars*/ + 1024 /*alignment slack*/;
 
 __device__ __forceinline__ float gelu_tanh(float x) {
   const float c = 0.7978845608028654f;  // sqrt(2/pi)
@@ -252,60 +254,114 @@ __device__ void role_mma(const GemmParams& p, uint8_t* A, uint8_t* B, Bars* bars
   }
 }
 
-__device__ void role_epilogue(const GemmParams& p, Bars* bars, int nU) {
+// Epilogue (warps 14-17, 128 threads).  Per unit: per-column (token) scale
+// factors are gathered into shared memory once; then per 32-column chunk the
+// accumulator is read from tensor memory, the values are finished (GELU for
+// gate/up; routing weight and range factor for down) and staged in shared
+// memory, and the 4 warps write the chunk's output rows with 16-byte stores.
+__device__ __forceinline__ void epi_sync() { named_sync(1, 128); }
+
+__device__ void role_epilogue(const GemmParams& p, Bars* bars, uint8_t* stage, float* meta, int nU) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = w & 3;  // tensor-memory lane quarter this warp may access
+  const int te = threadIdx.x - 14 * 32;  // 0..127
   const uint32_t tmem = bars->tmem_base;
   uint32_t uc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x, ++uc) {
     const GemmUnit un = p.units[u];
     const int acc = uc & 1;
+    // per-column factors (independent of the accumulator: overlap the wait)
+    for (int col = te; col < un.n; col += 128) {
+      const int brow = un.row0 + col;
+      if (p.mode == 0) {
+        const int tok = un.kind == 0 ? p.perm[brow] / p.topk : brow;
+        meta[col] = p.sigma[tok];
+        meta[kUnitTokens + col] = p.hscale[tok];
+      } else if (un.kind == 0) {
+        const int a = p.perm[brow];
+        meta[col] = p.wts[a] / p.hscale[a / p.topk];
+      } else {
+        meta[col] = 1.f / p.hscale[brow];
+      }
+    }
     if (!wait_bar(&bars->acc_full[acc], (uc >> 1) & 1, p, bars)) return;
     tc_fence_after();
-    const int row = 32 * q + lane;  // weight row within the tile
+    epi_sync();
     for (int c0 = 0; c0 < un.n; c0 += 32) {
       uint32_t r[32];
       tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + acc * 256 + c0, r);
       tmem_ld_wait();
+      const int nrow = min(32, un.n - c0);
       if (p.mode == 0) {
         // rows 2j / 2j+1 of the tile are gate / up of output column j:
         // the even lane takes columns c0..c0+15, the odd lane c0+16..c0+31
-        const int j = un.mt * 64 + 16 * q + (lane >> 1);
+        const int jl = 16 * q + (lane >> 1);  // column within the tile's 64
         const bool odd = lane & 1;
+        __half* st = reinterpret_cast<__half*>(stage);  // [32 tokens][64]
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float mine_lo = __uint_as_float(r[i]), mine_hi = __uint_as_float(r[16 + i]);
           const float recv = __shfl_xor_sync(0xffffffffu, odd ? mine_lo : mine_hi, 1);
           const float g = odd ? recv : mine_lo;
           const float v = odd ? mine_hi : recv;
-          const int col = c0 + (odd ? 16 : 0) + i;
+          const int cl = (odd ? 16 : 0) + i;
+          const int col = c0 + cl;
           if (col < un.n) {
-            const int brow = un.row0 + col;
-            const int tok = un.kind == 0 ? p.perm[brow] / p.topk : brow;
-            const float sg = p.sigma[tok];
-            const float h = gelu_tanh(g * sg) * (v * sg) * p.hscale[tok];
-            const __half hh = __float2half_rn(fminf(fmaxf(h, -65504.f), 65504.f));
-            reinterpret_cast<__half*>(p.hout[un.kind])[static_cast<int64_t>(brow) * p.hld[un.kind] + j] = hh;
+            const float sg = meta[col];
+            const float h = gelu_tanh(g * sg) * (v * sg) * meta[kUnitTokens + col];
+            st[cl * 64 + jl] = __float2half_rn(fminf(fmaxf(h, -65504.f), 65504.f));
           }
         }
-      } else {
-        const int d = un.mt * 128 + row;
+        epi_sync();
+        // 32 rows x 128 bytes: 4 threads per row, 32 bytes each
+        {
+          const int rr = te >> 2, part = te & 3;
+          if (rr < nrow) {
+            const uint4* src = reinterpret_cast<const uint4*>(st + rr * 64 + part * 16);
+            __half* dst = reinterpret_cast<__half*>(p.hout[un.kind]) +
+                          static_cast<int64_t>(un.row0 + c0 + rr) * p.hld[un.kind] + un.mt * 64 + part * 16;
+            reinterpret_cast<uint4*>(dst)[0] = src[0];
+            reinterpret_cast<uint4*>(dst)[1] = src[1];
+          }
+        }
+        epi_sync();
+      } else if (un.kind == 0) {
+        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage);  // [32 tokens][128]
+        const int dl = 32 * q + lane;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = c0 + i;
-          if (col < un.n) {
-            const int brow = un.row0 + col;
-            if (un.kind == 0) {
-              const int a = p.perm[brow];
-              const float v = __uint_as_float(r[i]) / p.hscale[a / p.topk];
-              const float wv = p.wts[a];
-              reinterpret_cast<__nv_bfloat16*>(p.eout)[static_cast<int64_t>(brow) * p.D + d] =
-                  __float2bfloat16_rn(v * wv);
-            } else {
-              p.sout[static_cast<int64_t>(brow) * p.D + d] = __uint_as_float(r[i]) / p.hscale[brow];
-            }
+        for (int i = 0; i < 32; ++i)
+          if (c0 + i < un.n) st[i * 128 + dl] = __float2bfloat16_rn(__uint_as_float(r[i]) * meta[c0 + i]);
+        epi_sync();
+        {  // 32 rows x 256 bytes: 4 threads per row, 64 bytes each
+          const int rr = te >> 2, part = te & 3;
+          if (rr < nrow) {
+            const uint4* src = reinterpret_cast<const uint4*>(st + rr * 128 + part * 32);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.eout) +
+                                                  static_cast<int64_t>(un.row0 + c0 + rr) * p.D +
+                                                  un.mt * 128 + part * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = src[k];
           }
         }
+        epi_sync();
+      } else {
+        float* st = reinterpret_cast<float*>(stage);  // [32 tokens][128]
+        const int dl = 32 * q + lane;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c0 + i < un.n) st[i * 128 + dl] = __uint_as_float(r[i]) * meta[c0 + i];
+        epi_sync();
+        {  // 32 rows x 512 bytes: 4 threads per row, 128 bytes each
+          const int rr = te >> 2, part = te & 3;
+          if (rr < nrow) {
+            const uint4* src = reinterpret_cast<const uint4*>(st + rr * 128 + part * 32);
+            uint4* dst = reinterpret_cast<uint4*>(p.sout + static_cast<int64_t>(un.row0 + c0 + rr) * p.D +
+                                                  un.mt * 128 + part * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) dst[k] = src[k];
+          }
+        }
+        epi_sync();
       }
     }
     tc_fence_before();
@@ -322,7 +378,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   uint8_t* P = smem;
   uint8_t* A = P + kNP * kPBytes;
   uint8_t* B = A + kNA * kABytes;
-  Bars* bars = reinterpret_cast<Bars*>(B + kNB * kBBytes);
+  uint8_t* stage = B + kNB * kBBytes;
+  float* meta = reinterpret_cast<float*>(stage + kStageBytes);
+  Bars* bars = reinterpret_cast<Bars*>(stage + kStageBytes + kMetaBytes);
   const int w = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNP; ++i) {
@@ -361,7 +419,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   } else if (w < 14) {
     role_dequant(p, P, A, bars, nU);
   } else {
-    role_epilogue(p, bars, nU);
+    role_epilogue(p, bars, stage, meta, nU);
   }
   tc_fence_before();
   __syncthreads();

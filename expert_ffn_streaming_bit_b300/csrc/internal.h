@@ -27,11 +27,11 @@ namespace moe {
 
 constexpr int kGroup = 64;
 constexpr int kMaxTopK = 32;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;   // threads that compute
 constexpr int kThreads = kConsumers + 32;         // + one producer warp
 constexpr int kChunkStride = 80;  // smem bytes per 32-element int16 chunk (64 data + 16 pad)
-constexpr int kPairsPerStage = 16;  // gate/up row pairs per B stage (8 warps x 2)
+constexpr int kPairsPerStage = 16;  // gate/up row pairs per B stage (one per consumer warp)
 constexpr int kMaxSlots = 6;
 
 inline int64_t qrow_bytes(int64_t K) { return (K * 9 / 16 + 15) / 16 * 16; }
@@ -50,12 +50,14 @@ enum : int { PH_ROUTER = 1, PH_BSHARED = 2, PH_BROUTED = 4, PH_C = 8, PH_ALL = 1
 
 // Device status word codes (bar[2]).
 enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_ID = 2 };
-// Grid synchronisation words (bar[]): [0] arrivals, [1] barrier generation,
-// [2] status, [3] generation whose routing (ids, weights) has been published.
-constexpr int kBarWords = 4;
+// Grid synchronisation words (bar[], 256 bytes): [0..1] 64-bit arrival
+// counter, [2] status, [32] release flag (its own 128-byte line).
+constexpr int kBarWords = 64;
+constexpr int kBarFlag = 32;
 // Decode trace events per layer (thread 0 of each CTA, %globaltimer ns):
-// layer start, x converted, shared gate/up done, ids known, routed gate/up
-// done, h complete (barrier), h converted, down done, next-layer barrier passed.
+// layer start, x (and router logits) converted, routing done, shared gate/up
+// done, routed gate/up done, h complete (barrier), h converted, down done,
+// next-layer barrier passed.
 constexpr int kTraceEvents = 9;
 constexpr int kTraceMaxLayers = 64;
 

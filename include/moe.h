@@ -304,9 +304,9 @@ moe_status moe_set_timeout_ms(moe_handle* h, int ms);
  * Decode tracing (for profiling the persistent decode kernel).
  * moe_trace_enable(h, 1): later decode launches of this handle record, per
  * CTA and layer, MOE_TRACE_EVENTS %globaltimer stamps (ns) taken by the CTA's
- * first consumer thread: layer start, input converted, shared gate/up done,
- * ids known, routed gate/up done, h complete, h converted, down done, next
- * barrier passed.  moe_trace_enable(h, 0) stops recording.
+ * first consumer thread: layer start, input (and router logits) loaded and
+ * converted, routing done, shared gate/up done, routed gate/up done, h
+ * complete (barrier), h converted, down done, next barrier passed.  moe_trace_enable(h, 0) stops recording.
  * moe_trace_read(h, out, n_layers): copies the last launch's stamps to host
  * out [num_sms][n_layers][MOE_TRACE_EVENTS] int64 (n_layers of that launch,
  * at most 64; synchronises).
