@@ -75,6 +75,8 @@ struct moe_handle {
     CUtensorMap gu_code[2], gu_sb[2], dn_code[2], dn_sb[2];  // [0] routed, [1] shared
   };
   std::vector<LayerMaps> maps;
+  CUtensorMap bmap_gu[2], bmap_dn[2];  // activation operands: [0] routed, [1] shared
+  uint16_t* pf_xperm = nullptr;        // x16 rows in bucket order (routed gate/up operand)
   bool prefill_ok = false;
   int mt_gu_r = 0, mt_dn = 0, mt_gu_s = 0;
   uint8_t* pf = nullptr;  // prefill scratch (one allocation)
@@ -236,6 +238,20 @@ EncodeTiledFn encode_tiled() {
 
 // A byte tensor of `rank` 2 or 3: rows of `row_bytes` (pitch `row_bytes`),
 // `rows` rows, and for rank 3 `planes` planes `plane_bytes` apart.
+// fp16 rows [rows][cols] (pitch cols): box 64 columns x 256 rows, 128-byte
+// swizzle (the UMMA K-major operand layout).
+bool make_act_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kUnitTokens)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_qrow_map(CUtensorMap* m, const void* base, int rank, uint64_t row_bytes, uint64_t rows,
                    uint64_t planes, uint64_t plane_bytes, uint32_t box_x, bool swizzle) {
   EncodeTiledFn enc = encode_tiled();
@@ -463,34 +479,16 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   p.wts = h->wts;
   p.bar = h->bar;
   p.rms_eps = 1e-6f;
-  // C-stage task split: each output row gets tasks_row tasks (k routed
-  // branches x nsub_i chunk strides + nsub_s for the shared branch); rows per
-  // stage are limited by the slot size (a C stage must fit the B stage's
-  // slot) and by tasks_row * rows <= kConsumers.  Pick the chunk stride that
-  // keeps the most consumers busy.
-  const int nch_i = d.I / 32, nch_s = d.S / 32;
-  const int rc_cap = std::max<int>(
+  // C phase: one (branch, 32-column chunk) task per consumer thread; rows per
+  // C stage limited by the slot size (a C stage fits the B stage's slot).
+  p.ntask = static_cast<int>(d.K * (d.I / 32) + d.S / 32);
+  p.rc_max = static_cast<int>(std::max<int64_t>(
       1, (kPairsPerStage * 2 * qrow_bytes(d.D) - 2 * d.E * 4) /
-             (d.K * qrow_bytes(d.I) + qrow_bytes(d.S) + d.E));
-  int best_busy = -1;
-  for (int cpt = 1; cpt <= nch_s; ++cpt) {
-    const int ni = (nch_i + cpt - 1) / cpt, ns = (nch_s + cpt - 1) / cpt;
-    const int tr = d.K * ni + ns;
-    if (tr > kConsumers) continue;
-    const int rc = std::min(rc_cap, kConsumers / tr);
-    const int busy = rc * tr;
-    if (busy > best_busy) {
-      best_busy = busy;
-      p.cpt_c = cpt;
-      p.nsub_i = ni;
-      p.nsub_s = ns;
-      p.tasks_row = tr;
-      p.rc_max = rc;
-    }
-  }
+             (d.K * qrow_bytes(d.I) + qrow_bytes(d.S) + d.E)));
+  const int best_busy = p.ntask <= kConsumers ? 1 : -1;
   if (best_busy < 0)
     CREATE_FAIL(MOE_ERR_INVALID_ARG, "top_k * d_expert too large for the decode kernel");
-  if (d.D > 8 * kConsumers * 2 || d.K * d.I + d.S > 4 * kConsumers * 4 || d.E > 2 * kConsumers)
+  if (d.D > 32 * 32 * 3 || d.K * d.I + d.S > 4 * kConsumers * 8 || d.E > 4 * kConsumers)
     CREATE_FAIL(MOE_ERR_INVALID_ARG, "d_model or top_k * d_expert + d_shared too large for the decode kernel");
   if ((d.D + std::min<int64_t>(G, d.D) - 1) / std::min<int64_t>(G, d.D) > 256)
     CREATE_FAIL(MOE_ERR_INVALID_ARG, "too few SMs for d_model in the decode kernel");
@@ -530,12 +528,14 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
       if (v > part) part = v;
     }
     const int64_t nt = Tm * K / kUnitTokens + E + 1, stl = (Tm + kUnitTokens - 1) / kUnitTokens;
-    const int64_t ngu = nt * h->mt_gu_r + stl * h->mt_gu_s, ndn = (nt + stl) * h->mt_dn;
+    const int64_t ngu = nt * ((h->mt_gu_r + 1) / 2) + stl * ((h->mt_gu_s + 1) / 2),
+                  ndn = (nt + stl) * ((h->mt_dn + 1) / 2);
     int64_t sizes[] = {Tm * d.D * 2,      Tm * 4,          Tm * 4,        Tm * 4,        part * 4,
                        L * Tm * K * 4,    L * Tm * K * 4,  Tm * K * 4,    E * 4,
                        (E + 1) * 4,       Tm * K * 4,      Tm * K * 4,    ngu * int64_t(sizeof(GemmUnit)),
                        ndn * int64_t(sizeof(GemmUnit)), 16, Tm * K * d.I * 2, Tm * d.S * 2,
-                       Tm * K * d.D * 2,  Tm * d.D * 4,    Tm * d.D * 2,  Tm * d.D * 2};
+                       Tm * K * d.D * 2,  Tm * d.D * 4,    Tm * d.D * 2,  Tm * d.D * 2,
+                       Tm * K * d.D * 2};
     const int ns = sizeof(sizes) / sizeof(sizes[0]);
     int64_t offs[32];
     int64_t tot = 0;
@@ -568,6 +568,12 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     h->pf_s = reinterpret_cast<float*>(h->pf + offs[i++]);
     h->pf_xs[0] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
     h->pf_xs[1] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    h->pf_xperm = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    if (!make_act_map(&h->bmap_gu[0], h->pf_xperm, d.D, Tm * K) ||
+        !make_act_map(&h->bmap_gu[1], h->pf_x16, d.D, Tm) ||
+        !make_act_map(&h->bmap_dn[0], h->pf_hr, d.I, Tm * K) ||
+        !make_act_map(&h->bmap_dn[1], h->pf_hs, d.S, Tm))
+      CREATE_FAIL(MOE_ERR_CUDA, "could not encode the prefill activation tensor maps");
     h->prefill_ok = true;
     h->pf_ev.resize(6 * kPhaseTimedCalls);
     for (auto& ev : h->pf_ev) CREATE_TRY(cudaEventCreate(&ev));
@@ -806,12 +812,14 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   gp.tm_code[1] = mp.gu_code[1];
   gp.tm_sb[0] = mp.gu_sb[0];
   gp.tm_sb[1] = mp.gu_sb[1];
+  e = gather_rows_launch(h->pf_x16, static_cast<int>(d.D), h->pf_perm, K, T * K, h->pf_xperm, s);
+  if (e) return fail(h, MOE_ERR_CUDA, "row gather: %s", cudaGetErrorString(cudaError_t(e)));
   gp.units = h->pf_units_gu;
   gp.n_units = h->pf_nunits;
   gp.mode = 0;
   gp.K[0] = gp.K[1] = static_cast<int>(d.D);
-  gp.bsrc[0] = gp.bsrc[1] = h->pf_x16;
-  gp.bld[0] = gp.bld[1] = static_cast<int>(d.D);
+  gp.tm_b[0] = h->bmap_gu[0];
+  gp.tm_b[1] = h->bmap_gu[1];
   gp.hout[0] = h->pf_hr;
   gp.hout[1] = h->pf_hs;
   gp.hld[0] = static_cast<int>(d.I);
@@ -829,10 +837,8 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   gp.mode = 1;
   gp.K[0] = static_cast<int>(d.I);
   gp.K[1] = static_cast<int>(d.S);
-  gp.bsrc[0] = h->pf_hr;
-  gp.bsrc[1] = h->pf_hs;
-  gp.bld[0] = static_cast<int>(d.I);
-  gp.bld[1] = static_cast<int>(d.S);
+  gp.tm_b[0] = h->bmap_dn[0];
+  gp.tm_b[1] = h->bmap_dn[1];
   gp.eout = h->pf_e;
   gp.sout = h->pf_s;
   e = gemm_tc_launch(gp, h->num_sms, s);

@@ -76,6 +76,7 @@ enum : int {
   M_R = 68,    // pre-norm factor r of the current layer input (float bits)
   M_TARGET = 70,  // [2] next grid-barrier target (64-bit; 0 before the first barrier)
   M_RED = 72,  // [8] per-warp reduction scratch
+  M_RED2 = 80, // [8] second per-warp reduction scratch
   M_SEG = 96,  // [K+1] per-branch max |h| (float bits)
   M_COUNT = 136
 };
@@ -108,6 +109,32 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 }
 
 __device__ __forceinline__ void csync() { named_sync(1, kConsumers); }
+
+// Integer dot product of the codes of 32-column chunk c of a qrow with an
+// int16 activation chunk held in registers (exact in int32).
+__device__ __forceinline__ int chunk_idot(const uint8_t* row, int c, const uint4 (&x)[4]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+  int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = words[j] & 0x0F0F0F0Fu;  // codes of columns 8j+0..3
+    const uint32_t hi = words[j] & 0xF0F0F0F0u;  // 16 x codes of columns 8j+4..7
+    lo_acc[j & 1] = dp2a_lo(x[j].x, lo, lo_acc[j & 1]);
+    lo_acc[j & 1] = dp2a_hi(x[j].y, lo, lo_acc[j & 1]);
+    hi_acc[j & 1] = dp2a_lo(x[j].z, hi, hi_acc[j & 1]);
+    hi_acc[j & 1] = dp2a_hi(x[j].w, hi, hi_acc[j & 1]);
+  }
+  return (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
+}
+
+// s * sum(q X) + bias * sum(X) for chunk c of a row with K/2 = halfK code bytes.
+__device__ __forceinline__ float chunk_contrib(const uint8_t* row, int halfK, int c,
+                                               const uint4 (&x)[4], float xs) {
+  const uint32_t sb = *reinterpret_cast<const uint32_t*>(row + halfK + (c >> 1) * 4);
+  const __half2 sbh = *reinterpret_cast<const __half2*>(&sb);
+  return fmaf(__low2float(sbh), static_cast<float>(chunk_idot(row, c, x)), __high2float(sbh) * xs);
+}
 
 // Contribution of 32-column chunk c of a qrow with K/2 = halfK code bytes
 // against an int16 activation vector in chunk layout (kChunkStride bytes per
@@ -148,16 +175,8 @@ __device__ LayerPlan layer_plan(const DecodeParams& p, const Part& pt, int li) {
   LayerPlan lp;
   lp.n_r = (li == 0 && (p.phases & PH_ROUTER) && pt.c_hi > pt.c_lo) ? 1 : 0;
   lp.n_bs = (p.phases & PH_BSHARED) ? ceil_div(pt.sh_hi - pt.sh_lo, kPairsPerStage) : 0;
-  lp.n_br = 0;
-  if (p.phases & PH_BROUTED) {
-    int q = pt.rt_lo;
-    while (q < pt.rt_hi) {
-      const int j = q % p.I;
-      const int n = min(kPairsPerStage, min(pt.rt_hi - q, p.I - j));
-      q += n;
-      ++lp.n_br;
-    }
-  }
+  // routed pairs (flattened k*I + j): near-equal stages, which may span two experts
+  lp.n_br = (p.phases & PH_BROUTED) ? ceil_div(pt.rt_hi - pt.rt_lo, kPairsPerStage) : 0;
   const int rows = pt.c_hi - pt.c_lo;
   lp.n_c = (p.phases & PH_C) ? ceil_div(rows, p.rc_max) : 0;
   lp.rc = lp.n_c ? ceil_div(rows, lp.n_c) : 0;
@@ -182,19 +201,12 @@ __device__ Stage stage_at(const DecodeParams& p, const Part& pt, const LayerPlan
   }
   s -= lp.n_bs;
   if (s < lp.n_br) {
-    int q = pt.rt_lo;
-    for (int t = 0;; ++t) {
-      const int j = q % p.I;
-      const int n = min(kPairsPerStage, min(pt.rt_hi - q, p.I - j));
-      if (t == s) {
-        st.kind = ST_BR;
-        st.k = q / p.I;
-        st.a = j;
-        st.n = n;
-        return st;
-      }
-      q += n;
-    }
+    const int len = pt.rt_hi - pt.rt_lo;
+    st.kind = ST_BR;
+    st.a = pt.rt_lo + static_cast<int>(static_cast<int64_t>(len) * s / lp.n_br);
+    st.n = pt.rt_lo + static_cast<int>(static_cast<int64_t>(len) * (s + 1) / lp.n_br) - st.a;
+    st.k = st.a / p.I;
+    return st;
   }
   s -= lp.n_br;
   st.kind = ST_C;
@@ -260,9 +272,18 @@ __device__ void issue_stage(const Ctx& cx, const Stage& st, int li, uint8_t* dst
       bulk_g2s(dst, L.shared_gu + static_cast<int64_t>(st.a) * 2 * p.rbD, st.n * 2 * p.rbD, bar);
       break;
     case ST_BR: {
-      const int id = cx.misc[M_IDS + st.k];
-      const uint8_t* blob = expert_blob(p, L, st.k, id);
-      bulk_g2s(dst, blob + static_cast<int64_t>(st.a) * 2 * p.rbD, st.n * 2 * p.rbD, bar);
+      // pairs [a, a+n) of the flattened k*I + j index; at most one expert boundary
+      int q = st.a, left = st.n;
+      uint8_t* d = dst;
+      while (left > 0) {
+        const int k = q / p.I, j = q % p.I;
+        const int n = min(left, p.I - j);
+        const uint8_t* blob = expert_blob(p, L, k, cx.misc[M_IDS + k]);
+        bulk_g2s(d, blob + static_cast<int64_t>(j) * 2 * p.rbD, n * 2 * p.rbD, bar);
+        d += n * 2 * p.rbD;
+        q += n;
+        left -= n;
+      }
       break;
     }
     default: {
@@ -384,6 +405,38 @@ __device__ float consumer_sum(const Ctx& cx, float v) {
   return s;
 }
 
+// Max of a and sum of b over all consumer threads in one pass (fixed order).
+__device__ void consumer_max_sum(const Ctx& cx, float& a, float& b) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  const int w = threadIdx.x >> 5;
+  volatile float* ra = reinterpret_cast<volatile float*>(cx.misc) + M_RED;
+  volatile float* rb = reinterpret_cast<volatile float*>(cx.misc) + M_RED2;
+  if ((threadIdx.x & 31) == 0) {
+    ra[w] = a;
+    rb[w] = b;
+  }
+  csync();
+  a = 0.f;
+  b = 0.f;
+  for (int i = 0; i < kConsumerWarps; ++i) {
+    a = fmaxf(a, ra[i]);
+    b += rb[i];
+  }
+  csync();
+}
+
+// Sum of the int16 pairs of a uint4 (8 values, exact).
+__device__ __forceinline__ int sum8_s16(const uint4& q) {
+  int s = dp2a_lo(q.x, 0x01010101u, 0);
+  s = dp2a_lo(q.y, 0x01010101u, s);
+  s = dp2a_lo(q.z, 0x01010101u, s);
+  return dp2a_lo(q.w, 0x01010101u, s);
+}
+
 // int16 quantisation factor for a vector with max |v| = m: X = rint(v * q).
 __device__ __forceinline__ float quant_factor(float m) { return m > 0.f ? 32767.f / m : 0.f; }
 
@@ -426,8 +479,8 @@ __device__ VecView vec_view(const Ctx& cx, int nchunks) {
 // Layer input x (bf16 [D], global) -> int16 chunks.  One batch of 16-byte
 // loads per thread (D <= 8 * kConsumers * kMaxXV); the CTA's own output rows
 // [c_lo, c_hi) are also kept as fp32 in xres for the residual.
-constexpr int kMaxXV = 2;
-constexpr int kMaxLogitLoads = 2;  // E <= 2 * kConsumers
+constexpr int kMaxXV = 2;  // D <= 8 * kConsumers * kMaxXV
+constexpr int kMaxLogitLoads = 4;  // E <= 4 * kConsumers
 
 __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long long* lacc) {
   const DecodeParams& p = *cx.p;
@@ -436,7 +489,6 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
   float* xres = reinterpret_cast<float*>(cx.smem + p.off_xres);
   const int nv = p.D / 8;
   uint4 r[kMaxXV];
-  float m = 0.f;
 #pragma unroll
   for (int i = 0; i < kMaxXV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
@@ -456,6 +508,7 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
       if (e < p.E) logits[e] = static_cast<float>(static_cast<double>(lv[i]) * 0x1p-32);
     }
   }
+  float m = 0.f, ss = 0.f;  // max |x|, sum of x^2
 #pragma unroll
   for (int i = 0; i < kMaxXV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
@@ -465,47 +518,42 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
       for (int j = 0; j < 4; ++j) {
         const float a = bf16_bits_to_f32(w[j] & 0xffffu), b = bf16_bits_to_f32(w[j] >> 16);
         m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
+        ss = fmaf(a, a, fmaf(b, b, ss));
         const int col = idx * 8 + 2 * j;
         if (col >= cx.part.c_lo && col < cx.part.c_hi) xres[col - cx.part.c_lo] = a;
         if (col + 1 >= cx.part.c_lo && col + 1 < cx.part.c_hi) xres[col + 1 - cx.part.c_lo] = b;
       }
     }
   }
-  const float m_all = consumer_max(cx, m);
-  const float q = quant_factor(m_all);
-  float ss = 0.f;  // sum of (q x)^2, for the pre-norm
+  consumer_max_sum(cx, m, ss);
+  const float q = quant_factor(m);
 #pragma unroll
   for (int i = 0; i < kMaxXV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
+    uint4 packed = make_uint4(0, 0, 0, 0);
     if (idx < nv) {
       const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
       uint32_t hv[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a = bf16_bits_to_f32(w[j] & 0xffffu) * q, b = bf16_bits_to_f32(w[j] >> 16) * q;
-        ss = fmaf(a, a, fmaf(b, b, ss));
-        hv[j] = pack_s16x2(a, b);
-      }
+      for (int j = 0; j < 4; ++j)
+        hv[j] = pack_s16x2(bf16_bits_to_f32(w[j] & 0xffffu) * q, bf16_bits_to_f32(w[j] >> 16) * q);
+      packed = make_uint4(hv[0], hv[1], hv[2], hv[3]);
       const int col = idx * 8;
-      *reinterpret_cast<uint4*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) =
-          make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      *reinterpret_cast<uint4*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) = packed;
     }
+    // chunk sums: the 4 consecutive lanes holding idx 4c .. 4c+3 form chunk c
+    int cs = sum8_s16(packed);
+    cs += __shfl_xor_sync(0xffffffffu, cs, 1);
+    cs += __shfl_xor_sync(0xffffffffu, cs, 2);
+    if (idx < nv && (idx & 3) == 0) v.xsum[idx >> 2] = static_cast<float>(cs);
   }
-  if (p.prenorm) {
-    // sum q X ~ q * (W x); the layer wants r * (W x) with
-    // r = 1 / sqrt(mean(x^2) + eps), so the factor is r / q = 1 / sqrt(mean((q x)^2) + eps q^2)
-    ss = consumer_sum(cx, ss);
-    if (threadIdx.x == 0) {
-      v.vscale[0] = q > 0.f ? rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps * q * q) : 0.f;
-      const double qd = q, msq = q > 0.f ? static_cast<double>(ss) / p.D / (qd * qd) : 0.0;
-      reinterpret_cast<volatile float*>(cx.misc)[M_R] = static_cast<float>(1.0 / sqrt(msq + p.rms_eps));
-    }
-  } else if (threadIdx.x == 0) {
-    v.vscale[0] = m_all / 32767.f;
-    reinterpret_cast<volatile float*>(cx.misc)[M_R] = 1.f;
+  if (threadIdx.x == 0) {
+    // dot products with X are q * (W x); the layer wants r * (W x), r the
+    // pre-norm factor 1 / sqrt(mean(x^2) + eps) (or 1)
+    const float rr = p.prenorm ? rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps) : 1.f;
+    v.vscale[0] = q > 0.f ? rr / q : 0.f;
+    reinterpret_cast<volatile float*>(cx.misc)[M_R] = rr;
   }
-  csync();
-  chunk_sums(v.vec, v.xsum, nc);
   csync();
   return v;
 }
@@ -514,7 +562,7 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
 // branch.  One batch of 16-byte loads per thread (K*I + S <= 4 * kConsumers *
 // kMaxHV); the per-branch max is an order-independent smem atomicMax on the
 // bit patterns of non-negative floats.
-constexpr int kMaxHV = 4;
+constexpr int kMaxHV = 8;
 
 __device__ VecView prep_h(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
@@ -545,48 +593,80 @@ __device__ VecView prep_h(const Ctx& cx) {
 #pragma unroll
   for (int i = 0; i < kMaxHV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
+    uint2 packed = make_uint2(0, 0);
     if (idx < n4) {
       const int seg = idx * 4 < KI ? idx * 4 / p.I : p.K;
       const float q = quant_factor(__int_as_float(segmax[seg]));
       const int col = idx * 4;
-      *reinterpret_cast<uint2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) =
-          make_uint2(pack_s16x2(r[i].x * q, r[i].y * q), pack_s16x2(r[i].z * q, r[i].w * q));
+      packed = make_uint2(pack_s16x2(r[i].x * q, r[i].y * q), pack_s16x2(r[i].z * q, r[i].w * q));
+      *reinterpret_cast<uint2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) = packed;
     }
+    // chunk sums: the 8 consecutive lanes holding idx 8c .. 8c+7 form chunk c
+    int cs = dp2a_lo(packed.y, 0x01010101u, dp2a_lo(packed.x, 0x01010101u, 0));
+    cs += __shfl_xor_sync(0xffffffffu, cs, 1);
+    cs += __shfl_xor_sync(0xffffffffu, cs, 2);
+    cs += __shfl_xor_sync(0xffffffffu, cs, 4);
+    if (idx < n4 && (idx & 7) == 0) v.xsum[idx >> 3] = static_cast<float>(cs);
   }
   if (threadIdx.x <= static_cast<unsigned>(p.K))
     v.vscale[threadIdx.x] = __int_as_float(segmax[threadIdx.x]) / 32767.f;
   csync();
-  chunk_sums(v.vec, v.xsum, nc);
-  csync();
   return v;
 }
 
-// B stage: n gate/up row pairs -> h_out[pair].  Each warp owns one pair and
-// each lane both rows of a strided set of chunks, so an activation chunk is
-// read once for the two rows.
-__device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const VecView& xv,
+// The layer input, as each lane holds it for the B stages: chunks lane + 32 i
+// (i < kXC) of the int16 vector, with their sums.
+constexpr int kXC = 3;  // D <= 32 * 32 * kXC
+
+struct XRegs {
+  uint4 v[kXC][4];
+  float s[kXC];
+};
+
+__device__ void load_xregs(const VecView& xv, int nc, XRegs& xr) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < kXC; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nc) {
+      const uint4* v = reinterpret_cast<const uint4*>(xv.vec + c * kChunkStride);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xr.v[i][j] = v[j];
+      xr.s[i] = xv.xsum[c];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xr.v[i][j] = make_uint4(0, 0, 0, 0);
+      xr.s[i] = 0.f;
+    }
+  }
+}
+
+// B stage: n gate/up row pairs -> h_out[pair].  Warp w owns pairs 2w and
+// 2w+1; each lane takes its chunks of all four rows against the activation
+// chunks it holds in registers, then a fixed-order warp sum per row.
+__device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const XRegs& xr, float vs,
                           float* h_out) {
   const DecodeParams& p = *cx.p;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int pair = warp;
-  const int nc = p.D / 32;
-  float g = 0.f, u = 0.f;
-  if (pair < n) {
-    const uint8_t* rg = buf + (2 * pair) * p.rbD;
-    const uint8_t* ru = rg + p.rbD;
-    for (int c = lane; c < nc; c += 32) {
-      g += chunk_dot(rg, p.D / 2, c, xv.vec, xv.xsum);
-      u += chunk_dot(ru, p.D / 2, c, xv.vec, xv.xsum);
+  const int nc = p.D / 32, halfK = p.D / 2;
+  const int p0 = 2 * warp;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // gate p0, up p0, gate p0+1, up p0+1
+#pragma unroll
+  for (int i = 0; i < kXC; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nc) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (p0 + (r >> 1) < n) acc[r] += chunk_contrib(buf + (2 * p0 + r) * p.rbD, halfK, c, xr.v[i], xr.s[i]);
     }
   }
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    g += __shfl_xor_sync(0xffffffffu, g, o);
-    u += __shfl_xor_sync(0xffffffffu, u, o);
-  }
-  if (pair < n && lane == 0) {
-    const float vs = xv.vscale[0];
-    h_out[pair] = gelu_tanh(g * vs) * (u * vs);
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+  if (lane == 0) {
+    if (p0 < n) h_out[p0] = gelu_tanh(acc[0] * vs) * (acc[1] * vs);
+    if (p0 + 1 < n) h_out[p0 + 1] = gelu_tanh(acc[2] * vs) * (acc[3] * vs);
   }
 }
 
@@ -610,42 +690,67 @@ __device__ void router_partial(const Ctx& cx, const uint8_t* blk, int r0, int n,
   }
 }
 
-// C stage: rows [r0, r0+n) of the layer output.
-__device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int li,
-                          const VecView& hv, uint16_t* x_next, float* rpart) {
+// C phase: consumer thread t < ntask owns one (branch, chunk) task for the
+// whole phase and holds that chunk of h in registers: routed branch k = t /
+// (I/32), chunk t % (I/32) for t < K*(I/32); the shared branch's chunks after
+// that.  The scale folds the routing weight and the branch's quantisation
+// factor.
+struct HTask {
+  uint4 v[4];
+  float s;       // chunk sum of the int16 values
+  float scale;   // w_k * sigma_k (routed) or sigma_S (shared)
+  int k;         // branch (K = shared)
+  int c;         // chunk within the branch
+};
+
+__device__ void load_htask(const Ctx& cx, const VecView& hv, HTask& ht) {
   const DecodeParams& p = *cx.p;
-  float* contrib = reinterpret_cast<float*>(cx.smem + p.off_contrib);
+  const int t = threadIdx.x;
+  const int nch_i = p.I / 32;
+  ht.k = -1;
+  if (t >= p.ntask) return;
+  int cg;  // chunk index in the whole h vector
+  if (t < p.K * nch_i) {
+    ht.k = t / nch_i;
+    ht.c = t % nch_i;
+    cg = t;
+    ht.scale = __int_as_float(cx.misc[M_WTS + ht.k]) * hv.vscale[ht.k];
+  } else {
+    ht.k = p.K;
+    ht.c = t - p.K * nch_i;
+    cg = t;
+    ht.scale = hv.vscale[p.K];
+  }
+  const uint4* v = reinterpret_cast<const uint4*>(hv.vec + cg * kChunkStride);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) ht.v[j] = v[j];
+  ht.s = hv.xsum[cg];
+}
+
+// C stage: rows [r0, r0+n) of the layer output.  contrib (aliasing the
+// activation region, free once the tasks are in registers) holds one partial
+// per (row, task); then one warp per row sums them in a fixed order.
+__device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int li,
+                          const HTask& ht, uint16_t* x_next, float* rpart) {
+  const DecodeParams& p = *cx.p;
+  float* contrib = reinterpret_cast<float*>(cx.smem + p.off_vec);  // [n][kConsumers]
   float* xnext = reinterpret_cast<float*>(cx.smem + p.off_xnext);
   const int t = threadIdx.x;
-  const int r = t / p.tasks_row, tt = t % p.tasks_row;
-  const int nch_i = p.I / 32;
-  if (r < n) {
-    float acc = 0.f;
-    const int nrout = p.K * p.nsub_i;
-    if (tt < nrout) {
-      const int k = tt / p.nsub_i, sub = tt % p.nsub_i;
-      const uint8_t* rp = buf + static_cast<int64_t>(k) * n * p.rbI + r * p.rbI;
-      const uint8_t* vb = hv.vec + k * nch_i * kChunkStride;
-      const float* xs = hv.xsum + k * nch_i;
-      for (int c = sub; c < nch_i; c += p.nsub_i) acc += chunk_dot(rp, p.I / 2, c, vb, xs);
-      acc *= __int_as_float(cx.misc[M_WTS + k]) * hv.vscale[k];
-    } else {
-      const int sub = tt - nrout;
-      const uint8_t* rp = buf + static_cast<int64_t>(p.K) * n * p.rbI + r * p.rbS;
-      const int cb = p.K * nch_i;
-      const uint8_t* vb = hv.vec + cb * kChunkStride;
-      const int nch_s = p.S / 32;
-      for (int c = sub; c < nch_s; c += p.nsub_s) acc += chunk_dot(rp, p.S / 2, c, vb, hv.xsum + cb);
-      acc *= hv.vscale[p.K];
-    }
-    contrib[r * p.tasks_row + tt] = acc;
+  if (ht.k >= 0) {
+    const bool shared = ht.k == p.K;
+    const uint8_t* base = shared ? buf + static_cast<int64_t>(p.K) * n * p.rbI
+                                 : buf + static_cast<int64_t>(ht.k) * n * p.rbI;
+    const int rb = shared ? p.rbS : p.rbI;
+    const int halfK = shared ? p.S / 2 : p.I / 2;
+    for (int r = 0; r < n; ++r)
+      contrib[r * kConsumers + t] = chunk_contrib(base + r * rb, halfK, ht.c, ht.v, ht.s) * ht.scale;
   }
   csync();
   {  // one warp per row: lanes take strided tasks, then a fixed-order tree sum
     const int warp = t >> 5, lane = t & 31;
     for (int rr = warp; rr < n; rr += kConsumerWarps) {
       float y = 0.f;
-      for (int j = lane; j < p.tasks_row; j += 32) y += contrib[rr * p.tasks_row + j];
+      for (int j = lane; j < p.ntask; j += 32) y += contrib[rr * kConsumers + j];
 #pragma unroll
       for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
       if (lane == 0) {
@@ -691,14 +796,16 @@ __device__ void route_all(const Ctx& cx, int li) {
   if (li == 0 && p.forced) {
     if (t < p.K) cx.misc[M_IDS + t] = p.forced_ids[t];
   } else {
-    for (int e = t; e < p.E; e += kConsumers) {
+    const int warp = t >> 5, lane = t & 31;
+    for (int e = warp; e < p.E; e += kConsumerWarps) {
       const float v = logits[e];
       int rank = 0;
-      for (int f = 0; f < p.E; ++f) {
-        const float u = logits[f];
-        rank += (u > v || (u == v && f < e)) ? 1 : 0;
+      for (int f0 = 0; f0 < p.E; f0 += 32) {
+        const int f = f0 + lane;
+        const float u = f < p.E ? logits[f] : -INFINITY;
+        rank += __popc(__ballot_sync(0xffffffffu, f < p.E && (u > v || (u == v && f < e))));
       }
-      if (rank < p.K) cx.misc[M_IDS + rank] = e;
+      if (lane == 0 && rank < p.K) cx.misc[M_IDS + rank] = e;
     }
   }
   csync();
@@ -875,11 +982,14 @@ __device__ void consumer(const Ctx& cx) {
     if (routed_here) route_all(cx, li);
     else if (needs_ids(p)) publish_ids_local(cx, li);  // ids from an earlier launch
     trace(cx, li, 2);
+    XRegs xr;
+    load_xregs(xv, p.D / 32, xr);
+    const float vs = xv.vscale[0];
     for (; s < lp.n_r + lp.n_bs; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
-      compute_b(cx, buf, st.n, xv, p.h + p.K * p.I + st.a);
+      compute_b(cx, buf, st.n, xr, vs, p.h + p.K * p.I + st.a);
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
@@ -890,7 +1000,7 @@ __device__ void consumer(const Ctx& cx) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
-      compute_b(cx, buf, st.n, xv, p.h + st.k * p.I + st.a);
+      compute_b(cx, buf, st.n, xr, vs, p.h + st.a);
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
@@ -905,15 +1015,17 @@ __device__ void consumer(const Ctx& cx) {
     if (blockIdx.x == 0)
       for (int e = threadIdx.x; e < p.E; e += kConsumers) lacc_l[e] = 0ull;
     const VecView hv = prep_h(cx);
+    HTask ht;
+    load_htask(cx, hv, ht);
     trace(cx, li, 6);
     const bool nr = c_has_router(p, li);
     for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
-    csync();
+    csync();  // the activation region is reused for the C-stage partials
     for (; s < lp.n_r + lp.n_bs + lp.n_br + lp.n_c; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
-      compute_c(cx, buf, st.a, st.n, li, hv, x_next, rpart);
+      compute_c(cx, buf, st.a, st.n, li, ht, x_next, rpart);
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
@@ -994,8 +1106,8 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
     fixed += (bytes + 127) / 128 * 128;
     return o;
   };
-  const int o_vec = take(vb);
-  const int o_contrib = take(kConsumers * 4);
+  if (vb < p->rc_max * kConsumers * 4) vb = (p->rc_max * kConsumers * 4 + 127) / 128 * 128;
+  const int o_vec = take(vb);  // also the C-stage partials [rc_max][kConsumers]
   const int o_rpart = take(p->E * 4);
   const int o_xnext = take(256 * 4);
   const int o_xres = take(256 * 4);
@@ -1009,7 +1121,6 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
   p->nslots = ns;
   const int base = ns * slot;
   p->off_vec = base + o_vec;
-  p->off_contrib = base + o_contrib;
   p->off_rpart = base + o_rpart;
   p->off_xnext = base + o_xnext;
   p->off_xres = base + o_xres;

@@ -27,11 +27,11 @@ namespace moe {
 
 constexpr int kGroup = 64;
 constexpr int kMaxTopK = 32;
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;   // threads that compute
 constexpr int kThreads = kConsumers + 32;         // + one producer warp
 constexpr int kChunkStride = 80;  // smem bytes per 32-element int16 chunk (64 data + 16 pad)
-constexpr int kPairsPerStage = 16;  // gate/up row pairs per B stage (one per consumer warp)
+constexpr int kPairsPerStage = 16;  // gate/up row pairs per B stage (two per consumer warp)
 constexpr int kMaxSlots = 6;
 
 inline int64_t qrow_bytes(int64_t K) { return (K * 9 / 16 + 15) / 16 * 16; }
@@ -84,12 +84,12 @@ struct DecodeParams {
   int32_t* ids;            // [n_layers][K], relative to layer0
   float* wts;              // [n_layers][K]
   uint32_t* bar;           // kBarWords grid synchronisation words
-  // C-phase task mapping
-  int cpt_c, nsub_i, nsub_s, tasks_row, rc_max;
+  // C phase: ntask = K * (I/32) + S/32 (branch, chunk) tasks, one per consumer
+  // thread; rc_max rows per C stage (limited by the slot size)
+  int ntask, rc_max;
   // shared memory carve-up (bytes)
   int slot_bytes, nslots;
-  int off_vec, off_contrib, off_rpart, off_xnext, off_xres, off_logits, off_misc, off_bars,
-      smem_total;
+  int off_vec, off_rpart, off_xnext, off_xres, off_logits, off_misc, off_bars, smem_total;
   uint64_t timeout_ns;     // bound on every device-side wait
   uint64_t* trace;         // optional: [grid][n_layers][kTraceEvents] %globaltimer stamps
 };
@@ -108,11 +108,12 @@ constexpr int kMaxPrefillExperts = 256;
 // against up to kUnitTokens activation rows.
 struct GemmUnit {
   int kind;    // 0 routed expert, 1 shared expert
-  int mt;      // weight row tile (rows mt*128 .. mt*128+127)
+  int mt;      // first weight row tile (rows mt*128 ..)
   int expert;  // routed: blob index of the expert
   int row0;    // routed: first bucket position; shared: first token
   int n;       // activation rows in the unit (1 .. kUnitTokens)
-  int pad[3];
+  int nmt;     // weight row tiles in the unit (1 or 2)
+  int pad[2];
 };
 
 struct PrefillDims {
@@ -172,12 +173,11 @@ int prefill_combine(const CombineArgs& a, void* stream);
 struct GemmParams {
   CUtensorMap tm_code[2];  // 4-bit codes: box 128 B x 128 rows, 128-byte swizzle
   CUtensorMap tm_sb[2];    // scale/bias words: box 16 B x 128 rows
+  CUtensorMap tm_b[2];     // activation rows (fp16): box 64 x 256, 128-byte swizzle
   const GemmUnit* units;
   const int32_t* n_units;  // device: number of units
   int mode;                // 0: gate/up (+ GELU epilogue), 1: down
   int K[2];                // reduction length (D for gate/up; I or S for down)
-  const void* bsrc[2];     // fp16 activation rows (x16, or h)
-  int bld[2];              // row pitch of bsrc in elements
   const int32_t* perm;     // bucket position -> assignment
   int topk;
   const float* sigma;      // per-token scale of dot products with x16 (gate/up)
@@ -193,6 +193,9 @@ struct GemmParams {
 };
 int gemm_tc_smem_bytes();
 int gemm_tc_launch(const GemmParams& p, int grid, void* stream);
+// out[pos] = x16[perm[pos] / topk] for pos < rows (fp16 rows of D).
+int gather_rows_launch(const void* x16, int D, const int32_t* perm, int topk, int rows, void* out,
+                       void* stream);
 
 // Host entry points implemented in decode.cu.
 int decode_smem_plan(DecodeParams* p, int max_smem);   // fills the carve-up; 0 if it fits
