@@ -359,6 +359,13 @@ def run_chunked(args):
         for l in range(L):
             touched += len(np.unique(ids[l])) * shape.expert_bytes()
     touched += 8 * L * (shape.shared_bytes() + shape.router_bytes())
+    # phase breakdown of one step (CUDA events between the kernels of each call)
+    moe.moe_prefill_phase_ms(h)
+    moe.moe_trace_enable(h, True)
+    step()
+    torch.cuda.synchronize()
+    moe.moe_trace_enable(h, False)
+    phases, calls = moe.moe_prefill_phase_ms(h)
     stream = torch.cuda.current_stream()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -383,6 +390,8 @@ def run_chunked(args):
                                "layers, Zipf(1.1)-biased routing" % L,
                    "tokens_per_step": 1024},
         "touched_weight_bytes_per_step": touched,
+        "phase_ms_per_chunk_layer": dict(zip(["router", "bucket", "gemm_gate_up", "gemm_down",
+                                              "combine"], [v / max(calls, 1) for v in phases])),
         "roofline": {"bound": "hbm", "kernel": "whole chunk step (touched weight bytes)",
                      "achieved": gbs, "peak": hbm, "peak_source": src, "unit": "GB/s",
                      "frac": gbs / hbm, "traffic": None},

@@ -651,15 +651,39 @@ __device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const XRegs&
   const int nc = p.D / 32, halfK = p.D / 2;
   const int p0 = 2 * warp;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};  // gate p0, up p0, gate p0+1, up p0+1
+  // all code and scale words of this lane first (in flight together), then
+  // the integer dot products
+  uint4 wv[4][kXC];
+  uint32_t sbv[4][kXC];
 #pragma unroll
-  for (int i = 0; i < kXC; ++i) {
-    const int c = lane + 32 * i;
-    if (c < nc) {
+  for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (p0 + (r >> 1) < n) acc[r] += chunk_contrib(buf + (2 * p0 + r) * p.rbD, halfK, c, xr.v[i], xr.s[i]);
+    for (int i = 0; i < kXC; ++i) {
+      const int c = lane + 32 * i;
+      const bool ok = c < nc && p0 + (r >> 1) < n;
+      const uint8_t* row = buf + (2 * p0 + r) * p.rbD;
+      wv[r][i] = ok ? *reinterpret_cast<const uint4*>(row + c * 16) : make_uint4(0, 0, 0, 0);
+      sbv[r][i] = ok ? *reinterpret_cast<const uint32_t*>(row + halfK + (c >> 1) * 4) : 0u;
     }
-  }
+#pragma unroll
+  for (int i = 0; i < kXC; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t words[4] = {wv[r][i].x, wv[r][i].y, wv[r][i].z, wv[r][i].w};
+      int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = words[j] & 0x0F0F0F0Fu;
+        const uint32_t hi = words[j] & 0xF0F0F0F0u;
+        lo_acc[j & 1] = dp2a_lo(xr.v[i][j].x, lo, lo_acc[j & 1]);
+        lo_acc[j & 1] = dp2a_hi(xr.v[i][j].y, lo, lo_acc[j & 1]);
+        hi_acc[j & 1] = dp2a_lo(xr.v[i][j].z, hi, hi_acc[j & 1]);
+        hi_acc[j & 1] = dp2a_hi(xr.v[i][j].w, hi, hi_acc[j & 1]);
+      }
+      const int tot = (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
+      const __half2 sbh = *reinterpret_cast<const __half2*>(&sbv[r][i]);
+      acc[r] += fmaf(__low2float(sbh), static_cast<float>(tot), __high2float(sbh) * xr.s[i]);
+    }
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -727,6 +751,8 @@ __device__ void load_htask(const Ctx& cx, const VecView& hv, HTask& ht) {
   ht.s = hv.xsum[cg];
 }
 
+constexpr int kRowBatch = 5;
+
 // C stage: rows [r0, r0+n) of the layer output.  contrib (aliasing the
 // activation region, free once the tasks are in registers) holds one partial
 // per (row, task); then one warp per row sums them in a fixed order.
@@ -742,8 +768,39 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
                                  : buf + static_cast<int64_t>(ht.k) * n * p.rbI;
     const int rb = shared ? p.rbS : p.rbI;
     const int halfK = shared ? p.S / 2 : p.I / 2;
-    for (int r = 0; r < n; ++r)
-      contrib[r * kConsumers + t] = chunk_contrib(base + r * rb, halfK, ht.c, ht.v, ht.s) * ht.scale;
+    // rows in batches of kRowBatch: the batch's code and scale words are in
+    // flight together, then the integer dot products
+    for (int r0b = 0; r0b < n; r0b += kRowBatch) {
+      uint4 wv[kRowBatch];
+      uint32_t sbv[kRowBatch];
+#pragma unroll
+      for (int k = 0; k < kRowBatch; ++k) {
+        const int r = r0b + k;
+        const uint8_t* row = base + r * rb;
+        wv[k] = r < n ? *reinterpret_cast<const uint4*>(row + ht.c * 16) : make_uint4(0, 0, 0, 0);
+        sbv[k] = r < n ? *reinterpret_cast<const uint32_t*>(row + halfK + (ht.c >> 1) * 4) : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < kRowBatch; ++k) {
+        const uint32_t words[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t lo = words[j] & 0x0F0F0F0Fu;
+          const uint32_t hi = words[j] & 0xF0F0F0F0u;
+          lo_acc[j & 1] = dp2a_lo(ht.v[j].x, lo, lo_acc[j & 1]);
+          lo_acc[j & 1] = dp2a_hi(ht.v[j].y, lo, lo_acc[j & 1]);
+          hi_acc[j & 1] = dp2a_lo(ht.v[j].z, hi, hi_acc[j & 1]);
+          hi_acc[j & 1] = dp2a_hi(ht.v[j].w, hi, hi_acc[j & 1]);
+        }
+        const int tot = (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
+        const __half2 sbh = *reinterpret_cast<const __half2*>(&sbv[k]);
+        const int r = r0b + k;
+        if (r < n)
+          contrib[r * kConsumers + t] =
+              fmaf(__low2float(sbh), static_cast<float>(tot), __high2float(sbh) * ht.s) * ht.scale;
+      }
+    }
   }
   csync();
   {  // one warp per row: lanes take strided tasks, then a fixed-order tree sum
@@ -796,16 +853,18 @@ __device__ void route_all(const Ctx& cx, int li) {
   if (li == 0 && p.forced) {
     if (t < p.K) cx.misc[M_IDS + t] = p.forced_ids[t];
   } else {
-    const int warp = t >> 5, lane = t & 31;
-    for (int e = warp; e < p.E; e += kConsumerWarps) {
+    // two threads per expert, each counting over half of the others
+    for (int e2 = t; e2 < 2 * p.E; e2 += kConsumers) {
+      const int e = e2 >> 1, half = e2 & 1;
       const float v = logits[e];
+      const int f0 = half ? p.E / 2 : 0, f1 = half ? p.E : p.E / 2;
       int rank = 0;
-      for (int f0 = 0; f0 < p.E; f0 += 32) {
-        const int f = f0 + lane;
-        const float u = f < p.E ? logits[f] : -INFINITY;
-        rank += __popc(__ballot_sync(0xffffffffu, f < p.E && (u > v || (u == v && f < e))));
+      for (int f = f0; f < f1; ++f) {
+        const float u = logits[f];
+        rank += (u > v || (u == v && f < e)) ? 1 : 0;
       }
-      if (lane == 0 && rank < p.K) cx.misc[M_IDS + rank] = e;
+      rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+      if (!half && rank < p.K) cx.misc[M_IDS + rank] = e;
     }
   }
   csync();
