@@ -278,7 +278,7 @@ def moe_last_buckets(handle: Handle, T: int):
     return counts, offsets, perm
 
 
-MOE_TRACE_EVENTS = 9
+MOE_TRACE_EVENTS = 13
 
 
 def moe_trace_enable(handle: Handle, on: bool = True):

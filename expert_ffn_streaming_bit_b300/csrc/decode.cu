@@ -31,11 +31,11 @@
 //           over the chosen logits;
 //   expert: h_j = gelu_tanh(g_j) u_j with g = W_gate u, u = W_up u;
 //           e = W_down h; y = sum_i w_i e_i + shared(u); optional residual.
-// Expert dot products are integer-exact: the activation vector (x, or one
-// branch of h) is held as int16 X = rint(v / sigma), sigma = max|v| / 32767,
-// the 4-bit codes as bytes, and a 2-way integer dot product accumulates
-// sum q X exactly in int32 per 32-column chunk; the chunk contributes
-// s * sum(q X) + bias * sum(X), and the row total is multiplied by sigma.
+// Expert dot products are integer-exact: the activation vector is held as
+// int16 X = rint(v / sigma) (sigma = max|v| / 32767 over the whole of x, or
+// over each 32-value chunk of h), the 4-bit codes as bytes, and a 2-way
+// integer dot product accumulates sum q X exactly in int32 per 32-column
+// chunk; the chunk contributes s * sum(q X) + bias * sum(X), times sigma.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -77,7 +77,6 @@ enum : int {
   M_TARGET = 70,  // [2] next grid-barrier target (64-bit; 0 before the first barrier)
   M_RED = 72,  // [8] per-warp reduction scratch
   M_RED2 = 80, // [8] second per-warp reduction scratch
-  M_SEG = 96,  // [K+1] per-branch max |h| (float bits)
   M_COUNT = 136
 };
 
@@ -321,19 +320,24 @@ __device__ void prefetch_fixed(const Ctx& cx, int li) {
   }
 }
 
-__device__ void prefetch_routed(const Ctx& cx, int li) {
+// Routed gate/up pairs [q, rt_hi) of this CTA (only those stages the ring
+// cannot take yet are worth a hint).
+__device__ void prefetch_routed_gu(const Ctx& cx, int li, int q) {
   const DecodeParams& p = *cx.p;
   const LayerDev& L = p.layers[p.layer0 + li];
-  if (p.phases & PH_BROUTED) {
-    int q = cx.part.rt_lo;
-    while (q < cx.part.rt_hi) {
-      const int k = q / p.I, j = q % p.I;
-      const int n = min(cx.part.rt_hi - q, p.I - j);
-      const uint8_t* blob = expert_blob(p, L, k, cx.misc[M_IDS + k]);
-      prefetch_l2(blob + static_cast<int64_t>(j) * 2 * p.rbD, n * 2 * p.rbD);
-      q += n;
-    }
+  while (q < cx.part.rt_hi) {
+    const int k = q / p.I, j = q % p.I;
+    const int n = min(cx.part.rt_hi - q, p.I - j);
+    const uint8_t* blob = expert_blob(p, L, k, cx.misc[M_IDS + k]);
+    prefetch_l2(blob + static_cast<int64_t>(j) * 2 * p.rbD, n * 2 * p.rbD);
+    q += n;
   }
+}
+
+// The k routed experts' down rows of this CTA's output rows.
+__device__ void prefetch_routed_dn(const Ctx& cx, int li) {
+  const DecodeParams& p = *cx.p;
+  const LayerDev& L = p.layers[p.layer0 + li];
   const int rows = cx.part.c_hi - cx.part.c_lo;
   if ((p.phases & PH_C) && rows > 0) {
     for (int k = 0; k < p.K; ++k) {
@@ -343,12 +347,17 @@ __device__ void prefetch_routed(const Ctx& cx, int li) {
   }
 }
 
+// Once the layer's ids are known the routed gate/up rows are needed first:
+// their bulk copies go out before the down-row hints, and only the stages
+// that find no free ring slot are hinted into L2 ahead of their copies.
 __device__ void producer(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
   int st_idx = 0;
   for (int li = 0; li < p.n_layers; ++li) {
     const LayerPlan lp = layer_plan(p, cx.part, li);
     const int total = lp.n_r + lp.n_bs + lp.n_br + lp.n_c;
+    const int br_end = lp.n_r + lp.n_bs + lp.n_br;
+    bool gu_hinted = false;
     prefetch_fixed(cx, li);
     for (int s = 0; s <= total; ++s) {
       if (s == lp.n_r + lp.n_bs && needs_ids(p)) {
@@ -357,12 +366,17 @@ __device__ void producer(const Ctx& cx) {
           cx.misc[M_ABORT] = 1;
           return;
         }
-        prefetch_routed(cx, li);
+        if (lp.n_br == 0) prefetch_routed_dn(cx, li);
       }
       if (s == total) break;
       const Stage st = stage_at(p, cx.part, lp, s);
       const int slot = st_idx % p.nslots;
       const uint32_t round = st_idx / p.nslots;
+      if (st.kind == ST_BR && !gu_hinted && !mbar_try_wait(&cx.empty[slot], (round & 1) ^ 1)) {
+        prefetch_routed_gu(cx, li, st.a);
+        prefetch_routed_dn(cx, li);
+        gu_hinted = true;
+      }
       if (!mbar_wait(&cx.empty[slot], (round & 1) ^ 1, p.timeout_ns, &cx.misc[M_ABORT])) {
         cx.misc[M_ABORT] = 1;
         return;
@@ -371,6 +385,7 @@ __device__ void producer(const Ctx& cx) {
       issue_stage(cx, st, li, cx.smem + static_cast<int64_t>(slot) * p.slot_bytes, &cx.full[slot]);
       ++st_idx;
       cx.misc[M_ISSUED] = st_idx;
+      if (s == br_end - 1 && !gu_hinted) prefetch_routed_dn(cx, li);
     }
   }
 }
@@ -482,7 +497,8 @@ __device__ VecView vec_view(const Ctx& cx, int nchunks) {
 constexpr int kMaxXV = 2;  // D <= 8 * kConsumers * kMaxXV
 constexpr int kMaxLogitLoads = 4;  // E <= 4 * kConsumers
 
-__device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long long* lacc) {
+__device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long long* lacc,
+                          const float* logit_bias) {
   const DecodeParams& p = *cx.p;
   const int nc = p.D / 32;
   VecView v = vec_view(cx, nc);
@@ -494,18 +510,16 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
     if (idx < nv) r[i] = __ldcg(reinterpret_cast<const uint4*>(xg) + idx);
   }
-  if (lacc) {  // the layer's raw router logits, in the same round trip
-    float* logits = reinterpret_cast<float*>(cx.smem + p.off_logits);
-    long long lv[kMaxLogitLoads];
+  long long lv[kMaxLogitLoads];  // the layer's raw router logits, in the same round trip
+  float lb[kMaxLogitLoads];
+  if (lacc) {
 #pragma unroll
     for (int i = 0; i < kMaxLogitLoads; ++i) {
       const int e = static_cast<int>(threadIdx.x) + i * kConsumers;
-      if (e < p.E) lv[i] = static_cast<long long>(__ldcg(lacc + e));
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxLogitLoads; ++i) {
-      const int e = static_cast<int>(threadIdx.x) + i * kConsumers;
-      if (e < p.E) logits[e] = static_cast<float>(static_cast<double>(lv[i]) * 0x1p-32);
+      if (e < p.E) {
+        lv[i] = static_cast<long long>(__ldcg(lacc + e));
+        lb[i] = logit_bias ? __ldg(logit_bias + e) : 0.f;
+      }
     }
   }
   float m = 0.f, ss = 0.f;  // max |x|, sum of x^2
@@ -527,6 +541,21 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
   }
   consumer_max_sum(cx, m, ss);
   const float q = quant_factor(m);
+  // r = 1 / sqrt(mean(x^2) + eps) with pre-norm, else 1 (the same value in every thread)
+  const float rr = p.prenorm ? rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps) : 1.f;
+  if (lacc) {
+    // logit_e = r * (sum of the fixed-point partials) + bias_e
+    float* logits = reinterpret_cast<float*>(cx.smem + p.off_logits);
+#pragma unroll
+    for (int i = 0; i < kMaxLogitLoads; ++i) {
+      const int e = static_cast<int>(threadIdx.x) + i * kConsumers;
+      if (e < p.E) {
+        float l = static_cast<float>(static_cast<double>(lv[i]) * 0x1p-32) * rr;
+        if (logit_bias) l += lb[i];
+        logits[e] = l;
+      }
+    }
+  }
 #pragma unroll
   for (int i = 0; i < kMaxXV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
@@ -547,69 +576,8 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
     cs += __shfl_xor_sync(0xffffffffu, cs, 2);
     if (idx < nv && (idx & 3) == 0) v.xsum[idx >> 2] = static_cast<float>(cs);
   }
-  if (threadIdx.x == 0) {
-    // dot products with X are q * (W x); the layer wants r * (W x), r the
-    // pre-norm factor 1 / sqrt(mean(x^2) + eps) (or 1)
-    const float rr = p.prenorm ? rsqrtf(ss / static_cast<float>(p.D) + p.rms_eps) : 1.f;
-    v.vscale[0] = q > 0.f ? rr / q : 0.f;
-    reinterpret_cast<volatile float*>(cx.misc)[M_R] = rr;
-  }
-  csync();
-  return v;
-}
-
-// h (fp32 [K*I + S], global) -> int16 chunks, one quantisation scale per
-// branch.  One batch of 16-byte loads per thread (K*I + S <= 4 * kConsumers *
-// kMaxHV); the per-branch max is an order-independent smem atomicMax on the
-// bit patterns of non-negative floats.
-constexpr int kMaxHV = 8;
-
-__device__ VecView prep_h(const Ctx& cx) {
-  const DecodeParams& p = *cx.p;
-  const int nh = p.K * p.I + p.S;
-  const int nc = nh / 32;
-  VecView v = vec_view(cx, nc);
-  volatile int* segmax = cx.misc + M_SEG;
-  if (threadIdx.x <= static_cast<unsigned>(p.K)) segmax[threadIdx.x] = 0;
-  const int n4 = nh / 4;
-  float4 r[kMaxHV];
-#pragma unroll
-  for (int i = 0; i < kMaxHV; ++i) {
-    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
-    if (idx < n4) r[i] = __ldcg(reinterpret_cast<const float4*>(p.h) + idx);
-  }
-  csync();
-  const int KI = p.K * p.I;
-#pragma unroll
-  for (int i = 0; i < kMaxHV; ++i) {
-    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
-    if (idx < n4) {
-      const int seg = idx * 4 < KI ? idx * 4 / p.I : p.K;
-      const float m = fmaxf(fmaxf(fabsf(r[i].x), fabsf(r[i].y)), fmaxf(fabsf(r[i].z), fabsf(r[i].w)));
-      atomicMax(const_cast<int*>(segmax) + seg, __float_as_int(m));
-    }
-  }
-  csync();
-#pragma unroll
-  for (int i = 0; i < kMaxHV; ++i) {
-    const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
-    uint2 packed = make_uint2(0, 0);
-    if (idx < n4) {
-      const int seg = idx * 4 < KI ? idx * 4 / p.I : p.K;
-      const float q = quant_factor(__int_as_float(segmax[seg]));
-      const int col = idx * 4;
-      packed = make_uint2(pack_s16x2(r[i].x * q, r[i].y * q), pack_s16x2(r[i].z * q, r[i].w * q));
-      *reinterpret_cast<uint2*>(v.vec + (col >> 5) * kChunkStride + (col & 31) * 2) = packed;
-    }
-    // chunk sums: the 8 consecutive lanes holding idx 8c .. 8c+7 form chunk c
-    int cs = dp2a_lo(packed.y, 0x01010101u, dp2a_lo(packed.x, 0x01010101u, 0));
-    cs += __shfl_xor_sync(0xffffffffu, cs, 1);
-    cs += __shfl_xor_sync(0xffffffffu, cs, 2);
-    cs += __shfl_xor_sync(0xffffffffu, cs, 4);
-    if (idx < n4 && (idx & 7) == 0) v.xsum[idx >> 3] = static_cast<float>(cs);
-  }
-  if (threadIdx.x <= static_cast<unsigned>(p.K))
-    v.vscale[threadIdx.x] = __int_as_float(segmax[threadIdx.x]) / 32767.f;
+  // dot products with X are q * (W x); the layer wants r * (W x)
+  if (threadIdx.x == 0) v.vscale[0] = q > 0.f ? rr / q : 0.f;
   csync();
   return v;
 }
@@ -715,52 +683,66 @@ __device__ void router_partial(const Ctx& cx, const uint8_t* blk, int r0, int n,
 }
 
 // C phase: consumer thread t < ntask owns one (branch, chunk) task for the
-// whole phase and holds that chunk of h in registers: routed branch k = t /
-// (I/32), chunk t % (I/32) for t < K*(I/32); the shared branch's chunks after
-// that.  The scale folds the routing weight and the branch's quantisation
-// factor.
+// whole phase: chunk t of h (32 values; routed branch k = t / (I/32) for t <
+// K*(I/32), the shared branch after that).  The thread loads its chunk from
+// global memory and quantises it on its own: X = rint(h * 32767 / m) with m
+// the chunk's max |h|, so the chunk carries its own scale sigma = m / 32767
+// and no reduction across threads is needed.  The task scale folds the
+// routing weight (routed) and sigma.
 struct HTask {
   uint4 v[4];
   float s;       // chunk sum of the int16 values
-  float scale;   // w_k * sigma_k (routed) or sigma_S (shared)
+  float scale;   // w_k * sigma (routed) or sigma (shared)
   int k;         // branch (K = shared)
   int c;         // chunk within the branch
 };
 
-__device__ void load_htask(const Ctx& cx, const VecView& hv, HTask& ht) {
+__device__ void load_htask(const Ctx& cx, HTask& ht) {
   const DecodeParams& p = *cx.p;
   const int t = threadIdx.x;
   const int nch_i = p.I / 32;
   ht.k = -1;
   if (t >= p.ntask) return;
-  int cg;  // chunk index in the whole h vector
+  const float4* src = reinterpret_cast<const float4*>(p.h) + t * 8;
+  float4 r[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) r[j] = __ldcg(src + j);
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(r[j].x), fabsf(r[j].y)), fmaxf(fabsf(r[j].z), fabsf(r[j].w))));
+  const float q = quant_factor(m);
+  int cs = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 a = r[2 * j], b = r[2 * j + 1];
+    ht.v[j] = make_uint4(pack_s16x2(a.x * q, a.y * q), pack_s16x2(a.z * q, a.w * q),
+                         pack_s16x2(b.x * q, b.y * q), pack_s16x2(b.z * q, b.w * q));
+    cs += sum8_s16(ht.v[j]);
+  }
+  ht.s = static_cast<float>(cs);
+  const float sigma = m / 32767.f;
   if (t < p.K * nch_i) {
     ht.k = t / nch_i;
     ht.c = t % nch_i;
-    cg = t;
-    ht.scale = __int_as_float(cx.misc[M_WTS + ht.k]) * hv.vscale[ht.k];
+    ht.scale = __int_as_float(cx.misc[M_WTS + ht.k]) * sigma;
   } else {
     ht.k = p.K;
     ht.c = t - p.K * nch_i;
-    cg = t;
-    ht.scale = hv.vscale[p.K];
+    ht.scale = sigma;
   }
-  const uint4* v = reinterpret_cast<const uint4*>(hv.vec + cg * kChunkStride);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) ht.v[j] = v[j];
-  ht.s = hv.xsum[cg];
 }
 
 constexpr int kRowBatch = 5;
 
 // C stage: rows [r0, r0+n) of the layer output.  contrib (aliasing the
 // activation region, free once the tasks are in registers) holds one partial
-// per (row, task); then one warp per row sums them in a fixed order.
+// per (row, task); then one warp per row sums them in a fixed order and adds
+// the row's term of the next router's logits.
 __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int li,
                           const HTask& ht, uint16_t* x_next, float* rpart) {
   const DecodeParams& p = *cx.p;
   float* contrib = reinterpret_cast<float*>(cx.smem + p.off_vec);  // [n][kConsumers]
-  float* xnext = reinterpret_cast<float*>(cx.smem + p.off_xnext);
   const int t = threadIdx.x;
   if (ht.k >= 0) {
     const bool shared = ht.k == p.K;
@@ -803,27 +785,37 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
     }
   }
   csync();
-  {  // one warp per row: lanes take strided tasks, then a fixed-order tree sum
-    const int warp = t >> 5, lane = t & 31;
-    for (int rr = warp; rr < n; rr += kConsumerWarps) {
-      float y = 0.f;
-      for (int j = lane; j < p.ntask; j += 32) y += contrib[rr * kConsumers + j];
+  // One warp per row: a fixed-order tree sum of the row's task partials, the
+  // output element, and the row's term of the next router's logits, which
+  // each warp accumulates in its own row of rpart ([kConsumerWarps][E]).
+  const int warp = t >> 5, lane = t & 31;
+  const bool nr = c_has_router(p, li);
+  const uint8_t* rq = buf + static_cast<int64_t>(n) * (p.K * p.rbI + p.rbS);  // [n][E] codes
+  const uint32_t* rsb = reinterpret_cast<const uint32_t*>(rq + n * p.E);     // [groups][E]
+  const int g0 = r0 / kGroup;
+  float* rp = rpart + warp * p.E;
+  const float* xres = reinterpret_cast<const float*>(cx.smem + p.off_xres);
+  for (int rr = warp; rr < n; rr += kConsumerWarps) {
+    float y = 0.f;
+    for (int j = lane; j < p.ntask; j += 32) y += contrib[rr * kConsumers + j];
 #pragma unroll
-      for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-      if (lane == 0) {
-        const int d = r0 + rr;
-        float out = y;
-        if (p.residual) out += reinterpret_cast<const float*>(cx.smem + p.off_xres)[d - cx.part.c_lo];
-        const uint16_t ob = f32_to_bf16_bits(out);
-        x_next[d] = ob;
-        xnext[rr] = bf16_bits_to_f32(ob);
+    for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+    const int d = r0 + rr;
+    float out = y;
+    if (p.residual) out += xres[d - cx.part.c_lo];
+    const uint16_t ob = f32_to_bf16_bits(out);
+    if (lane == 0) x_next[d] = ob;
+    if (nr) {
+      const float xd = bf16_bits_to_f32(ob);
+      const uint32_t* sbr = rsb + (d / kGroup - g0) * p.E;
+      const uint8_t* qr = rq + rr * p.E;
+      for (int e = lane; e < p.E; e += 32) {
+        const uint32_t w = sbr[e];
+        const __half2 h2 = *reinterpret_cast<const __half2*>(&w);
+        const float wv = fmaf(__low2float(h2), static_cast<float>(qr[e]), __high2float(h2));
+        rp[e] = fmaf(wv, xd, rp[e]);
       }
     }
-  }
-  csync();
-  if (c_has_router(p, li)) {
-    const uint8_t* blk = buf + static_cast<int64_t>(n) * (p.K * p.rbI + p.rbS);
-    router_partial(cx, blk, r0, n, xnext, rpart);
   }
 }
 
@@ -835,33 +827,37 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
 // layer's routed stages opens.
 __device__ void route_all(const Ctx& cx, int li) {
   const DecodeParams& p = *cx.p;
-  float* logits = reinterpret_cast<float*>(cx.smem + p.off_logits);
-  const LayerDev& L = p.layers[p.layer0 + li];
+  const float* logits = reinterpret_cast<const float*>(cx.smem + p.off_logits);
   const int t = threadIdx.x;
-  {
-    const float r = reinterpret_cast<volatile float*>(cx.misc)[M_R];
-    for (int e = t; e < p.E; e += kConsumers) {
-      float l = logits[e] * r;
-      if (L.logit_bias) l += L.logit_bias[e];
-      logits[e] = l;
-    }
-  }
-  csync();
   // Top k in parallel: the rank of expert e is the number of experts before it
   // in (logit desc, index asc) order; the experts of rank < k are the choice,
   // in that order (or the forced ids).  Slot i's id goes to misc[M_IDS + i].
   if (li == 0 && p.forced) {
     if (t < p.K) cx.misc[M_IDS + t] = p.forced_ids[t];
   } else {
-    // two threads per expert, each counting over half of the others
+    // two threads per expert, each counting over half of the others (16-byte
+    // broadcast reads of the logits when the halves are multiples of 4)
+    const bool vec4 = (p.E & 7) == 0;
     for (int e2 = t; e2 < 2 * p.E; e2 += kConsumers) {
       const int e = e2 >> 1, half = e2 & 1;
       const float v = logits[e];
       const int f0 = half ? p.E / 2 : 0, f1 = half ? p.E : p.E / 2;
       int rank = 0;
-      for (int f = f0; f < f1; ++f) {
-        const float u = logits[f];
-        rank += (u > v || (u == v && f < e)) ? 1 : 0;
+      if (vec4) {
+        const float4* l4 = reinterpret_cast<const float4*>(logits);
+#pragma unroll 4
+        for (int f = f0; f < f1; f += 4) {
+          const float4 u = l4[f >> 2];
+          rank += (u.x > v || (u.x == v && f < e)) ? 1 : 0;
+          rank += (u.y > v || (u.y == v && f + 1 < e)) ? 1 : 0;
+          rank += (u.z > v || (u.z == v && f + 2 < e)) ? 1 : 0;
+          rank += (u.w > v || (u.w == v && f + 3 < e)) ? 1 : 0;
+        }
+      } else {
+        for (int f = f0; f < f1; ++f) {
+          const float u = logits[f];
+          rank += (u > v || (u == v && f < e)) ? 1 : 0;
+        }
       }
       rank += __shfl_xor_sync(0xffffffffu, rank, 1);
       if (!half && rank < p.K) cx.misc[M_IDS + rank] = e;
@@ -983,12 +979,16 @@ __device__ void release_slot(const Ctx& cx, int st_idx) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(&cx.empty[slot]);
 }
 
-// Add this CTA's partial logits into the layer's accumulators: fp32 -> 64-bit
-// fixed point in units of 2^-32 (|partial| < 2^31), integer atomic add.
+// Add this CTA's partial logits (the sum of the warps' rows of rpart, in warp
+// order) into the layer's accumulators: fp32 -> 64-bit fixed point in units
+// of 2^-32 (|partial| < 2^31), integer atomic add.
 __device__ void add_partials(const Ctx& cx, const float* rpart, unsigned long long* lacc) {
   const DecodeParams& p = *cx.p;
   for (int e = threadIdx.x; e < p.E; e += kConsumers) {
-    const long long v = __float2ll_rn(rpart[e] * 0x1p32f);
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) sum += rpart[w * p.E + e];
+    const long long v = __float2ll_rn(sum * 0x1p32f);
     red_add_gpu_u64(lacc + e, static_cast<unsigned long long>(v));
   }
 }
@@ -1014,7 +1014,7 @@ __device__ void consumer(const Ctx& cx) {
     trace(cx, li, 0);
     // ---- router of the launch's first layer (later layers: folded into C)
     if (li == 0 && (p.phases & PH_ROUTER)) {
-      for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
+      for (int e = threadIdx.x; e < kConsumerWarps * p.E; e += kConsumers) rpart[e] = 0.f;
       csync();
       if (lp.n_r) {
         if (!wait_full(cx, st_idx)) return;
@@ -1036,7 +1036,7 @@ __device__ void consumer(const Ctx& cx) {
     // expert's gate/up (which needs no ids) while the routed rows arrive
     VecView xv{};
     unsigned long long* lacc_l = p.lacc + (li & 1) * p.E;
-    xv = prep_x(cx, x_l, routed_here ? lacc_l : nullptr);
+    xv = prep_x(cx, x_l, routed_here ? lacc_l : nullptr, p.layers[p.layer0 + li].logit_bias);
     trace(cx, li, 1);
     if (routed_here) route_all(cx, li);
     else if (needs_ids(p)) publish_ids_local(cx, li);  // ids from an earlier launch
@@ -1047,53 +1047,56 @@ __device__ void consumer(const Ctx& cx) {
     for (; s < lp.n_r + lp.n_bs; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
+      if (s == lp.n_r) trace(cx, li, 3);
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
       compute_b(cx, buf, st.n, xr, vs, p.h + p.K * p.I + st.a);
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
     }
-    trace(cx, li, 3);
+    trace(cx, li, 4);
     // ---- routed gate/up
     for (; s < lp.n_r + lp.n_bs + lp.n_br; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
+      if (s == lp.n_r + lp.n_bs) trace(cx, li, 5);
+      if (s == lp.n_r + lp.n_bs + lp.n_br - 1) trace(cx, li, 6);
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
       compute_b(cx, buf, st.n, xr, vs, p.h + st.a);
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
     }
-    trace(cx, li, 4);
+    trace(cx, li, 7);
     if (!(p.phases & PH_C)) continue;
     // ---- down + combine (+ next router's partial logits)
     if (!grid_barrier(cx)) return;
-    trace(cx, li, 5);
+    trace(cx, li, 8);
     // every CTA has read layer li's logit accumulators: clear them for the
     // layer after next (their next additions come after the next barrier)
     if (blockIdx.x == 0)
       for (int e = threadIdx.x; e < p.E; e += kConsumers) lacc_l[e] = 0ull;
-    const VecView hv = prep_h(cx);
     HTask ht;
-    load_htask(cx, hv, ht);
-    trace(cx, li, 6);
+    load_htask(cx, ht);
+    trace(cx, li, 9);
     const bool nr = c_has_router(p, li);
-    for (int e = threadIdx.x; e < p.E; e += kConsumers) rpart[e] = 0.f;
+    for (int e = threadIdx.x; e < kConsumerWarps * p.E; e += kConsumers) rpart[e] = 0.f;
     csync();  // the activation region is reused for the C-stage partials
     for (; s < lp.n_r + lp.n_bs + lp.n_br + lp.n_c; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       if (!wait_full(cx, st_idx)) return;
+      if (s == lp.n_r + lp.n_bs + lp.n_br) trace(cx, li, 10);
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
       compute_c(cx, buf, st.a, st.n, li, ht, x_next, rpart);
       csync();
       release_slot(cx, st_idx);
       ++st_idx;
     }
-    trace(cx, li, 7);
+    trace(cx, li, 11);
     if (nr) {
       add_partials(cx, rpart, p.lacc + ((li + 1) & 1) * p.E);
       if (!grid_barrier(cx)) return;
-      trace(cx, li, 8);
+      trace(cx, li, 12);
     }
   }
 }
@@ -1147,11 +1150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int decode_smem_plan(DecodeParams* p, int max_smem) {
   const int nc_x = p->D / 32;
-  const int nc_h = (p->K * p->I + p->S) / 32;
   auto vec_bytes = [](int nc, int nscale) { return nc * kChunkStride + nc * 8 + nscale * 4; };
-  int vb = vec_bytes(nc_x, 1);
-  const int vh = vec_bytes(nc_h, p->K + 1);
-  if (vh > vb) vb = vh;
+  int vb = vec_bytes(nc_x, 1);  // the layer input's int16 chunks
   vb = (vb + 127) / 128 * 128;
   const int b_stage = kPairsPerStage * 2 * p->rbD;
   const int rsb = 2 * p->E * 4;
@@ -1167,7 +1167,7 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
   };
   if (vb < p->rc_max * kConsumers * 4) vb = (p->rc_max * kConsumers * 4 + 127) / 128 * 128;
   const int o_vec = take(vb);  // also the C-stage partials [rc_max][kConsumers]
-  const int o_rpart = take(p->E * 4);
+  const int o_rpart = take(kConsumerWarps * p->E * 4);
   const int o_xnext = take(256 * 4);
   const int o_xres = take(256 * 4);
   const int o_logits = take(p->E * 4);

@@ -58,7 +58,7 @@ constexpr int kBarFlag = 32;
 // layer start, x (and router logits) converted, routing done, shared gate/up
 // done, routed gate/up done, h complete (barrier), h converted, down done,
 // next-layer barrier passed.
-constexpr int kTraceEvents = 9;
+constexpr int kTraceEvents = 13;
 constexpr int kTraceMaxLayers = 64;
 
 struct DecodeParams {

@@ -304,14 +304,19 @@ moe_status moe_set_timeout_ms(moe_handle* h, int ms);
  * Decode tracing (for profiling the persistent decode kernel).
  * moe_trace_enable(h, 1): later decode launches of this handle record, per
  * CTA and layer, MOE_TRACE_EVENTS %globaltimer stamps (ns) taken by the CTA's
- * first consumer thread: layer start, input (and router logits) loaded and
- * converted, routing done, shared gate/up done, routed gate/up done, h
- * complete (barrier), h converted, down done, next barrier passed.  moe_trace_enable(h, 0) stops recording.
+ * first consumer thread: (0) layer start, (1) input and router logits loaded
+ * and converted, (2) routing done, (3) first shared gate/up stage in shared
+ * memory, (4) shared gate/up done, (5) first and (6) last routed gate/up
+ * stage in shared memory, (7) routed gate/up done, (8) h complete (grid
+ * barrier), (9) h loaded and converted, (10) first down stage in shared
+ * memory, (11) down done, (12) next grid barrier passed.  A stamp that does
+ * not occur in a layer is left as it was.  moe_trace_enable(h, 0) stops
+ * recording.
  * moe_trace_read(h, out, n_layers): copies the last launch's stamps to host
  * out [num_sms][n_layers][MOE_TRACE_EVENTS] int64 (n_layers of that launch,
  * at most 64; synchronises).
  */
-#define MOE_TRACE_EVENTS 9
+#define MOE_TRACE_EVENTS 13
 moe_status moe_trace_enable(moe_handle* h, int on);
 moe_status moe_trace_read(moe_handle* h, int64_t* out, int n_layers);
 
