@@ -684,11 +684,10 @@ __device__ void router_partial(const Ctx& cx, const uint8_t* blk, int r0, int n,
 
 // C phase: consumer thread t < ntask owns one (branch, chunk) task for the
 // whole phase: chunk t of h (32 values; routed branch k = t / (I/32) for t <
-// K*(I/32), the shared branch after that).  The thread loads its chunk from
-// global memory and quantises it on its own: X = rint(h * 32767 / m) with m
-// the chunk's max |h|, so the chunk carries its own scale sigma = m / 32767
-// and no reduction across threads is needed.  The task scale folds the
-// routing weight (routed) and sigma.
+// K*(I/32), the shared branch after that).  Each chunk is quantised on its
+// own: X = rint(h * 32767 / m) with m the chunk's max |h|, so it carries its
+// own scale sigma = m / 32767.  The task scale folds the routing weight
+// (routed) and sigma.
 struct HTask {
   uint4 v[4];
   float s;       // chunk sum of the int16 values
@@ -697,39 +696,66 @@ struct HTask {
   int c;         // chunk within the branch
 };
 
+constexpr int kMaxHV = 8;  // K*I + S <= 4 * kConsumers * kMaxHV
+
+// h (fp32, global) -> the tasks' registers.  The loads are warp-contiguous
+// (a warp instruction reads 512 consecutive bytes, which the L2 serves far
+// faster than a line per thread); the 8 lanes that hold one chunk find its
+// max and sum with shuffles, and the packed chunks pass through the
+// activation region of shared memory to their task threads.
 __device__ void load_htask(const Ctx& cx, HTask& ht) {
   const DecodeParams& p = *cx.p;
   const int t = threadIdx.x;
+  const int nh = p.K * p.I + p.S;
+  const int n4 = nh / 4;
+  uint8_t* stage = cx.smem + p.off_vec;  // [nchunks] x kChunkStride bytes
+  float* csig = reinterpret_cast<float*>(stage + (nh / 32) * kChunkStride);
+  float* csum = csig + nh / 32;
+  float4 r[kMaxHV];
+#pragma unroll
+  for (int i = 0; i < kMaxHV; ++i) {
+    const int idx = t + i * kConsumers;
+    r[i] = idx < n4 ? __ldcg(reinterpret_cast<const float4*>(p.h) + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxHV; ++i) {
+    const int idx = t + i * kConsumers;  // chunk idx / 8, part idx % 8
+    float m = fmaxf(fmaxf(fabsf(r[i].x), fabsf(r[i].y)), fmaxf(fabsf(r[i].z), fabsf(r[i].w)));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    const float q = quant_factor(m);
+    const uint2 packed = make_uint2(pack_s16x2(r[i].x * q, r[i].y * q), pack_s16x2(r[i].z * q, r[i].w * q));
+    int cs = dp2a_lo(packed.y, 0x01010101u, dp2a_lo(packed.x, 0x01010101u, 0));
+    cs += __shfl_xor_sync(0xffffffffu, cs, 1);
+    cs += __shfl_xor_sync(0xffffffffu, cs, 2);
+    cs += __shfl_xor_sync(0xffffffffu, cs, 4);
+    if (idx < n4) {
+      *reinterpret_cast<uint2*>(stage + (idx >> 3) * kChunkStride + (idx & 7) * 8) = packed;
+      if ((idx & 7) == 0) {
+        csig[idx >> 3] = m / 32767.f;
+        csum[idx >> 3] = static_cast<float>(cs);
+      }
+    }
+  }
+  csync();
   const int nch_i = p.I / 32;
   ht.k = -1;
-  if (t >= p.ntask) return;
-  const float4* src = reinterpret_cast<const float4*>(p.h) + t * 8;
-  float4 r[8];
+  if (t < p.ntask) {
+    const uint4* v = reinterpret_cast<const uint4*>(stage + t * kChunkStride);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) r[j] = __ldcg(src + j);
-  float m = 0.f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(r[j].x), fabsf(r[j].y)), fmaxf(fabsf(r[j].z), fabsf(r[j].w))));
-  const float q = quant_factor(m);
-  int cs = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float4 a = r[2 * j], b = r[2 * j + 1];
-    ht.v[j] = make_uint4(pack_s16x2(a.x * q, a.y * q), pack_s16x2(a.z * q, a.w * q),
-                         pack_s16x2(b.x * q, b.y * q), pack_s16x2(b.z * q, b.w * q));
-    cs += sum8_s16(ht.v[j]);
-  }
-  ht.s = static_cast<float>(cs);
-  const float sigma = m / 32767.f;
-  if (t < p.K * nch_i) {
-    ht.k = t / nch_i;
-    ht.c = t % nch_i;
-    ht.scale = __int_as_float(cx.misc[M_WTS + ht.k]) * sigma;
-  } else {
-    ht.k = p.K;
-    ht.c = t - p.K * nch_i;
-    ht.scale = sigma;
+    for (int j = 0; j < 4; ++j) ht.v[j] = v[j];
+    ht.s = csum[t];
+    const float sigma = csig[t];
+    if (t < p.K * nch_i) {
+      ht.k = t / nch_i;
+      ht.c = t % nch_i;
+      ht.scale = __int_as_float(cx.misc[M_WTS + ht.k]) * sigma;
+    } else {
+      ht.k = p.K;
+      ht.c = t - p.K * nch_i;
+      ht.scale = sigma;
+    }
   }
 }
 
@@ -973,6 +999,20 @@ __device__ bool wait_full(const Ctx& cx, int st_idx) {
   return !cx.misc[M_ABORT];
 }
 
+// Per-warp wait for a stage (no CTA barrier): every lane waits on the
+// mbarrier phase itself, so each sees the copy engine's writes.  A timeout
+// sets the abort flag; the warp then skips its work and the CTA leaves at its
+// next CTA-wide check, so no warp is left waiting at a barrier.
+__device__ bool wait_full_warp(const Ctx& cx, int st_idx) {
+  const DecodeParams& p = *cx.p;
+  const int slot = st_idx % p.nslots;
+  const uint32_t round = st_idx / p.nslots;
+  bool ok = mbar_wait(&cx.full[slot], round & 1, p.timeout_ns, &cx.misc[M_ABORT]);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0) cx.misc[M_ABORT] = 1;
+  return ok;
+}
+
 __device__ void release_slot(const Ctx& cx, int st_idx) {
   const int slot = st_idx % cx.p->nslots;
   __syncwarp();
@@ -1046,29 +1086,35 @@ __device__ void consumer(const Ctx& cx) {
     const float vs = xv.vscale[0];
     for (; s < lp.n_r + lp.n_bs; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
-      if (!wait_full(cx, st_idx)) return;
+      const bool ok = wait_full_warp(cx, st_idx);
       if (s == lp.n_r) trace(cx, li, 3);
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
-      compute_b(cx, buf, st.n, xr, vs, p.h + p.K * p.I + st.a);
-      csync();
-      release_slot(cx, st_idx);
+      if (ok) {
+        compute_b(cx, buf, st.n, xr, vs, p.h + p.K * p.I + st.a);
+        release_slot(cx, st_idx);
+      }
       ++st_idx;
     }
     trace(cx, li, 4);
     // ---- routed gate/up
     for (; s < lp.n_r + lp.n_bs + lp.n_br; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
-      if (!wait_full(cx, st_idx)) return;
+      const bool ok = wait_full_warp(cx, st_idx);
       if (s == lp.n_r + lp.n_bs) trace(cx, li, 5);
       if (s == lp.n_r + lp.n_bs + lp.n_br - 1) trace(cx, li, 6);
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
-      compute_b(cx, buf, st.n, xr, vs, p.h + st.a);
-      csync();
-      release_slot(cx, st_idx);
+      if (ok) {
+        compute_b(cx, buf, st.n, xr, vs, p.h + st.a);
+        release_slot(cx, st_idx);
+      }
       ++st_idx;
     }
     trace(cx, li, 7);
-    if (!(p.phases & PH_C)) continue;
+    if (!(p.phases & PH_C)) {
+      csync();  // the warps waited on their own: agree on the abort flag
+      if (cx.misc[M_ABORT]) return;
+      continue;
+    }
     // ---- down + combine (+ next router's partial logits)
     if (!grid_barrier(cx)) return;
     trace(cx, li, 8);
@@ -1166,7 +1212,10 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
     return o;
   };
   if (vb < p->rc_max * kConsumers * 4) vb = (p->rc_max * kConsumers * 4 + 127) / 128 * 128;
-  const int o_vec = take(vb);  // also the C-stage partials [rc_max][kConsumers]
+  const int nc_h = (p->K * p->I + p->S) / 32;
+  const int hb = nc_h * kChunkStride + 2 * nc_h * 4;  // staged int16 chunks of h + sigma, sum
+  if (vb < hb) vb = (hb + 127) / 128 * 128;
+  const int o_vec = take(vb);  // also h's staging and the C-stage partials [rc_max][kConsumers]
   const int o_rpart = take(kConsumerWarps * p->E * 4);
   const int o_xnext = take(256 * 4);
   const int o_xres = take(256 * 4);
