@@ -348,15 +348,16 @@ __device__ void prefetch_routed_dn(const Ctx& cx, int li) {
 }
 
 // Once the layer's ids are known the routed gate/up rows are needed first:
-// their bulk copies go out before the down-row hints, and only the stages
-// that find no free ring slot are hinted into L2 ahead of their copies.
+// their bulk copies go out at once, and only the stages that find no free
+// ring slot are hinted into L2 ahead of their copies (with the down rows).
+// Otherwise the down rows come with the C stages' own copies, which the ring
+// issues while the gate/up stages are consumed, behind the gate/up data.
 __device__ void producer(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
   int st_idx = 0;
   for (int li = 0; li < p.n_layers; ++li) {
     const LayerPlan lp = layer_plan(p, cx.part, li);
     const int total = lp.n_r + lp.n_bs + lp.n_br + lp.n_c;
-    const int br_end = lp.n_r + lp.n_bs + lp.n_br;
     bool gu_hinted = false;
     prefetch_fixed(cx, li);
     for (int s = 0; s <= total; ++s) {
@@ -385,7 +386,6 @@ __device__ void producer(const Ctx& cx) {
       issue_stage(cx, st, li, cx.smem + static_cast<int64_t>(slot) * p.slot_bytes, &cx.full[slot]);
       ++st_idx;
       cx.misc[M_ISSUED] = st_idx;
-      if (s == br_end - 1 && !gu_hinted) prefetch_routed_dn(cx, li);
     }
   }
 }
@@ -811,9 +811,11 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
     }
   }
   csync();
-  // One warp per row: a fixed-order tree sum of the row's task partials, the
-  // output element, and the row's term of the next router's logits, which
-  // each warp accumulates in its own row of rpart ([kConsumerWarps][E]).
+  // One warp per row, two rows per warp at a time (rows rr and rr + 8, for
+  // independent work in flight): a fixed-order tree sum of the row's task
+  // partials, the output element, and the row's term of the next router's
+  // logits, which each warp accumulates in its own row of rpart
+  // ([kConsumerWarps][E]).
   const int warp = t >> 5, lane = t & 31;
   const bool nr = c_has_router(p, li);
   const uint8_t* rq = buf + static_cast<int64_t>(n) * (p.K * p.rbI + p.rbS);  // [n][E] codes
@@ -821,25 +823,57 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
   const int g0 = r0 / kGroup;
   float* rp = rpart + warp * p.E;
   const float* xres = reinterpret_cast<const float*>(cx.smem + p.off_xres);
-  for (int rr = warp; rr < n; rr += kConsumerWarps) {
-    float y = 0.f;
-    for (int j = lane; j < p.ntask; j += 32) y += contrib[rr * kConsumers + j];
+  constexpr int kPer = kConsumers / 32;  // task partials per lane and row
+  for (int rb = warp; rb < n; rb += 2 * kConsumerWarps) {
+    const int rr[2] = {rb, rb + kConsumerWarps};
+    float y[2];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-    const int d = r0 + rr;
-    float out = y;
-    if (p.residual) out += xres[d - cx.part.c_lo];
-    const uint16_t ob = f32_to_bf16_bits(out);
-    if (lane == 0) x_next[d] = ob;
+    for (int q = 0; q < 2; ++q) {
+      float v[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int j = lane + 32 * i;
+        v[i] = (rr[q] < n && j < p.ntask) ? contrib[rr[q] * kConsumers + j] : 0.f;
+      }
+#pragma unroll
+      for (int w = 1; w < kPer; w *= 2)
+#pragma unroll
+        for (int i = 0; i < kPer; i += 2 * w) v[i] += v[i + w];
+      y[q] = v[0];
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      y[0] += __shfl_xor_sync(0xffffffffu, y[0], o);
+      y[1] += __shfl_xor_sync(0xffffffffu, y[1], o);
+    }
+    float xd[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      xd[q] = 0.f;
+      if (rr[q] < n) {
+        const int d = r0 + rr[q];
+        float out = y[q];
+        if (p.residual) out += xres[d - cx.part.c_lo];
+        const uint16_t ob = f32_to_bf16_bits(out);
+        if (lane == 0) x_next[d] = ob;
+        xd[q] = bf16_bits_to_f32(ob);
+      }
+    }
     if (nr) {
-      const float xd = bf16_bits_to_f32(ob);
-      const uint32_t* sbr = rsb + (d / kGroup - g0) * p.E;
-      const uint8_t* qr = rq + rr * p.E;
+      const bool two = rr[1] < n;
+      const uint32_t* sb0 = rsb + ((r0 + rr[0]) / kGroup - g0) * p.E;
+      const uint32_t* sb1 = rsb + ((r0 + (two ? rr[1] : rr[0])) / kGroup - g0) * p.E;
+      const uint8_t* q0 = rq + rr[0] * p.E;
+      const uint8_t* q1 = rq + (two ? rr[1] : rr[0]) * p.E;
+#pragma unroll 4
       for (int e = lane; e < p.E; e += 32) {
-        const uint32_t w = sbr[e];
-        const __half2 h2 = *reinterpret_cast<const __half2*>(&w);
-        const float wv = fmaf(__low2float(h2), static_cast<float>(qr[e]), __high2float(h2));
-        rp[e] = fmaf(wv, xd, rp[e]);
+        const uint32_t w0 = sb0[e], w1 = sb1[e];
+        const __half2 h0 = *reinterpret_cast<const __half2*>(&w0);
+        const __half2 h1 = *reinterpret_cast<const __half2*>(&w1);
+        const float wv0 = fmaf(__low2float(h0), static_cast<float>(q0[e]), __high2float(h0));
+        const float wv1 = fmaf(__low2float(h1), static_cast<float>(q1[e]), __high2float(h1));
+        const float acc = fmaf(wv0, xd[0], rp[e]);
+        rp[e] = two ? fmaf(wv1, xd[1], acc) : acc;
       }
     }
   }

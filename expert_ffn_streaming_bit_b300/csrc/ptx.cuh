@@ -53,14 +53,31 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Wait on a phase of an mbarrier for at most `timeout_ns`, giving up early
-// when *abort becomes non-zero.  Returns false if the phase did not complete.
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// is suspended until the phase completes or about `hint_ns` pass, instead of
+// returning at once, so a waiting warp takes no issue slots from the
+// computing ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait on a phase of an mbarrier for at most `timeout_ns` (checked between
+// suspensions of at most 20 us), giving up early when *abort becomes
+// non-zero.  Returns false if the phase did not complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
                                           const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (abort && *abort) return false;
     if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
