@@ -969,10 +969,11 @@ __device__ bool grid_barrier(const Ctx& cx) {
   const DecodeParams& p = *cx.p;
   csync();
   if (threadIdx.x == 0) {
+    // The CTA barrier above orders the other threads' writes before this
+    // thread's release, which carries them (release is cumulative).
     unsigned long long* ctr = reinterpret_cast<unsigned long long*>(p.bar);
     const unsigned long long G = static_cast<unsigned long long>(cx.G);
     volatile unsigned long long* tgt = reinterpret_cast<volatile unsigned long long*>(cx.misc + M_TARGET);
-    __threadfence();
     unsigned long long target;
     if (*tgt == 0ull) {
       const unsigned long long old = atom_add_acq_rel_gpu_u64(ctr, 1ull);
@@ -982,18 +983,20 @@ __device__ bool grid_barrier(const Ctx& cx) {
       target = *tgt + G;
     }
     *tgt = target;
-    bool ok = ld_acquire_gpu_u64(ctr) >= target;
-    if (!ok) {
-      const uint64_t t0 = globaltimer_ns();
-      for (;;) {
-        if (ld_acquire_gpu_u64(ctr) >= target) {
-          ok = true;
-          break;
-        }
-        if (ld_acquire_gpu(p.bar + 2) != DEV_OK) break;
-        if (globaltimer_ns() - t0 > p.timeout_ns) break;
-        __nanosleep(16);
+    // Poll with relaxed loads of the counter and the status word issued
+    // together (one round trip per poll); one acquire load once it is done.
+    bool ok = false;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      const unsigned long long c = ld_relaxed_gpu_u64(ctr);
+      const uint32_t st = ld_relaxed_gpu(p.bar + 2);
+      if (c >= target) {
+        (void)ld_acquire_gpu_u64(ctr);
+        ok = true;
+        break;
       }
+      if (st != DEV_OK) break;
+      if (globaltimer_ns() - t0 > p.timeout_ns) break;
     }
     if (!ok) {
       atomicCAS(p.bar + 2, DEV_OK, DEV_TIMEOUT);
