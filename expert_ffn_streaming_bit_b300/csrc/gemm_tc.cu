@@ -24,7 +24,9 @@
 //   warps 10-17  epilogue: tensor memory -> registers; gate/up units write
 //                h = gelu(g) * u (fp16, times a per-token power of two that
 //                keeps it in range), down units undo that factor and write the
-//                routing-weighted expert output (bf16) or the shared output (fp32)
+//                routing-weighted expert output (bf16) or the shared output
+//                (fp32), each chunk transposed through shared memory into
+//                16-byte row-segment stores
 // Rings are mbarrier-pipelined; every wait is bounded in time and a wait that
 // runs out sets the status word and ends the CTA's work.
 #include <cuda.h>
@@ -62,8 +64,9 @@ struct Bars {
 };
 
 constexpr int kMetaBytes = 2 * kUnitTokens * 4;  // per-column factors
+constexpr int kStageBytes = 2048;                // per epilogue warp: output transpose
 constexpr int kSmemBytes = kNP * kPBytes + kNA * kABytes + kNB * kBBytes + kMetaBytes +
-                           1024 /*Bars*/ + 1024 /*alignment slack*/;
+                           kEpiWarps * kStageBytes + 1024 /*Bars*/ + 1024 /*alignment slack*/;
 
 __device__ __forceinline__ float gelu_tanh(float x) {
   const float c = 0.7978845608028654f;  // sqrt(2/pi)
@@ -226,15 +229,20 @@ __device__ void role_mma(const GemmParams& p, uint8_t* A, uint8_t* B, Bars* bars
 
 // Epilogue (8 warps): warp w reads tensor-memory lanes of quarter w % 4 and
 // the 32-column chunks of parity (w - 10) / 4.  Per unit, per-column (token)
-// factors are first gathered into shared memory.
+// factors are first gathered into shared memory.  A thread holds one output
+// feature for 32 tokens; the warp transposes each chunk through its own
+// 2 KB of shared memory so that the global stores are 16-byte vectors
+// covering whole output row segments (one token row per group of lanes).
 __device__ __forceinline__ void epi_sync() { named_sync(1, kEpiWarps * 32); }
 
-__device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, int nU) {
+__device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint8_t* stage,
+                              int nU) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = w & 3;
   const int chalf = (w - kEpiWarp0) >> 2;
   const int te = threadIdx.x - kEpiWarp0 * 32;  // 0..255
   const uint32_t tmem = bars->tmem_base;
+  uint8_t* stg = stage + (w - kEpiWarp0) * kStageBytes;
   uint32_t uc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x, ++uc) {
     const GemmUnit un = p.units[u];
@@ -262,37 +270,86 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, int 
         tmem_ld_wait();
         if (p.mode == 0) {
           // rows 2j / 2j+1 of the tile are gate / up of output column j:
-          // the even lane takes columns c0..c0+15, the odd lane c0+16..c0+31
-          const int j = mt * 64 + 16 * q + (lane >> 1);
+          // the even lane takes columns c0..c0+15, the odd lane c0+16..c0+31.
+          // Stage: [32 tokens][16 columns] fp16 (32-byte rows).
+          const int jj = lane >> 1;
           const bool odd = lane & 1;
-          __half* hout = reinterpret_cast<__half*>(p.hout[un.kind]);
+          __half* sh = reinterpret_cast<__half*>(stg);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float mine_lo = __uint_as_float(r[i]), mine_hi = __uint_as_float(r[16 + i]);
             const float recv = __shfl_xor_sync(0xffffffffu, odd ? mine_lo : mine_hi, 1);
             const float g = odd ? recv : mine_lo;
             const float v = odd ? mine_hi : recv;
-            const int col = c0 + (odd ? 16 : 0) + i;
+            const int tc = (odd ? 16 : 0) + i;  // token within the chunk
+            const int col = c0 + tc;
+            float h = 0.f;
             if (col < un.n) {
               const float sg = meta[col];
-              const float h = gelu_tanh(g * sg) * (v * sg) * meta[kUnitTokens + col];
-              hout[static_cast<int64_t>(un.row0 + col) * p.hld[un.kind] + j] =
-                  __float2half_rn(fminf(fmaxf(h, -65504.f), 65504.f));
+              h = gelu_tanh(g * sg) * (v * sg) * meta[kUnitTokens + col];
+            }
+            sh[tc * 16 + jj] = __float2half_rn(fminf(fmaxf(h, -65504.f), 65504.f));
+          }
+          __syncwarp();
+          __half* hout = reinterpret_cast<__half*>(p.hout[un.kind]);
+          const int j0 = mt * 64 + 16 * q;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int tc = 16 * k + (lane >> 1);
+            const int col = c0 + tc;
+            if (col < un.n) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + tc * 32 + (lane & 1) * 16);
+              *reinterpret_cast<uint4*>(hout + static_cast<int64_t>(un.row0 + col) * p.hld[un.kind] +
+                                        j0 + (lane & 1) * 8) = v;
             }
           }
-        } else {
-          const int d = mt * 128 + 32 * q + lane;
+          __syncwarp();
+        } else if (un.kind == 0) {
+          // routed down: bf16 [32 tokens][32 features] (64-byte rows)
+          const int d0 = mt * 128 + 32 * q;
+          __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int col = c0 + i;
+            const float v = col < un.n ? __uint_as_float(r[i]) * meta[col] : 0.f;
+            sb[i * 32 + lane] = __float2bfloat16_rn(v);
+          }
+          __syncwarp();
+          __nv_bfloat16* eout = reinterpret_cast<__nv_bfloat16*>(p.eout);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int tc = 8 * k + (lane >> 2);
+            const int col = c0 + tc;
             if (col < un.n) {
-              const float v = __uint_as_float(r[i]) * meta[col];
-              const int64_t o = static_cast<int64_t>(un.row0 + col) * p.D + d;
-              if (un.kind == 0)
-                reinterpret_cast<__nv_bfloat16*>(p.eout)[o] = __float2bfloat16_rn(v);
-              else
-                p.sout[o] = v;
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + tc * 64 + (lane & 3) * 16);
+              *reinterpret_cast<uint4*>(eout + static_cast<int64_t>(un.row0 + col) * p.D + d0 +
+                                        (lane & 3) * 8) = v;
             }
+          }
+          __syncwarp();
+        } else {
+          // shared down: fp32 [16 tokens][32 features] (128-byte rows), twice
+          const int d0 = mt * 128 + 32 * q;
+          float* sf = reinterpret_cast<float*>(stg);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = c0 + 16 * hh + i;
+              sf[i * 32 + lane] = col < un.n ? __uint_as_float(r[16 * hh + i]) * meta[col] : 0.f;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int tc = 4 * k + (lane >> 3);
+              const int col = c0 + 16 * hh + tc;
+              if (col < un.n) {
+                const uint4 v = *reinterpret_cast<const uint4*>(stg + tc * 128 + (lane & 7) * 16);
+                *reinterpret_cast<uint4*>(p.sout + static_cast<int64_t>(un.row0 + col) * p.D + d0 +
+                                          (lane & 7) * 4) = v;
+              }
+            }
+            __syncwarp();
           }
         }
       }
@@ -312,7 +369,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   uint8_t* A = P + kNP * kPBytes;
   uint8_t* B = A + kNA * kABytes;
   float* meta = reinterpret_cast<float*>(B + kNB * kBBytes);
-  Bars* bars = reinterpret_cast<Bars*>(B + kNB * kBBytes + kMetaBytes);
+  uint8_t* stage = B + kNB * kBBytes + kMetaBytes;
+  Bars* bars = reinterpret_cast<Bars*>(stage + kEpiWarps * kStageBytes);
   const int w = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNP; ++i) {
@@ -347,7 +405,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   } else if (w < kEpiWarp0) {
     role_dequant(p, P, A, bars, nU);
   } else {
-    role_epilogue(p, bars, meta, nU);
+    role_epilogue(p, bars, meta, stage, nU);
   }
   tc_fence_before();
   __syncthreads();
