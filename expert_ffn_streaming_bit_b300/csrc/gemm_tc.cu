@@ -3,24 +3,35 @@
 //
 // One work unit = up to two 128-row tiles of one 4-bit weight matrix (an
 // expert's interleaved gate/up rows, its down rows, or the shared expert's)
-// against up to 256 activation rows (the tokens routed to that expert, in
+// against up to 96 activation rows (the tokens routed to that expert, in
 // bucket order, or a tile of all tokens for the shared expert).  The weight
-// tiles are the MMA's M side (128 each), the tokens its N side (16..256 in
+// tiles are the MMA's M side (128 each), the tokens its N side (16..96 in
 // steps of 16), so the tile shape follows the ragged per-expert token counts
 // without padding M; the two weight tiles share each activation tile, which
 // halves the activation traffic per FLOP.
 //
+// The dequantised weights never touch shared memory: the dequantisation
+// warps write them straight into tensor memory, and the MMA reads its A
+// operand from there (only the activations come from shared memory).  That
+// keeps the shared-memory traffic per FLOP well under its bandwidth, which
+// A tiles written to and read back from shared memory would exceed.
+// Tensor memory (512 columns): two accumulator sets of 2 tiles x 96 columns
+// (the epilogue drains one unit while the MMA fills the next) and two A
+// stages of 2 tiles x 32 columns (64 fp16 of K per row).
+//
 // Per CTA (persistent, one per SM, 18 warps):
 //   warp 0       TMA: packed 4-bit codes (128 B x 128 rows, 128-byte swizzle)
 //                and scale/bias words (16 B x 128 rows) of a 256-column slice
-//                of each weight tile -> P ring (2 stages); the activation
-//                tile (64 fp16 columns x 256 rows, 128-byte swizzle, the
-//                UMMA K-major layout) -> B ring (2 stages)
+//                of each weight tile -> P ring (4 stages); the activation
+//                tile (64 fp16 columns x 96 rows, 128-byte swizzle, the UMMA
+//                K-major layout) -> B ring (4 stages)
 //   warp 1       MMA: one thread issues tcgen05.mma kind::f16 (M=128,
-//                N=tokens, K=16), 4 k-steps x 2 tiles per 64-column block,
-//                fp32 accumulators in tensor memory (2 x 256 columns)
-//   warps 2-9    dequantisation: P stage -> fp16 weights w = fp16(s q + b)
-//                (one rounding) in the swizzled K-major layout -> A ring
+//                N=tokens, K=16, A in tensor memory), 4 k-steps x 2 tiles per
+//                64-column block, fp32 accumulators in tensor memory
+//   warps 2-9    dequantisation: warp w takes tile (w-2)/4 and the 32 rows of
+//                its tensor-memory lane quarter w%4; per 64-column block each
+//                thread turns its row's codes into fp16 w = fp16(s q + b) (one
+//                rounding) and stores them into the A stage
 //   warps 10-17  epilogue: tensor memory -> registers; gate/up units write
 //                h = gelu(g) * u (fp16, times a per-token power of two that
 //                keeps it in range), down units undo that factor and write the
@@ -41,15 +52,18 @@ namespace moe {
 
 namespace {
 
-constexpr int kNP = 2, kNA = 2, kNB = 2;
+constexpr int kNP = 4, kNA = 2, kNB = 4;
 constexpr int kPCodeBytes = 128 * 128;             // 128 rows x 256 columns of 4-bit codes
 constexpr int kPSbBytes = 128 * 16;                // 128 rows x 4 scale/bias words
 constexpr int kPTile = kPCodeBytes + kPSbBytes;    // 18 KB per weight tile
 constexpr int kPBytes = 2 * kPTile;                // two weight tiles per P stage
-constexpr int kATile = 128 * 128;                  // 128 rows x 64 fp16
-constexpr int kABytes = 2 * kATile;
-constexpr int kBBytes = kUnitTokens * 128;         // 256 rows x 64 fp16
-constexpr int kTmemCols = 512;                     // 2 tiles x 256 columns
+constexpr int kBBytes = kUnitTokens * 128;         // 96 rows x 64 fp16
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = kUnitTokens;              // per tile
+constexpr int kAccSet = 2 * kAccCols;              // one unit's accumulators
+constexpr int kACol0 = 2 * kAccSet;                // A stages after the two sets
+constexpr int kAStage = 2 * 32;                    // 2 tiles x 32 columns
+static_assert(kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
 constexpr int kDqWarps = 8, kEpiWarps = 8;
 constexpr int kGemmThreads = (2 + kDqWarps + kEpiWarps) * 32;
 constexpr int kEpiWarp0 = 2 + kDqWarps;
@@ -58,15 +72,15 @@ struct Bars {
   uint64_t p_full[kNP], p_empty[kNP];
   uint64_t a_full[kNA], a_empty[kNA];
   uint64_t b_full[kNB], b_empty[kNB];
-  uint64_t acc_full, acc_empty;
+  uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   int abort;
 };
 
 constexpr int kMetaBytes = 2 * kUnitTokens * 4;  // per-column factors
 constexpr int kStageBytes = 2048;                // per epilogue warp: output transpose
-constexpr int kSmemBytes = kNP * kPBytes + kNA * kABytes + kNB * kBBytes + kMetaBytes +
-                           kEpiWarps * kStageBytes + 1024 /*Bars*/ + 1024 /*alignment slack*/;
+constexpr int kSmemBytes = kNP * kPBytes + kNB * kBBytes + kMetaBytes + kEpiWarps * kStageBytes +
+                           1024 /*Bars*/ + 1024 /*alignment slack*/;
 
 __device__ __forceinline__ float gelu_tanh(float x) {
   const float c = 0.7978845608028654f;  // sqrt(2/pi)
@@ -132,10 +146,12 @@ __device__ void role_tma(const GemmParams& p, uint8_t* P, uint8_t* B, Bars* bars
     mbar_wait(&bars->b_full[q % kNB], (q / kNB) & 1, p.timeout_ns, nullptr);
 }
 
-__device__ void role_dequant(const GemmParams& p, const uint8_t* P, uint8_t* A, Bars* bars,
-                             int nU) {
-  const int t = threadIdx.x - 2 * 32;  // 0..255
-  const int lane = threadIdx.x & 31;
+__device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, int nU) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = (w - 2) >> 2;          // weight tile
+  const int qd = w & 3;                // tensor-memory lane quarter
+  const int row = 32 * qd + lane;      // row of the weight tile
+  const uint32_t tbase = bars->tmem_base + (static_cast<uint32_t>(32 * qd) << 16);
   uint32_t pc = 0, ac = 0;
   const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
   for (int u = blockIdx.x; u < nU; u += gridDim.x) {
@@ -143,51 +159,49 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, uint8_t* A, 
     const int K = p.K[un.kind];
     const int nkb = K / 64;
     const int np = (K + 255) / 256;
+    const bool active = m < un.nmt;  // warp-uniform
     for (int sp = 0; sp < np; ++sp, ++pc) {
       const int st = pc % kNP;
       if (!wait_bar(&bars->p_full[st], (pc / kNP) & 1, p, bars)) return;
       const int nsub = min(4, nkb - 4 * sp);
+      const uint8_t* codes = P + st * kPBytes + m * kPTile;
+      const uint32_t* sbw = reinterpret_cast<const uint32_t*>(codes + kPCodeBytes);
       for (int sb = 0; sb < nsub; ++sb, ++ac) {
         const int as = ac % kNA;
         if (!wait_bar(&bars->a_empty[as], ((ac / kNA) & 1) ^ 1, p, bars)) return;
-        // tasks (tile m, row, half): 2 per thread
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int task = t + 256 * h;
-          const int m = task >> 8, row = task & 127, half = (task >> 7) & 1;
-          if (m >= un.nmt) continue;
-          const uint8_t* codes = P + st * kPBytes + m * kPTile;
-          const uint32_t* sbw = reinterpret_cast<const uint32_t*>(codes + kPCodeBytes);
-          // packed chunk c (32 columns) of this row, stored at chunk c ^ (row & 7)
-          const int c = 2 * sb + half;
-          const uint4 w = *reinterpret_cast<const uint4*>(codes + row * 128 + ((c ^ (row & 7)) << 4));
+        if (active) {
           const uint32_t word = sbw[row * 4 + sb];
           const __half2 s2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word & 0xffffu)));
           const __half2 b2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word >> 16)));
-          uint8_t* arow = A + as * kABytes + m * kATile + row * 128;
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          uint32_t o[32];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // word j: columns 8j..8j+7 of the chunk; byte i = col i (low) | col 4+i (high)
-            const uint32_t lo = ws[j] & 0x0F0F0F0Fu;
-            const uint32_t hi = (ws[j] >> 4) & 0x0F0F0F0Fu;
-            // fp16 1024 + q pairs: bytes (q, 0x64) per half
-            const uint32_t mm[4] = {__byte_perm(lo, 0x64646464u, 0x5140),
-                                    __byte_perm(lo, 0x64646464u, 0x7362),
-                                    __byte_perm(hi, 0x64646464u, 0x5140),
-                                    __byte_perm(hi, 0x64646464u, 0x7362)};
-            uint32_t o[4];
+          for (int half = 0; half < 2; ++half) {
+            // packed chunk c (32 columns) of this row, stored at chunk c ^ (row & 7)
+            const int c = 2 * sb + half;
+            const uint4 wq = *reinterpret_cast<const uint4*>(codes + row * 128 + ((c ^ (row & 7)) << 4));
+            const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&mm[i]), k1024);
-              const __half2 v = __hfma2(q, s2, b2);
-              o[i] = *reinterpret_cast<const uint32_t*>(&v);
+            for (int j = 0; j < 4; ++j) {
+              // word j: columns 8j..8j+7 of the chunk; byte i = col i (low) | col 4+i (high)
+              const uint32_t lo = ws[j] & 0x0F0F0F0Fu;
+              const uint32_t hi = (ws[j] >> 4) & 0x0F0F0F0Fu;
+              // fp16 1024 + q pairs: bytes (q, 0x64) per half
+              const uint32_t mm[4] = {__byte_perm(lo, 0x64646464u, 0x5140),
+                                      __byte_perm(lo, 0x64646464u, 0x7362),
+                                      __byte_perm(hi, 0x64646464u, 0x5140),
+                                      __byte_perm(hi, 0x64646464u, 0x7362)};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&mm[i]), k1024);
+                const __half2 v = __hfma2(q, s2, b2);
+                o[16 * half + 4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
+              }
             }
-            const int lc = 4 * half + j;  // logical 16-byte chunk in the 128-byte row
-            *reinterpret_cast<uint4*>(arow + ((lc ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
+          tmem_st32(tbase + kACol0 + as * kAStage + m * 32, o);
+          tmem_st_wait();
         }
-        fence_proxy_async_smem();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->a_full[as]);
       }
@@ -197,34 +211,50 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, uint8_t* A, 
   }
 }
 
-__device__ void role_mma(const GemmParams& p, uint8_t* A, uint8_t* B, Bars* bars, int nU) {
+// The issue loop is kept to a few instructions per MMA: descriptors are
+// precomputed (a B stage is the stage-0 descriptor plus its offset in 16-byte
+// units, a k-step adds 32 bytes), the k-steps and tiles are unrolled.
+__device__ __forceinline__ void mma_kblock(uint32_t acc, uint32_t a0, uint64_t bd, uint32_t idesc,
+                                           int nmt, uint32_t first) {
+  if (nmt == 2) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t f = kk == 0 ? first : 1u;
+      tc_mma_f16_ts(acc, a0 + 8 * kk, bd + 2 * kk, idesc, f);
+      tc_mma_f16_ts(acc + kAccCols, a0 + 32 + 8 * kk, bd + 2 * kk, idesc, f);
+    }
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) tc_mma_f16_ts(acc, a0 + 8 * kk, bd + 2 * kk, idesc, kk == 0 ? first : 1u);
+  }
+}
+
+__device__ void role_mma(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
   const uint32_t tmem = bars->tmem_base;
+  const uint64_t bdesc0 = tc_desc_sw128(smem_u32(B));
   uint32_t ac = 0, bc = 0, uc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x, ++uc) {
     const GemmUnit un = p.units[u];
     const int K = p.K[un.kind];
     const int nkb = K / 64;
     const uint32_t idesc = tc_idesc_f16(128, unit_nmma(un.n));
-    if (!wait_bar(&bars->acc_empty, (uc & 1) ^ 1, p, bars)) return;
+    const uint32_t acc = tmem + (uc & 1) * kAccSet;  // this unit's accumulator set
+    if (!wait_bar(&bars->acc_empty[uc & 1], ((uc >> 1) & 1) ^ 1, p, bars)) return;
     tc_fence_after();
     for (int kb = 0; kb < nkb; ++kb, ++ac, ++bc) {
       const int as = ac % kNA, bs = bc % kNB;
       if (!wait_bar(&bars->a_full[as], (ac / kNA) & 1, p, bars)) return;
       if (!wait_bar(&bars->b_full[bs], (bc / kNB) & 1, p, bars)) return;
       tc_fence_after();
-      const uint32_t a0 = smem_u32(A + as * kABytes), b0 = smem_u32(B + bs * kBBytes);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        for (int m = 0; m < un.nmt; ++m)
-          tc_mma_f16(tmem + m * 256, tc_desc_sw128(a0 + m * kATile + 32 * kk),
-                     tc_desc_sw128(b0 + 32 * kk), idesc, (kb | kk) != 0);
+      mma_kblock(acc, tmem + kACol0 + as * kAStage,
+                 bdesc0 + static_cast<uint64_t>(bs * (kBBytes >> 4)), idesc, un.nmt, kb != 0);
       tc_commit(&bars->a_empty[as]);
       tc_commit(&bars->b_empty[bs]);
     }
-    tc_commit(&bars->acc_full);
+    tc_commit(&bars->acc_full[uc & 1]);
   }
   // the last commits must complete before the CTA exits
-  if (uc > 0) mbar_wait(&bars->acc_full, (uc - 1) & 1, p.timeout_ns, nullptr);
+  if (uc > 0) mbar_wait(&bars->acc_full[(uc - 1) & 1], ((uc - 1) >> 1) & 1, p.timeout_ns, nullptr);
 }
 
 // Epilogue (8 warps): warp w reads tensor-memory lanes of quarter w % 4 and
@@ -259,14 +289,20 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
         meta[col] = 1.f / p.hscale[brow];
       }
     }
-    if (!wait_bar(&bars->acc_full, uc & 1, p, bars)) return;
+    if (!wait_bar(&bars->acc_full[uc & 1], (uc >> 1) & 1, p, bars)) return;
     tc_fence_after();
     epi_sync();
-    for (int m = 0; m < un.nmt; ++m) {
+    const uint32_t acc = tmem + (uc & 1) * kAccSet;
+    // the unit's 32-column chunks (3 per tile), alternating between the two
+    // warps of this lane quarter
+    constexpr int kChunks = kAccCols / 32;
+    for (int idx = chalf; idx < un.nmt * kChunks; idx += 2) {
+      const int m = idx / kChunks, c0 = (idx % kChunks) * 32;
+      if (c0 >= un.n) continue;
       const int mt = un.mt + m;
-      for (int c0 = 32 * chalf; c0 < un.n; c0 += 64) {
+      {
         uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + m * 256 + c0, r);
+        tmem_ld32(acc + (static_cast<uint32_t>(32 * q) << 16) + m * kAccCols + c0, r);
         tmem_ld_wait();
         if (p.mode == 0) {
           // rows 2j / 2j+1 of the tile are gate / up of output column j:
@@ -356,7 +392,7 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
     }
     tc_fence_before();
     epi_sync();  // all reads of this unit's accumulator and factors are done
-    if (te == 0) mbar_arrive(&bars->acc_empty);
+    if (te == 0) mbar_arrive(&bars->acc_empty[uc & 1]);
   }
 }
 
@@ -366,8 +402,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (base & 1023u)) & 1023u);
   uint8_t* P = smem;
-  uint8_t* A = P + kNP * kPBytes;
-  uint8_t* B = A + kNA * kABytes;
+  uint8_t* B = P + kNP * kPBytes;
   float* meta = reinterpret_cast<float*>(B + kNB * kBBytes);
   uint8_t* stage = B + kNB * kBBytes + kMetaBytes;
   Bars* bars = reinterpret_cast<Bars*>(stage + kEpiWarps * kStageBytes);
@@ -385,8 +420,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
       mbar_init(&bars->b_full[i], 1);
       mbar_init(&bars->b_empty[i], 1);
     }
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->acc_full[i], 1);
+      mbar_init(&bars->acc_empty[i], 1);
+    }
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -401,9 +438,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   if (w == 0) {
     if ((threadIdx.x & 31) == 0) role_tma(p, P, B, bars, nU);
   } else if (w == 1) {
-    if ((threadIdx.x & 31) == 0) role_mma(p, A, B, bars, nU);
+    if ((threadIdx.x & 31) == 0) role_mma(p, B, bars, nU);
   } else if (w < kEpiWarp0) {
-    role_dequant(p, P, A, bars, nU);
+    role_dequant(p, P, bars, nU);
   } else {
     role_epilogue(p, bars, meta, stage, nU);
   }

@@ -101,7 +101,7 @@ struct DecodeParams {
 // GEMM's work units), two grouped GEMMs on the tensor cores (gate/up with the
 // GELU epilogue, then down), and a gather combine.
 
-constexpr int kUnitTokens = 256;   // max B rows (tokens) of one GEMM work unit
+constexpr int kUnitTokens = 96;    // max B rows (tokens) of one GEMM work unit
 constexpr int kMaxPrefillExperts = 256;
 
 // One work unit of the grouped GEMM: a 128-row tile of one weight matrix
