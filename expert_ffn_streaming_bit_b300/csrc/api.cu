@@ -1,9 +1,11 @@
 // C ABI of libmoe_b300 (declared in include/moe.h): handle lifetime, weight
 // repack and upload, the resident and streaming forward paths, and the
 // per-layer expert-slot cache.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <chrono>
 #include <cstdarg>
 #include <cstdio>
@@ -73,10 +75,13 @@ struct moe_handle {
   // prefill (T >= 2, resident mode)
   struct LayerMaps {
     CUtensorMap gu_code[2], gu_sb[2], dn_code[2], dn_sb[2];  // [0] routed, [1] shared
+    CUtensorMap rt;  // router weight as two fp16 parts, [2 Epad][D]
   };
   std::vector<LayerMaps> maps;
   CUtensorMap bmap_gu[2], bmap_dn[2];  // activation operands: [0] routed, [1] shared
   uint16_t* pf_xperm = nullptr;        // x16 rows in bucket order (routed gate/up operand)
+  uint16_t* pf_rw = nullptr;           // router weights as fp16 parts, [L][2 Epad][D]
+  CUtensorMap bmap_rt;                 // x16 in 64 x 128 boxes (router operand)
   bool prefill_ok = false;
   int mt_gu_r = 0, mt_dn = 0, mt_gu_s = 0;
   uint8_t* pf = nullptr;  // prefill scratch (one allocation)
@@ -151,6 +156,7 @@ void free_all(moe_handle* h) {
   cudaFree(h->dev_layers);
   cudaFree(h->scratch);
   cudaFree(h->pf);
+  cudaFree(h->pf_rw);
   cudaFreeHost(h->pool);
   cudaFreeHost(h->pin_x);
   cudaFreeHost(h->pin_y);
@@ -240,12 +246,13 @@ EncodeTiledFn encode_tiled() {
 // `rows` rows, and for rank 3 `planes` planes `plane_bytes` apart.
 // fp16 rows [rows][cols] (pitch cols): box 64 columns x 256 rows, 128-byte
 // swizzle (the UMMA K-major operand layout).
-bool make_act_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+bool make_act_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                  uint32_t box_rows = kUnitTokens) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kUnitTokens)};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -524,7 +531,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     const int64_t Tm = c.max_tokens, K = d.K, E = d.E;
     int64_t part = 0;
     for (int64_t t = 2; t <= Tm; ++t) {
-      const int64_t v = int64_t(router_gemm_splits(int(t), int(E), int(d.D), G)) * t * E;
+      const int64_t v = int64_t(router_tc_splits(int(t), int(E), int(d.D), G)) * t * E;
       if (v > part) part = v;
     }
     const int64_t nt = Tm * K / kUnitTokens + E + 1, stl = (Tm + kUnitTokens - 1) / kUnitTokens;
@@ -572,8 +579,37 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     if (!make_act_map(&h->bmap_gu[0], h->pf_xperm, d.D, Tm * K) ||
         !make_act_map(&h->bmap_gu[1], h->pf_x16, d.D, Tm) ||
         !make_act_map(&h->bmap_dn[0], h->pf_hr, d.I, Tm * K) ||
-        !make_act_map(&h->bmap_dn[1], h->pf_hs, d.S, Tm))
+        !make_act_map(&h->bmap_dn[1], h->pf_hs, d.S, Tm) ||
+        !make_act_map(&h->bmap_rt, h->pf_x16, d.D, Tm, 128))
       CREATE_FAIL(MOE_ERR_CUDA, "could not encode the prefill activation tensor maps");
+    // Router weights for the tensor-core router GEMM: w = s q + b (fp32, one
+    // rounding) split into fp16(w) and fp16(w - fp16(w)); rows E..Epad-1 zero.
+    {
+      const int64_t Epad = (E + 127) / 128 * 128, ng = d.D / 64;
+      const int64_t per = 2 * Epad * d.D;
+      std::vector<__half> rw(static_cast<size_t>(per));
+      CREATE_TRY(cudaMalloc(&h->pf_rw, per * 2 * L));
+      for (int l = 0; l < L; ++l) {
+        const moe_qtensor& r = layers[l].router;
+        std::fill(rw.begin(), rw.end(), __float2half_rn(0.f));
+        parallel_for(E, [&](int64_t e) {
+          for (int64_t c = 0; c < d.D; ++c) {
+            __half_raw sr, br;
+            sr.x = r.scale[e * ng + c / 64];
+            br.x = r.bias[e * ng + c / 64];
+            const float w = std::fma(__half2float(__half(sr)), static_cast<float>(r.q[e * d.D + c]),
+                                     __half2float(__half(br)));
+            const __half hi = __float2half_rn(w);
+            rw[static_cast<size_t>(e * d.D + c)] = hi;
+            rw[static_cast<size_t>((Epad + e) * d.D + c)] = __float2half_rn(w - __half2float(hi));
+          }
+        });
+        uint16_t* dst = h->pf_rw + int64_t(l) * per;
+        CREATE_TRY(cudaMemcpy(dst, rw.data(), per * 2, cudaMemcpyHostToDevice));
+        if (!make_act_map(&h->maps[l].rt, dst, d.D, 2 * Epad, 128))
+          CREATE_FAIL(MOE_ERR_CUDA, "could not encode the router tensor map");
+      }
+    }
     h->prefill_ok = true;
     h->pf_ev.resize(6 * kPhaseTimedCalls);
     for (auto& ev : h->pf_ev) CREATE_TRY(cudaEventCreate(&ev));
@@ -763,8 +799,8 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   ra.K = K;
   ra.prenorm = (flags & MOE_FWD_PRENORM) ? 1 : 0;
   ra.rms_eps = h->base.rms_eps;
-  ra.router_t = ld.router_t;
-  ra.router_sb = ld.router_sb;
+  ra.wmap = &h->maps[layer].rt;
+  ra.xmap = &h->bmap_rt;
   ra.logit_bias = ld.logit_bias;
   ra.forced = forced ? h->pf_forced : nullptr;
   ra.x16 = h->pf_x16;
@@ -772,7 +808,9 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   ra.rscale = h->pf_rscale;
   ra.hscale = h->pf_hscale;
   ra.partials = h->pf_partials;
-  ra.nsplit = router_gemm_splits(T, ra.E, ra.D, h->num_sms);
+  ra.nsplit = router_tc_splits(T, ra.E, ra.D, h->num_sms);
+  ra.status = h->bar + 2;
+  ra.timeout_ns = h->base.timeout_ns;
   ra.ids = ids;
   ra.wts = wts;
   int e = prefill_route(ra, s);

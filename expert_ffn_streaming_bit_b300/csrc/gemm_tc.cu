@@ -452,6 +452,122 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   }
 }
 
+// ------------------------------------------------------------ router GEMM
+// partial[split][t][e] = sum over the split's 64-column blocks of
+// (Whi[e] + Wlo[e]) . x16[t], fp32 accumulation on the tensor cores.  The
+// 8-bit router weight w = s q + b (fp32) is held as two fp16 parts, Whi =
+// fp16(w) and Wlo = fp16(w - Whi), so the pair carries w to about 2^-22 of
+// its size, and x16 = f_t x is exact: the logits come out as accurate as an
+// fp32 product, which the exact top-k selection needs.  CTA = 128 experts x
+// 128 tokens x one range of 64-column blocks; warp 0 lane 0 issues TMA
+// loads, warp 1 lane 0 the MMAs (M=128, N=128, K=16, both operands in shared
+// memory), then all four warps write their tensor-memory lane quarter.
+constexpr int kRtStages = 4;
+constexpr int kRtTile = 128 * 128;        // 128 rows x 64 fp16 (128-byte swizzle)
+constexpr int kRtStage = 3 * kRtTile;     // Whi, Wlo, x16
+constexpr int kRtSmem = kRtStages * kRtStage + 1024 /*bars*/ + 1024 /*alignment*/;
+
+struct RtBars {
+  uint64_t full[kRtStages], empty[kRtStages], done;
+  uint32_t tmem;
+  int abort;
+};
+
+__device__ __forceinline__ bool rt_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                        RtBars* b, uint32_t* status) {
+  if (mbar_wait(bar, parity, timeout_ns, &b->abort)) return true;
+  if (!b->abort) atomicCAS(status, DEV_OK, DEV_TIMEOUT);
+  b->abort = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(128, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                     int T, int E, int Epad, int nkb, int kbs, float* __restrict__ partials,
+                     uint32_t* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (base & 1023u)) & 1023u);
+  RtBars* bars = reinterpret_cast<RtBars*>(smem + kRtStages * kRtStage);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * 128, mt = blockIdx.y, split = blockIdx.z;
+  const int kb0 = split * kbs, kb1 = min(nkb, kb0 + kbs);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRtStages; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (w == 0) {
+    tmem_alloc(&bars->tmem, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t acc = bars->tmem;
+  if (w == 0 && lane == 0) {
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int i = kb - kb0, st = i % kRtStages;
+      if (!rt_wait(&bars->empty[st], ((i / kRtStages) & 1) ^ 1, timeout_ns, bars, status)) break;
+      uint8_t* dst = smem + st * kRtStage;
+      mbar_arrive_expect_tx(&bars->full[st], kRtStage);
+      tma_load_2d(dst, &wmap, kb * 64, mt * 128, &bars->full[st]);
+      tma_load_2d(dst + kRtTile, &wmap, kb * 64, Epad + mt * 128, &bars->full[st]);
+      tma_load_2d(dst + 2 * kRtTile, &xmap, kb * 64, t0, &bars->full[st]);
+    }
+  } else if (w == 1 && lane == 0) {
+    const uint32_t idesc = tc_idesc_f16(128, 128);
+    const uint64_t d0 = tc_desc_sw128(smem_u32(smem));
+    bool ok = true;
+    for (int kb = kb0; kb < kb1 && ok; ++kb) {
+      const int i = kb - kb0, st = i % kRtStages;
+      if (!rt_wait(&bars->full[st], (i / kRtStages) & 1, timeout_ns, bars, status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t dh = d0 + static_cast<uint64_t>(st * (kRtStage >> 4));
+      const uint64_t dl = dh + (kRtTile >> 4), dx = dh + 2 * (kRtTile >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        tc_mma_f16(acc, dh + 2 * kk, dx + 2 * kk, idesc, (i | kk) != 0);
+        tc_mma_f16(acc, dl + 2 * kk, dx + 2 * kk, idesc, 1u);
+      }
+      tc_commit(&bars->empty[st]);
+    }
+    tc_commit(&bars->done);
+  }
+  // epilogue: warp w reads tensor-memory lanes 32w.. (experts), 32 tokens per load
+  __syncwarp();
+  const bool done = __all_sync(0xffffffffu, rt_wait(&bars->done, 0, timeout_ns, bars, status));
+  if (done) {
+    tc_fence_after();
+    const int e = mt * 128 + 32 * w + lane;
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(acc + (static_cast<uint32_t>(32 * w) << 16) + c0, r);
+      tmem_ld_wait();
+      if (e < E) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int t = t0 + c0 + i;
+          if (t < T) partials[(static_cast<int64_t>(split) * T + t) * E + e] = __uint_as_float(r[i]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (w == 0) {
+    tc_fence_after();
+    tmem_dealloc(acc, 128);
+  }
+}
+
 // Token rows of x16 into bucket order (the routed gate/up activation operand).
 __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restrict__ x16, int D8,
                                                           const int32_t* __restrict__ perm, int topk,
@@ -476,6 +592,35 @@ int gemm_tc_launch(const GemmParams& p, int grid, void* stream) {
     attr = true;
   }
   gemm_tc_kernel<<<grid, kGemmThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int router_tc_splits(int T, int E, int D, int num_sms) {
+  const int tiles = ((T + 127) / 128) * ((E + 127) / 128);
+  const int nkb = D / 64;
+  int splits = (num_sms + tiles - 1) / tiles;
+  const int cap = nkb / 4 > 1 ? nkb / 4 : 1;  // at least 4 blocks per split
+  if (splits > cap) splits = cap;
+  if (splits < 1) splits = 1;
+  const int kbs = (nkb + splits - 1) / splits;
+  return (nkb + kbs - 1) / kbs;
+}
+
+int router_tc_launch(const CUtensorMap& wmap, const CUtensorMap& xmap, int T, int E, int D,
+                     int nsplit, float* partials, uint32_t* status, uint64_t timeout_ns, void* stream) {
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    attr = true;
+  }
+  const int nkb = D / 64;
+  const int kbs = (nkb + nsplit - 1) / nsplit;
+  const int Epad = (E + 127) / 128 * 128;
+  dim3 grid((T + 127) / 128, Epad / 128, nsplit);
+  router_tc_kernel<<<grid, 128, kRtSmem, static_cast<cudaStream_t>(stream)>>>(
+      wmap, xmap, T, E, Epad, nkb, kbs, partials, status, timeout_ns);
   return static_cast<int>(cudaGetLastError());
 }
 

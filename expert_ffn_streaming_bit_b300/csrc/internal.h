@@ -121,24 +121,29 @@ struct PrefillDims {
   int mt_gu_r, mt_dn, mt_gu_s;  // 128-row tiles: routed gate/up, down, shared gate/up
 };
 
-// Router GEMM: logits partials [nsplit][T][E].
-int router_gemm_splits(int T, int E, int D, int num_sms);
+// Router GEMM on the tensor cores: logits partials [nsplit][T][E].
+int router_tc_splits(int T, int E, int D, int num_sms);
+int router_tc_launch(const CUtensorMap& wmap, const CUtensorMap& xmap, int T, int E, int D,
+                     int nsplit, float* partials, uint32_t* status, uint64_t timeout_ns, void* stream);
 
 struct RouteArgs {
   const uint16_t* x;  // bf16 [T][D]
   int T, D, E, K;
   int prenorm;
   float rms_eps;
-  const uint8_t* router_t;    // [D][E] codes
-  const uint32_t* router_sb;  // [D/64][E]
+  const CUtensorMap* wmap;    // router weight as fp16 parts: rows [0, Epad) = fp16(w),
+                              // rows [Epad, 2 Epad) = fp16(w - fp16(w)), [2 Epad][D]
+  const CUtensorMap* xmap;    // x16 [T][D], 64 x 128 boxes
   const float* logit_bias;    // [E] or nullptr
   const int32_t* forced;      // device [T][K] or nullptr
   uint16_t* x16;              // fp16 [T][D] out: x * f_t
   float* sigma;               // [T] out: (r_t / f_t), the scale of dot products with x16
   float* rscale;              // [T] out: r_t (pre-norm factor, 1 without)
   float* hscale;              // [T] out: power-of-two scale of the fp16 intermediate h
-  float* partials;            // [nsplit][T][E]
+  float* partials;            // [nsplit][T][E]: sums of w . x16
   int nsplit;
+  uint32_t* status;           // device status word
+  uint64_t timeout_ns;
   int32_t* ids;               // [T][K] out
   float* wts;                 // [T][K] out
 };

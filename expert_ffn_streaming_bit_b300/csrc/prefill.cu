@@ -1,7 +1,8 @@
-// Multi-token (prefill) layer step, SIMT parts: token preparation, the 8-bit
-// router GEMM with top-k and softmax, bucketing of the T*k (token, expert)
+// Multi-token (prefill) layer step, SIMT parts: token preparation, the
+// router's top-k and softmax, bucketing of the T*k (token, expert)
 // assignments by expert together with the grouped GEMM's work units, and the
-// gather combine.  The grouped GEMMs themselves are in gemm_tc.cu.
+// gather combine.  The router GEMM and the grouped GEMMs run on the tensor
+// cores (gemm_tc.cu).
 //
 // Passages (sh.edu-sjtu.cn article, section 三件事, third bullet; shilu.ai
 // "drumih/turbo-fieldfare", section 推理引擎的工作原理): prompts are prefilled in
@@ -104,107 +105,15 @@ __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restric
   }
 }
 
-// ------------------------------------------------------------ router GEMM
-// partial[split][t][e] = sum over the split's groups g of sum_{c in g}
-// (s[e,g] q[c,e] + b[e,g]) x[t,c], fp32, fixed order.  Tile: 32 tokens x 64
-// experts per CTA, 4 x 4 outputs per thread.
-constexpr int kRtTok = 32, kRtExp = 64;
-
-__global__ void __launch_bounds__(128) router_gemm_kernel(const uint16_t* __restrict__ x, int T,
-                                                          int D, int E,
-                                                          const uint8_t* __restrict__ rt,
-                                                          const uint32_t* __restrict__ rsb,
-                                                          int groups_per_split,
-                                                          float* __restrict__ partial) {
-  __shared__ float xs[64][kRtTok + 1];
-  __shared__ __align__(16) float ws[64][kRtExp];
-  const int t0 = blockIdx.x * kRtTok, e0 = blockIdx.y * kRtExp, split = blockIdx.z;
-  const int ng = D / 64;
-  const int g0 = split * groups_per_split, g1 = min(ng, g0 + groups_per_split);
-  const int tid = threadIdx.x;
-  const int tg = tid >> 4, eg = tid & 15;
-  float acc[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int g = g0; g < g1; ++g) {
-    {  // x tile: token tid/4, 16 columns at (tid%4)*16
-      const int tt = tid >> 2, c0 = (tid & 3) * 16;
-      const int t = t0 + tt;
-      uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
-      if (t < T) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * D + g * 64 + c0);
-        a = __ldg(src);
-        b = __ldg(src + 1);
-      }
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        xs[c0 + 2 * j][tt] = bf16f(w[j] & 0xffffu);
-        xs[c0 + 2 * j + 1][tt] = bf16f(w[j] >> 16);
-      }
-    }
-    {  // weight tile: column k = tid/2 of the group, 32 experts at (tid%2)*32
-      const int k = tid >> 1, eo = (tid & 1) * 32;
-      const uint8_t* src = rt + static_cast<size_t>(g * 64 + k) * E + e0 + eo;
-      const uint32_t* sbp = rsb + static_cast<size_t>(g) * E + e0 + eo;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int eb = e0 + eo + 16 * h;
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (eb < E) q = __ldg(reinterpret_cast<const uint4*>(src + 16 * h));
-        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float wv = 0.f;
-          if (eb + i < E) {
-            const uint32_t sb = __ldg(sbp + 16 * h + i);
-            const __half2 h2 = *reinterpret_cast<const __half2*>(&sb);
-            const float code = static_cast<float>((qw[i >> 2] >> (8 * (i & 3))) & 0xffu);
-            wv = fmaf(__low2float(h2), code, __high2float(h2));
-          }
-          ws[k][eo + 16 * h + i] = wv;
-        }
-      }
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < 64; ++k) {
-      float xv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) xv[i] = xs[k][tg * 4 + i];
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[k][eg * 4]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[i][0] = fmaf(xv[i], wv.x, acc[i][0]);
-        acc[i][1] = fmaf(xv[i], wv.y, acc[i][1]);
-        acc[i][2] = fmaf(xv[i], wv.z, acc[i][2]);
-        acc[i][3] = fmaf(xv[i], wv.w, acc[i][3]);
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + tg * 4 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + eg * 4 + j;
-      if (e < E) partial[(static_cast<size_t>(split) * T + t) * E + e] = acc[i][j];
-    }
-  }
-}
-
 // ------------------------------------------------------------ router top-k
-// One warp per token: logits = rscale * (sum of the splits, in order) + bias;
+// One warp per token: logits = sigma * (sum of the splits of w . x16, in
+// order) + bias, sigma = r / f (so the logit is r * (w . x));
 // top-k by (logit desc, index asc) (or the forced ids); softmax over the k.
 constexpr int kMaxEPerLane = kMaxPrefillExperts / 32;
 
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ partial,
                                                           int nsplit, int T, int E, int K,
-                                                          const float* __restrict__ rscale,
+                                                          const float* __restrict__ sigma,
                                                           const float* __restrict__ bias,
                                                           const int32_t* __restrict__ forced,
                                                           int32_t* __restrict__ ids,
@@ -213,7 +122,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   float lv[kMaxEPerLane];
-  const float r = rscale[t];
+  const float r = sigma[t];
 #pragma unroll
   for (int i = 0; i < kMaxEPerLane; ++i) {
     const int e = lane + 32 * i;
@@ -447,27 +356,17 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
 
 }  // namespace
 
-int router_gemm_splits(int T, int E, int D, int num_sms) {
-  const int tiles = ((T + kRtTok - 1) / kRtTok) * ((E + kRtExp - 1) / kRtExp);
-  const int ng = D / 64;
-  int splits = (2 * num_sms + tiles - 1) / tiles;
-  if (splits < 1) splits = 1;
-  if (splits > ng) splits = ng;
-  const int gps = (ng + splits - 1) / splits;
-  return (ng + gps - 1) / gps;
-}
-
 int prefill_route(const RouteArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   tok_prep_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a.x, a.T, a.D, a.prenorm, a.rms_eps,
                                                 reinterpret_cast<__half*>(a.x16), a.sigma, a.rscale,
                                                 a.hscale);
-  const int ng = a.D / 64;
-  const int gps = (ng + a.nsplit - 1) / a.nsplit;
-  dim3 grid((a.T + kRtTok - 1) / kRtTok, (a.E + kRtExp - 1) / kRtExp, a.nsplit);
-  router_gemm_kernel<<<grid, 128, 0, s>>>(a.x, a.T, a.D, a.E, a.router_t, a.router_sb, gps,
-                                          a.partials);
-  router_topk_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a.partials, a.nsplit, a.T, a.E, a.K, a.rscale,
+  int e = static_cast<int>(cudaGetLastError());
+  if (e) return e;
+  e = router_tc_launch(*a.wmap, *a.xmap, a.T, a.E, a.D, a.nsplit, a.partials, a.status,
+                       a.timeout_ns, stream);
+  if (e) return e;
+  router_topk_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a.partials, a.nsplit, a.T, a.E, a.K, a.sigma,
                                                    a.logit_bias, a.forced, a.ids, a.wts);
   return static_cast<int>(cudaGetLastError());
 }
