@@ -497,18 +497,24 @@ __device__ VecView vec_view(const Ctx& cx, int nchunks) {
 constexpr int kMaxXV = 2;  // D <= 8 * kConsumers * kMaxXV
 constexpr int kMaxLogitLoads = 4;  // E <= 4 * kConsumers
 
-__device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long long* lacc,
-                          const float* logit_bias) {
+// The layer input as loaded: this thread's bf16 words of x, the int16
+// quantisation factor q and the pre-norm factor r.
+struct XIn {
+  uint4 r[kMaxXV];
+  float q, rr;
+};
+
+__device__ XIn prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long long* lacc,
+                      const float* logit_bias) {
   const DecodeParams& p = *cx.p;
-  const int nc = p.D / 32;
-  VecView v = vec_view(cx, nc);
   float* xres = reinterpret_cast<float*>(cx.smem + p.off_xres);
   const int nv = p.D / 8;
-  uint4 r[kMaxXV];
+  XIn xin;
+  uint4 (&r)[kMaxXV] = xin.r;
 #pragma unroll
   for (int i = 0; i < kMaxXV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
-    if (idx < nv) r[i] = __ldcg(reinterpret_cast<const uint4*>(xg) + idx);
+    r[i] = idx < nv ? __ldcg(reinterpret_cast<const uint4*>(xg) + idx) : make_uint4(0, 0, 0, 0);
   }
   long long lv[kMaxLogitLoads];  // the layer's raw router logits, in the same round trip
   float lb[kMaxLogitLoads];
@@ -556,12 +562,25 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
       }
     }
   }
+  xin.q = q;
+  xin.rr = rr;
+  csync();  // the logits are read by every thread next
+  return xin;
+}
+
+// x -> int16 chunks with their sums, in the activation region (after the
+// routing, while the routed rows are in flight).
+__device__ VecView pack_x(const Ctx& cx, const XIn& xin) {
+  const DecodeParams& p = *cx.p;
+  const int nc = p.D / 32, nv = p.D / 8;
+  VecView v = vec_view(cx, nc);
+  const float q = xin.q;
 #pragma unroll
   for (int i = 0; i < kMaxXV; ++i) {
     const int idx = static_cast<int>(threadIdx.x) + i * kConsumers;
     uint4 packed = make_uint4(0, 0, 0, 0);
     if (idx < nv) {
-      const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+      const uint32_t w[4] = {xin.r[i].x, xin.r[i].y, xin.r[i].z, xin.r[i].w};
       uint32_t hv[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -577,7 +596,7 @@ __device__ VecView prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long
     if (idx < nv && (idx & 3) == 0) v.xsum[idx >> 2] = static_cast<float>(cs);
   }
   // dot products with X are q * (W x); the layer wants r * (W x)
-  if (threadIdx.x == 0) v.vscale[0] = q > 0.f ? rr / q : 0.f;
+  if (threadIdx.x == 0) v.vscale[0] = q > 0.f ? xin.rr / q : 0.f;
   csync();
   return v;
 }
@@ -1111,13 +1130,13 @@ __device__ void consumer(const Ctx& cx) {
     }
     // ---- layer input (+ its router logits), routing, then the shared
     // expert's gate/up (which needs no ids) while the routed rows arrive
-    VecView xv{};
     unsigned long long* lacc_l = p.lacc + (li & 1) * p.E;
-    xv = prep_x(cx, x_l, routed_here ? lacc_l : nullptr, p.layers[p.layer0 + li].logit_bias);
+    const XIn xin = prep_x(cx, x_l, routed_here ? lacc_l : nullptr, p.layers[p.layer0 + li].logit_bias);
     trace(cx, li, 1);
     if (routed_here) route_all(cx, li);
     else if (needs_ids(p)) publish_ids_local(cx, li);  // ids from an earlier launch
     trace(cx, li, 2);
+    const VecView xv = pack_x(cx, xin);
     XRegs xr;
     load_xregs(xv, p.D / 32, xr);
     const float vs = xv.vscale[0];

@@ -305,7 +305,7 @@ moe_status moe_set_timeout_ms(moe_handle* h, int ms);
  * moe_trace_enable(h, 1): later decode launches of this handle record, per
  * CTA and layer, MOE_TRACE_EVENTS %globaltimer stamps (ns) taken by the CTA's
  * first consumer thread: (0) layer start, (1) input and router logits loaded
- * and converted, (2) routing done, (3) first shared gate/up stage in shared
+ * and reduced, (2) routing done, (3) first shared gate/up stage in shared
  * memory, (4) shared gate/up done, (5) first and (6) last routed gate/up
  * stage in shared memory, (7) routed gate/up done, (8) h complete (grid
  * barrier), (9) h loaded and converted, (10) first down stage in shared
