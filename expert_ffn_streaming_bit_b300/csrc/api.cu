@@ -535,8 +535,9 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
       if (v > part) part = v;
     }
     const int64_t nt = Tm * K / kUnitTokens + E + 1, stl = (Tm + kUnitTokens - 1) / kUnitTokens;
-    const int64_t ngu = nt * ((h->mt_gu_r + 1) / 2) + stl * ((h->mt_gu_s + 1) / 2),
-                  ndn = (nt + stl) * ((h->mt_dn + 1) / 2);
+    auto groups = [](int64_t tiles) { return (tiles + kTilesPerUnit - 1) / kTilesPerUnit; };
+    const int64_t ngu = nt * groups(h->mt_gu_r) + stl * groups(h->mt_gu_s),
+                  ndn = (nt + stl) * groups(h->mt_dn);
     int64_t sizes[] = {Tm * d.D * 2,      Tm * 4,          Tm * 4,        Tm * 4,        part * 4,
                        L * Tm * K * 4,    L * Tm * K * 4,  Tm * K * 4,    E * 4,
                        (E + 1) * 4,       Tm * K * 4,      Tm * K * 4,    ngu * int64_t(sizeof(GemmUnit)),

@@ -52,18 +52,20 @@ namespace moe {
 
 namespace {
 
-constexpr int kNP = 4, kNA = 2, kNB = 4;
+constexpr int kTU = kTilesPerUnit;                 // weight tiles per unit (1 or 2)
 constexpr int kPCodeBytes = 128 * 128;             // 128 rows x 256 columns of 4-bit codes
 constexpr int kPSbBytes = 128 * 16;                // 128 rows x 4 scale/bias words
 constexpr int kPTile = kPCodeBytes + kPSbBytes;    // 18 KB per weight tile
-constexpr int kPBytes = 2 * kPTile;                // two weight tiles per P stage
-constexpr int kBBytes = kUnitTokens * 128;         // 96 rows x 64 fp16
+constexpr int kPBytes = kTU * kPTile;              // the unit's weight tiles per P stage
+constexpr int kBBytes = kUnitTokens * 128;         // tokens x 64 fp16
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = kUnitTokens;              // per tile
-constexpr int kAccSet = 2 * kAccCols;              // one unit's accumulators
+constexpr int kAccSet = kTU * kAccCols;            // one unit's accumulators
 constexpr int kACol0 = 2 * kAccSet;                // A stages after the two sets
-constexpr int kAStage = 2 * 32;                    // 2 tiles x 32 columns
-static_assert(kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
+constexpr int kAStage = kTU * 32;                  // per tile 32 columns (64 fp16 of K)
+constexpr int kNA = (kTmemCols - kACol0) / kAStage;
+constexpr int kNP = kTU == 1 ? 6 : 4, kNB = 4;
+static_assert(kNA >= 2 && kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
 constexpr int kDqWarps = 8, kEpiWarps = 8;
 constexpr int kGemmThreads = (2 + kDqWarps + kEpiWarps) * 32;
 constexpr int kEpiWarp0 = 2 + kDqWarps;
@@ -146,9 +148,13 @@ __device__ void role_tma(const GemmParams& p, uint8_t* P, uint8_t* B, Bars* bars
     mbar_wait(&bars->b_full[q % kNB], (q / kNB) & 1, p.timeout_ns, nullptr);
 }
 
+// Dequantisation.  With two tiles per unit warp w takes tile (w-2)/4 and
+// whole rows (64 values per 64-column block); with one tile the two warps of
+// a lane quarter take the two 32-column halves of each row.
 __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, int nU) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = (w - 2) >> 2;          // weight tile
+  const int grp = (w - 2) >> 2;        // tile (two tiles) or half of the row (one tile)
+  const int m = kTU == 2 ? grp : 0;    // weight tile
   const int qd = w & 3;                // tensor-memory lane quarter
   const int row = 32 * qd + lane;      // row of the weight tile
   const uint32_t tbase = bars->tmem_base + (static_cast<uint32_t>(32 * qd) << 16);
@@ -173,9 +179,11 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
           const uint32_t word = sbw[row * 4 + sb];
           const __half2 s2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word & 0xffffu)));
           const __half2 b2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word >> 16)));
-          uint32_t o[32];
+          constexpr int kHalves = kTU == 2 ? 2 : 1;
+          uint32_t o[16 * kHalves];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          for (int hh = 0; hh < kHalves; ++hh) {
+            const int half = kTU == 2 ? hh : grp;
             // packed chunk c (32 columns) of this row, stored at chunk c ^ (row & 7)
             const int c = 2 * sb + half;
             const uint4 wq = *reinterpret_cast<const uint4*>(codes + row * 128 + ((c ^ (row & 7)) << 4));
@@ -194,11 +202,17 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
               for (int i = 0; i < 4; ++i) {
                 const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&mm[i]), k1024);
                 const __half2 v = __hfma2(q, s2, b2);
-                o[16 * half + 4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
+                o[16 * hh + 4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
               }
             }
           }
-          tmem_st32(tbase + kACol0 + as * kAStage + m * 32, o);
+          if constexpr (kTU == 2) {
+            tmem_st32(tbase + kACol0 + as * kAStage + m * 32,
+                      *reinterpret_cast<const uint32_t(*)[32]>(o));
+          } else {
+            tmem_st16(tbase + kACol0 + as * kAStage + grp * 16,
+                      *reinterpret_cast<const uint32_t(*)[16]>(o));
+          }
           tmem_st_wait();
         }
         tc_fence_before();
@@ -216,7 +230,7 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
 // units, a k-step adds 32 bytes), the k-steps and tiles are unrolled.
 __device__ __forceinline__ void mma_kblock(uint32_t acc, uint32_t a0, uint64_t bd, uint32_t idesc,
                                            int nmt, uint32_t first) {
-  if (nmt == 2) {
+  if (kTU == 2 && nmt == 2) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint32_t f = kk == 0 ? first : 1u;

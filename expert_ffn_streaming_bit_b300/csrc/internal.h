@@ -101,7 +101,8 @@ struct DecodeParams {
 // GEMM's work units), two grouped GEMMs on the tensor cores (gate/up with the
 // GELU epilogue, then down), and a gather combine.
 
-constexpr int kUnitTokens = 96;    // max B rows (tokens) of one GEMM work unit
+constexpr int kUnitTokens = 192;   // max B rows (tokens) of one GEMM work unit
+constexpr int kTilesPerUnit = 1;   // 128-row weight tiles per GEMM work unit
 constexpr int kMaxPrefillExperts = 256;
 
 // One work unit of the grouped GEMM: a 128-row tile of one weight matrix
@@ -112,7 +113,7 @@ struct GemmUnit {
   int expert;  // routed: blob index of the expert
   int row0;    // routed: first bucket position; shared: first token
   int n;       // activation rows in the unit (1 .. kUnitTokens)
-  int nmt;     // weight row tiles in the unit (1 or 2)
+  int nmt;     // weight row tiles in the unit (1 .. kTilesPerUnit)
   int pad[2];
 };
 

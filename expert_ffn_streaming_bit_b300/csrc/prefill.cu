@@ -273,9 +273,11 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
     if (act && (peers & ((1u << lane) - 1u)) == 0) hist[warp][e] += __popc(peers);
     __syncwarp();
   }
-  // ---- work units: pairs of weight row tiles (the last one single when the
-  // tile count is odd) x token tiles
-  const int pgu_r = (a.mt_gu_r + 1) / 2, pdn = (a.mt_dn + 1) / 2, pgu_s = (a.mt_gu_s + 1) / 2;
+  // ---- work units: groups of kTilesPerUnit weight row tiles (the last one
+  // shorter when the tile count is not a multiple) x token tiles
+  constexpr int kTU = kTilesPerUnit;
+  const int pgu_r = (a.mt_gu_r + kTU - 1) / kTU, pdn = (a.mt_dn + kTU - 1) / kTU,
+            pgu_s = (a.mt_gu_s + kTU - 1) / kTU;
   const int routed_tiles = toff[E];
   const int st = (a.T + kUnitTokens - 1) / kUnitTokens;  // shared token tiles
   const int ngu = routed_tiles * pgu_r + st * pgu_s;
@@ -291,11 +293,11 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
       const int r1 = static_cast<int>(static_cast<int64_t>(c) * (tt + 1) / nt);
       const int tile = toff[e] + tt;
       for (int m = lane; m < pgu_r; m += 32) {
-        GemmUnit u{0, 2 * m, e, off[e] + r0, r1 - r0, min(2, a.mt_gu_r - 2 * m), {0, 0}};
+        GemmUnit u{0, kTU * m, e, off[e] + r0, r1 - r0, min(kTU, a.mt_gu_r - kTU * m), {0, 0}};
         a.units_gu[tile * pgu_r + m] = u;
       }
       for (int m = lane; m < pdn; m += 32) {
-        GemmUnit u{0, 2 * m, e, off[e] + r0, r1 - r0, min(2, a.mt_dn - 2 * m), {0, 0}};
+        GemmUnit u{0, kTU * m, e, off[e] + r0, r1 - r0, min(kTU, a.mt_dn - kTU * m), {0, 0}};
         a.units_dn[tile * pdn + m] = u;
       }
     }
@@ -304,11 +306,11 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
     const int r0 = static_cast<int>(static_cast<int64_t>(a.T) * tt / st);
     const int r1 = static_cast<int>(static_cast<int64_t>(a.T) * (tt + 1) / st);
     for (int m = lane; m < pgu_s; m += 32) {
-      GemmUnit u{1, 2 * m, 0, r0, r1 - r0, min(2, a.mt_gu_s - 2 * m), {0, 0}};
+      GemmUnit u{1, kTU * m, 0, r0, r1 - r0, min(kTU, a.mt_gu_s - kTU * m), {0, 0}};
       a.units_gu[routed_tiles * pgu_r + tt * pgu_s + m] = u;
     }
     for (int m = lane; m < pdn; m += 32) {
-      GemmUnit u{1, 2 * m, 0, r0, r1 - r0, min(2, a.mt_dn - 2 * m), {0, 0}};
+      GemmUnit u{1, kTU * m, 0, r0, r1 - r0, min(kTU, a.mt_dn - kTU * m), {0, 0}};
       a.units_dn[(routed_tiles + tt) * pdn + m] = u;
     }
   }
