@@ -67,7 +67,8 @@ constexpr int kNA = (kTmemCols - kACol0) / kAStage;
 constexpr int kNP = kTU == 1 ? 6 : 4, kNB = 4;
 static_assert(kNA >= 2 && kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
 constexpr int kDqWarps = 8, kEpiWarps = 8;
-constexpr int kGemmThreads = (2 + kDqWarps + kEpiWarps) * 32;
+constexpr int kGemmThreads = (3 + kDqWarps + kEpiWarps) * 32;  // + the activation loader warp
+constexpr int kBLoadWarp = 2 + kDqWarps + kEpiWarps;
 constexpr int kEpiWarp0 = 2 + kDqWarps;
 
 struct Bars {
@@ -103,47 +104,54 @@ __device__ __forceinline__ int unit_nmma(int n) { return (n + 15) & ~15; }
 
 // ---------------------------------------------------------------- roles
 
-// Weight slices are issued one 256-column P stage ahead of the activation
-// blocks that need them.
-__device__ void role_tma(const GemmParams& p, uint8_t* P, uint8_t* B, Bars* bars, int nU) {
-  uint32_t pc = 0, bc = 0;
+// Two loader threads, so that neither ring waits for the other: the weight
+// slices (P ring, one stage per 256 columns) and the activation tiles (B
+// ring, one stage per 64-column block) are issued independently, each as far
+// ahead as its ring allows.
+__device__ void role_tma_p(const GemmParams& p, uint8_t* P, Bars* bars, int nU) {
+  uint32_t pc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x) {
     const GemmUnit un = p.units[u];
     const int K = p.K[un.kind];
-    const int nkb = K / 64;
+    const int np = (K + 255) / 256;
     const void* tc = &p.tm_code[un.kind];
     const void* ts = &p.tm_sb[un.kind];
-    const void* tb = &p.tm_b[un.kind];
-    for (int kb = 0; kb < nkb; ++kb) {
-      if ((kb & 3) == 0) {
-        const int sp = kb >> 2;
-        const int st = pc % kNP;
-        if (!wait_bar(&bars->p_empty[st], ((pc / kNP) & 1) ^ 1, p, bars)) return;
-        uint8_t* dst = P + st * kPBytes;
-        mbar_arrive_expect_tx(&bars->p_full[st], un.nmt * kPTile);
-        const int xc = sp * 128, xs = K / 2 + sp * 16;
-        for (int m = 0; m < un.nmt; ++m) {
-          const int y = (un.mt + m) * 128;
-          if (un.kind == 0) {
-            tma_load_3d(dst + m * kPTile, tc, xc, y, un.expert, &bars->p_full[st]);
-            tma_load_3d(dst + m * kPTile + kPCodeBytes, ts, xs, y, un.expert, &bars->p_full[st]);
-          } else {
-            tma_load_2d(dst + m * kPTile, tc, xc, y, &bars->p_full[st]);
-            tma_load_2d(dst + m * kPTile + kPCodeBytes, ts, xs, y, &bars->p_full[st]);
-          }
+    for (int sp = 0; sp < np; ++sp, ++pc) {
+      const int st = pc % kNP;
+      if (!wait_bar(&bars->p_empty[st], ((pc / kNP) & 1) ^ 1, p, bars)) return;
+      uint8_t* dst = P + st * kPBytes;
+      mbar_arrive_expect_tx(&bars->p_full[st], un.nmt * kPTile);
+      const int xc = sp * 128, xs = K / 2 + sp * 16;
+      for (int m = 0; m < un.nmt; ++m) {
+        const int y = (un.mt + m) * 128;
+        if (un.kind == 0) {
+          tma_load_3d(dst + m * kPTile, tc, xc, y, un.expert, &bars->p_full[st]);
+          tma_load_3d(dst + m * kPTile + kPCodeBytes, ts, xs, y, un.expert, &bars->p_full[st]);
+        } else {
+          tma_load_2d(dst + m * kPTile, tc, xc, y, &bars->p_full[st]);
+          tma_load_2d(dst + m * kPTile + kPCodeBytes, ts, xs, y, &bars->p_full[st]);
         }
-        ++pc;
       }
-      const int bs = bc % kNB;
-      if (!wait_bar(&bars->b_empty[bs], ((bc / kNB) & 1) ^ 1, p, bars)) return;
-      mbar_arrive_expect_tx(&bars->b_full[bs], kBBytes);
-      tma_load_2d(B + bs * kBBytes, tb, kb * 64, un.row0, &bars->b_full[bs]);
-      ++bc;
     }
   }
   // drain: copies still in flight must land before the CTA exits
   for (uint32_t q = pc > kNP ? pc - kNP : 0; q < pc; ++q)
     mbar_wait(&bars->p_full[q % kNP], (q / kNP) & 1, p.timeout_ns, nullptr);
+}
+
+__device__ void role_tma_b(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
+  uint32_t bc = 0;
+  for (int u = blockIdx.x; u < nU; u += gridDim.x) {
+    const GemmUnit un = p.units[u];
+    const int nkb = p.K[un.kind] / 64;
+    const void* tb = &p.tm_b[un.kind];
+    for (int kb = 0; kb < nkb; ++kb, ++bc) {
+      const int bs = bc % kNB;
+      if (!wait_bar(&bars->b_empty[bs], ((bc / kNB) & 1) ^ 1, p, bars)) return;
+      mbar_arrive_expect_tx(&bars->b_full[bs], kBBytes);
+      tma_load_2d(B + bs * kBBytes, tb, kb * 64, un.row0, &bars->b_full[bs]);
+    }
+  }
   for (uint32_t q = bc > kNB ? bc - kNB : 0; q < bc; ++q)
     mbar_wait(&bars->b_full[q % kNB], (q / kNB) & 1, p.timeout_ns, nullptr);
 }
@@ -450,7 +458,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   tc_fence_after();
   const int nU = *p.n_units;
   if (w == 0) {
-    if ((threadIdx.x & 31) == 0) role_tma(p, P, B, bars, nU);
+    if ((threadIdx.x & 31) == 0) role_tma_p(p, P, bars, nU);
+  } else if (w == kBLoadWarp) {
+    if ((threadIdx.x & 31) == 0) role_tma_b(p, B, bars, nU);
   } else if (w == 1) {
     if ((threadIdx.x & 31) == 0) role_mma(p, B, bars, nU);
   } else if (w < kEpiWarp0) {
