@@ -64,7 +64,7 @@ constexpr int kAccSet = kTU * kAccCols;            // one unit's accumulators
 constexpr int kACol0 = 2 * kAccSet;                // A stages after the two sets
 constexpr int kAStage = kTU * 32;                  // per tile 32 columns (64 fp16 of K)
 constexpr int kNA = (kTmemCols - kACol0) / kAStage;
-constexpr int kNP = kTU == 1 ? 6 : 4, kNB = 4;
+constexpr int kNP = kTU == 1 ? 3 : 4, kNB = kTU == 1 ? 6 : 4;
 static_assert(kNA >= 2 && kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
 constexpr int kDqWarps = 8, kEpiWarps = 8;
 constexpr int kGemmThreads = (3 + kDqWarps + kEpiWarps) * 32;  // + the activation loader warp
