@@ -216,13 +216,25 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
   __syncthreads();
   const int seg = (n + kBucketWarps - 1) / kBucketWarps;
   const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
-  for (int i = s0 + lane; i < s1; i += 32) {
-    int e = a.ids[i];
-    if (e < 0 || e >= E) {
-      atomicCAS(a.status, DEV_OK, DEV_BAD_ID);
-      e = 0;
+  // ids in batches of kBatch per lane, all loads of a batch in flight together
+  constexpr int kBatch = 8;
+  for (int i0 = s0; i0 < s1; i0 += 32 * kBatch) {
+    int eb[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + 32 * j + lane;
+      eb[j] = i < s1 ? __ldg(a.ids + i) : 0;
     }
-    atomicAdd(&hist[warp][e], 1);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (i0 + 32 * j + lane >= s1) continue;
+      int e = eb[j];
+      if (e < 0 || e >= E) {
+        atomicCAS(a.status, DEV_OK, DEV_BAD_ID);
+        e = 0;
+      }
+      atomicAdd(&hist[warp][e], 1);
+    }
   }
   __syncthreads();
   if (tid < E) {
@@ -257,21 +269,30 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
   }
   if (tid == 0) a.offsets[E] = off[E];
   __syncthreads();
-  for (int i0 = s0; i0 < s1; i0 += 32) {
-    const int i = i0 + lane;
-    const bool act = i < s1;
-    int e = act ? a.ids[i] : -1;
-    if (act && (e < 0 || e >= E)) e = 0;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (act) {
-      const unsigned lower = peers & ((1u << lane) - 1u);
-      const int pos = hist[warp][e] + __popc(lower);
-      a.perm[pos] = i;
-      a.inv[i] = pos;
+  for (int i00 = s0; i00 < s1; i00 += 32 * kBatch) {
+    int eb[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i00 + 32 * j + lane;
+      eb[j] = i < s1 ? __ldg(a.ids + i) : -1;
     }
-    __syncwarp();
-    if (act && (peers & ((1u << lane) - 1u)) == 0) hist[warp][e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i00 + 32 * j + lane;
+      const bool act = i < s1;
+      int e = eb[j];
+      if (act && (e < 0 || e >= E)) e = 0;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (act) {
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        const int pos = hist[warp][e] + __popc(lower);
+        a.perm[pos] = i;
+        a.inv[i] = pos;
+      }
+      __syncwarp();
+      if (act && (peers & ((1u << lane) - 1u)) == 0) hist[warp][e] += __popc(peers);
+      __syncwarp();
+    }
   }
   // ---- work units: groups of kTilesPerUnit weight row tiles (the last one
   // shorter when the tile count is not a multiple) x token tiles
