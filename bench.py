@@ -537,6 +537,40 @@ def run_streaming(args):
     print(json.dumps(line), flush=True)
 
 
+TRACE_NAMES = ["start", "input_reduced", "routed", "bs_ready", "bs_done", "br_first_ready",
+               "br_last_ready", "br_done", "h_complete", "h_converted", "c_first_ready", "c_done",
+               "next_barrier"]
+
+
+def run_trace(args):
+    """Per-phase device trace of one decode launch: the median over CTAs of
+    each phase's duration (us), per layer, from the kernel's %globaltimer
+    stamps (moe_trace_enable / moe_trace_read)."""
+    import torch
+    import synth
+    import expert_ffn_streaming_bit_b300 as moe
+    torch.cuda.set_device(0)
+    shape = synth.GEMMA
+    L = args.layers or 4
+    layers = make_layers(shape, "decode", L, "cuda")
+    h = moe.moe_create(shape, layers, max_tokens=1)
+    x = synth.make_tokens(shape, "decode", 1, index=5).cuda()
+    y = torch.empty_like(x)
+    for _ in range(5):
+        moe.moe_forward_stack(h, x, y, L)
+    torch.cuda.synchronize()
+    moe.moe_trace_enable(h, True)
+    moe.moe_forward_stack(h, x, y, L)
+    torch.cuda.synchronize()
+    tr = moe.moe_trace_read(h, L).astype(np.float64)
+    moe.moe_trace_enable(h, False)
+    for l in range(L):
+        d = np.diff(tr[:, l, :], axis=1) / 1000.0
+        phases = {TRACE_NAMES[e + 1]: round(float(np.median(d[:, e])), 3) for e in range(d.shape[1])
+                  if np.all(np.isfinite(d[:, e])) and np.median(d[:, e]) >= 0}
+        print(json.dumps({"layer": l, "phase_us_median_over_ctas": phases}), flush=True)
+
+
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
@@ -587,6 +621,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", action="store_true",
+                    help="print the decode kernel's per-phase device trace instead of timing")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "chunked_prefill", "streaming_decode"],
                     help="decode (default, the headline line), a prefill workload, or "
@@ -599,6 +635,9 @@ def main():
             args.steps = 20
     if args.warmup < 3:
         args.warmup = 3
+    if args.trace:
+        run_trace(args)
+        return
     if args.impl == "reference":
         if args.steps > 20:
             args.steps = 20   # each reference step is a whole oracle layer on the host
