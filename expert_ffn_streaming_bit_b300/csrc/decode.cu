@@ -73,7 +73,6 @@ enum : int {
   M_LAST = 65,
   M_GEN = 66,
   M_ISSUED = 67,
-  M_R = 68,    // pre-norm factor r of the current layer input (float bits)
   M_TARGET = 70,  // [2] next grid-barrier target (64-bit; 0 before the first barrier)
   M_RED = 72,  // [8] per-warp reduction scratch
   M_RED2 = 80, // [8] second per-warp reduction scratch
@@ -109,10 +108,11 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 
 __device__ __forceinline__ void csync() { named_sync(1, kConsumers); }
 
-// Integer dot product of the codes of 32-column chunk c of a qrow with an
-// int16 activation chunk held in registers (exact in int32).
-__device__ __forceinline__ int chunk_idot(const uint8_t* row, int c, const uint4 (&x)[4]) {
-  const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
+// Integer dot product of one 32-column chunk: the chunk's 16 code bytes
+// (byte i of word j = column 8j+i in the low nibble, column 8j+4+i in the
+// high nibble) against the int16 activation chunk x (x[j] = columns 8j..8j+7
+// as four int16 pairs).  Exact in int32; two chains per nibble half.
+__device__ __forceinline__ int idot_chunk(const uint4& w, const uint4 (&x)[4]) {
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
   int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};
 #pragma unroll
@@ -126,42 +126,6 @@ __device__ __forceinline__ int chunk_idot(const uint8_t* row, int c, const uint4
   }
   return (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
 }
-
-// s * sum(q X) + bias * sum(X) for chunk c of a row with K/2 = halfK code bytes.
-__device__ __forceinline__ float chunk_contrib(const uint8_t* row, int halfK, int c,
-                                               const uint4 (&x)[4], float xs) {
-  const uint32_t sb = *reinterpret_cast<const uint32_t*>(row + halfK + (c >> 1) * 4);
-  const __half2 sbh = *reinterpret_cast<const __half2*>(&sb);
-  return fmaf(__low2float(sbh), static_cast<float>(chunk_idot(row, c, x)), __high2float(sbh) * xs);
-}
-
-// Contribution of 32-column chunk c of a qrow with K/2 = halfK code bytes
-// against an int16 activation vector in chunk layout (kChunkStride bytes per
-// chunk, chunk sums in xsum): s * sum(q X) + bias * sum(X).
-__device__ __forceinline__ float chunk_dot(const uint8_t* row, int halfK, int c, const uint8_t* vec,
-                                           const float* xsum) {
-  const uint4 w = *reinterpret_cast<const uint4*>(row + c * 16);
-  const uint32_t sb = *reinterpret_cast<const uint32_t*>(row + halfK + (c >> 1) * 4);
-  const uint4* v = reinterpret_cast<const uint4*>(vec + c * kChunkStride);
-  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-  int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};  // independent chains; integer sums are exact
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 xq = v[j];  // int16 pairs of columns 8j+{0,1}, {2,3}, {4,5}, {6,7}
-    const uint32_t lo = words[j] & 0x0F0F0F0Fu;  // codes of columns 8j+0..3
-    const uint32_t hi = words[j] & 0xF0F0F0F0u;  // 16 x codes of columns 8j+4..7
-    lo_acc[j & 1] = dp2a_lo(xq.x, lo, lo_acc[j & 1]);
-    lo_acc[j & 1] = dp2a_hi(xq.y, lo, lo_acc[j & 1]);
-    hi_acc[j & 1] = dp2a_lo(xq.z, hi, hi_acc[j & 1]);
-    hi_acc[j & 1] = dp2a_hi(xq.w, hi, hi_acc[j & 1]);
-  }
-  // the high-nibble sums are exact multiples of 16
-  const int total = (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
-  const __half2 sbh = *reinterpret_cast<const __half2*>(&sb);
-  return fmaf(__low2float(sbh), static_cast<float>(total), __high2float(sbh) * xsum[c]);
-}
-
-// ------------------------------------------------------------ stage lists
 
 struct LayerPlan {
   int n_r, n_bs, n_br, n_c;  // stage counts
@@ -393,33 +357,6 @@ __device__ void producer(const Ctx& cx) {
 // ------------------------------------------------------------- consumers
 
 // Max of a value over all consumer threads.
-__device__ float consumer_max(const Ctx& cx, float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int w = threadIdx.x >> 5;
-  volatile float* red = reinterpret_cast<volatile float*>(cx.misc) + M_RED;
-  if ((threadIdx.x & 31) == 0) red[w] = v;
-  csync();
-  float m = 0.f;
-  for (int i = 0; i < kConsumerWarps; ++i) m = fmaxf(m, red[i]);
-  csync();
-  return m;
-}
-
-// Sum of a value over all consumer threads (fixed order over warps).
-__device__ float consumer_sum(const Ctx& cx, float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5;
-  volatile float* red = reinterpret_cast<volatile float*>(cx.misc) + M_RED;
-  if ((threadIdx.x & 31) == 0) red[w] = v;
-  csync();
-  float s = 0.f;
-  for (int i = 0; i < kConsumerWarps; ++i) s += red[i];
-  csync();
-  return s;
-}
-
 // Max of a and sum of b over all consumer threads in one pass (fixed order).
 __device__ void consumer_max_sum(const Ctx& cx, float& a, float& b) {
 #pragma unroll
@@ -458,23 +395,6 @@ __device__ __forceinline__ float quant_factor(float m) { return m > 0.f ? 32767.
 __device__ __forceinline__ uint32_t pack_s16x2(float a, float b) {
   const int ia = __float2int_rn(a), ib = __float2int_rn(b);
   return (static_cast<uint32_t>(ia) & 0xffffu) | (static_cast<uint32_t>(ib) << 16);
-}
-
-// Per-chunk sums of the int16 values of chunks [0, nc) (exact in fp32).
-__device__ void chunk_sums(uint8_t* vec, float* xsum, int nc) {
-  for (int c = threadIdx.x; c < nc; c += kConsumers) {
-    const uint4* v = reinterpret_cast<const uint4*>(vec + c * kChunkStride);
-    int s = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 q = v[j];
-      s = dp2a_lo(q.x, 0x01010101u, s);
-      s = dp2a_lo(q.y, 0x01010101u, s);
-      s = dp2a_lo(q.z, 0x01010101u, s);
-      s = dp2a_lo(q.w, 0x01010101u, s);
-    }
-    xsum[c] = static_cast<float>(s);
-  }
 }
 
 struct VecView {
@@ -656,18 +576,7 @@ __device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const XRegs&
   for (int i = 0; i < kXC; ++i)
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const uint32_t words[4] = {wv[r][i].x, wv[r][i].y, wv[r][i].z, wv[r][i].w};
-      int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = words[j] & 0x0F0F0F0Fu;
-        const uint32_t hi = words[j] & 0xF0F0F0F0u;
-        lo_acc[j & 1] = dp2a_lo(xr.v[i][j].x, lo, lo_acc[j & 1]);
-        lo_acc[j & 1] = dp2a_hi(xr.v[i][j].y, lo, lo_acc[j & 1]);
-        hi_acc[j & 1] = dp2a_lo(xr.v[i][j].z, hi, hi_acc[j & 1]);
-        hi_acc[j & 1] = dp2a_hi(xr.v[i][j].w, hi, hi_acc[j & 1]);
-      }
-      const int tot = (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
+      const int tot = idot_chunk(wv[r][i], xr.v[i]);
       const __half2 sbh = *reinterpret_cast<const __half2*>(&sbv[r][i]);
       acc[r] += fmaf(__low2float(sbh), static_cast<float>(tot), __high2float(sbh) * xr.s[i]);
     }
@@ -809,18 +718,7 @@ __device__ void compute_c(const Ctx& cx, const uint8_t* buf, int r0, int n, int 
       }
 #pragma unroll
       for (int k = 0; k < kRowBatch; ++k) {
-        const uint32_t words[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
-        int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t lo = words[j] & 0x0F0F0F0Fu;
-          const uint32_t hi = words[j] & 0xF0F0F0F0u;
-          lo_acc[j & 1] = dp2a_lo(ht.v[j].x, lo, lo_acc[j & 1]);
-          lo_acc[j & 1] = dp2a_hi(ht.v[j].y, lo, lo_acc[j & 1]);
-          hi_acc[j & 1] = dp2a_lo(ht.v[j].z, hi, hi_acc[j & 1]);
-          hi_acc[j & 1] = dp2a_hi(ht.v[j].w, hi, hi_acc[j & 1]);
-        }
-        const int tot = (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
+        const int tot = idot_chunk(wv[k], ht.v);
         const __half2 sbh = *reinterpret_cast<const __half2*>(&sbv[k]);
         const int r = r0b + k;
         if (r < n)
@@ -1140,30 +1038,22 @@ __device__ void consumer(const Ctx& cx) {
     XRegs xr;
     load_xregs(xv, p.D / 32, xr);
     const float vs = xv.vscale[0];
-    for (; s < lp.n_r + lp.n_bs; ++s) {
+    // ---- shared gate/up stages, then the routed ones (one loop, so the dot
+    // product code is emitted once)
+    const int bs_end = lp.n_r + lp.n_bs, br_end = bs_end + lp.n_br;
+    for (; s < br_end; ++s) {
       const Stage st = stage_at(p, cx.part, lp, s);
       const bool ok = wait_full_warp(cx, st_idx);
       if (s == lp.n_r) trace(cx, li, 3);
+      if (s == bs_end) trace(cx, li, 5);
+      if (s == br_end - 1) trace(cx, li, 6);
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
       if (ok) {
-        compute_b(cx, buf, st.n, xr, vs, p.h + p.K * p.I + st.a);
+        compute_b(cx, buf, st.n, xr, vs, p.h + (s < bs_end ? p.K * p.I : 0) + st.a);
         release_slot(cx, st_idx);
       }
       ++st_idx;
-    }
-    trace(cx, li, 4);
-    // ---- routed gate/up
-    for (; s < lp.n_r + lp.n_bs + lp.n_br; ++s) {
-      const Stage st = stage_at(p, cx.part, lp, s);
-      const bool ok = wait_full_warp(cx, st_idx);
-      if (s == lp.n_r + lp.n_bs) trace(cx, li, 5);
-      if (s == lp.n_r + lp.n_bs + lp.n_br - 1) trace(cx, li, 6);
-      const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
-      if (ok) {
-        compute_b(cx, buf, st.n, xr, vs, p.h + st.a);
-        release_slot(cx, st_idx);
-      }
-      ++st_idx;
+      if (s == bs_end - 1) trace(cx, li, 4);
     }
     trace(cx, li, 7);
     if (!(p.phases & PH_C)) {
