@@ -480,7 +480,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   p.blob_bytes = h->blob;
   p.dn_off = d.I * 2 * qrow_bytes(d.D);
   p.xbuf = h->xbuf;
-  p.h = h->h;
+  p.h = reinterpret_cast<uint16_t*>(h->h);
   p.lacc = h->lacc;
   p.ids = h->ids;
   p.wts = h->wts;

@@ -422,6 +422,7 @@ constexpr int kMaxLogitLoads = 4;  // E <= 4 * kConsumers
 struct XIn {
   uint4 r[kMaxXV];
   float q, rr;
+  float hsc;  // h is held as fp16(h * hsc): hsc = 2^(-2 ceil(log2 max|r x|))
 };
 
 __device__ XIn prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long long* lacc,
@@ -484,6 +485,14 @@ __device__ XIn prep_x(const Ctx& cx, const uint16_t* xg, const unsigned long lon
   }
   xin.q = q;
   xin.rr = rr;
+  {
+    // the gated h grows like |u|^2 (u = r x): scaling it by 2^(-2e), e =
+    // ceil(log2 max|u|), keeps fp16(h * hsc) in range for tiny and huge inputs
+    const float umax = m * rr;
+    int e = 0;
+    if (umax > 0.f) e = max(-60, min(60, static_cast<int>(ceilf(log2f(umax)))));
+    xin.hsc = ldexpf(1.f, -2 * e);
+  }
   csync();  // the logits are read by every thread next
   return xin;
 }
@@ -551,8 +560,12 @@ __device__ void load_xregs(const VecView& xv, int nc, XRegs& xr) {
 // B stage: n gate/up row pairs -> h_out[pair].  Warp w owns pairs 2w and
 // 2w+1; each lane takes its chunks of all four rows against the activation
 // chunks it holds in registers, then a fixed-order warp sum per row.
+__device__ __forceinline__ uint16_t h_bits(float h, float hsc) {
+  return __half_as_ushort(__float2half_rn(fminf(fmaxf(h * hsc, -65504.f), 65504.f)));
+}
+
 __device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const XRegs& xr, float vs,
-                          float* h_out) {
+                          float hsc, uint16_t* h_out) {
   const DecodeParams& p = *cx.p;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nc = p.D / 32, halfK = p.D / 2;
@@ -585,8 +598,8 @@ __device__ void compute_b(const Ctx& cx, const uint8_t* buf, int n, const XRegs&
 #pragma unroll
     for (int o = 16; o; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
   if (lane == 0) {
-    if (p0 < n) h_out[p0] = gelu_tanh(acc[0] * vs) * (acc[1] * vs);
-    if (p0 + 1 < n) h_out[p0 + 1] = gelu_tanh(acc[2] * vs) * (acc[3] * vs);
+    if (p0 < n) h_out[p0] = h_bits(gelu_tanh(acc[0] * vs) * (acc[1] * vs), hsc);
+    if (p0 + 1 < n) h_out[p0 + 1] = h_bits(gelu_tanh(acc[2] * vs) * (acc[3] * vs), hsc);
   }
 }
 
@@ -624,45 +637,54 @@ struct HTask {
   int c;         // chunk within the branch
 };
 
-constexpr int kMaxHV = 8;  // K*I + S <= 4 * kConsumers * kMaxHV
+constexpr int kMaxHV = 4;  // K*I + S <= 8 * kConsumers * kMaxHV
 
-// h (fp32, global) -> the tasks' registers.  The loads are warp-contiguous
-// (a warp instruction reads 512 consecutive bytes, which the L2 serves far
-// faster than a line per thread); the 8 lanes that hold one chunk find its
-// max and sum with shuffles, and the packed chunks pass through the
-// activation region of shared memory to their task threads.
-__device__ void load_htask(const Ctx& cx, HTask& ht) {
+// h (fp16 of h * hsc, global) -> the tasks' registers.  The loads are
+// warp-contiguous (a warp instruction reads 512 consecutive bytes, which the
+// L2 serves far faster than a line per thread); the 4 lanes that hold one
+// chunk find its max and sum with shuffles, and the packed chunks pass
+// through the activation region of shared memory to their task threads.
+__device__ void load_htask(const Ctx& cx, HTask& ht, float hsc) {
   const DecodeParams& p = *cx.p;
   const int t = threadIdx.x;
   const int nh = p.K * p.I + p.S;
-  const int n4 = nh / 4;
+  const int n8 = nh / 8;                 // 16-byte groups of 8 fp16 values
   uint8_t* stage = cx.smem + p.off_vec;  // [nchunks] x kChunkStride bytes
   float* csig = reinterpret_cast<float*>(stage + (nh / 32) * kChunkStride);
   float* csum = csig + nh / 32;
-  float4 r[kMaxHV];
+  uint4 r[kMaxHV];
 #pragma unroll
   for (int i = 0; i < kMaxHV; ++i) {
     const int idx = t + i * kConsumers;
-    r[i] = idx < n4 ? __ldcg(reinterpret_cast<const float4*>(p.h) + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+    r[i] = idx < n8 ? __ldcg(reinterpret_cast<const uint4*>(p.h) + idx) : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int i = 0; i < kMaxHV; ++i) {
-    const int idx = t + i * kConsumers;  // chunk idx / 8, part idx % 8
-    float m = fmaxf(fmaxf(fabsf(r[i].x), fabsf(r[i].y)), fmaxf(fabsf(r[i].z), fabsf(r[i].w)));
+    const int idx = t + i * kConsumers;  // chunk idx / 4, part idx % 4
+    const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+      f[2 * j] = v.x;
+      f[2 * j + 1] = v.y;
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
     const float q = quant_factor(m);
-    const uint2 packed = make_uint2(pack_s16x2(r[i].x * q, r[i].y * q), pack_s16x2(r[i].z * q, r[i].w * q));
-    int cs = dp2a_lo(packed.y, 0x01010101u, dp2a_lo(packed.x, 0x01010101u, 0));
+    const uint4 packed = make_uint4(pack_s16x2(f[0] * q, f[1] * q), pack_s16x2(f[2] * q, f[3] * q),
+                                    pack_s16x2(f[4] * q, f[5] * q), pack_s16x2(f[6] * q, f[7] * q));
+    int cs = sum8_s16(packed);
     cs += __shfl_xor_sync(0xffffffffu, cs, 1);
     cs += __shfl_xor_sync(0xffffffffu, cs, 2);
-    cs += __shfl_xor_sync(0xffffffffu, cs, 4);
-    if (idx < n4) {
-      *reinterpret_cast<uint2*>(stage + (idx >> 3) * kChunkStride + (idx & 7) * 8) = packed;
-      if ((idx & 7) == 0) {
-        csig[idx >> 3] = m / 32767.f;
-        csum[idx >> 3] = static_cast<float>(cs);
+    if (idx < n8) {
+      *reinterpret_cast<uint4*>(stage + (idx >> 2) * kChunkStride + (idx & 3) * 16) = packed;
+      if ((idx & 3) == 0) {
+        csig[idx >> 2] = m / 32767.f / hsc;  // back to units of h
+        csum[idx >> 2] = static_cast<float>(cs);
       }
     }
   }
@@ -1049,7 +1071,7 @@ __device__ void consumer(const Ctx& cx) {
       if (s == br_end - 1) trace(cx, li, 6);
       const uint8_t* buf = cx.smem + static_cast<int64_t>(st_idx % p.nslots) * p.slot_bytes;
       if (ok) {
-        compute_b(cx, buf, st.n, xr, vs, p.h + (s < bs_end ? p.K * p.I : 0) + st.a);
+        compute_b(cx, buf, st.n, xr, vs, xin.hsc, p.h + (s < bs_end ? p.K * p.I : 0) + st.a);
         release_slot(cx, st_idx);
       }
       ++st_idx;
@@ -1069,7 +1091,7 @@ __device__ void consumer(const Ctx& cx) {
     if (blockIdx.x == 0)
       for (int e = threadIdx.x; e < p.E; e += kConsumers) lacc_l[e] = 0ull;
     HTask ht;
-    load_htask(cx, ht);
+    load_htask(cx, ht, xin.hsc);
     trace(cx, li, 9);
     const bool nr = c_has_router(p, li);
     for (int e = threadIdx.x; e < kConsumerWarps * p.E; e += kConsumers) rpart[e] = 0.f;

@@ -78,7 +78,8 @@ struct DecodeParams {
   const uint16_t* x_in;    // bf16 [D], input of layer0
   uint16_t* y_out;         // bf16 [D], output of the last layer
   uint16_t* xbuf;          // bf16 [2][D] scratch
-  float* h;                // [K*I + S] fp32 scratch
+  uint16_t* h;             // [K*I + S] fp16 bits of h * hscale (hscale: a power of two
+                           // from the layer input's range, the same in every CTA)
   unsigned long long* lacc;  // [2][E] router logit accumulators, fixed point (units of
                              // 2^-32, two's complement), one per layer parity
   int32_t* ids;            // [n_layers][K], relative to layer0

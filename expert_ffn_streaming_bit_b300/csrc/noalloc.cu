@@ -78,7 +78,7 @@ extern "C" moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, vo
   // logit accumulators, ids, weights (the same pieces as the handle's own scratch).
   const size_t bar = 256;
   const size_t xbuf = align256(size_t(2) * p.D * 2);
-  const size_t hb = align256(size_t(p.K * p.I + p.S) * 4);
+  const size_t hb = align256(size_t(p.K * p.I + p.S) * 2);
   const size_t part = align256(size_t(2) * p.E * 8);
   const size_t ids = align256(size_t(n_layers) * p.K * 4);
   const size_t need = bar + xbuf + hb + part + 2 * ids;
@@ -96,7 +96,7 @@ extern "C" moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, vo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   p.bar = reinterpret_cast<uint32_t*>(base);
   p.xbuf = reinterpret_cast<uint16_t*>(base + bar);
-  p.h = reinterpret_cast<float*>(base + bar + xbuf);
+  p.h = reinterpret_cast<uint16_t*>(base + bar + xbuf);
   p.lacc = reinterpret_cast<unsigned long long*>(base + bar + xbuf + hb);
   p.ids = reinterpret_cast<int32_t*>(base + bar + xbuf + hb + part);
   p.wts = reinterpret_cast<float*>(base + bar + xbuf + hb + part + ids);
