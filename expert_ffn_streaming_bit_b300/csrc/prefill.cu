@@ -49,6 +49,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // like |u|^2, so it is held as fp16(h * hscale), inside fp16's normal range
 // for tiny and huge inputs alike, and the down output is divided by hscale
 // again (exact powers of two).
+constexpr int kPrepV = 12;  // D <= 8 * 32 * kPrepV
+
 __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restrict__ x, int T, int D,
                                                        int prenorm, float eps,
                                                        __half* __restrict__ x16,
@@ -60,10 +62,17 @@ __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restric
   if (t >= T) return;
   const uint4* row = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * D);
   const int nv = D / 8;
+  // the row is read once, all of a lane's loads in flight together
+  uint4 rv[kPrepV];
+#pragma unroll
+  for (int k = 0; k < kPrepV; ++k) {
+    const int i = lane + 32 * k;
+    rv[k] = i < nv ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
+  }
   float m = 0.f;
-  for (int i = lane; i < nv; i += 32) {
-    const uint4 v = __ldg(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < kPrepV; ++k) {
+    const uint32_t w[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16f(w[j] & 0xffffu)), fabsf(bf16f(w[j] >> 16))));
   }
@@ -73,9 +82,11 @@ __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restric
   const float f = ldexpf(1.f, 14 - e);
   uint4* out = reinterpret_cast<uint4*>(x16 + static_cast<size_t>(t) * D);
   float ss = 0.f;
-  for (int i = lane; i < nv; i += 32) {
-    const uint4 v = __ldg(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < kPrepV; ++k) {
+    const int i = lane + 32 * k;
+    if (i >= nv) break;
+    const uint32_t w[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -128,8 +139,17 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
     const int e = lane + 32 * i;
     float v = -INFINITY;
     if (e < E) {
+      // the splits in order, their loads four at a time in flight
       float s = 0.f;
-      for (int sp = 0; sp < nsplit; ++sp) s += partial[(static_cast<size_t>(sp) * T + t) * E + e];
+      for (int sp0 = 0; sp0 < nsplit; sp0 += 4) {
+        float pv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          pv[k] = sp0 + k < nsplit ? partial[(static_cast<size_t>(sp0 + k) * T + t) * E + e] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (sp0 + k < nsplit) s += pv[k];
+      }
       v = s * r;
       if (bias) v += bias[e];
     }
