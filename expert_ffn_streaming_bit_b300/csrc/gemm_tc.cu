@@ -1,37 +1,40 @@
 // Grouped GEMM of the multi-token layer step on the 5th-generation tensor
 // cores (tcgen05, accumulators in tensor memory).
 //
-// One work unit = up to two 128-row tiles of one 4-bit weight matrix (an
-// expert's interleaved gate/up rows, its down rows, or the shared expert's)
-// against up to 96 activation rows (the tokens routed to that expert, in
-// bucket order, or a tile of all tokens for the shared expert).  The weight
-// tiles are the MMA's M side (128 each), the tokens its N side (16..96 in
-// steps of 16), so the tile shape follows the ragged per-expert token counts
-// without padding M; the two weight tiles share each activation tile, which
-// halves the activation traffic per FLOP.
+// One work unit = kTilesPerUnit (here 1) 128-row tiles of one 4-bit weight
+// matrix (an expert's interleaved gate/up rows, its down rows, or the shared
+// expert's) against up to 192 activation rows (the tokens routed to that
+// expert, in bucket order, or a tile of all tokens for the shared expert).
+// The weight tile is the MMA's M side (128), the tokens its N side (16..192
+// in steps of 16), so the tile shape follows the ragged per-expert token
+// counts without padding M.  An MMA of M = 128, K = 16 costs a roughly fixed
+// number of cycles up to N = 128, so one wide token tile per weight tile
+// beats two weight tiles sharing a narrower one.
 //
 // The dequantised weights never touch shared memory: the dequantisation
 // warps write them straight into tensor memory, and the MMA reads its A
 // operand from there (only the activations come from shared memory).  That
-// keeps the shared-memory traffic per FLOP well under its bandwidth, which
-// A tiles written to and read back from shared memory would exceed.
-// Tensor memory (512 columns): two accumulator sets of 2 tiles x 96 columns
-// (the epilogue drains one unit while the MMA fills the next) and two A
-// stages of 2 tiles x 32 columns (64 fp16 of K per row).
+// keeps the shared-memory traffic per FLOP under its bandwidth, which A tiles
+// written to and read back from shared memory would exceed.
+// Tensor memory (512 columns): two accumulator sets of 192 columns (the
+// epilogue drains one unit while the MMA fills the next) and four A stages
+// of 32 columns (64 fp16 of K per row).
 //
-// Per CTA (persistent, one per SM, 18 warps):
-//   warp 0       TMA: packed 4-bit codes (128 B x 128 rows, 128-byte swizzle)
-//                and scale/bias words (16 B x 128 rows) of a 256-column slice
-//                of each weight tile -> P ring (4 stages); the activation
-//                tile (64 fp16 columns x 96 rows, 128-byte swizzle, the UMMA
-//                K-major layout) -> B ring (4 stages)
+// Per CTA (persistent, one per SM, 19 warps):
+//   warp 0       weight loader: packed 4-bit codes (128 B x 128 rows, 128-byte
+//                swizzle) and scale/bias words (16 B x 128 rows) of a
+//                256-column slice of the weight tile -> P ring (3 stages)
+//   warp 18      activation loader: the tile (64 fp16 columns x 192 rows,
+//                128-byte swizzle, the UMMA K-major layout) -> B ring (6
+//                stages), independent of the P ring
 //   warp 1       MMA: one thread issues tcgen05.mma kind::f16 (M=128,
-//                N=tokens, K=16, A in tensor memory), 4 k-steps x 2 tiles per
-//                64-column block, fp32 accumulators in tensor memory
-//   warps 2-9    dequantisation: warp w takes tile (w-2)/4 and the 32 rows of
-//                its tensor-memory lane quarter w%4; per 64-column block each
-//                thread turns its row's codes into fp16 w = fp16(s q + b) (one
-//                rounding) and stores them into the A stage
+//                N=tokens, K=16, A in tensor memory), 4 k-steps per 64-column
+//                block, fp32 accumulators in tensor memory
+//   warps 2-9    dequantisation: the two warps of tensor-memory lane quarter
+//                w%4 take the two 32-column halves of its 32 rows; per
+//                64-column block each thread turns its codes into fp16
+//                w = fp16(s q + b) (one rounding) and stores them into the A
+//                stage
 //   warps 10-17  epilogue: tensor memory -> registers; gate/up units write
 //                h = gelu(g) * u (fp16, times a per-token power of two that
 //                keeps it in range), down units undo that factor and write the
