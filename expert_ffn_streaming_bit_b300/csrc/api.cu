@@ -81,6 +81,7 @@ struct moe_handle {
   CUtensorMap bmap_gu[2], bmap_dn[2];  // activation operands: [0] routed, [1] shared
   uint16_t* pf_xperm = nullptr;        // x16 rows in bucket order (routed gate/up operand)
   uint16_t* pf_rw = nullptr;           // router weights as fp16 parts, [L][2 Epad][D]
+  int32_t* pf_hist = nullptr;          // bucketing counts / write bases
   CUtensorMap bmap_rt;                 // x16 in 64 x 128 boxes (router operand)
   bool prefill_ok = false;
   int mt_gu_r = 0, mt_dn = 0, mt_gu_s = 0;
@@ -543,7 +544,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
                        (E + 1) * 4,       Tm * K * 4,      Tm * K * 4,    ngu * int64_t(sizeof(GemmUnit)),
                        ndn * int64_t(sizeof(GemmUnit)), 16, Tm * K * d.I * 2, Tm * d.S * 2,
                        Tm * K * d.D * 2,  Tm * d.D * 4,    Tm * d.D * 2,  Tm * d.D * 2,
-                       Tm * K * d.D * 2};
+                       Tm * K * d.D * 2,  int64_t(bucket_blocks(int(Tm * K))) * 8 * E * 4};
     const int ns = sizeof(sizes) / sizeof(sizes[0]);
     int64_t offs[32];
     int64_t tot = 0;
@@ -577,6 +578,7 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     h->pf_xs[0] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
     h->pf_xs[1] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
     h->pf_xperm = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
+    h->pf_hist = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
     if (!make_act_map(&h->bmap_gu[0], h->pf_xperm, d.D, Tm * K) ||
         !make_act_map(&h->bmap_gu[1], h->pf_x16, d.D, Tm) ||
         !make_act_map(&h->bmap_dn[0], h->pf_hr, d.I, Tm * K) ||
@@ -832,6 +834,7 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   ba.units_gu = h->pf_units_gu;
   ba.units_dn = h->pf_units_dn;
   ba.n_units = h->pf_nunits;
+  ba.hist = h->pf_hist;
   ba.status = h->bar + 2;
   e = prefill_bucket(ba, s);
   if (e) return fail(h, MOE_ERR_CUDA, "prefill bucketing: %s", cudaGetErrorString(cudaError_t(e)));

@@ -162,8 +162,10 @@ struct BucketArgs {
   GemmUnit* units_gu;  // gate/up units
   GemmUnit* units_dn;  // down units
   int32_t* n_units;    // [2] gate/up, down
+  int32_t* hist;       // [bucket_blocks(T*K)][8][E] scratch: counts, then write bases
   uint32_t* status;
 };
+int bucket_blocks(int n);  // blocks of the bucketing launches for n assignments
 int prefill_bucket(const BucketArgs& a, void* stream);
 
 struct CombineArgs {

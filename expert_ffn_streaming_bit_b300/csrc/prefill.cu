@@ -211,149 +211,209 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 }
 
 // -------------------------------------------------------------- bucketing
-// One CTA of 1024 threads.  Stable counting sort of the n = T*K assignments
-// a = t*K + j by expert: each warp owns a contiguous segment of assignments;
-// per-(warp, expert) counts give every warp its write base, and a warp places
-// its assignments in order with a match/rank step, so the result is in
-// (expert, t, j) order.  Then the GEMM work units: each expert's rows are cut
-// into ceil(count / kUnitTokens) nearly equal token tiles, times the weight
-// row tiles of the gate/up and of the down matrix; the shared expert's units
-// (all T tokens) follow the routed ones.
-constexpr int kBucketThreads = 1024;
-constexpr int kBucketWarps = kBucketThreads / 32;
+// Stable counting sort of the n = T*K assignments a = t*K + j by expert, in
+// three launches so that no single SM carries the whole sort:
+//   bk_hist   block b, warp w count the experts of their 256-assignment
+//             segment -> hist[b][w][e];
+//   bk_scan   one block: counts, offsets (exclusive scan over experts), the
+//             write base of every (block, warp, expert) in (block, warp)
+//             order (in place in hist), and the GEMM work units;
+//   bk_place  block b, warp w place their segment in order with a
+//             match/rank step: the result is in (expert, t, j) order.
+// Work units: each expert's rows are cut into ceil(count / kUnitTokens)
+// nearly equal token tiles, times the groups of kTilesPerUnit weight row
+// tiles of the gate/up and of the down matrix; the shared expert's units (all
+// T tokens) follow the routed ones.
+constexpr int kBkWarps = 8;
+constexpr int kBkThreads = 32 * kBkWarps;
+constexpr int kBkPerLane = 8;                     // assignments per lane
+constexpr int kBkWarpSeg = 32 * kBkPerLane;       // 256 per warp
+constexpr int kBkBlockSeg = kBkWarps * kBkWarpSeg;  // 2048 per block
 
-__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(BucketArgs a) {
-  __shared__ int hist[kBucketWarps][kMaxPrefillExperts];
+__global__ void __launch_bounds__(kBkThreads) bk_hist_kernel(BucketArgs a) {
+  __shared__ int h[kBkWarps][kMaxPrefillExperts];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, n = a.T * a.K;
+  for (int i = tid; i < kBkWarps * kMaxPrefillExperts; i += kBkThreads) (&h[0][0])[i] = 0;
+  __syncthreads();
+  const int s0 = blockIdx.x * kBkBlockSeg + warp * kBkWarpSeg;
+  int eb[kBkPerLane];
+#pragma unroll
+  for (int j = 0; j < kBkPerLane; ++j) {
+    const int i = s0 + 32 * j + lane;
+    eb[j] = i < n ? __ldg(a.ids + i) : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < kBkPerLane; ++j) {
+    if (s0 + 32 * j + lane >= n) continue;
+    int e = eb[j];
+    if (e < 0 || e >= E) {
+      atomicCAS(a.status, DEV_OK, DEV_BAD_ID);
+      e = 0;
+    }
+    atomicAdd(&h[warp][e], 1);
+  }
+  __syncthreads();
+  int* out = a.hist + static_cast<int64_t>(blockIdx.x) * kBkWarps * E;
+  for (int i = tid; i < kBkWarps * E; i += kBkThreads) out[i] = h[i / E][i % E];
+}
+
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads) bk_scan_kernel(BucketArgs a, int nb) {
+  __shared__ int part[kScanThreads];
   __shared__ int cnt[kMaxPrefillExperts];
   __shared__ int off[kMaxPrefillExperts + 1];
-  __shared__ int tiles[kMaxPrefillExperts];
   __shared__ int toff[kMaxPrefillExperts + 1];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int E = a.E;
-  const int n = a.T * a.K;
-  for (int i = tid; i < kBucketWarps * kMaxPrefillExperts; i += kBucketThreads)
-    (&hist[0][0])[i] = 0;
-  __syncthreads();
-  const int seg = (n + kBucketWarps - 1) / kBucketWarps;
-  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
-  // ids in batches of kBatch per lane, all loads of a batch in flight together
-  constexpr int kBatch = 8;
-  for (int i0 = s0; i0 < s1; i0 += 32 * kBatch) {
-    int eb[kBatch];
+  const int rows = nb * kBkWarps;          // (block, warp) rows of hist, in order
+  const int np = kScanThreads / E;         // threads per expert (E <= 256 -> >= 4)
+  const int e = tid % E, pi = tid / E;     // this thread: expert e, row chunk pi
+  const bool active = pi < np;
+  const int rper = (rows + np - 1) / np;
+  const int r0 = min(rows, pi * rper), r1 = min(rows, r0 + rper);
+  // per (expert, chunk) sums, loads in flight 8 at a time
+  int sum = 0;
+  if (active) {
+    for (int r = r0; r < r1; r += 8) {
+      int v[8];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int i = i0 + 32 * j + lane;
-      eb[j] = i < s1 ? __ldg(a.ids + i) : 0;
-    }
+      for (int k = 0; k < 8; ++k) v[k] = r + k < r1 ? a.hist[static_cast<int64_t>(r + k) * E + e] : 0;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      if (i0 + 32 * j + lane >= s1) continue;
-      int e = eb[j];
-      if (e < 0 || e >= E) {
-        atomicCAS(a.status, DEV_OK, DEV_BAD_ID);
-        e = 0;
-      }
-      atomicAdd(&hist[warp][e], 1);
+      for (int k = 0; k < 8; ++k) sum += v[k];
     }
   }
+  part[tid] = sum;
   __syncthreads();
   if (tid < E) {
     int c = 0;
-    for (int w = 0; w < kBucketWarps; ++w) c += hist[w][tid];
+    for (int q = 0; q < np; ++q) c += part[q * E + tid];
     cnt[tid] = c;
   }
   __syncthreads();
-  if (tid == 0) {  // E <= 256: a serial scan is cheap
+  if (tid < 32) {  // exclusive scans over experts (counts, token tiles), one warp
     int acc = 0, tacc = 0;
-    for (int e = 0; e < E; ++e) {
-      off[e] = acc;
-      acc += cnt[e];
-      const int nt = (cnt[e] + kUnitTokens - 1) / kUnitTokens;
-      tiles[e] = nt;
-      toff[e] = tacc;
-      tacc += nt;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int ee = e0 + tid;
+      const int c = ee < E ? cnt[ee] : 0;
+      const int nt = (c + kUnitTokens - 1) / kUnitTokens;
+      int x = c, y = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int xs = __shfl_up_sync(0xffffffffu, x, o), ys = __shfl_up_sync(0xffffffffu, y, o);
+        if (tid >= o) {
+          x += xs;
+          y += ys;
+        }
+      }
+      if (ee < E) {
+        off[ee] = acc + x - c;
+        toff[ee] = tacc + y - nt;
+      }
+      acc += __shfl_sync(0xffffffffu, x, 31);
+      tacc += __shfl_sync(0xffffffffu, y, 31);
     }
-    off[E] = acc;
-    toff[E] = tacc;
+    if (tid == 0) {
+      off[E] = acc;
+      toff[E] = tacc;
+    }
   }
   __syncthreads();
-  if (tid < E) {  // per-(warp, expert) write bases, in warp order
-    int base = off[tid];
-    for (int w = 0; w < kBucketWarps; ++w) {
-      const int c = hist[w][tid];
-      hist[w][tid] = base;
-      base += c;
+  // write bases: chunk pi of expert e starts at off[e] + the earlier chunks' sums
+  if (active) {
+    int base = off[e];
+    for (int q = 0; q < pi; ++q) base += part[q * E + e];
+    for (int r = r0; r < r1; r += 8) {  // loads 8 at a time in flight
+      int v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = r + k < r1 ? a.hist[static_cast<int64_t>(r + k) * E + e] : 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (r + k < r1) a.hist[static_cast<int64_t>(r + k) * E + e] = base;
+        base += v[k];
+      }
     }
+  }
+  if (tid < E) {
     a.counts[tid] = cnt[tid];
     a.offsets[tid] = off[tid];
   }
   if (tid == 0) a.offsets[E] = off[E];
-  __syncthreads();
-  for (int i00 = s0; i00 < s1; i00 += 32 * kBatch) {
-    int eb[kBatch];
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int i = i00 + 32 * j + lane;
-      eb[j] = i < s1 ? __ldg(a.ids + i) : -1;
-    }
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int i = i00 + 32 * j + lane;
-      const bool act = i < s1;
-      int e = eb[j];
-      if (act && (e < 0 || e >= E)) e = 0;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (act) {
-        const unsigned lower = peers & ((1u << lane) - 1u);
-        const int pos = hist[warp][e] + __popc(lower);
-        a.perm[pos] = i;
-        a.inv[i] = pos;
-      }
-      __syncwarp();
-      if (act && (peers & ((1u << lane) - 1u)) == 0) hist[warp][e] += __popc(peers);
-      __syncwarp();
-    }
-  }
-  // ---- work units: groups of kTilesPerUnit weight row tiles (the last one
-  // shorter when the tile count is not a multiple) x token tiles
+  // ---- work units
   constexpr int kTU = kTilesPerUnit;
   const int pgu_r = (a.mt_gu_r + kTU - 1) / kTU, pdn = (a.mt_dn + kTU - 1) / kTU,
             pgu_s = (a.mt_gu_s + kTU - 1) / kTU;
   const int routed_tiles = toff[E];
   const int st = (a.T + kUnitTokens - 1) / kUnitTokens;  // shared token tiles
-  const int ngu = routed_tiles * pgu_r + st * pgu_s;
-  const int ndn = (routed_tiles + st) * pdn;
   if (tid == 0) {
-    a.n_units[0] = ngu;
-    a.n_units[1] = ndn;
+    a.n_units[0] = routed_tiles * pgu_r + st * pgu_s;
+    a.n_units[1] = (routed_tiles + st) * pdn;
   }
-  for (int e = warp; e < E; e += kBucketWarps) {
-    const int c = cnt[e], nt = tiles[e];
-    for (int tt = 0; tt < nt; ++tt) {
-      const int r0 = static_cast<int>(static_cast<int64_t>(c) * tt / nt);
-      const int r1 = static_cast<int>(static_cast<int64_t>(c) * (tt + 1) / nt);
-      const int tile = toff[e] + tt;
-      for (int m = lane; m < pgu_r; m += 32) {
-        GemmUnit u{0, kTU * m, e, off[e] + r0, r1 - r0, min(kTU, a.mt_gu_r - kTU * m), {0, 0}};
-        a.units_gu[tile * pgu_r + m] = u;
-      }
-      for (int m = lane; m < pdn; m += 32) {
-        GemmUnit u{0, kTU * m, e, off[e] + r0, r1 - r0, min(kTU, a.mt_dn - kTU * m), {0, 0}};
-        a.units_dn[tile * pdn + m] = u;
-      }
+  // routed: one thread per (token tile, weight group); the tile's expert is
+  // found by a binary search over toff
+  for (int idx = tid; idx < routed_tiles * (pgu_r + pdn); idx += kScanThreads) {
+    const bool gu = idx < routed_tiles * pgu_r;
+    const int j = gu ? idx : idx - routed_tiles * pgu_r;
+    const int per = gu ? pgu_r : pdn;
+    const int tile = j / per, m = j % per;
+    int lo = 0, hi = E - 1;  // the last expert with toff[e] <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (toff[mid] <= tile) lo = mid;
+      else hi = mid - 1;
     }
+    const int ex = lo, tt = tile - toff[ex], nt = toff[ex + 1] - toff[ex];
+    const int c = cnt[ex];
+    const int r0t = c * tt / nt, r1t = c * (tt + 1) / nt;
+    const int mt_all = gu ? a.mt_gu_r : a.mt_dn;
+    GemmUnit u{0, kTU * m, ex, off[ex] + r0t, r1t - r0t, min(kTU, mt_all - kTU * m), {0, 0}};
+    if (gu) a.units_gu[tile * pgu_r + m] = u;
+    else a.units_dn[tile * pdn + m] = u;
   }
-  for (int tt = warp; tt < st; tt += kBucketWarps) {
-    const int r0 = static_cast<int>(static_cast<int64_t>(a.T) * tt / st);
-    const int r1 = static_cast<int>(static_cast<int64_t>(a.T) * (tt + 1) / st);
-    for (int m = lane; m < pgu_s; m += 32) {
-      GemmUnit u{1, kTU * m, 0, r0, r1 - r0, min(kTU, a.mt_gu_s - kTU * m), {0, 0}};
-      a.units_gu[routed_tiles * pgu_r + tt * pgu_s + m] = u;
+  for (int idx = tid; idx < st * (pgu_s + pdn); idx += kScanThreads) {
+    const bool gu = idx < st * pgu_s;
+    const int j = gu ? idx : idx - st * pgu_s;
+    const int per = gu ? pgu_s : pdn;
+    const int tt = j / per, m = j % per;
+    const int r0t = a.T * tt / st, r1t = a.T * (tt + 1) / st;
+    const int mt_all = gu ? a.mt_gu_s : a.mt_dn;
+    GemmUnit u{1, kTU * m, 0, r0t, r1t - r0t, min(kTU, mt_all - kTU * m), {0, 0}};
+    if (gu) a.units_gu[routed_tiles * pgu_r + tt * pgu_s + m] = u;
+    else a.units_dn[(routed_tiles + tt) * pdn + m] = u;
+  }
+}
+
+__global__ void __launch_bounds__(kBkThreads) bk_place_kernel(BucketArgs a) {
+  __shared__ int base[kBkWarps][kMaxPrefillExperts];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = a.E, n = a.T * a.K;
+  const int* hb = a.hist + static_cast<int64_t>(blockIdx.x) * kBkWarps * E;
+  for (int i = tid; i < kBkWarps * E; i += kBkThreads) base[i / E][i % E] = hb[i];
+  __syncthreads();
+  const int s0 = blockIdx.x * kBkBlockSeg + warp * kBkWarpSeg;
+  int eb[kBkPerLane];
+#pragma unroll
+  for (int j = 0; j < kBkPerLane; ++j) {
+    const int i = s0 + 32 * j + lane;
+    eb[j] = i < n ? __ldg(a.ids + i) : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < kBkPerLane; ++j) {
+    const int i = s0 + 32 * j + lane;
+    const bool act = i < n;
+    int e = eb[j];
+    if (act && (e < 0 || e >= E)) e = 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    if (act) {
+      const int pos = base[warp][e] + __popc(lower);
+      a.perm[pos] = i;
+      a.inv[i] = pos;
     }
-    for (int m = lane; m < pdn; m += 32) {
-      GemmUnit u{1, kTU * m, 0, r0, r1 - r0, min(kTU, a.mt_dn - kTU * m), {0, 0}};
-      a.units_dn[(routed_tiles + tt) * pdn + m] = u;
-    }
+    __syncwarp();
+    if (act && lower == 0) base[warp][e] += __popc(peers);
+    __syncwarp();
   }
 }
 
@@ -414,8 +474,14 @@ int prefill_route(const RouteArgs& a, void* stream) {
   return static_cast<int>(cudaGetLastError());
 }
 
+int bucket_blocks(int n) { return (n + kBkBlockSeg - 1) / kBkBlockSeg; }
+
 int prefill_bucket(const BucketArgs& a, void* stream) {
-  bucket_kernel<<<1, kBucketThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int nb = bucket_blocks(a.T * a.K);
+  bk_hist_kernel<<<nb, kBkThreads, 0, s>>>(a);
+  bk_scan_kernel<<<1, kScanThreads, 0, s>>>(a, nb);
+  bk_place_kernel<<<nb, kBkThreads, 0, s>>>(a);
   return static_cast<int>(cudaGetLastError());
 }
 
