@@ -107,8 +107,9 @@ constexpr int kTilesPerUnit = 1;   // 128-row weight tiles per GEMM work unit
 constexpr int kMaxPrefillExperts = 256;
 
 // One work unit of the grouped GEMM: a 128-row tile of one weight matrix
-// against up to kUnitTokens activation rows.
-struct GemmUnit {
+// against up to kUnitTokens activation rows.  16-byte aligned so that a unit
+// is written and read as two vector accesses.
+struct alignas(16) GemmUnit {
   int kind;    // 0 routed expert, 1 shared expert
   int mt;      // first weight row tile (rows mt*128 ..)
   int expert;  // routed: blob index of the expert
