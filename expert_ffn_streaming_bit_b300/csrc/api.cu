@@ -65,6 +65,7 @@ struct moe_handle {
   cudaStream_t side = nullptr;
   std::vector<cudaEvent_t> layer_done, copy_done;
   cudaEvent_t ev_ids = nullptr;
+  cudaEvent_t ev_sync = nullptr;  // host waits on the caller's stream (sync_stream)
   std::vector<SlotTable> tables;
   DecodeParams base{};
   int grid = 0;
@@ -152,6 +153,7 @@ void free_all(moe_handle* h) {
   for (auto e : h->copy_done) cudaEventDestroy(e);
   for (auto e : h->pf_ev) cudaEventDestroy(e);
   if (h->ev_ids) cudaEventDestroy(h->ev_ids);
+  if (h->ev_sync) cudaEventDestroy(h->ev_sync);
   if (h->side) cudaStreamDestroy(h->side);
   cudaFree(h->dev_weights);
   cudaFree(h->dev_layers);
@@ -165,33 +167,32 @@ void free_all(moe_handle* h) {
   cudaFreeHost(h->pin_status);
 }
 
-// Host wait on an event with the handle's deadline.
+// Host wait on an event with the handle's deadline.  The first kSpinUs are
+// spent polling without sleeping: a decode token takes well under that, and
+// a sleep of a few microseconds costs tens of them in scheduler latency on
+// the host.  Longer waits poll every 20 us so that they do not hold a core.
+constexpr int64_t kSpinUs = 5000;
+
 moe_status wait_event(moe_handle* h, cudaEvent_t ev) {
   const auto t0 = std::chrono::steady_clock::now();
   for (;;) {
     const cudaError_t e = cudaEventQuery(ev);
     if (e == cudaSuccess) return MOE_OK;
     if (e != cudaErrorNotReady) return fail(h, MOE_ERR_CUDA, "event wait: %s", cudaGetErrorString(e));
-    const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
-                        std::chrono::steady_clock::now() - t0)
-                        .count();
-    if (ms > h->timeout_ms)
+    const int64_t us = std::chrono::duration_cast<std::chrono::microseconds>(
+                           std::chrono::steady_clock::now() - t0)
+                           .count();
+    if (us > int64_t(h->timeout_ms) * 1000)
       return fail(h, MOE_ERR_TIMEOUT, "device work did not finish in %d ms", h->timeout_ms);
-    std::this_thread::sleep_for(std::chrono::microseconds(20));
+    if (us < kSpinUs) std::this_thread::yield();
+    else std::this_thread::sleep_for(std::chrono::microseconds(20));
   }
 }
 
 moe_status sync_stream(moe_handle* h, cudaStream_t s) {
-  cudaEvent_t ev;
-  CUDA_TRY(h, cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
-  cudaError_t e = cudaEventRecord(ev, s);
-  if (e != cudaSuccess) {
-    cudaEventDestroy(ev);
-    return fail(h, MOE_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
-  }
-  moe_status st = wait_event(h, ev);
-  cudaEventDestroy(ev);
-  return st;
+  if (!h->ev_sync) CUDA_TRY(h, cudaEventCreateWithFlags(&h->ev_sync, cudaEventDisableTiming));
+  CUDA_TRY(h, cudaEventRecord(h->ev_sync, s));
+  return wait_event(h, h->ev_sync);
 }
 
 // Reads the device status word (synchronising) and maps it to a status.
