@@ -625,7 +625,7 @@ int gemm_tc_launch(const GemmParams& p, int grid, void* stream) {
 int router_tc_splits(int T, int E, int D, int num_sms) {
   const int tiles = ((T + 127) / 128) * ((E + 127) / 128);
   const int nkb = D / 64;
-  int splits = (num_sms + tiles - 1) / tiles;
+  int splits = num_sms / tiles;  // one wave: a partial second wave doubles the time
   const int cap = nkb / 4 > 1 ? nkb / 4 : 1;  // at least 4 blocks per split
   if (splits > cap) splits = cap;
   if (splits < 1) splits = 1;
