@@ -55,6 +55,40 @@ def test_tiny_prefill_matches_oracle(moe, T):
     check_output(y, ref["y"])
 
 
+@pytest.mark.parametrize("T", [1024, 1025])
+def test_tiny_prefill_bucketing_paths_at_the_boundary(moe, T):
+    """T*k = 2048 assignments are bucketed by the one-launch path, 2050 by the
+    three-launch one: both must give the oracle's buckets and outputs."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 4)
+    h = moe.moe_create(sh, [L], max_tokens=T)
+    x = synth.make_tokens(sh, "tiny", T, index=90 + T)
+    y, st = _forward(moe, h, x)
+    ref = oracle.moe_layer(oracle.LayerView(sh, L), x)
+    assert check_ids(st["ids"], ref, sh.top_k) <= max(1, T // 200)
+    check_weights(st["weights"], ref, st["ids"])
+    _check_buckets(moe, h, st["ids"], sh.n_experts)
+    check_output(y, ref["y"])
+
+
+def test_tiny_prefill_rejects_bad_forced_ids(moe):
+    """Out-of-range or repeated forced ids are refused on the host before any
+    launch, and the handle stays usable."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 2)
+    T = 3
+    h = moe.moe_create(sh, [L], max_tokens=T)
+    x = synth.make_tokens(sh, "tiny", T, index=8)
+    for bad in ([[0, 1], [2, 16], [4, 5]], [[0, 1], [-1, 3], [4, 5]], [[0, 1], [7, 7], [4, 5]]):
+        with pytest.raises(moe.MoEError) as ei:
+            _forward(moe, h, x, forced=np.array(bad, np.int32))
+        assert ei.value.status == -1
+    good = np.array([[0, 1], [2, 15], [4, 5]], np.int32)
+    y, st = _forward(moe, h, x, forced=good)
+    assert np.array_equal(st["ids"], good)
+    check_output(y, oracle.moe_layer(oracle.LayerView(sh, L), x, good)["y"])
+
+
 def test_tiny_prefill_multi_tile_experts_prenorm_residual(moe):
     """2600 tokens x top-2 over 16 experts: every expert gets more than 256
     rows, so each is split into several token tiles."""
