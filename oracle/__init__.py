@@ -5,11 +5,12 @@ benchmark's CPU-baseline leg are the only callers.  It shares no code with the
 CUDA path.  Each function cites the passage it follows in ``moe_oracle.c``.
 
 Parity status per function (pins live in ``tests/test_oracle_pins.py``):
-quantise/dequantise, router top-k and weights, GELU, the layer (through its
-single-expert and invariance cases), bucketing and the LFU step are pinned.
-The whole-layer float result beyond those special cases is checked only
-through them ("parity unpinned" for general routed layers beyond the
-reductions the tests construct).
+quantise/dequantise, router logits, top-k and weights, GELU, the pre-norm,
+the layer, bucketing and the LFU step are all pinned.  The layer is pinned
+through its single-expert and invariance cases, and through a k = 2
+decomposition: every token's output against the weighted sum of its
+experts' FFNs plus the shared FFN, each computed by an independent numpy
+path from the canonical bytes.
 """
 from __future__ import annotations
 

@@ -294,6 +294,39 @@ def test_expert_relabelling_permutes_ids_and_keeps_output():
     assert np.array_equal(out["w"], base["w"])
 
 
+def _numpy_rms(x, eps=1e-6):
+    return x / math.sqrt(float(np.mean(x * x)) + eps)
+
+
+@pytest.mark.parametrize("prenorm", [False, True])
+def test_general_layer_is_the_weighted_sum_of_its_experts_plus_shared(prenorm):
+    """k = 2 of 16 distinct experts with the shared branch on: for every token,
+    y equals sum_i w_i FFN_{id_i}(u) + FFN_shared(u), each FFN computed by the
+    independent numpy path from the canonical bytes (u = x, or its RMS
+    normalisation).  A dropped term, a weight paired with the wrong expert or
+    a shared branch scaled by a routing weight all fail here."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 7)
+    T = 5
+    x = synth.make_tokens(sh, "tiny", T, index=17)
+    out = oracle.moe_layer(oracle.LayerView(sh, L), x, prenorm=prenorm)
+    sg = _numpy_dequant(L["shared_gate"], 4, 64)
+    su = _numpy_dequant(L["shared_up"], 4, 64)
+    sd = _numpy_dequant(L["shared_down"], 4, 64)
+    c = math.sqrt(2 / math.pi)
+    for t in range(T):
+        u = _bf16_to_f64(x[t])
+        if prenorm:
+            u = _numpy_rms(u)
+        ids = out["ids"][t]
+        assert len(set(ids.tolist())) == sh.top_k
+        a = sg @ u
+        ref = sd @ (0.5 * a * (1 + np.tanh(c * (a + 0.044715 * a ** 3))) * (su @ u))
+        for i in range(sh.top_k):
+            ref = ref + out["w"][t, i] * _dense_ffn_numpy(L, int(ids[i]), u, sh)
+        assert np.allclose(out["y"][t], ref, rtol=1e-10, atol=1e-12)
+
+
 def test_forced_ids_use_router_softmax_over_the_forced_set():
     sh = synth.TINY
     L = synth.make_layer(sh, "tiny", 4)
