@@ -30,7 +30,7 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 }
 
 // ceil(log2(u)) for a positive float, exactly, from its bits (an infinity
-// gives 129).
+// gives 128).
 __device__ __forceinline__ int ceil_log2(float u) {
   const uint32_t b = __float_as_uint(u);
   const int ex = static_cast<int>((b >> 23) & 0xffu);
