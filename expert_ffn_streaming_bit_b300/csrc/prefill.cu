@@ -113,8 +113,9 @@ __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restric
   ss = warp_sum(ss);
   if (lane == 0) {
     // fp32 arithmetic: B300's fp64 pipe is narrow, and eight warps of a block
-    // queue on it.  f = 2^k; only rows with max|x| outside [2^-26, 2^54]
-    // (|k| > 40, where f^2 leaves the float range) take the fp64 branch.
+    // queue on it.  f = 2^k; the fp32 branch keeps f^2 and eps f^2 far inside
+    // the float range (|k| <= 40, max|x| in [2^-26, 2^55)); other rows take
+    // the fp64 one.
     const int k = 14 - e;
     float r = 1.f;
     if (prenorm) {
