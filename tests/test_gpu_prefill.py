@@ -141,6 +141,26 @@ def test_tiny_prefill_large_unnormalised_inputs(moe):
         check_output(y[t:t + 1], ref["y"][t:t + 1])
 
 
+def test_tiny_prefill_prenorm_at_extreme_input_scales(moe):
+    """With the pre-norm, token rows scaled by 2^-40 or 2^60 (whose per-token
+    scalars leave the token prep's fp32 branch for its fp64 one) match the
+    oracle like unit-scale rows; each token is held to its own output scale."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 0)
+    T = 6
+    h = moe.moe_create(sh, [L], max_tokens=T)
+    x = synth.make_tokens(sh, "tiny", T, index=12)
+    for t, c in enumerate([1.0, 2.0 ** -40, 2.0 ** 60, 2.0 ** -20, 2.0 ** 30, 1.0]):
+        x[t] = (x[t].float() * c).to(torch.bfloat16)
+    y, st = _forward(moe, h, x, flags=moe.MOE_FWD_PRENORM)
+    ref = oracle.moe_layer(oracle.LayerView(sh, L), x, prenorm=True)
+    check_ids(st["ids"], ref, sh.top_k)
+    assert np.array_equal(st["ids"], ref["ids"])
+    check_weights(st["weights"], ref, st["ids"])
+    for t in range(T):
+        check_output(y[t:t + 1], ref["y"][t:t + 1])
+
+
 def test_tiny_prefill_repeated_runs_are_bit_identical(moe):
     sh = synth.TINY
     L = synth.make_layer(sh, "tiny", 3)
