@@ -28,6 +28,7 @@ int g_inject_pinned_fail = 0;
 struct Inject {
   int h2d_fail_in = 0;  // fail the n-th next miss copy (1 = next)
   int slow_copy_ms = 0;
+  int stall_ms = 0;     // next decode launch: first grid barrier cannot complete, this wait limit
 };
 
 }  // namespace
@@ -217,7 +218,16 @@ constexpr int kPhaseTimedCalls = 256;  // multi-token calls timed per moe_prefil
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status launch(moe_handle* h, const DecodeParams& p, cudaStream_t s) {
-  const int e = decode_launch(p, h->grid, s, true);
+  int e;
+  if (h->inj.stall_ms > 0) {  // injected: a barrier that nothing completes, a short wait limit
+    DecodeParams q = p;
+    q.stall_first_barrier = 1;
+    q.timeout_ns = uint64_t(h->inj.stall_ms) * 1000000ull;
+    h->inj.stall_ms = 0;
+    e = decode_launch(q, h->grid, s, true);
+  } else {
+    e = decode_launch(p, h->grid, s, true);
+  }
   if (e != 0)
     return fail(h, MOE_ERR_CUDA, "decode kernel launch: %s",
                 cudaGetErrorString(static_cast<cudaError_t>(e)));
@@ -662,6 +672,10 @@ moe_status moe_debug_inject(moe_handle* h, int what, int arg) {
     case MOE_INJECT_SLOW_COPY:
       if (!h || arg < 0) return MOE_ERR_INVALID_ARG;
       h->inj.slow_copy_ms = arg;
+      return MOE_OK;
+    case MOE_INJECT_DEVICE_STALL:
+      if (!h || arg < 1 || arg > 2000) return MOE_ERR_INVALID_ARG;
+      h->inj.stall_ms = arg;
       return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;

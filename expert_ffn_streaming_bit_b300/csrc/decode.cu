@@ -916,7 +916,7 @@ __device__ bool grid_barrier(const Ctx& cx) {
     unsigned long long target;
     if (*tgt == 0ull) {
       const unsigned long long old = atom_add_acq_rel_gpu_u64(ctr, 1ull);
-      target = (old / G + 1ull) * G;
+      target = (old / G + 1ull) * G + (p.stall_first_barrier ? G : 0ull);
     } else {
       red_add_release_gpu_u64(ctr, 1ull);
       target = *tgt + G;

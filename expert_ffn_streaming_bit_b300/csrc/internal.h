@@ -93,6 +93,8 @@ struct DecodeParams {
   int off_vec, off_rpart, off_xnext, off_xres, off_logits, off_misc, off_bars, smem_total;
   uint64_t timeout_ns;     // bound on every device-side wait
   uint64_t* trace;         // optional: [grid][n_layers][kTraceEvents] %globaltimer stamps
+  int stall_first_barrier; // test injection: the launch's first grid barrier waits for
+                           // one more round of arrivals, which never comes
 };
 
 // ------------------------------------------------------------------ prefill

@@ -289,11 +289,19 @@ moe_status moe_get_info(const moe_handle* h, moe_info* out);
  *     miss copy is enqueued (results must not change).
  *   MOE_INJECT_PINNED_ALLOC_FAIL: the next moe_create in this process fails
  *     its pinned-pool allocation (h may be NULL).
+ *   MOE_INJECT_DEVICE_STALL: the next decode-kernel launch of h waits at its
+ *     first grid barrier for a round of arrivals that never comes, with a
+ *     device-side wait limit of `arg` ms (1..2000) instead of 2 s.  The wait
+ *     runs out, every CTA leaves after its copies in flight have landed, and
+ *     the next status check (a synchronising call) returns MOE_ERR_TIMEOUT
+ *     and resets the barrier counter and logit accumulators, so the handle
+ *     and the CUDA context stay usable.  No memory is touched out of bounds.
  *   MOE_INJECT_NONE: clear everything. */
 #define MOE_INJECT_NONE 0
 #define MOE_INJECT_H2D_FAIL 1
 #define MOE_INJECT_SLOW_COPY 2
 #define MOE_INJECT_PINNED_ALLOC_FAIL 3
+#define MOE_INJECT_DEVICE_STALL 4
 moe_status moe_debug_inject(moe_handle* h, int what, int arg);
 
 /* Host waits on device work poll with this deadline (default 10000 ms) and

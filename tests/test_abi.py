@@ -132,3 +132,5 @@ def test_fault_injection_switches_are_host_side(moe):
     moe.moe_debug_inject(None, moe.MOE_INJECT_NONE)
     with pytest.raises(moe.MoEError):
         moe.moe_debug_inject(None, moe.MOE_INJECT_H2D_FAIL, 1)   # needs a handle
+    with pytest.raises(moe.MoEError):
+        moe.moe_debug_inject(None, moe.MOE_INJECT_DEVICE_STALL, 50)   # needs a handle

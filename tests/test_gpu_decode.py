@@ -99,6 +99,26 @@ def test_tiny_edge_inputs(moe, tiny_layer):
     check_output(y[1:], ref["y"][1:])
 
 
+def test_tiny_device_wait_runs_out_and_the_handle_recovers(moe, tiny_layer):
+    """Failure detection without a fault: the injected launch's first grid
+    barrier waits for arrivals that never come, its 50 ms device-side limit
+    runs out, and the status check reports MOE_ERR_TIMEOUT.  The context and
+    the handle stay usable: the next token is correct, and so is a token
+    after a second injected stall."""
+    sh = synth.TINY
+    h = moe.moe_create(sh, [tiny_layer], max_tokens=1)
+    x = synth.make_tokens(sh, "tiny", 2, index=21)
+    ref = oracle.moe_layer(oracle.LayerView(sh, tiny_layer), x)
+    for _ in range(2):
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_debug_inject(h, moe.MOE_INJECT_DEVICE_STALL, 50)
+            _run_layer(moe, h, x[:1])
+        assert ei.value.status == -4
+        y, st = _run_layer(moe, h, x)
+        assert check_ids(st["ids"], ref, sh.top_k) == 0
+        check_output(y, ref["y"])
+
+
 def test_tiny_prenorm_matches_oracle_at_any_input_scale(moe, tiny_layer):
     """MOE_FWD_PRENORM: the layer reads x / sqrt(mean(x^2) + 1e-6); inputs far
     outside the fp16 range give the same ids and output as unit-scale ones."""
