@@ -419,6 +419,85 @@ def h2d_link_gbs(device_index: int) -> float:
     return n / (best / 1e3) / 1e9
 
 
+def run_batched(args):
+    """Batched decode: a batch of B tokens (default 32) through the 30-layer
+    decode stack per step, on the same weights as the decode workload.  From
+    10 tokens on, each layer takes the multi-token path (router GEMM,
+    bucketing, grouped tensor-core GEMMs, combine), so each chosen expert's
+    weights are read once for all the batch's rows routed to it; fewer tokens
+    run as one single-token decode launch each (moe_forward_stack decides)."""
+    import torch
+    import synth
+    import expert_ffn_streaming_bit_b300 as moe
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    shape = synth.GEMMA
+    L = args.layers or shape.n_layers
+    B = args.batch
+    layers = make_layers(shape, "decode", L, "cuda")
+    h = moe.moe_create(shape, layers, max_tokens=B)
+    x = synth.make_tokens(shape, "decode", B, index=3000 + rank).cuda()
+    y = torch.empty_like(x)
+
+    def step():
+        moe.moe_forward_stack(h, x, y, L)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    # touched expert bytes: distinct experts per layer from the ids
+    ids, _ = moe.moe_stack_ids(h, L, B)
+    touched = sum(len(np.unique(ids[l])) * shape.expert_bytes() for l in range(L))
+    touched += L * (shape.shared_bytes() + shape.router_bytes())
+    moe.moe_prefill_phase_ms(h)
+    moe.moe_trace_enable(h, True)
+    step()
+    torch.cuda.synchronize()
+    moe.moe_trace_enable(h, False)
+    phases, calls = moe.moe_prefill_phase_ms(h)
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    value = B / (ms / 1e3)
+    hbm, bf16, src = peaks()
+    gbs = touched / (ms / 1e3) / 1e9
+    multi = B >= 10  # moe_forward_stack's split between the two paths
+    per_layer = 8 if B * shape.top_k <= 2048 else 10
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 x f16 -> f32 (tcgen05 kind::f16), 4-bit weights",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 tokens, router-driven ids)",
+        "config": {"workload": "batched decode: %d tokens per step through %d layers "
+                               "(the decode stack's weights), router-driven routing" % (B, L),
+                   "tokens_per_step": B,
+                   "l2": "inputs larger than L2: %d MB of touched weights per layer"
+                         % round(touched / L / 1e6)},
+        "touched_weight_bytes_per_step": touched,
+        "path": "multi-token, layer by layer" if multi else "one decode launch per token",
+        "phase_ms_per_layer": dict(zip(["router", "bucket", "gemm_gate_up", "gemm_down",
+                                        "combine"], [v / max(calls, 1) for v in phases]))
+                              if multi else None,
+        "roofline": {"bound": "hbm", "kernel": "whole step (touched weight bytes)",
+                     "achieved": gbs, "peak": hbm, "peak_source": src, "unit": "GB/s",
+                     "frac": gbs / hbm, "traffic": None},
+        "gpu_launches": (per_layer * L if multi else B) * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_streaming(args):
     """Streaming decode with the expert-slot cache: the 30 x 128 routed experts
     live in a pinned host pool, each layer has 16 HBM slots under LFU, and the
@@ -615,7 +694,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: decode 5000, prefill 3, chunked_prefill 2, "
-                         "streaming_decode 256)")
+                         "streaming_decode 256, batched_decode 200)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
@@ -624,13 +703,15 @@ def main():
     ap.add_argument("--trace", action="store_true",
                     help="print the decode kernel's per-phase device trace instead of timing")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "chunked_prefill", "streaming_decode"],
-                    help="decode (default, the headline line), a prefill workload, or "
-                         "streaming decode with the expert-slot cache")
+                    choices=["decode", "prefill", "chunked_prefill", "streaming_decode",
+                             "batched_decode"],
+                    help="decode (default, the headline line), a prefill workload, "
+                         "streaming decode with the expert-slot cache, or batched decode")
+    ap.add_argument("--batch", type=int, default=32, help="tokens per step of batched_decode")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {"decode": 5000, "prefill": 3, "chunked_prefill": 2,
-                      "streaming_decode": 256}[args.workload]
+                      "streaming_decode": 256, "batched_decode": 200}[args.workload]
         if args.impl == "reference":
             args.steps = 20
     if args.warmup < 3:
@@ -648,6 +729,8 @@ def main():
         run_chunked(args)
     elif args.workload == "streaming_decode":
         run_streaming(args)
+    elif args.workload == "batched_decode":
+        run_batched(args)
     else:
         run_ours(args)
 

@@ -194,6 +194,33 @@ def test_tiny_prefill_stack_matches_decode_stack(moe):
     assert float(d.max()) <= 4e-2 * float(scale) + 2.0 ** -7 * float(yd.float().abs().max())
 
 
+def test_tiny_stack_small_batches_run_as_single_token_launches(moe):
+    """moe_forward_stack runs fewer than 10 tokens as one single-token decode
+    launch each: the batch's outputs, ids and weights are bit-identical to
+    running each token alone.  From 10 tokens on the multi-token path runs
+    (its buckets exist afterwards)."""
+    sh = synth.MoEShape("tiny4", 256, 16, 128, 2, 256, 64, 4)
+    layers = [synth.make_layer(sh, "tiny", l) for l in range(4)]
+    h = moe.moe_create(sh, layers, max_tokens=10)
+    x = synth.make_tokens(sh, "tiny", 10, index=9).cuda()
+    yb = torch.empty_like(x[:8])
+    moe.moe_forward_stack(h, x[:8], yb, 4)
+    ids_b, w_b = moe.moe_stack_ids(h, 4, 8)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_last_buckets(h, 8)
+    assert ei.value.status == -6
+    for t in range(8):
+        yt = torch.empty_like(x[:1])
+        moe.moe_forward_stack(h, x[t:t + 1], yt, 4)
+        ids_t, w_t = moe.moe_stack_ids(h, 4, 1)
+        assert torch.equal(yt, yb[t:t + 1])
+        assert np.array_equal(ids_t[:, 0], ids_b[:, t]) and np.array_equal(w_t[:, 0], w_b[:, t])
+    y10 = torch.empty_like(x)
+    moe.moe_forward_stack(h, x, y10, 4)
+    counts, _, _ = moe.moe_last_buckets(h, 10)
+    assert counts.sum() == 10 * sh.top_k
+
+
 # ---------------------------------------------------------------- full shape
 
 @pytest.fixture(scope="module")
@@ -248,3 +275,21 @@ def test_gemma_large_prefill_4096(moe, gemma_layer):
     assert counts.sum() == T * sh.top_k
     sample = np.sort(np.random.default_rng(1).choice(T, 16, replace=False))
     _sample_check(moe, sh, gemma_layer, x, y, st, sample, prenorm=True)
+
+
+def test_gemma_batched_decode_32_tokens(moe, gemma_layer):
+    """A batch of 32 decode tokens through one full-size layer with the pre-norm
+    and the residual, as the batched-decode benchmark runs them: every token
+    checked against the oracle (about 2 rows per expert, so every MMA is the
+    narrowest N)."""
+    sh = synth.GEMMA
+    T = 32
+    h = moe.moe_create(sh, [gemma_layer], max_tokens=T)
+    x = synth.make_tokens(sh, "decode", T, index=3)
+    flags = moe.MOE_FWD_PRENORM | moe.MOE_FWD_RESIDUAL
+    y, st = _forward(moe, h, x, flags=flags)
+    _check_buckets(moe, h, st["ids"], sh.n_experts)
+    ref = oracle.moe_layer(oracle.LayerView(sh, gemma_layer), x, prenorm=True)
+    assert check_ids(st["ids"], ref, sh.top_k) <= 1
+    check_weights(st["weights"], ref, st["ids"])
+    check_output(y, ref["y"], x_bf16=x)
