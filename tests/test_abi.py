@@ -134,3 +134,16 @@ def test_fault_injection_switches_are_host_side(moe):
         moe.moe_debug_inject(None, moe.MOE_INJECT_H2D_FAIL, 1)   # needs a handle
     with pytest.raises(moe.MoEError):
         moe.moe_debug_inject(None, moe.MOE_INJECT_DEVICE_STALL, 50)   # needs a handle
+
+
+def test_binding_constants_match_the_header(moe):
+    """Every integer #define and status code of include/moe.h has the same
+    value in the Python binding."""
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    defines = dict((n, int(v)) for n, v in re.findall(r"#define\s+(MOE_[A-Z_0-9]+)\s+(-?\d+)\b", text))
+    statuses = dict((n, int(v)) for n, v in re.findall(r"\b(MOE_(?:OK|ERR_[A-Z_]+))\s*=\s*(-?\d+)", text))
+    assert "MOE_INJECT_DEVICE_STALL" in defines and "MOE_ERR_DEVICE" in statuses
+    for name, value in defines.items():
+        assert getattr(moe, name) == value, name
+    for name, value in statuses.items():
+        assert moe.STATUS[value] == name
