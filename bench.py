@@ -212,7 +212,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u4 weights x f16 activations -> f32 accumulate",
+        "dtype": "u4 x s16 -> s32 (dp2a) per 32-column chunk, f32 scale and sum",
         "data": "synthetic (seeded N(0,0.02) weights quantised to affine 4-bit g64; N(0,1) bf16 tokens)",
         "config": {"workload": "decode: %d stacked MoE layers, d_model 2816, 128 experts x 704, "
                                "top-8, shared 2112, 4-bit g64 experts, 8-bit router, T=1, all "
@@ -573,7 +573,7 @@ def run_streaming(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u4 weights x f16 activations -> f32 accumulate",
+        "vs_baseline": None, "dtype": "u4 x s16 -> s32 (dp2a) per 32-column chunk, f32 scale and sum",
         "data": "synthetic (seeded; forced ids from a Zipf(1.1) trace, 4 of 8 kept per step)",
         "config": {"workload": "streaming decode: %d layers, 16 HBM slots per layer under LFU, "
                                "routed experts in a %.2f GB pinned host pool, %d decode steps"
