@@ -1038,7 +1038,7 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
 
 // Fewer tokens than this run the stack as one single-token decode launch per
 // token: on the 30-layer stack at 8 tokens that is 4.8 ms against 5.4 ms for
-// the multi-token path, whose per-layer fixed cost (ten launches, MMAs at
+// the multi-token path, whose per-layer fixed cost (eight launches, MMAs at
 // their narrowest width) only pays from about 10 tokens on.
 constexpr int kStackBatchMin = 10;
 
