@@ -127,6 +127,37 @@ def make_layers(shape, workload, n_layers, device):
     return out
 
 
+def decode_config(L: int, world: int) -> dict:
+    """`config` of the decode line; the reference arm prints the same one."""
+    return {"workload": "decode: %d stacked MoE layers, d_model 2816, 128 experts x 704, "
+                        "top-8, shared 2112, 4-bit g64 experts, 8-bit router, T=1, all "
+                        "experts resident in HBM" % L,
+            "layers": L, "tokens_per_step": 1,
+            "l2": "inputs larger than L2: 1.12 GB of expert weights read per token, "
+                  "64 distinct tokens cycled",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def cpu_baseline_decode(shape, layers, L, budget_s: float) -> dict:
+    """The oracle as it stands, one token through the stack, timed on the host
+    at all cores and at one core (each a bounded sample of layers)."""
+    import oracle
+    import synth
+    x0 = synth.make_tokens(shape, "decode", 1, index=3000)
+    all_cores = oracle.set_threads(os.cpu_count() or 1)
+    dt, n = oracle_sample(shape, layers, x0, budget_s)
+    one = oracle.set_threads(1)
+    dt1, n1 = oracle_sample(shape, layers, x0, budget_s)
+    oracle.set_threads(all_cores)
+    return {"value": 1.0 / (dt / n * L), "unit": "tokens/s", "cores": all_cores,
+            "kind": "oracle",
+            "sample": "one token through %d of the %d layers (%.1f s), scaled to %d layers"
+                      % (n, L, dt, L),
+            "one_core": {"value": 1.0 / (dt1 / n1 * L), "unit": "tokens/s", "cores": one,
+                         "sample": "one token through %d of the %d layers (%.1f s), scaled "
+                                   "to %d layers" % (n1, L, dt1, L)}}
+
+
 def oracle_sample(shape, layers, x_cpu, budget_s: float):
     """Time the oracle on one token through as many layers as fit the budget."""
     import oracle
@@ -197,7 +228,7 @@ def run_ours(args):
     yh = np.empty((1, shape.d_model), np.uint16)
     for i in range(min(args.warmup, 10)):
         moe.moe_forward_stack_host(h, xh[i % P:i % P + 1], yh, L)
-    n_e2e = max(10, min(args.steps, 2000))
+    n_e2e = max(200, min(args.steps, 2000))
     te0 = time.perf_counter()
     for i in range(n_e2e):
         moe.moe_forward_stack_host(h, xh[i % P:i % P + 1], yh, L)
@@ -214,13 +245,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u4 x s16 -> s32 (dp2a) per 32-column chunk, f32 scale and sum",
         "data": "synthetic (seeded N(0,0.02) weights quantised to affine 4-bit g64; N(0,1) bf16 tokens)",
-        "config": {"workload": "decode: %d stacked MoE layers, d_model 2816, 128 experts x 704, "
-                               "top-8, shared 2112, 4-bit g64 experts, 8-bit router, T=1, all "
-                               "experts resident in HBM" % L,
-                   "layers": L, "tokens_per_step": 1,
-                   "l2": "inputs larger than L2: %.2f GB of expert weights read per token, "
-                         "64 distinct tokens cycled" % (algo / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": decode_config(L, world),
         "expert_weight_gbs": algo * value / world / 1e9,
         "hbm_frac_of_measured": algo * value / world / 1e9 / hbm,
         "hbm_frac_of_8tbs": algo * value / world / 1e9 / 8000.0,
@@ -234,13 +259,16 @@ def run_ours(args):
         "device": {"name": torch.cuda.get_device_name(local), "weight_bytes": info["device_weight_bytes"]},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        x0 = synth.make_tokens(shape, "decode", 1, index=3000)
-        dt, n = oracle_sample(shape, layers, x0, args.cpu_budget)
-        line["cpu_baseline"] = {
-            "value": 1.0 / (dt / n * shape.n_layers), "unit": "tokens/s",
-            "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "one token through %d of the %d layers (%.1f s), scaled to %d layers"
-                      % (n, L, dt, shape.n_layers)}
+        line["cpu_baseline"] = cpu_baseline_decode(shape, layers, L, args.cpu_budget)
+    del layers
+    moe.moe_destroy(h)
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_sub_records:
+        # the other workloads, timed in the same run on fewer steps
+        line["sub_records"] = {
+            "prefill_4096": compact(measure_prefill(args, steps=3, warmup=3)),
+            "chunked_128": compact(measure_chunked(args, steps=2, warmup=3)),
+        }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -254,7 +282,19 @@ def gemm_flops_per_layer(shape, T):
     return 2 * T * k * (2 * I * D + D * I) + 2 * T * (2 * S * D + D * S)
 
 
+def compact(line: dict) -> dict:
+    """A workload's line without the keys the headline line already carries."""
+    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline",
+            "whole_layer", "phase_ms_per_layer", "phase_ms_per_chunk_layer",
+            "touched_weight_bytes_per_step", "clocks", "dtype")
+    return {k: line[k] for k in keep if k in line}
+
+
 def run_prefill(args):
+    print(json.dumps(measure_prefill(args, args.steps, args.warmup)), flush=True)
+
+
+def measure_prefill(args, steps, warmup):
     """Large-batch prefill: T = 4096 tokens through one Gemma-shape layer,
     repeated 30 times (each repetition reads the previous one's output, with
     pre-norm and residual).  One step = 30 layer calls."""
@@ -264,7 +304,7 @@ def run_prefill(args):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     shape = synth.GEMMA
-    T, R = 4096, args.layers or 30
+    T, R = 4096, (args.layers if args.workload == "prefill" and args.layers else 30)
     layer = make_layers(shape, "prefill", 1, "cuda")[0]
     h = moe.moe_create(shape, [layer], max_tokens=T)
     x = synth.make_tokens(shape, "prefill", T, index=rank).cuda()
@@ -277,7 +317,7 @@ def run_prefill(args):
             moe.moe_layer_forward(h, 0, src, bufs[r & 1], flags=flags)
             src = bufs[r & 1]
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     moe.moe_prefill_phase_ms(h)  # clear
@@ -288,13 +328,13 @@ def run_prefill(args):
     clocks.start()
     time.sleep(0.3)
     t0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     moe.moe_trace_enable(h, False)
-    ms = t0.elapsed_time(t1) / args.steps
+    ms = t0.elapsed_time(t1) / steps
     phases, calls = moe.moe_prefill_phase_ms(h)
     per_call = [v / max(calls, 1) for v in phases]
     fl = gemm_flops_per_layer(shape, T)
@@ -302,8 +342,8 @@ def run_prefill(args):
     hbm, bf16, src = peaks()
     value = T / (ms / 1e3)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 x f16 -> f32 (tcgen05 kind::f16), 4-bit weights",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 tokens)",
         "config": {"workload": "large prefill: 4096 tokens, one Gemma-shape MoE layer repeated %d "
@@ -318,12 +358,24 @@ def run_prefill(args):
                      "unit": "TFLOP/s", "frac": fl / (gemm_ms / 1e3) / 1e12 / bf16,
                      "flops_per_layer": fl, "avg_gemm_ms_per_layer": gemm_ms, "traffic": None},
         "layer_tflops": (fl + 2 * T * shape.n_experts * shape.d_model) / (ms / R / 1e3) / 1e12,
+        "whole_layer": {"ms": ms / R, "flops": fl + 2 * T * shape.n_experts * shape.d_model,
+                        "tflops": (fl + 2 * T * shape.n_experts * shape.d_model) / (ms / R / 1e3) / 1e12,
+                        "frac": (fl + 2 * T * shape.n_experts * shape.d_model) / (ms / R / 1e3)
+                                / 1e12 / bf16,
+                        "peak": bf16, "peak_source": src + " bf16 dense, burst"},
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
+    moe.moe_destroy(h)
+    del layer
+    torch.cuda.empty_cache()
+    return line
 
 
 def run_chunked(args):
+    print(json.dumps(measure_chunked(args, args.steps, args.warmup)), flush=True)
+
+
+def measure_chunked(args, steps, warmup):
     """Chunked prefill: 1024 tokens in 8 chunks of 128 through the 30-layer
     stack, router biased so expert popularity follows Zipf(1.1).  One step =
     8 chunks x 30 layers."""
@@ -333,7 +385,7 @@ def run_chunked(args):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     shape = synth.GEMMA
-    L = args.layers or shape.n_layers
+    L = (args.layers if args.workload == "chunked_prefill" and args.layers else shape.n_layers)
     out = []
     for l in range(L):
         Lw = synth.make_layer(shape, "chunked_prefill", l, device="cuda", logit_bias=True)
@@ -348,7 +400,7 @@ def run_chunked(args):
         for c in range(8):
             moe.moe_forward_stack(h, x[c * 128:(c + 1) * 128], y[c * 128:(c + 1) * 128], L)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     # touched expert bytes: distinct experts per (chunk, layer) from the ids
@@ -372,17 +424,17 @@ def run_chunked(args):
     clocks.start()
     time.sleep(0.3)
     t0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
+    ms = t0.elapsed_time(t1) / steps
     hbm, bf16, src = peaks()
     gbs = touched / (ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": 1024 / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 x f16 -> f32 (tcgen05 kind::f16), 4-bit weights",
         "data": "synthetic (seeded; Zipf(1.1) router logit bias)",
@@ -397,7 +449,10 @@ def run_chunked(args):
                      "frac": gbs / hbm, "traffic": None},
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
+    moe.moe_destroy(h)
+    del out
+    torch.cuda.empty_cache()
+    return line
 
 
 def h2d_link_gbs(device_index: int) -> float:
@@ -651,38 +706,45 @@ def run_trace(args):
 
 
 def run_reference(args):
+    """The oracle as it stands on the host cores, on the decode workload: one
+    step = one token through all the layers (pre-norm and residual between
+    layers, as the GPU arm's stack)."""
     rank, world, local = dist_env()
     if rank != 0:
         return
     import torch
     import synth
-    shape = synth.GEMMA
-    device = "cuda" if torch.cuda.is_available() else "cpu"
-    layers = make_layers(shape, "decode", 1, device)
     import oracle
-    view = oracle.LayerView(shape, layers[0])
+    shape = synth.GEMMA
+    L = args.layers or shape.n_layers
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    layers = make_layers(shape, "decode", L, device)
     xs = synth.make_tokens(shape, "decode", args.warmup + args.steps, index=4000)
+    cores = oracle.set_threads(os.cpu_count() or 1)
+
+    def token(i):
+        dt, n = oracle_sample(shape, layers, xs[i:i + 1], float("inf"))
+        assert n == L
+        return dt
+
     for i in range(args.warmup):
-        oracle.moe_layer(view, xs[i:i + 1], prenorm=True)
+        token(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle.moe_layer(view, xs[args.warmup + i:args.warmup + i + 1], prenorm=True)
+        token(args.warmup + i)
     dt = time.perf_counter() - t0
-    per_layer = dt / args.steps
-    value = 1.0 / (per_layer * shape.n_layers)
+    per_token = dt / args.steps
+    value = 1.0 / per_token
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_layer * shape.n_layers * 1e3, "higher_is_better": True,
+        "ms_per_step": per_token * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)",
-        "config": {"workload": "decode: 30 stacked MoE layers, d_model 2816, 128 experts x 704, "
-                               "top-8, shared 2112, 4-bit g64 experts, 8-bit router, T=1",
-                   "layers": shape.n_layers, "tokens_per_step": 1},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
-                         "kind": "oracle",
-                         "sample": "each step: one token through one layer (fp64 C oracle), "
-                                   "scaled to 30 layers"},
+        "data": "synthetic (seeded N(0,0.02) weights quantised to affine 4-bit g64; N(0,1) bf16 tokens)",
+        "config": decode_config(L, 1),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: one token through all %d layers (fp64 C oracle, "
+                                   "OpenMP over rows)" % L},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -698,8 +760,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work per CPU-baseline sample (all cores, 1 core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-records", action="store_true",
+                    help="decode line only, without the prefill and chunked-prefill sub-records")
     ap.add_argument("--trace", action="store_true",
                     help="print the decode kernel's per-phase device trace instead of timing")
     ap.add_argument("--workload", default="decode",
@@ -721,7 +786,7 @@ def main():
         return
     if args.impl == "reference":
         if args.steps > 20:
-            args.steps = 20   # each reference step is a whole oracle layer on the host
+            args.steps = 20   # each reference step is one token through the whole stack
         run_reference(args)
     elif args.workload == "prefill":
         run_prefill(args)

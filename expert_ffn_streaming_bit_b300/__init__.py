@@ -64,14 +64,15 @@ class moe_layer_weights(ctypes.Structure):
                 ("exp_up", ctypes.POINTER(moe_qtensor)), ("exp_down", ctypes.POINTER(moe_qtensor))]
 
 
-class moe_layer_stats(ctypes.Structure):
-    _fields_ = [("ids", ctypes.c_void_p), ("weights", ctypes.c_void_p), ("hits", ctypes.c_int),
-                ("misses", ctypes.c_int), ("bytes_h2d", ctypes.c_int64)]
-
-
 class moe_cache_result(ctypes.Structure):
     _fields_ = [("hit", ctypes.c_int32 * 64), ("slot", ctypes.c_int32 * 64),
                 ("evicted", ctypes.c_int32 * 64), ("misses", ctypes.c_int)]
+
+
+class moe_layer_stats(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("weights", ctypes.c_void_p), ("hits", ctypes.c_int),
+                ("misses", ctypes.c_int), ("bytes_h2d", ctypes.c_int64),
+                ("cache", ctypes.POINTER(moe_cache_result))]
 
 
 class moe_info(ctypes.Structure):
@@ -88,7 +89,7 @@ _sig = {
     "moe_layer_forward": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, ctypes.POINTER(moe_layer_stats)]),
     "moe_forward_stack": (_I, [_P, _P, _I, _P, _I, _P]),
     "moe_forward_stack_host": (_I, [_P, _P, _I, _P, _I, _P]),
-    "moe_forward_stack_noalloc": (_I, [_P, _P, _P, _I, _P]),
+    "moe_forward_stack_noalloc": (_I, [_P, _P, _P, _I, _P, _P]),
     "moe_stack_ids": (_I, [_P, _I, _I, _P, _P]),
     "moe_cache_step": (_I, [_P, _I, _P, _I, _I, ctypes.POINTER(moe_cache_result)]),
     "moe_cache_reset": (_I, [_P]),
@@ -210,10 +211,13 @@ def _stream_ptr(stream) -> Optional[int]:
 
 def moe_layer_forward(handle: Handle, layer: int, x, y, flags: int = 0, forced_ids=None,
                       stream=None, want_ids: bool = False):
-    """x, y: CUDA bf16 tensors [T, D].  Returns a dict of stats (ids/weights on request)."""
+    """x, y: CUDA bf16 tensors [T, D].  Returns a dict of stats (ids/weights on
+    request; in streaming mode also the cache step: hit, slot and evicted per id)."""
     T = x.shape[0]
     K = handle.cfg.top_k
     st = moe_layer_stats()
+    cr = moe_cache_result()
+    st.cache = ctypes.pointer(cr)
     ids = w = None
     if want_ids:
         ids = np.empty((T, K), np.int32)
@@ -225,7 +229,11 @@ def moe_layer_forward(handle: Handle, layer: int, x, y, flags: int = 0, forced_i
         fptr = forced_ids.ctypes.data
     _check(_lib.moe_layer_forward(handle.ptr, layer, _dev_ptr(x), T, _dev_ptr(y), flags, fptr,
                                   _stream_ptr(stream), ctypes.byref(st)), handle)
-    return dict(ids=ids, weights=w, hits=st.hits, misses=st.misses, bytes_h2d=st.bytes_h2d)
+    out = dict(ids=ids, weights=w, hits=st.hits, misses=st.misses, bytes_h2d=st.bytes_h2d)
+    if handle.cfg.n_slots > 0:
+        out.update(hit=np.array(cr.hit[:K], np.int32), slot=np.array(cr.slot[:K], np.int32),
+                   evicted=np.array(cr.evicted[:K], np.int32))
+    return out
 
 
 def moe_forward_stack(handle: Handle, x, y, n_layers: int, stream=None):
@@ -242,12 +250,18 @@ def moe_forward_stack_host(handle: Handle, x: np.ndarray, y: np.ndarray, n_layer
                                        n_layers, _stream_ptr(stream)), handle)
 
 
-def moe_forward_stack_noalloc(handle: Handle, x, y, n_layers: int, stream=None):
+def moe_forward_stack_noalloc(handle: Handle, x, y, n_layers: int, stream=None,
+                              want_status: bool = False):
     """One token through the stack with the library's fixed scratch array
-    (no allocation of any kind).  x, y: CUDA bf16 tensors [1, D]."""
+    (no allocation of any kind).  x, y: CUDA bf16 tensors [1, D].  With
+    want_status, returns the kernel's device status word (0 ok, 1 a device
+    wait ran out, 2 an expert id out of range); the call then waits for it."""
     assert x.shape[0] == 1 and y.shape[0] == 1
+    status = np.zeros(1, np.int32) if want_status else None
     _check(_lib.moe_forward_stack_noalloc(handle.ptr, _dev_ptr(x), _dev_ptr(y), n_layers,
-                                          _stream_ptr(stream)), handle)
+                                          _stream_ptr(stream),
+                                          status.ctypes.data if want_status else None), handle)
+    return int(status[0]) if want_status else None
 
 
 def moe_stack_ids(handle: Handle, n_layers: int, T: int):

@@ -10,7 +10,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <memory>
+#include <mutex>
 #include <string>
 #include <thread>
 #include <vector>
@@ -310,6 +312,11 @@ int stack_launch_params(moe_handle* h, const void* x, void* y, int n_layers, Dec
   if (h->cfg.n_slots > 0) return fail(h, MOE_ERR_STATE, "the decode stack needs resident mode");
   if (n_layers < 1 || n_layers > h->cfg.n_layers) return fail(h, MOE_ERR_INVALID_ARG, "bad n_layers");
   *p = params_for(h, 0, n_layers, x, y, PH_ALL, MOE_FWD_RESIDUAL | MOE_FWD_PRENORM);
+  if (h->inj.stall_ms > 0) {  // a pending injected stall applies to this launch
+    p->stall_first_barrier = 1;
+    p->timeout_ns = uint64_t(h->inj.stall_ms) * 1000000ull;
+    h->inj.stall_ms = 0;
+  }
   *grid = h->grid;
   *device = h->device;
   return MOE_OK;
@@ -317,6 +324,21 @@ int stack_launch_params(moe_handle* h, const void* x, void* y, int n_layers, Dec
 
 int handle_error(moe_handle* h, int status, const char* msg) {
   return fail(h, static_cast<moe_status>(status), "%s", msg);
+}
+
+int set_smem_limit(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;  // (kernel, device) -> bytes set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  std::lock_guard<std::mutex> lock(mu);
+  int& have = done[std::make_pair(kernel, dev)];
+  if (bytes <= have) return 0;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  have = bytes;
+  return 0;
 }
 
 }  // namespace moe
@@ -961,6 +983,7 @@ static moe_status decode_layer_streaming(moe_handle* h, int layer, const void* x
     stats->hits = K - cr.misses;
     stats->misses = cr.misses;
     stats->bytes_h2d = int64_t(cr.misses) * h->blob;
+    if (stats->cache) *stats->cache = cr;
   }
   return MOE_OK;
 }

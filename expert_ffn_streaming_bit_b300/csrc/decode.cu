@@ -1208,13 +1208,8 @@ int decode_smem_plan(DecodeParams* p, int max_smem) {
 }
 
 int decode_launch(const DecodeParams& p, int grid, void* stream, bool cooperative) {
-  static int attr_bytes = 0;  // largest dynamic shared memory size enabled so far
-  if (p.smem_total > attr_bytes) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_total);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    attr_bytes = p.smem_total;
-  }
+  const int e = set_smem_limit(reinterpret_cast<const void*>(decode_kernel), p.smem_total);
+  if (e != 0) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -611,13 +611,8 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restric
 int gemm_tc_smem_bytes() { return kSmemBytes; }
 
 int gemm_tc_launch(const GemmParams& p, int grid, void* stream) {
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    attr = true;
-  }
+  const int e = set_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel), kSmemBytes);
+  if (e != 0) return e;
   gemm_tc_kernel<<<grid, kGemmThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
   return static_cast<int>(cudaGetLastError());
 }
@@ -635,13 +630,8 @@ int router_tc_splits(int T, int E, int D, int num_sms) {
 
 int router_tc_launch(const CUtensorMap& wmap, const CUtensorMap& xmap, int T, int E, int D,
                      int nsplit, float* partials, uint32_t* status, uint64_t timeout_ns, void* stream) {
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    attr = true;
-  }
+  const int e = set_smem_limit(reinterpret_cast<const void*>(router_tc_kernel), kRtSmem);
+  if (e != 0) return e;
   const int nkb = D / 64;
   const int kbs = (nkb + nsplit - 1) / nsplit;
   const int Epad = (E + 127) / 128 * 128;

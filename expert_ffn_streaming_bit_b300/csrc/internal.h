@@ -221,8 +221,14 @@ namespace moe {
 // Launch parameters of a one-token resident decode stack over layers
 // [0, n_layers) with pre-norm and residual (the moe_forward_stack recipe),
 // without scratch pointers.  Fails like moe_forward_stack on bad arguments.
+// A pending injected device stall of the handle is applied to (and consumed
+// by) the returned parameters.
 int stack_launch_params(moe_handle* h, const void* x, void* y, int n_layers, DecodeParams* p,
                         int* grid, int* device);
 // Records an error message on the handle and returns `status`.
 int handle_error(moe_handle* h, int status, const char* msg);
+// Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute belongs to the device context, so it is
+// set once per (kernel, device); thread-safe.  Returns a cudaError_t.
+int set_smem_limit(const void* kernel, int bytes);
 }  // namespace moe

@@ -65,7 +65,8 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 #pragma GCC visibility push(default)
 extern "C" moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, void* y,
-                                                int n_layers, void* stream) {
+                                                int n_layers, void* stream,
+                                                int32_t* device_status) {
   moe::DecodeParams p;
   int grid = 0, device = -1;
   int st = moe::stack_launch_params(h, x, y, n_layers, &p, &grid, &device);
@@ -110,6 +111,11 @@ extern "C" moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, vo
     const int le = moe::decode_launch(p, grid, s, true);
     e = static_cast<cudaError_t>(le);
   }
+  // The kernel's status word (timeout, bad id) lives in the fixed array, and
+  // the next call clears it: hand it to the caller if asked.  A copy into
+  // caller-owned host memory allocates nothing.
+  if (e == cudaSuccess && device_status)
+    e = cudaMemcpyAsync(device_status, p.bar + 2, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) {
     char msg[256];
     std::snprintf(msg, sizeof msg, "moe_forward_stack_noalloc: %s", cudaGetErrorString(e));

@@ -108,6 +108,11 @@ typedef struct {
 
 /*
  * moe_create — build a handle for `cfg` on the current CUDA device.
+ * Follows shilu.ai "drumih/turbo-fieldfare", overview table (row 权重: the
+ * affine 4-bit g64 experts and 8-bit router this call repacks) and section
+ * 推理引擎的工作原理 (weights are prepared once into the runtime's own layout,
+ * and the expert set sits in a backing store while a per-layer slot cache is
+ * resident); one owner per model.
  * Copies and repacks all weights (`layers`: n_layers entries, host memory) into
  * the GPU layout: into HBM when cfg->n_slots == 0, else into a pinned host
  * pool plus n_slots HBM slots per layer.  The caller may free `layers` when
@@ -118,7 +123,9 @@ typedef struct {
 moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, moe_handle** out);
 
 /* moe_destroy — synchronise the handle's own streams and free everything.
- * NULL is accepted. */
+ * NULL is accepted.  The counterpart of moe_create: it releases the resident
+ * weights, the slot cache and the backing pool that shilu.ai
+ * "drumih/turbo-fieldfare", section 推理引擎的工作原理, has one owner hold. */
 void moe_destroy(moe_handle* h);
 
 /* Flags for the forward calls. */
@@ -128,6 +135,14 @@ void moe_destroy(moe_handle* h);
                               normalisation kernels beside the MoE kernels; the pages'
                               model normalises each FFN block's input. */
 
+/* Outcome of one cache step for k ids (k <= 64). */
+typedef struct {
+  int32_t hit[64];     /* 1 if ids[i] was resident */
+  int32_t slot[64];    /* HBM slot holding ids[i] after the step */
+  int32_t evicted[64]; /* expert evicted to make room for ids[i], or -1 */
+  int misses;
+} moe_cache_result;
+
 /* Per-call statistics (all fields written by the call when non-NULL). */
 typedef struct {
   int32_t* ids;     /* host [T][k] or NULL: chosen expert ids (a copy, synchronising) */
@@ -135,10 +150,18 @@ typedef struct {
   int hits;         /* streaming mode: cache hits of this call */
   int misses;       /* streaming mode: cache misses (experts copied host->HBM) */
   int64_t bytes_h2d;/* streaming mode: weight bytes copied host->HBM */
+  moe_cache_result* cache; /* host or NULL; streaming mode: the layer's cache step for
+                              this call's ids, in slot order i = 0..k-1 of `ids` (the
+                              forced ids, or the router's choice in rank order) */
 } moe_layer_stats;
 
 /*
  * moe_layer_forward — one MoE layer step for T tokens (1 <= T <= max_tokens).
+ * Follows sh.edu-sjtu.cn article, section 三件事 (route to the top-8 experts,
+ * compute the resident shared expert while the routed ones are fetched,
+ * combine; prefill runs in chunks so each fetched expert serves many rows)
+ * and shilu.ai "drumih/turbo-fieldfare", section 推理引擎的工作原理 (the
+ * per-layer route / plan / fill / overlap / combine sequence).
  * Resident mode: T == 1 runs the persistent decode kernel; T >= 2 runs the
  *   prefill path: router GEMM + top-k, token-to-expert bucketing, grouped
  *   GEMMs on the tensor cores (fp16 operands: weights dequantised to fp16 in
@@ -198,6 +221,12 @@ moe_status moe_forward_stack_host(moe_handle* h, const void* x, int T, void* y, 
  *   x, y: device [1][D] bf16, y may not alias x (caller-owned, as for
  *   moe_forward_stack).  Resident mode only; the handle's device must be
  *   current.
+ *   device_status: host int32 or NULL.  When given, the call enqueues on
+ *   `stream`, after the kernel, a copy of the kernel's device status word
+ *   into *device_status: 0 no error, 1 a device-side bounded wait ran out,
+ *   2 an expert id out of range (y is then undefined).  The value is valid
+ *   once `stream` has synchronised; with pageable host memory the copy, and
+ *   so the kernel, has finished when the call returns.
  * The per-call scratch (grid-barrier words, activation double buffer, h,
  * router partials, ids, weights) lives in one statically sized device array
  * of 1 MiB inside the library.  Every GPU that loads the library holds that
@@ -208,11 +237,12 @@ moe_status moe_forward_stack_host(moe_handle* h, const void* x, int T, void* y, 
  * stream capture.  Every call shares the one array and overwrites what the
  * previous call left there: calls that overlap on the GPU (other streams, or
  * other handles on the same device) race and must be serialised by the
- * caller.  Ids, weights and device-side error status of this call are not
- * retrievable (moe_stack_ids reads the handle's own scratch).
+ * caller.  Ids and weights of this call are not retrievable (moe_stack_ids
+ * reads the handle's own scratch).  A pending MOE_INJECT_DEVICE_STALL of the
+ * handle applies to this call's launch.
  */
 moe_status moe_forward_stack_noalloc(moe_handle* h, const void* x, void* y, int n_layers,
-                                     void* stream);
+                                     void* stream, int32_t* device_status);
 
 /*
  * moe_stack_ids — copy the expert ids and weights chosen by the most recent
@@ -239,16 +269,13 @@ moe_status moe_last_buckets(moe_handle* h, int32_t* counts, int32_t* offsets, in
 /* Flags for moe_cache_step. */
 #define MOE_PLAN_ONLY 1 /* update the slot table but copy no weights */
 
-/* Outcome of one cache step for k ids (k <= 64). */
-typedef struct {
-  int32_t hit[64];     /* 1 if ids[i] was resident */
-  int32_t slot[64];    /* HBM slot holding ids[i] after the step */
-  int32_t evicted[64]; /* expert evicted to make room for ids[i], or -1 */
-  int misses;
-} moe_cache_result;
-
 /*
- * moe_cache_step — plan k distinct expert ids (host, each in [0, E)) against
+ * moe_cache_step — the per-layer expert-slot cache of shilu.ai
+ * "drumih/turbo-fieldfare", section 推理引擎的工作原理 (the CPU plans the
+ * chosen ids against the layer's LFU slots and the misses are read into
+ * GPU-visible buffers) and sh.edu-sjtu.cn article, section 三件事 (a bounded
+ * cache of recently used experts per layer).
+ * Plan k distinct expert ids (host, each in [0, E)) against
  * layer `layer`'s slots: hits first (use count + 1, last use = this step), then
  * misses in ascending expert id take the lowest empty slot, or else evict,
  * among slots this step has not used, the least-used slot (then the least

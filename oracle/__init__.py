@@ -33,7 +33,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (OpenMP over independent rows)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp.%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+        subprocess.check_call(["gcc", "-O3", "-fopenmp", "-fPIC", "-shared", "-std=c11",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -58,6 +58,8 @@ def lib():
             L = ctypes.CDLL(build())
             P = ctypes.c_void_p
             i64, i32 = ctypes.c_int64, ctypes.c_int
+            L.orc_set_threads.restype = i32
+            L.orc_set_threads.argtypes = [i32]
             L.orc_half_to_double.restype = ctypes.c_double
             L.orc_half_to_double.argtypes = [ctypes.c_uint16]
             L.orc_bf16_to_double.restype = ctypes.c_double
@@ -106,6 +108,12 @@ def _np(x, dtype=None):
 
 
 # ------------------------------------------------------------------ scalars
+
+def set_threads(n: int = 0) -> int:
+    """OpenMP threads of the oracle's loops from now on (n <= 0: leave as is);
+    returns the count in effect.  Results do not depend on it."""
+    return int(lib().orc_set_threads(int(n)))
+
 
 def half_to_double(h: int) -> float:
     return lib().orc_half_to_double(int(h) & 0xFFFF)

@@ -24,6 +24,7 @@
  * are stated at each function.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -51,6 +52,14 @@ static double bf16_to_double(uint16_t b) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/* Threads the OpenMP loops below use from now on (timing at 1 core and at all
+ * cores); returns the count in effect.  Changes no result: every loop that
+ * is split writes disjoint outputs. */
+int orc_set_threads(int n) {
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
 }
 
 double orc_half_to_double(uint16_t h) { return half_to_double(h); }

@@ -213,6 +213,13 @@ def test_gemma_30_layer_stack_teacher_forced(moe, gemma_layers):
         check_ids(ids[l], ref, sh.top_k)
         check_weights(w[l], ref, ids[l])
         check_output(xs[l + 1], ref["y"], x_bf16=xs[l])
+        # the same layer on its captured input without the residual: the
+        # output itself against 2e-2 x RMS(y), not the bf16 rounding of x + y
+        xl = xs[l].cuda()
+        yl = torch.empty_like(xl)
+        st = moe.moe_layer_forward(h, l, xl, yl, flags=moe.MOE_FWD_PRENORM, want_ids=True)
+        check_ids(st["ids"], ref, sh.top_k)
+        check_output(yl.cpu(), ref["y"])
 
 
 def test_gemma_stack_host_io_matches_device_io(moe, gemma_layers):

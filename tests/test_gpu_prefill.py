@@ -185,10 +185,15 @@ def test_tiny_prefill_stack_matches_decode_stack(moe):
     torch.cuda.synchronize()
     ids_p, _ = moe.moe_stack_ids(h, 4, T)
     yd = torch.empty_like(x)
+    differ = 0
     for t in range(T):
         moe.moe_forward_stack(h, x[t:t + 1], yd[t:t + 1], 4)
+        ids_t, _ = moe.moe_stack_ids(h, 4, 1)
+        differ += int((ids_t[:, 0] != ids_p[:, t]).any(axis=-1).sum())
     torch.cuda.synchronize()
-    agree = (ids_p[0] == moe.moe_stack_ids(h, 4, 1)[0][0][0]).all()  # noqa: F841 (last token only)
+    # both paths rank fp32 logits summed in different orders: a near-tie may
+    # flip one (layer, token), and a flip changes that token's later layers
+    assert differ <= 1, differ
     d = (yp.float() - yd.float()).abs()
     scale = (yd.float() - x.float()).pow(2).mean().sqrt()
     assert float(d.max()) <= 4e-2 * float(scale) + 2.0 ** -7 * float(yd.float().abs().max())
@@ -235,7 +240,7 @@ def gemma_zipf_layer():
 
 def _sample_check(moe, sh, L, x, y, st, sample, prenorm=False):
     ref = oracle.moe_layer(oracle.LayerView(sh, L), x[sample], prenorm=prenorm)
-    assert check_ids(st["ids"][sample], ref, sh.top_k) <= 1
+    assert check_ids(st["ids"][sample], ref, sh.top_k) <= max(1, len(sample) // 128)
     check_weights(st["weights"][sample], ref, st["ids"][sample])
     check_output(y[sample], ref["y"])
 
@@ -249,8 +254,7 @@ def test_gemma_chunked_prefill_128_zipf(moe, gemma_zipf_layer):
     y, st = _forward(moe, h, x)
     counts = _check_buckets(moe, h, st["ids"], sh.n_experts)
     assert counts.max() > 4 * counts.mean()      # uneven, Zipf-like popularity
-    sample = np.random.default_rng(0).choice(T, 24, replace=False)
-    _sample_check(moe, sh, gemma_zipf_layer, x, y, st, np.sort(sample))
+    _sample_check(moe, sh, gemma_zipf_layer, x, y, st, np.arange(T))   # every token
 
 
 @pytest.fixture(scope="module")
@@ -273,7 +277,7 @@ def test_gemma_large_prefill_4096(moe, gemma_layer):
     y, st = _forward(moe, h, x, flags=moe.MOE_FWD_PRENORM)
     counts = _check_buckets(moe, h, st["ids"], sh.n_experts)
     assert counts.sum() == T * sh.top_k
-    sample = np.sort(np.random.default_rng(1).choice(T, 16, replace=False))
+    sample = np.sort(np.random.default_rng(1).choice(T, 256, replace=False))
     _sample_check(moe, sh, gemma_layer, x, y, st, sample, prenorm=True)
 
 
@@ -293,3 +297,47 @@ def test_gemma_batched_decode_32_tokens(moe, gemma_layer):
     assert check_ids(st["ids"], ref, sh.top_k) <= 1
     check_weights(st["weights"], ref, st["ids"])
     check_output(y, ref["y"], x_bf16=x)
+
+
+@pytest.fixture(scope="module")
+def gemma_decode_layers4():
+    sh = synth.GEMMA
+    out = []
+    for l in range(4):
+        L = synth.make_layer(sh, "decode", l, device="cuda")
+        out.append(synth.layer_to(L, "cpu"))
+        del L
+    torch.cuda.empty_cache()
+    return out
+
+
+def test_gemma_multi_token_stack_teacher_forced(moe, gemma_decode_layers4):
+    """moe_forward_stack at T = 32 (the multi-token path the batched-decode
+    benchmark times) over four full-size layers.  Prefix runs give each
+    layer's bf16 input exactly; the oracle is teacher-forced on it, and every
+    token's ids, weights and output are checked.  Each layer is also run on
+    its captured input without the residual, so the output is held to
+    2e-2 x RMS(y) itself rather than to the bf16 rounding of x + y."""
+    sh = synth.GEMMA
+    layers = gemma_decode_layers4
+    T, L = 32, len(layers)
+    h = moe.moe_create(sh, layers, max_tokens=T)
+    x0 = synth.make_tokens(sh, "decode", T, index=200)
+    xd = x0.cuda()
+    xs = [x0]
+    for n in range(1, L + 1):
+        y = torch.empty_like(xd)
+        moe.moe_forward_stack(h, xd, y, n)
+        torch.cuda.synchronize()
+        xs.append(y.cpu())
+    ids, w = moe.moe_stack_ids(h, L, T)
+    for l in range(L):
+        ref = oracle.moe_layer(oracle.LayerView(sh, layers[l]), xs[l], prenorm=True)
+        assert check_ids(ids[l], ref, sh.top_k) <= 1
+        check_weights(w[l], ref, ids[l])
+        check_output(xs[l + 1], ref["y"], x_bf16=xs[l])
+        xl = xs[l].cuda()
+        yl = torch.empty_like(xl)
+        st = moe.moe_layer_forward(h, l, xl, yl, flags=moe.MOE_FWD_PRENORM, want_ids=True)
+        assert np.array_equal(st["ids"], ids[l])
+        check_output(yl.cpu(), ref["y"])

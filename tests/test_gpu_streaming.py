@@ -2,7 +2,8 @@
 a per-layer set of HBM slots is filled on demand under the LFU policy, the
 misses copied on a side stream while the shared expert runs.
 
-Checked: the per-step hit/miss counts against the oracle's LFU replay (exact),
+Checked: every step's cache plan as the forward call made it (per id: hit,
+slot, evicted expert) against the oracle's LFU replay, element by element,
 the layer output against the oracle (forced and router-driven ids), and the
 injected host->HBM copy failure path (error status, slot left empty, the next
 step refetches).  Every call goes through the C ABI."""
@@ -30,6 +31,14 @@ def _step(moe, h, x, layer=0, forced=None, flags=0):
     return y, st
 
 
+def _check_plan(st, hit, slot, ev, where):
+    """The forward call's cache step, id by id, equals the oracle's."""
+    assert np.array_equal(st["hit"], hit), (where, st["hit"], hit)
+    assert np.array_equal(st["slot"], slot), (where, st["slot"], slot)
+    assert np.array_equal(st["evicted"], ev), (where, st["evicted"], ev)
+    assert st["misses"] == int((hit == 0).sum()), where
+
+
 def test_tiny_streaming_trace_hits_and_outputs(moe):
     sh = synth.TINY
     L = synth.make_layer(sh, "tiny", 0)
@@ -42,8 +51,8 @@ def test_tiny_streaming_trace_hits_and_outputs(moe):
     for step in range(40):
         x = xs[step:step + 1]
         y, st = _step(moe, h, x.cuda(), forced=trace[step:step + 1])
-        hit, _, _ = lfu.step(trace[step])
-        assert st["misses"] == int((hit == 0).sum()), step
+        hit, slot, ev = lfu.step(trace[step])
+        _check_plan(st, hit, slot, ev, step)
         assert st["hits"] == int(hit.sum()), step
         assert st["bytes_h2d"] == st["misses"] * moe.moe_get_info(h)["expert_blob_bytes"]
         ref = oracle.moe_layer(view, x, trace[step:step + 1])
@@ -58,11 +67,13 @@ def test_tiny_streaming_router_driven_matches_resident(moe):
     hs = moe.moe_create(sh, [L], n_slots=3, max_tokens=1)
     view = oracle.LayerView(sh, L)
     xs = synth.make_tokens(sh, "tiny", 12, index=12)
+    lfu = oracle.LFUCache(3, sh.n_experts)
     for t in range(12):
         x = xs[t:t + 1]
         y, st = _step(moe, hs, x.cuda(), flags=moe.MOE_FWD_PRENORM | moe.MOE_FWD_RESIDUAL)
         ref = oracle.moe_layer(view, x, prenorm=True)
         assert check_ids(st["ids"], ref, sh.top_k) == 0
+        _check_plan(st, *lfu.step(st["ids"][0]), t)
         check_weights(st["weights"], ref, st["ids"])
         check_output(y.cpu(), ref["y"], x_bf16=x)
 
@@ -121,8 +132,8 @@ def test_gemma_streaming_two_layers(moe, gemma_two_layers):
         xl = x.cuda()
         for l in range(2):
             y, st = _step(moe, h, xl, layer=l, forced=traces[l][step:step + 1], flags=flags)
-            hit, _, _ = lfus[l].step(traces[l][step])
-            assert st["misses"] == int((hit == 0).sum()), (step, l)
+            hit, slot, ev = lfus[l].step(traces[l][step])
+            _check_plan(st, hit, slot, ev, (step, l))
             if step % 8 == 7:
                 ref = oracle.moe_layer(oracle.LayerView(sh, gemma_two_layers[l]), xl.cpu(),
                                        traces[l][step:step + 1], prenorm=True)

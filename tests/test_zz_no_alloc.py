@@ -23,13 +23,16 @@ def moe():
     return m
 
 
-def _assert_close(y, y_ref, x0):
-    """Same tolerance as the parity tests: 2e-2 of the RMS of the stack's
-    contribution, plus the bf16 rounding of the output."""
+def _assert_same(y, y_ref, x0):
+    """Both entry points run the same deterministic kernel on the same inputs,
+    so the outputs must be bit-identical.  The tolerance of the parity tests
+    (2e-2 of the RMS of the stack's contribution plus the bf16 rounding of
+    the output) is checked first, so a failure says how far apart they are."""
     g, r, x = bf16_to_f64(y), bf16_to_f64(y_ref), bf16_to_f64(x0)
     rms = float(np.sqrt(np.mean((r - x) ** 2)))
     tol = TOL_REL_RMS * rms + 2.0 ** -8 * np.abs(r)
     assert np.all(np.abs(g - r) <= tol), float(np.abs(g - r).max())
+    assert torch.equal(y, y_ref), "within tolerance but not bit-identical"
 
 
 def _compare(moe, shape, layers, index):
@@ -42,18 +45,18 @@ def _compare(moe, shape, layers, index):
     outs = []
     for _ in range(2):                      # two calls in a row share the array
         y = torch.full_like(x0, float("nan"))
-        moe.moe_forward_stack_noalloc(h, x0, y, L)
+        assert moe.moe_forward_stack_noalloc(h, x0, y, L, want_status=True) == 0
         torch.cuda.synchronize()
         outs.append(y.cpu())
     for y in outs:
-        _assert_close(y, y_ref.cpu(), x0.cpu())
+        _assert_same(y, y_ref.cpu(), x0.cpu())
     # a shorter stack on the same handle after the longer one
     y_ref1 = torch.empty_like(x0)
     moe.moe_forward_stack(h, x0, y_ref1, 1)
     y1 = torch.empty_like(x0)
     moe.moe_forward_stack_noalloc(h, x0, y1, 1)
     torch.cuda.synchronize()
-    _assert_close(y1.cpu(), y_ref1.cpu(), x0.cpu())
+    _assert_same(y1.cpu(), y_ref1.cpu(), x0.cpu())
     moe.moe_destroy(h)
 
 
@@ -82,4 +85,28 @@ def test_noalloc_rejects_bad_arguments(moe):
         moe.moe_forward_stack_noalloc(h, x, x, 1)            # y aliases x
     with pytest.raises(moe.MoEError):
         moe.moe_forward_stack_noalloc(h, x, torch.empty_like(x), 2)   # only 1 layer
+    moe.moe_destroy(h)
+
+
+def test_noalloc_reports_a_device_wait_that_ran_out(moe):
+    """A device-side failure inside the no-allocation call reaches the caller
+    through the status word it asks for, without any allocation: the injected
+    launch's first grid barrier waits for arrivals that never come, its 50 ms
+    device-side limit runs out and the status reads 1.  The next call on the
+    same handle clears the array, reports 0 and matches moe_forward_stack."""
+    sh = synth.MoEShape("tiny4", 256, 16, 128, 2, 256, 64, 4)
+    layers = [synth.make_layer(sh, "tiny", l) for l in range(4)]
+    h = moe.moe_create(sh, layers, max_tokens=1)
+    x0 = synth.make_tokens(sh, "tiny", 1, index=24).cuda()
+    y_ref = torch.empty_like(x0)
+    moe.moe_forward_stack(h, x0, y_ref, 4)
+    torch.cuda.synchronize()
+    moe.moe_debug_inject(h, moe.MOE_INJECT_DEVICE_STALL, 50)
+    y = torch.empty_like(x0)
+    assert moe.moe_forward_stack_noalloc(h, x0, y, 4, want_status=True) == 1
+    torch.cuda.synchronize()
+    y = torch.full_like(x0, float("nan"))
+    assert moe.moe_forward_stack_noalloc(h, x0, y, 4, want_status=True) == 0
+    torch.cuda.synchronize()
+    _assert_same(y.cpu(), y_ref.cpu(), x0.cpu())
     moe.moe_destroy(h)
