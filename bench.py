@@ -268,6 +268,9 @@ def run_ours(args):
         line["sub_records"] = {
             "prefill_4096": compact(measure_prefill(args, steps=3, warmup=3)),
             "chunked_128": compact(measure_chunked(args, steps=2, warmup=3)),
+            "streaming_pinned_4l": compact(measure_streaming(args, 32, 3, 4, None, False)),
+            "streaming_store_4l": compact(measure_streaming(args, 32, 3, 4, args.store or "/tmp",
+                                                            False)),
         }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -286,7 +289,8 @@ def compact(line: dict) -> dict:
     """A workload's line without the keys the headline line already carries."""
     keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline",
             "whole_layer", "phase_ms_per_layer", "phase_ms_per_chunk_layer",
-            "touched_weight_bytes_per_step", "clocks", "dtype")
+            "touched_weight_bytes_per_step", "hit_rate", "misses_per_layer_step",
+            "h2d_gbs", "h2d_link_gbs", "store", "e2e", "clocks", "dtype")
     return {k: line[k] for k in keep if k in line}
 
 
@@ -554,27 +558,41 @@ def run_batched(args):
 
 
 def run_streaming(args):
-    """Streaming decode with the expert-slot cache: the 30 x 128 routed experts
-    live in a pinned host pool, each layer has 16 HBM slots under LFU, and the
-    top-8 ids of each (step, layer) come from a Zipf(1.1) trace that keeps 4 of
-    the previous step's ids.  One step = one token through the 30 layers; the
-    misses are copied host -> HBM on the side stream while the shared expert
-    runs."""
+    L = args.layers or 30
+    print(json.dumps(measure_streaming(args, args.steps, args.warmup, L, args.store)), flush=True)
+
+
+def measure_streaming(args, steps, warmup, L, store_dir=None, cpu_baseline=True):
+    """Streaming decode with the expert-slot cache: the L x 128 routed experts
+    live in a pinned host pool (or, with store_dir, in an expert store file
+    written there and read with bounded parallel pread on each miss), each
+    layer has 16 HBM slots under LFU, and the top-8 ids of each (step, layer)
+    come from a Zipf(1.1) trace that keeps 4 of the previous step's ids.  One
+    step = one token through the L layers; the misses are fetched while the
+    shared expert runs."""
     import torch
     import synth
     import expert_ffn_streaming_bit_b300 as moe
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     shape = synth.GEMMA
-    L = args.layers or shape.n_layers
     n_slots = 16
     link = h2d_link_gbs(local)
     layers = make_layers(shape, "streaming_decode", L, "cuda")
-    h = moe.moe_create(shape, layers, n_slots=n_slots, max_tokens=1)
+    store_path = None
+    t_write = 0.0
+    if store_dir:
+        os.makedirs(store_dir, exist_ok=True)
+        store_path = os.path.join(store_dir, "experts_%d_%d.moestore" % (os.getpid(), L))
+        t0 = time.perf_counter()
+        moe.moe_store_write(shape, layers, store_path)
+        t_write = time.perf_counter() - t0
+    h = moe.moe_create(shape, layers, n_slots=n_slots, max_tokens=1, expert_store=store_path,
+                       io_threads=args.io_threads)
     del layers
     info = moe.moe_get_info(h)
     blob = info["expert_blob_bytes"]
-    W, K = args.warmup, args.steps
+    W, K = warmup, steps
     n = W + 2 * K
     traces = [synth.streaming_trace(shape.n_experts, shape.top_k, n, 1.1, 4,
                                     seed=synth.seed_of(3, l, 9)) for l in range(L)]
@@ -631,8 +649,10 @@ def run_streaming(args):
         "vs_baseline": None, "dtype": "u4 x s16 -> s32 (dp2a) per 32-column chunk, f32 scale and sum",
         "data": "synthetic (seeded; forced ids from a Zipf(1.1) trace, 4 of 8 kept per step)",
         "config": {"workload": "streaming decode: %d layers, 16 HBM slots per layer under LFU, "
-                               "routed experts in a %.2f GB pinned host pool, %d decode steps"
-                               % (L, L * shape.n_experts * blob / 1e9, K),
+                               "routed experts in a %.2f GB %s, %d decode steps"
+                               % (L, L * shape.n_experts * blob / 1e9,
+                                  "expert store file read with pread" if store_path
+                                  else "pinned host pool", K),
                    "layers": L, "n_slots": n_slots, "tokens_per_step": 1,
                    "l2": "inputs larger than L2: 1.12 GB of weights per token"},
         "hit_rate": hits / max(hits + misses, 1),
@@ -650,7 +670,14 @@ def run_streaming(args):
         "gpu_launches": 2 * L * K,
         "clocks": clk,
     }
-    if not args.no_cpu_baseline:
+    if store_path:
+        line["store"] = {"path_dir": store_dir, "direct_io": bool(info["store_direct_io"]),
+                         "io_threads": info["io_threads"], "write_s": t_write,
+                         "read_gbs": h2d / (ms / 1e3) / 1e9}
+    moe.moe_destroy(h)
+    if store_path:
+        os.unlink(store_path)
+    if cpu_baseline and not args.no_cpu_baseline:
         import oracle
         layers_cpu = make_layers(shape, "streaming_decode", min(L, 4), "cuda")
         t_c = time.perf_counter()
@@ -668,7 +695,8 @@ def run_streaming(args):
                                 "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": "one token through %d layers with the LFU replay "
                                           "(%.1f s), scaled to %d layers" % (done, dt, L)}
-    print(json.dumps(line), flush=True)
+    torch.cuda.empty_cache()
+    return line
 
 
 TRACE_NAMES = ["start", "input_reduced", "routed", "bs_ready", "bs_done", "br_first_ready",
@@ -773,6 +801,11 @@ def main():
                     help="decode (default, the headline line), a prefill workload, "
                          "streaming decode with the expert-slot cache, or batched decode")
     ap.add_argument("--batch", type=int, default=32, help="tokens per step of batched_decode")
+    ap.add_argument("--store", default=None,
+                    help="streaming_decode: directory for an expert store file to stream from "
+                         "(default: the pinned host pool)")
+    ap.add_argument("--io-threads", type=int, default=8,
+                    help="expert store: concurrent pread calls per miss batch")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {"decode": 5000, "prefill": 3, "chunked_prefill": 2,

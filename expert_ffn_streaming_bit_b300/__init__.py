@@ -35,9 +35,10 @@ MOE_FWD_PRENORM = 2
 MOE_PLAN_ONLY = 1
 MOE_INJECT_NONE, MOE_INJECT_H2D_FAIL, MOE_INJECT_SLOW_COPY, MOE_INJECT_PINNED_ALLOC_FAIL = 0, 1, 2, 3
 MOE_INJECT_DEVICE_STALL = 4
+MOE_INJECT_READ_FAIL = 5
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "MOE_ERR_CUDA",
           -4: "MOE_ERR_TIMEOUT", -5: "MOE_ERR_INJECTED", -6: "MOE_ERR_STATE",
-          -7: "MOE_ERR_DEVICE"}
+          -7: "MOE_ERR_DEVICE", -8: "MOE_ERR_IO"}
 
 
 class MoEError(RuntimeError):
@@ -50,7 +51,8 @@ class moe_config(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int), ("n_experts", ctypes.c_int),
                 ("d_expert", ctypes.c_int), ("top_k", ctypes.c_int), ("d_shared", ctypes.c_int),
                 ("group", ctypes.c_int), ("n_layers", ctypes.c_int), ("n_slots", ctypes.c_int),
-                ("max_tokens", ctypes.c_int)]
+                ("max_tokens", ctypes.c_int), ("expert_store", ctypes.c_char_p),
+                ("io_threads", ctypes.c_int)]
 
 
 class moe_qtensor(ctypes.Structure):
@@ -78,7 +80,8 @@ class moe_layer_stats(ctypes.Structure):
 class moe_info(ctypes.Structure):
     _fields_ = [("device_weight_bytes", ctypes.c_int64), ("pinned_pool_bytes", ctypes.c_int64),
                 ("device_scratch_bytes", ctypes.c_int64), ("expert_blob_bytes", ctypes.c_int64),
-                ("num_sms", ctypes.c_int)]
+                ("num_sms", ctypes.c_int), ("store_direct_io", ctypes.c_int),
+                ("io_threads", ctypes.c_int)]
 
 
 _P, _I = ctypes.c_void_p, ctypes.c_int
@@ -86,6 +89,8 @@ _sig = {
     "moe_create": (_I, [ctypes.POINTER(moe_config), ctypes.POINTER(moe_layer_weights),
                         ctypes.POINTER(ctypes.c_void_p)]),
     "moe_destroy": (None, [_P]),
+    "moe_store_write": (_I, [ctypes.POINTER(moe_config), ctypes.POINTER(moe_layer_weights),
+                             ctypes.c_char_p]),
     "moe_layer_forward": (_I, [_P, _I, _P, _I, _P, _I, _P, _P, ctypes.POINTER(moe_layer_stats)]),
     "moe_forward_stack": (_I, [_P, _P, _I, _P, _I, _P]),
     "moe_forward_stack_host": (_I, [_P, _P, _I, _P, _I, _P]),
@@ -155,7 +160,7 @@ def _qt(t, keep: list) -> moe_qtensor:
     return moe_qtensor(q.ctypes.data, s.ctypes.data, b.ctypes.data)
 
 
-def _layer_struct(layer: Dict[str, object], keep: list) -> moe_layer_weights:
+def _layer_struct(layer: Dict[str, object], keep: list, experts: bool = True) -> moe_layer_weights:
     w = moe_layer_weights()
     w.router = _qt(layer["router"], keep)
     lb = layer.get("logit_bias")
@@ -167,6 +172,8 @@ def _layer_struct(layer: Dict[str, object], keep: list) -> moe_layer_weights:
     w.shared_up = _qt(layer["shared_up"], keep)
     w.shared_down = _qt(layer["shared_down"], keep)
     for name, field in (("gate", "exp_gate"), ("up", "exp_up"), ("down", "exp_down")):
+        if not experts:
+            continue
         t = layer[name]
         q, s, b = _host(t.q), _host(t.scale), _host(t.bias)
         keep.extend([q, s, b])
@@ -180,15 +187,31 @@ def _layer_struct(layer: Dict[str, object], keep: list) -> moe_layer_weights:
 
 
 def moe_create(shape, layers: Sequence[Dict[str, object]], n_slots: int = 0,
-               max_tokens: int = 1) -> Handle:
-    """shape: a synth.MoEShape-like object; layers: per-layer canonical weights."""
+               max_tokens: int = 1, expert_store: Optional[str] = None,
+               io_threads: int = 8) -> Handle:
+    """shape: a synth.MoEShape-like object; layers: per-layer canonical weights.
+    expert_store: path of a file written by moe_store_write (streaming mode
+    then reads the routed experts from it; only the router and shared
+    tensors of `layers` are passed)."""
     cfg = moe_config(shape.d_model, shape.n_experts, shape.d_expert, shape.top_k,
-                     shape.d_shared, shape.group, len(layers), n_slots, max_tokens)
+                     shape.d_shared, shape.group, len(layers), n_slots, max_tokens,
+                     expert_store.encode() if expert_store else None,
+                     io_threads if expert_store else 0)
     keep: List[object] = []
-    arr = (moe_layer_weights * len(layers))(*[_layer_struct(l, keep) for l in layers])
+    arr = (moe_layer_weights * len(layers))(
+        *[_layer_struct(l, keep, experts=expert_store is None) for l in layers])
     out = ctypes.c_void_p()
     _check(_lib.moe_create(ctypes.byref(cfg), arr, ctypes.byref(out)))
     return Handle(out.value, cfg)
+
+
+def moe_store_write(shape, layers: Sequence[Dict[str, object]], path: str):
+    """Write the expert store file of `layers` (routed experts only) to path."""
+    cfg = moe_config(shape.d_model, shape.n_experts, shape.d_expert, shape.top_k,
+                     shape.d_shared, shape.group, len(layers), 0, 1, None, 0)
+    keep: List[object] = []
+    arr = (moe_layer_weights * len(layers))(*[_layer_struct(l, keep) for l in layers])
+    _check(_lib.moe_store_write(ctypes.byref(cfg), arr, path.encode()))
 
 
 def moe_destroy(handle: Handle):

@@ -19,6 +19,7 @@
 
 #include "internal.h"
 #include "repack.h"
+#include "store.h"
 
 using namespace moe;
 
@@ -31,6 +32,7 @@ struct Inject {
   int h2d_fail_in = 0;  // fail the n-th next miss copy (1 = next)
   int slow_copy_ms = 0;
   int stall_ms = 0;     // next decode launch: first grid barrier cannot complete, this wait limit
+  int read_fail_in = 0; // fail the first read of the n-th next expert-store batch (1 = next)
 };
 
 }  // namespace
@@ -60,6 +62,9 @@ struct moe_handle {
   // host memory
   uint8_t* pool = nullptr;  // pinned expert pool (streaming)
   int64_t pool_bytes = 0;
+  std::unique_ptr<ExpertStore> store;  // expert store file (streaming from the SSD tier)
+  uint8_t* staging = nullptr;          // pinned: top_k blobs read from the store
+  cudaEvent_t staging_free = nullptr;  // the staging buffers' last copies are done
   uint16_t* pin_x = nullptr;
   uint16_t* pin_y = nullptr;
   int32_t* pin_ids = nullptr;
@@ -157,6 +162,7 @@ void free_all(moe_handle* h) {
   for (auto e : h->pf_ev) cudaEventDestroy(e);
   if (h->ev_ids) cudaEventDestroy(h->ev_ids);
   if (h->ev_sync) cudaEventDestroy(h->ev_sync);
+  if (h->staging_free) cudaEventDestroy(h->staging_free);
   if (h->side) cudaStreamDestroy(h->side);
   cudaFree(h->dev_weights);
   cudaFree(h->dev_layers);
@@ -164,6 +170,8 @@ void free_all(moe_handle* h) {
   cudaFree(h->pf);
   cudaFree(h->pf_rw);
   cudaFreeHost(h->pool);
+  cudaFreeHost(h->staging);
+  h->store.reset();
   cudaFreeHost(h->pin_x);
   cudaFreeHost(h->pin_y);
   cudaFreeHost(h->pin_ids);
@@ -234,6 +242,52 @@ moe_status launch(moe_handle* h, const DecodeParams& p, cudaStream_t s) {
     return fail(h, MOE_ERR_CUDA, "decode kernel launch: %s",
                 cudaGetErrorString(static_cast<cudaError_t>(e)));
   return MOE_OK;
+}
+
+// The misses of one cache step from the expert store: the blobs are read
+// into the pinned staging buffers by the store's reader threads (bounded
+// parallel pread), then each is copied into its slot on the side stream.
+// A blob that could not be read leaves its slot empty.
+moe_status cache_fill_from_store(moe_handle* h, int layer, const int32_t* ids, int k,
+                                 moe_cache_result* out, uint8_t* slots) {
+  // the staging buffers may still feed the previous step's copies
+  if (h->staging_free) {
+    const cudaError_t e = cudaEventSynchronize(h->staging_free);
+    if (e != cudaSuccess) return fail(h, MOE_ERR_CUDA, "staging wait: %s", cudaGetErrorString(e));
+  }
+  std::vector<int> lay, exp, miss_i;
+  std::vector<uint8_t*> dst;
+  for (int i = 0; i < k; ++i) {
+    if (out->hit[i]) continue;
+    miss_i.push_back(i);
+    lay.push_back(layer);
+    exp.push_back(ids[i]);
+    dst.push_back(h->staging + int64_t(dst.size()) * h->store->stride());
+  }
+  int fail_chunk = 0;
+  if (!miss_i.empty() && h->inj.read_fail_in > 0 && --h->inj.read_fail_in == 0) fail_chunk = 1;
+  std::vector<int> failed;
+  h->store->read(lay, exp, dst, &failed, fail_chunk);
+  moe_status result = MOE_OK;
+  SlotTable& t = h->tables[layer];
+  for (size_t j = 0; j < miss_i.size(); ++j) {
+    const int i = miss_i[j];
+    if (failed[j]) {
+      t.clear_slot(out->slot[i]);
+      result = fail(h, MOE_ERR_IO, "reading expert %d of layer %d from the store failed", ids[i],
+                    layer);
+      continue;
+    }
+    const cudaError_t e = cudaMemcpyAsync(slots + int64_t(out->slot[i]) * h->blob, dst[j], h->blob,
+                                          cudaMemcpyHostToDevice, h->side);
+    if (e != cudaSuccess) {
+      t.clear_slot(out->slot[i]);
+      result = fail(h, MOE_ERR_CUDA, "expert copy: %s", cudaGetErrorString(e));
+    }
+  }
+  CUDA_TRY(h, cudaEventRecord(h->copy_done[layer], h->side));
+  CUDA_TRY(h, cudaEventRecord(h->staging_free, h->side));
+  return result;
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver at run time (the library
@@ -356,31 +410,59 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_INJECTED: return "injected fault";
     case MOE_ERR_STATE: return "invalid state";
     case MOE_ERR_DEVICE: return "device-reported error";
+    case MOE_ERR_IO: return "expert store I/O error";
   }
   return "unknown status";
 }
 
 const char* moe_last_error(const moe_handle* h) { return h ? h->err.c_str() : g_create_error.c_str(); }
 
+static bool config_ok(const moe_config& c) {
+  return c.group == kGroup && c.d_model > 0 && c.d_model % 256 == 0 && c.d_expert > 0 &&
+         c.d_expert % 64 == 0 && c.d_shared > 0 && c.d_shared % 64 == 0 && c.top_k >= 1 &&
+         c.top_k <= kMaxTopK && c.n_experts >= c.top_k && c.n_experts <= 1024 &&
+         c.n_experts % 16 == 0 && c.n_layers >= 1 && c.max_tokens >= 1 &&
+         (c.n_slots == 0 || (c.n_slots >= c.top_k && c.n_slots <= c.n_experts)) &&
+         (!c.expert_store || (c.n_slots > 0 && c.io_threads >= 1 && c.io_threads <= 256));
+}
+
+static bool experts_ok(const moe_config& c, const moe_layer_weights& w) {
+  if (!w.exp_gate || !w.exp_up || !w.exp_down) return false;
+  for (int e = 0; e < c.n_experts; ++e)
+    if (!valid_qt(w.exp_gate[e]) || !valid_qt(w.exp_up[e]) || !valid_qt(w.exp_down[e]))
+      return false;
+  return true;
+}
+
+moe_status moe_store_write(const moe_config* cfg, const moe_layer_weights* layers, const char* path) {
+  if (!cfg || !layers || !path) return fail(nullptr, MOE_ERR_INVALID_ARG, "cfg, layers or path is NULL");
+  moe_config c = *cfg;
+  c.expert_store = nullptr;  // the file is being written, not read
+  if (!config_ok(c)) return fail(nullptr, MOE_ERR_INVALID_ARG, "unsupported configuration");
+  for (int l = 0; l < c.n_layers; ++l)
+    if (!experts_ok(c, layers[l]))
+      return fail(nullptr, MOE_ERR_INVALID_ARG, "layer %d: missing expert weights", l);
+  const Dims d{c.d_model, c.n_experts, c.d_expert, c.top_k, c.d_shared};
+  std::string err;
+  if (store_write(d, c.n_layers, layers, path, &err) != 0)
+    return fail(nullptr, MOE_ERR_IO, "%s", err.c_str());
+  return MOE_OK;
+}
+
 moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, moe_handle** out) {
   if (!out) return fail(nullptr, MOE_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!cfg || !layers) return fail(nullptr, MOE_ERR_INVALID_ARG, "cfg or layers is NULL");
   const moe_config& c = *cfg;
-  if (c.group != kGroup || c.d_model <= 0 || c.d_model % 256 || c.d_expert <= 0 ||
-      c.d_expert % 64 || c.d_shared <= 0 || c.d_shared % 64 || c.top_k < 1 ||
-      c.top_k > kMaxTopK || c.n_experts < c.top_k || c.n_experts > 1024 || c.n_experts % 16 ||
-      c.n_layers < 1 || c.max_tokens < 1 ||
-      (c.n_slots != 0 && (c.n_slots < c.top_k || c.n_slots > c.n_experts)))
-    return fail(nullptr, MOE_ERR_INVALID_ARG, "unsupported configuration");
+  if (!config_ok(c)) return fail(nullptr, MOE_ERR_INVALID_ARG, "unsupported configuration");
+  const bool from_store = c.expert_store != nullptr;
   for (int l = 0; l < c.n_layers; ++l) {
     const moe_layer_weights& w = layers[l];
     if (!valid_qt(w.router) || !valid_qt(w.shared_gate) || !valid_qt(w.shared_up) ||
-        !valid_qt(w.shared_down) || !w.exp_gate || !w.exp_up || !w.exp_down)
+        !valid_qt(w.shared_down))
       return fail(nullptr, MOE_ERR_INVALID_ARG, "layer %d: missing weights", l);
-    for (int e = 0; e < c.n_experts; ++e)
-      if (!valid_qt(w.exp_gate[e]) || !valid_qt(w.exp_up[e]) || !valid_qt(w.exp_down[e]))
-        return fail(nullptr, MOE_ERR_INVALID_ARG, "layer %d expert %d: missing weights", l, e);
+    if (!from_store && !experts_ok(c, w))
+      return fail(nullptr, MOE_ERR_INVALID_ARG, "layer %d: missing expert weights", l);
   }
   std::unique_ptr<moe_handle> h(new moe_handle());
   h->cfg = c;
@@ -417,7 +499,22 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
   const int64_t per_layer_experts = (streaming ? c.n_slots : c.n_experts) * h->blob;
   h->dev_weight_bytes = L * (h->fixed + per_layer_experts);
   CREATE_TRY(cudaMalloc(&h->dev_weights, h->dev_weight_bytes));
-  if (streaming) {
+  if (streaming && from_store) {
+    // the SSD tier: staging buffers for the misses of one step, page aligned
+    // for direct I/O, and the file with its reader threads
+    const int64_t stride = store_stride(h->blob);
+    CREATE_TRY(cudaHostAlloc(&h->staging, int64_t(c.top_k) * stride, cudaHostAllocDefault));
+    CREATE_TRY(cudaEventCreateWithFlags(&h->staging_free, cudaEventDisableTiming));
+    const bool aligned = (reinterpret_cast<uintptr_t>(h->staging) % kStorePage) == 0;
+    h->store.reset(new ExpertStore());
+    std::string err;
+    if (h->store->open(c.expert_store, d, L, h->blob, c.io_threads, aligned, &err) != 0) {
+      st = fail(nullptr, err.find("match") != std::string::npos ? MOE_ERR_INVALID_ARG : MOE_ERR_IO,
+                "%s", err.c_str());
+      free_all(h.get());
+      return st;
+    }
+  } else if (streaming) {
     h->pool_bytes = static_cast<int64_t>(L) * c.n_experts * h->blob;
     if (g_inject_pinned_fail) {
       g_inject_pinned_fail = 0;
@@ -431,11 +528,13 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     for (int l = 0; l < L; ++l) {
       const moe_layer_weights& w = layers[l];
       repack_layer_fixed(d, w, stage.data());
-      uint8_t* exp_dst = streaming ? h->pool + static_cast<int64_t>(l) * c.n_experts * h->blob
-                                   : stage.data() + h->fixed;
-      parallel_for(c.n_experts, [&](int64_t e) {
-        repack_expert(d, w.exp_gate[e], w.exp_up[e], w.exp_down[e], exp_dst + e * h->blob);
-      });
+      if (!from_store) {
+        uint8_t* exp_dst = streaming ? h->pool + static_cast<int64_t>(l) * c.n_experts * h->blob
+                                     : stage.data() + h->fixed;
+        parallel_for(c.n_experts, [&](int64_t e) {
+          repack_expert(d, w.exp_gate[e], w.exp_up[e], w.exp_down[e], exp_dst + e * h->blob);
+        });
+      }
       CREATE_TRY(cudaMemcpy(h->dev_weights + l * (h->fixed + per_layer_experts), stage.data(),
                             stage.size(), cudaMemcpyHostToDevice));
     }
@@ -669,6 +768,8 @@ moe_status moe_get_info(const moe_handle* h, moe_info* out) {
   out->device_scratch_bytes = h->scratch_bytes + h->pf_bytes;
   out->expert_blob_bytes = h->blob;
   out->num_sms = h->grid;
+  out->store_direct_io = h->store && h->store->direct() ? 1 : 0;
+  out->io_threads = h->store ? h->store->threads() : 0;
   return MOE_OK;
 }
 
@@ -698,6 +799,10 @@ moe_status moe_debug_inject(moe_handle* h, int what, int arg) {
     case MOE_INJECT_DEVICE_STALL:
       if (!h || arg < 1 || arg > 2000) return MOE_ERR_INVALID_ARG;
       h->inj.stall_ms = arg;
+      return MOE_OK;
+    case MOE_INJECT_READ_FAIL:
+      if (!h || arg < 1) return MOE_ERR_INVALID_ARG;
+      h->inj.read_fail_in = arg;
       return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
@@ -739,6 +844,7 @@ moe_status moe_cache_step(moe_handle* h, int layer, const int32_t* ids, int k, i
   CUDA_TRY(h, cudaStreamWaitEvent(h->side, h->layer_done[layer], 0));
   uint8_t* slots =
       h->dev_weights + layer * (h->fixed + int64_t(h->cfg.n_slots) * h->blob) + h->fixed;
+  if (h->store) return cache_fill_from_store(h, layer, ids, k, out, slots);
   const uint8_t* pool = h->pool + int64_t(layer) * h->cfg.n_experts * h->blob;
   moe_status result = MOE_OK;
   for (int i = 0; i < k; ++i) {
@@ -947,37 +1053,47 @@ static moe_status decode_layer_streaming(moe_handle* h, int layer, const void* x
   int32_t ids[kMaxTopK];
   moe_cache_result cr;
   moe_status st;
+  // The first launch adds the layer's router logits into the accumulators,
+  // and only the second one (the owner of the output rows) clears them.  If
+  // the step stops in between, clear them here so the next step starts from
+  // zero.
+  auto abandon = [&](moe_status why) {
+    cudaMemsetAsync(h->lacc, 0, 2 * h->d.E * 8, s);
+    return why;
+  };
   if (forced) {
-    // ids known up front: start the copies, then route + shared expert meanwhile
+    // ids known up front: the router and the shared expert go to the GPU
+    // first, then the misses are fetched (read from the store on the host,
+    // copied on the side stream) while they run
     std::memcpy(ids, forced, sizeof(int32_t) * K);
-    st = moe_cache_step(h, layer, ids, K, 0, &cr);
-    if (st != MOE_OK) return st;
     p1.phases = PH_ROUTER | PH_BSHARED;
     p1.forced = 1;
     std::memcpy(p1.forced_ids, ids, sizeof(int32_t) * K);
     st = launch(h, p1, s);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK) return abandon(st);
+    st = moe_cache_step(h, layer, ids, K, 0, &cr);
+    if (st != MOE_OK) return abandon(st);
   } else {
     p1.phases = PH_ROUTER;
     st = launch(h, p1, s);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK) return abandon(st);
     CUDA_TRY(h, cudaMemcpyAsync(h->pin_ids, h->ids, sizeof(int32_t) * K, cudaMemcpyDeviceToHost, s));
     CUDA_TRY(h, cudaEventRecord(h->ev_ids, s));
     p1.phases = PH_BSHARED;  // shared expert runs while the host plans and copies
     st = launch(h, p1, s);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK) return abandon(st);
     st = wait_event(h, h->ev_ids);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK) return abandon(st);
     std::memcpy(ids, h->pin_ids, sizeof(int32_t) * K);
     st = moe_cache_step(h, layer, ids, K, 0, &cr);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK) return abandon(st);
   }
   CUDA_TRY(h, cudaStreamWaitEvent(s, h->copy_done[layer], 0));
   DecodeParams p2 = params_for(h, layer, 1, x, y, PH_BROUTED | PH_C, flags);
   p2.use_slots = 1;
   for (int i = 0; i < K; ++i) p2.slots[i] = cr.slot[i];
   st = launch(h, p2, s);
-  if (st != MOE_OK) return st;
+  if (st != MOE_OK) return abandon(st);
   CUDA_TRY(h, cudaEventRecord(h->layer_done[layer], s));
   if (stats) {
     stats->hits = K - cr.misses;

@@ -58,7 +58,8 @@ typedef enum {
   MOE_ERR_TIMEOUT = -4,     /* a bounded wait (host or device) ran out */
   MOE_ERR_INJECTED = -5,    /* a fault injected with moe_debug_inject() */
   MOE_ERR_STATE = -6,       /* call not valid in this handle's mode or state */
-  MOE_ERR_DEVICE = -7       /* a kernel reported an inconsistent input (e.g. id out of range) */
+  MOE_ERR_DEVICE = -7,      /* a kernel reported an inconsistent input (e.g. id out of range) */
+  MOE_ERR_IO = -8           /* reading or writing the expert store file failed */
 } moe_status;
 
 typedef struct moe_handle moe_handle;
@@ -78,6 +79,11 @@ typedef struct {
                      count (top_k <= n_slots <= n_experts); the full expert
                      set then lives in a pinned host pool owned by the handle. */
   int max_tokens; /* largest T passed to any forward call */
+  const char* expert_store; /* NULL, or (n_slots > 0) the path of an expert store file
+                               written by moe_store_write: the routed experts are then
+                               read from it on each cache miss instead of being held in
+                               a pinned host pool */
+  int io_threads; /* expert store only: concurrent pread() calls per miss batch (>= 1) */
 } moe_config;
 
 /* One affine-quantised matrix in canonical form, HOST memory, row-major
@@ -107,6 +113,22 @@ typedef struct {
 } moe_layer_weights;
 
 /*
+ * moe_store_write — write the expert store file for `cfg` at `path`: the
+ * storage tier of the slot cache (blog.hypho.cn "TurboFieldfare gemma4
+ * out-of-core inference", section "为什么不用 mmap？", and shilu.ai
+ * "drumih/turbo-fieldfare", section 推理引擎的工作原理: cold experts live on
+ * the SSD and are read with bounded parallel pread() calls, not mapped).
+ * Host only (no GPU is touched).  Every routed expert of every layer
+ * (`layers`: cfg->n_layers entries, host memory, canonical form; only the
+ * exp_* tensors are read) is repacked into the GPU blob layout and written
+ * at a page-aligned offset after a 4096-byte header that records the
+ * shape.  An existing file is replaced.  Fails with MOE_ERR_INVALID_ARG on
+ * a bad configuration or missing tensors, MOE_ERR_IO if the file cannot be
+ * written (then the file may be left partial).
+ */
+moe_status moe_store_write(const moe_config* cfg, const moe_layer_weights* layers, const char* path);
+
+/*
  * moe_create — build a handle for `cfg` on the current CUDA device.
  * Follows shilu.ai "drumih/turbo-fieldfare", overview table (row 权重: the
  * affine 4-bit g64 experts and 8-bit router this call repacks) and section
@@ -115,8 +137,12 @@ typedef struct {
  * resident); one owner per model.
  * Copies and repacks all weights (`layers`: n_layers entries, host memory) into
  * the GPU layout: into HBM when cfg->n_slots == 0, else into a pinned host
- * pool plus n_slots HBM slots per layer.  The caller may free `layers` when
- * the call returns.  Allocates the handle's device scratch (sized by
+ * pool plus n_slots HBM slots per layer.  With cfg->expert_store set (and
+ * n_slots > 0) the routed experts come from that file instead: `layers`
+ * then only needs the router and shared tensors (exp_* may be NULL), the
+ * store's header must match cfg (else MOE_ERR_INVALID_ARG), and the handle
+ * holds top_k pinned staging buffers and cfg->io_threads reader threads in
+ * place of the pool.  The caller may free `layers` when the call returns.  Allocates the handle's device scratch (sized by
  * max_tokens), a side copy stream and events.  On failure *out is NULL and
  * nothing is leaked.
  */
@@ -282,8 +308,13 @@ moe_status moe_last_buckets(moe_handle* h, int32_t* counts, int32_t* offsets, in
  * recently used, then the lowest slot index); newcomers start at count 1.
  * Unless MOE_PLAN_ONLY, each miss is copied from the pinned pool into its
  * slot with one cudaMemcpyAsync on the handle's side stream; the copies are
- * ordered before the next forward call on this layer.  Streaming mode only.
- * If a copy cannot be enqueued the slot is left empty and the call fails.
+ * ordered before the next forward call on this layer.  With an expert store
+ * the misses are first read from the file into the pinned staging buffers,
+ * each blob in 1 MiB pread() calls of which up to io_threads run at once
+ * (page-aligned direct I/O where the file system allows it); the call
+ * returns once the reads are done and the copies enqueued.  Streaming mode
+ * only.  If a read fails (MOE_ERR_IO) or a copy cannot be enqueued, the slot
+ * is left empty and the call fails; the next step refetches that expert.
  */
 moe_status moe_cache_step(moe_handle* h, int layer, const int32_t* ids, int k, int flags,
                           moe_cache_result* out);
@@ -309,6 +340,8 @@ typedef struct {
   int64_t device_scratch_bytes; /* HBM scratch */
   int64_t expert_blob_bytes;    /* bytes of one repacked routed expert */
   int num_sms;                  /* SMs used by the persistent kernels */
+  int store_direct_io;          /* expert store: 1 if reads bypass the page cache */
+  int io_threads;               /* expert store: reader threads (0 without a store) */
 } moe_info;
 moe_status moe_get_info(const moe_handle* h, moe_info* out);
 
@@ -326,12 +359,16 @@ moe_status moe_get_info(const moe_handle* h, moe_info* out);
  *     the next status check (a synchronising call) returns MOE_ERR_TIMEOUT
  *     and resets the barrier counter and logit accumulators, so the handle
  *     and the CUDA context stay usable.  No memory is touched out of bounds.
+ *   MOE_INJECT_READ_FAIL: in the `arg`-th next expert-store read batch the
+ *     first 1 MiB read fails (as if the device returned an error): that
+ *     expert's slot is left empty and moe_cache_step returns MOE_ERR_IO.
  *   MOE_INJECT_NONE: clear everything. */
 #define MOE_INJECT_NONE 0
 #define MOE_INJECT_H2D_FAIL 1
 #define MOE_INJECT_SLOW_COPY 2
 #define MOE_INJECT_PINNED_ALLOC_FAIL 3
 #define MOE_INJECT_DEVICE_STALL 4
+#define MOE_INJECT_READ_FAIL 5
 moe_status moe_debug_inject(moe_handle* h, int what, int arg);
 
 /* Host waits on device work poll with this deadline (default 10000 ms) and
