@@ -24,6 +24,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "attn_oracle.c")]
 _LIB = os.path.join(_HERE, "_moe_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -31,10 +32,11 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (OpenMP over independent rows)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or any(
+            os.path.getmtime(_LIB) < os.path.getmtime(f) for f in _SRCS):
         tmp = _LIB + ".tmp.%d" % os.getpid()
         subprocess.check_call(["gcc", "-O3", "-fopenmp", "-fPIC", "-shared", "-std=c11",
-                               "-o", tmp, _SRC, "-lm"])
+                               "-o", tmp, *_SRCS, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -49,6 +51,12 @@ class Layer(ctypes.Structure):
                 ("router", QT), ("logit_bias", ctypes.c_void_p),
                 ("shared_gate", QT), ("shared_up", QT), ("shared_down", QT),
                 ("gate", QT), ("up", QT), ("down", QT)]
+
+
+class AttnLayer(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("group", ctypes.c_int),
+                ("wq", QT), ("wk", QT), ("wv", QT), ("wo", QT)]
 
 
 def lib():
@@ -86,6 +94,13 @@ def lib():
             L.orc_bucket.argtypes = [P, i32, i32, i32, P, P, P]
             L.orc_lfu_step.restype = i32
             L.orc_lfu_step.argtypes = [i32, P, P, P, i64, P, i32, i32, P, P, P]
+            L.ora_rms.restype = None
+            L.ora_rms.argtypes = [P, i32, ctypes.c_double]
+            L.ora_rope.restype = None
+            L.ora_rope.argtypes = [P, i32, i64, ctypes.c_double]
+            L.ora_attn_step.restype = i32
+            L.ora_attn_step.argtypes = [ctypes.POINTER(AttnLayer), P, i64, i32, ctypes.c_double,
+                                        P, P, i64, P]
             _lib = L
     return _lib
 
@@ -283,3 +298,51 @@ class LFUCache:
             raise ValueError("orc_lfu_step: bad ids")
         self.step_no += 1
         return hit, slot, ev
+
+
+# ------------------------------------------------------- decode attention
+
+def head_rms(v: np.ndarray, eps: float = RMS_EPS) -> np.ndarray:
+    """v / sqrt(mean(v^2) + eps) (unit-gain RMS normalisation of one head)."""
+    vv = np.ascontiguousarray(v, dtype=np.float64).copy()
+    lib().ora_rms(_p(vv), vv.shape[0], eps)
+    return vv
+
+
+def rope(v: np.ndarray, pos: int, theta: float) -> np.ndarray:
+    """Rotary embedding of one head vector at position pos (rotate-half pairs)."""
+    vv = np.ascontiguousarray(v, dtype=np.float64).copy()
+    lib().ora_rope(_p(vv), vv.shape[0], int(pos), float(theta))
+    return vv
+
+
+class AttnState:
+    """One attention layer of the oracle: its canonical 4-bit weights and its
+    own fp16 KV cache ([Hkv][cap][d], position p in slot p % cap)."""
+
+    def __init__(self, shape, weights: Dict[str, object], cap: int, window: int, theta: float):
+        self.keep = []
+
+        def qt(name):
+            t = weights[name]
+            if hasattr(t, "q"):
+                return _qt(t.q, t.scale, t.bias, self.keep)
+            return _qt(*t, self.keep)
+
+        self.s = AttnLayer(shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                           shape.group, qt("wq"), qt("wk"), qt("wv"), qt("wo"))
+        self.shape, self.cap, self.window, self.theta = shape, cap, window, theta
+        n = shape.n_kv_heads * cap * shape.head_dim
+        self.k = np.zeros(n, np.uint16)
+        self.v = np.zeros(n, np.uint16)
+
+    def step(self, x_bf16, pos: int) -> np.ndarray:
+        """The attention block's output (fp64 [D], before the residual) for the
+        token x at position pos; stores the token's k, v in the cache."""
+        x = _np(x_bf16, np.uint16).reshape(-1)
+        y = np.empty(self.shape.d_model, np.float64)
+        rc = lib().ora_attn_step(ctypes.byref(self.s), _p(x), int(pos), int(self.window),
+                                 float(self.theta), _p(self.k), _p(self.v), int(self.cap), _p(y))
+        if rc != 0:
+            raise ValueError("ora_attn_step: bad arguments")
+        return y

@@ -264,3 +264,67 @@ def layer_to(layer: Dict[str, object], device) -> Dict[str, object]:
         else:
             out[key] = val
     return out
+
+
+# ------------------------------------------------------- decode attention
+
+@dataclasses.dataclass(frozen=True)
+class AttnShape:
+    """Dimensions of the attention blocks in front of the MoE layers.
+
+    The pages give no head shapes; this is the reading used (stated with the
+    other readings of the pages): the MoE block's hidden size, grouped-query
+    heads, sliding-window layers with a ring cache and full-attention layers
+    with a linear cache."""
+
+    name: str
+    d_model: int      # D
+    n_heads: int      # Hq, query heads
+    n_kv_heads: int   # Hkv, key/value heads (Hq % Hkv == 0)
+    head_dim: int     # d
+    group: int        # quantisation group along the input dimension
+    n_layers: int
+    window: int       # sliding-window length (the ring cache's capacity)
+    max_seq: int      # capacity of a full-attention layer's linear cache
+    sliding: tuple    # per layer: 1 sliding window, 0 full attention
+
+    def theta(self, layer: int) -> float:
+        return ROPE_THETA_SLIDING if self.sliding[layer] else ROPE_THETA_FULL
+
+    def attn_weight_bytes(self) -> int:
+        """Canonical bytes of one layer's 4-bit q, k, v and output projections."""
+        qd, kd = self.n_heads * self.head_dim, self.n_kv_heads * self.head_dim
+        return (qbytes(qd, self.d_model, 4, self.group) + 2 * qbytes(kd, self.d_model, 4, self.group)
+                + qbytes(self.d_model, qd, 4, self.group))
+
+
+ROPE_THETA_SLIDING = 10000.0
+ROPE_THETA_FULL = 1000000.0
+
+TINY_ATTN = AttnShape("tiny-attn", d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, group=64,
+                      n_layers=2, window=8, max_seq=64, sliding=(1, 0))
+# Gemma 4 26B-A4B reading: 16 query heads and 8 key/value heads of 256, a
+# 1024-token window; 25 sliding layers and 5 full-attention layers (every
+# sixth layer full).
+GEMMA_ATTN = AttnShape("gemma4-26b-a4b-attn", d_model=2816, n_heads=16, n_kv_heads=8,
+                       head_dim=256, group=64, n_layers=30, window=1024, max_seq=8192,
+                       sliding=tuple(0 if l % 6 == 5 else 1 for l in range(30)))
+
+ATTN_TENSOR_IDS = {name: 16 + i for i, name in enumerate(["wq", "wk", "wv", "wo"])}
+
+
+def make_attn_layer(shape: AttnShape, workload: str, layer: int, device="cpu",
+                    std: float = WEIGHT_STD) -> Dict[str, object]:
+    """Canonical 4-bit weights of one attention block: wq [Hq d, D],
+    wk / wv [Hkv d, D], wo [D, Hq d] (N(0, std^2) fp32 draws, affine g64)."""
+    D, qd, kd = shape.d_model, shape.n_heads * shape.head_dim, shape.n_kv_heads * shape.head_dim
+    wid = WORKLOAD_IDS[workload]
+
+    def draw(tag, rows, cols):
+        w = normal((rows, cols), std, seed_of(wid, layer, ATTN_TENSOR_IDS[tag]), device)
+        out = qtensor(w, 4, shape.group)
+        del w
+        return out
+
+    return {"wq": draw("wq", qd, D), "wk": draw("wk", kd, D), "wv": draw("wv", kd, D),
+            "wo": draw("wo", D, qd)}
