@@ -84,6 +84,17 @@ class moe_info(ctypes.Structure):
                 ("io_threads", ctypes.c_int)]
 
 
+class moe_attn_config(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("n_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("group", ctypes.c_int), ("n_layers", ctypes.c_int),
+                ("window", ctypes.c_int), ("max_seq", ctypes.c_int),
+                ("sliding", ctypes.c_void_p), ("rope_theta", ctypes.c_void_p)]
+
+
+class moe_attn_weights(ctypes.Structure):
+    _fields_ = [("wq", moe_qtensor), ("wk", moe_qtensor), ("wv", moe_qtensor), ("wo", moe_qtensor)]
+
+
 _P, _I = ctypes.c_void_p, ctypes.c_int
 _sig = {
     "moe_create": (_I, [ctypes.POINTER(moe_config), ctypes.POINTER(moe_layer_weights),
@@ -108,6 +119,13 @@ _sig = {
     "moe_get_info": (_I, [_P, ctypes.POINTER(moe_info)]),
     "moe_debug_inject": (_I, [_P, _I, _I]),
     "moe_set_timeout_ms": (_I, [_P, _I]),
+    "moe_attn_create": (_I, [ctypes.POINTER(moe_attn_config), ctypes.POINTER(moe_attn_weights),
+                             ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_attn_destroy": (None, [_P]),
+    "moe_attn_last_error": (ctypes.c_char_p, [_P]),
+    "moe_attn_forward": (_I, [_P, _I, _P, ctypes.c_longlong, _P, _I, _P]),
+    "moe_attn_reset": (_I, [_P]),
+    "moe_decode_step": (_I, [_P, _P, _P, ctypes.c_longlong, _P, _I, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_last_error": (ctypes.c_char_p, [_P]),
 }
@@ -390,3 +408,64 @@ def moe_debug_inject(handle: Optional[Handle], what: int, arg: int = 0):
 
 def moe_set_timeout_ms(handle: Handle, ms: int):
     _check(_lib.moe_set_timeout_ms(handle.ptr, ms), handle)
+
+
+# ------------------------------------------------------- decode attention
+
+class AttnHandle:
+    """Owns a moe_attn*; destroyed with the object or by moe_attn_destroy."""
+
+    def __init__(self, ptr: int, cfg: moe_attn_config):
+        self.ptr = ptr
+        self.cfg = cfg
+
+    def __del__(self):
+        if getattr(self, "ptr", None):
+            _lib.moe_attn_destroy(self.ptr)
+            self.ptr = None
+
+
+def _attn_check(status: int, handle: Optional[AttnHandle] = None):
+    if status != MOE_OK:
+        msg = _lib.moe_attn_last_error(handle.ptr if handle else None).decode()
+        raise MoEError(status, msg)
+
+
+def moe_attn_create(shape, layers: Sequence[Dict[str, object]]) -> AttnHandle:
+    """shape: a synth.AttnShape-like object (sliding flags and RoPE bases per
+    layer); layers: per-layer canonical weights wq, wk, wv, wo."""
+    L = len(layers)
+    sliding = np.ascontiguousarray([int(shape.sliding[l]) for l in range(L)], np.int32)
+    theta = np.ascontiguousarray([shape.theta(l) for l in range(L)], np.float32)
+    cfg = moe_attn_config(shape.d_model, shape.n_heads, shape.n_kv_heads, shape.head_dim,
+                          shape.group, L, shape.window, shape.max_seq, sliding.ctypes.data,
+                          theta.ctypes.data)
+    keep: List[object] = [sliding, theta]
+    arr = (moe_attn_weights * L)(*[moe_attn_weights(_qt(l["wq"], keep), _qt(l["wk"], keep),
+                                                    _qt(l["wv"], keep), _qt(l["wo"], keep))
+                                   for l in layers])
+    out = ctypes.c_void_p()
+    _attn_check(_lib.moe_attn_create(ctypes.byref(cfg), arr, ctypes.byref(out)))
+    return AttnHandle(out.value, cfg)
+
+
+def moe_attn_destroy(handle: AttnHandle):
+    if handle.ptr:
+        _lib.moe_attn_destroy(handle.ptr)
+        handle.ptr = None
+
+
+def moe_attn_forward(handle: AttnHandle, layer: int, x, pos: int, y, flags: int = 0, stream=None):
+    """x, y: CUDA bf16 tensors [1, D] (or [D])."""
+    _attn_check(_lib.moe_attn_forward(handle.ptr, layer, _dev_ptr(x), int(pos), _dev_ptr(y), flags,
+                                      _stream_ptr(stream)), handle)
+
+
+def moe_attn_reset(handle: AttnHandle):
+    _attn_check(_lib.moe_attn_reset(handle.ptr), handle)
+
+
+def moe_decode_step(attn: AttnHandle, moe: Handle, x, pos: int, y, n_layers: int, stream=None):
+    """One decode token through n_layers (attention, then the MoE layer)."""
+    _attn_check(_lib.moe_decode_step(attn.ptr, moe.ptr, _dev_ptr(x), int(pos), _dev_ptr(y),
+                                     n_layers, _stream_ptr(stream)), attn)

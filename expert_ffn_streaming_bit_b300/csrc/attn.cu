@@ -1,0 +1,634 @@
+// Decode attention: the step before the router, one token per call.
+//
+// shilu.ai "drumih/turbo-fieldfare", sections 推理引擎的工作原理 and
+// 状态和范围: in every layer the GPU computes attention and then the router
+// from resident weights; attention weights are 4-bit MLX affine; the KV
+// store is FP16, a bounded ring for the sliding-window layers and linear for
+// the full-attention layers; decode attention is exact split-K/V with
+// distinct normalised K and V paths.  The pages give no formulas; the
+// readings (the same as the oracle's):
+//   u = x / sqrt(mean(x^2) + 1e-6); q, k, v = Wq u, Wk u, Wv u;
+//   per head q, k, v divided by their RMS (eps 1e-6); RoPE on q and k
+//   (rotate-half pairs (i, i + d/2), angle pos * theta^(-2i/d));
+//   k, v stored as fp16 in slot pos % capacity;
+//   scores q . k / sqrt(d) over the visible positions, softmax, o = sum w v;
+//   y = Wo o, optionally + x (residual), rounded to bf16.
+//
+// Launches per layer and token:
+//   qgemv_kernel        q, k, v = W u (4-bit integer dot products; the
+//                       pre-norm is a scale applied after the dot product)
+//   attn_prep_kernel    per-head RMS norms, RoPE, the fp16 KV append
+//   attn_split_kernel   (head, split) blocks: scores and an online softmax
+//                       over the split's positions -> (o, max, sum) partials
+//   attn_combine_kernel per head: the partials rescaled to one maximum
+//   qgemv_kernel        y = Wo o (+ x), bf16
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "internal.h"
+#include "ptx.cuh"
+#include "qdot.cuh"
+#include "repack.h"
+
+namespace moe {
+namespace {
+
+constexpr int kGemvWarps = 8;
+constexpr int kGemvRows = 2 * kGemvWarps;  // rows per block (two per warp)
+constexpr int kGemvMaxK = 4096;            // input length <= 4096
+constexpr int kGemvXC = kGemvMaxK / 1024;  // activation chunks per lane
+constexpr int kMaxSplits = 64;
+constexpr int kSplitWarps = 8;
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x40u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+struct GemvArgs {
+  const uint8_t* w;        // qrows [R] of K inputs, rb bytes each
+  int R, K, rb;
+  const uint16_t* x_bf16;  // input, bf16 [K] (or NULL)
+  const float* x_f32;      // input, fp32 [K] (or NULL)
+  int prenorm;             // dot products scaled by 1 / sqrt(mean(x^2) + eps)
+  float eps;
+  float* y_f32;            // output fp32 [R] (or NULL)
+  uint16_t* y_bf16;        // output bf16 [R] = bf16(res + W x) (or NULL)
+  const uint16_t* res;     // residual bf16 [R] for y_bf16 (or NULL)
+};
+
+// y = W x for a 4-bit matrix in qrows.  Every block quantises the whole
+// input to int16 chunks in shared memory (one scale: max|x|), then each warp
+// takes two rows: each lane loads its 32-column chunks of both rows (codes
+// and scale/bias words, coalesced across the warp) and accumulates
+// s * sum(q X) + b * sum(X) per chunk; a fixed-order warp sum finishes the row.
+__global__ void __launch_bounds__(kGemvWarps * 32) qgemv_kernel(GemvArgs a) {
+  __shared__ __align__(16) uint8_t xs[(kGemvMaxK / 32) * 80];
+  __shared__ float xsum[kGemvMaxK / 32];
+  __shared__ float red[2][kGemvWarps];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int nc = a.K / 32, nv = a.K / 8;
+  // ---- the input, 8 values per thread and group of 256 threads
+  float v[2][8];
+  float m = 0.f, ss = 0.f;
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int idx = t + 256 * g;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[g][j] = 0.f;
+    if (idx < nv) {
+      if (a.x_bf16) {
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(a.x_bf16) + idx);
+        const uint32_t ww[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[g][2 * j] = bf16_to_f32(ww[j] & 0xffffu);
+          v[g][2 * j + 1] = bf16_to_f32(ww[j] >> 16);
+        }
+      } else {
+        const float4 p0 = __ldg(reinterpret_cast<const float4*>(a.x_f32) + 2 * idx);
+        const float4 p1 = __ldg(reinterpret_cast<const float4*>(a.x_f32) + 2 * idx + 1);
+        v[g][0] = p0.x; v[g][1] = p0.y; v[g][2] = p0.z; v[g][3] = p0.w;
+        v[g][4] = p1.x; v[g][5] = p1.y; v[g][6] = p1.z; v[g][7] = p1.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        m = fmaxf(m, fabsf(v[g][j]));
+        ss = fmaf(v[g][j], v[g][j], ss);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  }
+  if (lane == 0) {
+    red[0][w] = m;
+    red[1][w] = ss;
+  }
+  __syncthreads();
+  m = 0.f;
+  ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kGemvWarps; ++i) {
+    m = fmaxf(m, red[0][i]);
+    ss += red[1][i];
+  }
+  const float q = quant_factor(m);
+  const float r = a.prenorm ? rsqrtf(ss / static_cast<float>(a.K) + a.eps) : 1.f;
+  const float vs = q > 0.f ? r / q : 0.f;
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int idx = t + 256 * g;
+    uint4 packed = make_uint4(0, 0, 0, 0);
+    if (idx < nv) {
+      packed = make_uint4(pack_s16x2(v[g][0] * q, v[g][1] * q), pack_s16x2(v[g][2] * q, v[g][3] * q),
+                          pack_s16x2(v[g][4] * q, v[g][5] * q), pack_s16x2(v[g][6] * q, v[g][7] * q));
+      *reinterpret_cast<uint4*>(xs + (idx >> 2) * 80 + (idx & 3) * 16) = packed;
+    }
+    // chunk sums: the 4 consecutive lanes holding idx 4c .. 4c+3 form chunk c
+    int cs = sum8_s16(packed);
+    cs += __shfl_xor_sync(0xffffffffu, cs, 1);
+    cs += __shfl_xor_sync(0xffffffffu, cs, 2);
+    if (idx < nv && (idx & 3) == 0) xsum[idx >> 2] = static_cast<float>(cs);
+  }
+  __syncthreads();
+  // ---- two rows per warp
+  const int r0 = blockIdx.x * kGemvRows + 2 * w;
+  uint4 wv[2][kGemvXC];
+  uint32_t sbv[2][kGemvXC];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const bool row_ok = r0 + k < a.R;
+    const uint8_t* row = a.w + static_cast<int64_t>(row_ok ? r0 + k : 0) * a.rb;
+#pragma unroll
+    for (int i = 0; i < kGemvXC; ++i) {
+      const int c = lane + 32 * i;
+      const bool ok = row_ok && c < nc;
+      wv[k][i] = ok ? __ldg(reinterpret_cast<const uint4*>(row + c * 16)) : make_uint4(0, 0, 0, 0);
+      sbv[k][i] = ok ? __ldg(reinterpret_cast<const uint32_t*>(row + a.K / 2 + (c >> 1) * 4)) : 0u;
+    }
+  }
+  float acc[2] = {0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < kGemvXC; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nc) {
+      uint4 xc[4];
+      const uint4* src = reinterpret_cast<const uint4*>(xs + c * 80);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xc[j] = src[j];
+      const float sx = xsum[c];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int tot = idot_chunk(wv[k][i], xc);
+        const __half2 sb = *reinterpret_cast<const __half2*>(&sbv[k][i]);
+        acc[k] += fmaf(__low2float(sb), static_cast<float>(tot), __high2float(sb) * sx);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int row = r0 + k;
+      if (row >= a.R) continue;
+      const float out = acc[k] * vs;
+      if (a.y_f32) a.y_f32[row] = out;
+      if (a.y_bf16) a.y_bf16[row] = f32_to_bf16((a.res ? bf16_to_f32(a.res[row]) : 0.f) + out);
+    }
+  }
+}
+
+struct PrepArgs {
+  const float* qkv;  // raw projections: Hq query heads, then Hkv key heads, then Hkv value heads
+  int Hq, Hkv, d;
+  float eps;
+  long long pos, cap;
+  double theta;
+  float* qn;         // [Hq][d] normalised, rotated queries
+  __half* kc;        // this layer's key cache [Hkv][cap][d]
+  __half* vc;        // this layer's value cache [Hkv][cap][d]
+};
+
+// One block per head (blockDim = d): RMS norm; RoPE for query and key heads;
+// the key and value of this position go to cache slot pos % cap as fp16.
+// The rotation angle is formed in fp64 (positions reach 10^4 and more).
+__global__ void attn_prep_kernel(PrepArgs a) {
+  __shared__ float vals[256];
+  __shared__ float red[8];
+  const int b = blockIdx.x, t = threadIdx.x, d = a.d;
+  float v = a.qkv[static_cast<int64_t>(b) * d + t];
+  float ss = v * v;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((t & 31) == 0) red[t >> 5] = ss;
+  __syncthreads();
+  ss = 0.f;
+  for (int i = 0; i < d / 32; ++i) ss += red[i];
+  v *= rsqrtf(ss / static_cast<float>(d) + a.eps);
+  const bool is_v = b >= a.Hq + a.Hkv;
+  if (!is_v) {  // rotate pairs (i, i + d/2)
+    vals[t] = v;
+    __syncthreads();
+    const int h = d / 2, i = t < h ? t : t - h;
+    const double ang = static_cast<double>(a.pos) * pow(a.theta, -2.0 * i / d);
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    const float x0 = vals[i], x1 = vals[i + h];
+    v = t < h ? static_cast<float>(x0 * cs - x1 * sn) : static_cast<float>(x0 * sn + x1 * cs);
+  }
+  const long long slot = a.pos % a.cap;
+  if (b < a.Hq) {
+    a.qn[static_cast<int64_t>(b) * d + t] = v;
+  } else if (!is_v) {
+    a.kc[(static_cast<int64_t>(b - a.Hq) * a.cap + slot) * d + t] = __float2half_rn(v);
+  } else {
+    a.vc[(static_cast<int64_t>(b - a.Hq - a.Hkv) * a.cap + slot) * d + t] = __float2half_rn(v);
+  }
+}
+
+struct SplitArgs {
+  const float* qn;
+  const __half* kc;
+  const __half* vc;
+  int Hq, Hkv, d;
+  long long cap, first, n;  // visible positions [first, first + n)
+  int nsplit;
+  float scale;              // 1 / sqrt(d)
+  float* part;              // [Hq][nsplit][d + 2]: unnormalised o, then max and sum
+};
+
+template <int PER>  // head dims per lane: d = 32 * PER
+__device__ __forceinline__ void load_half(const __half* p, float (&out)[PER]) {
+  if constexpr (PER == 8) {
+    const uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t ww[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[j]));
+      out[2 * j] = f.x;
+      out[2 * j + 1] = f.y;
+    }
+  } else if constexpr (PER == 4) {
+    const uint2 r = __ldg(reinterpret_cast<const uint2*>(p));
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+    out[0] = f0.x; out[1] = f0.y; out[2] = f1.x; out[3] = f1.y;
+  } else {
+    const uint32_t r = __ldg(reinterpret_cast<const uint32_t*>(p));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&r));
+    out[0] = f.x; out[1] = f.y;
+  }
+}
+
+// Block (h, s): the split's positions of query head h (kv head h / (Hq/Hkv)).
+// Warp w takes positions first + lo + w, + 8, ...; lane l holds head dims
+// [l * PER, (l + 1) * PER).  Each warp keeps an online softmax (running max,
+// running sum, rescaled output); the 8 warps are then merged in a fixed order.
+template <int PER>
+__global__ void __launch_bounds__(kSplitWarps * 32) attn_split_kernel(SplitArgs a) {
+  constexpr int D = 32 * PER;
+  __shared__ float wm[kSplitWarps], wl[kSplitWarps];
+  __shared__ float wo[kSplitWarps][D];
+  const int h = blockIdx.x, s = blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int g = h / (a.Hq / a.Hkv);
+  const long long lo = a.first + a.n * s / a.nsplit, hi = a.first + a.n * (s + 1) / a.nsplit;
+  float q[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) q[i] = a.qn[static_cast<int64_t>(h) * D + lane * PER + i];
+  float m = -INFINITY, l = 0.f, o[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) o[i] = 0.f;
+  const __half* kbase = a.kc + static_cast<int64_t>(g) * a.cap * D + lane * PER;
+  const __half* vbase = a.vc + static_cast<int64_t>(g) * a.cap * D + lane * PER;
+  for (long long p = lo + w; p < hi; p += kSplitWarps) {
+    const long long slot = p % a.cap;
+    float kf[PER], vf[PER];
+    load_half<PER>(kbase + slot * D, kf);
+    load_half<PER>(vbase + slot * D, vf);
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) dot = fmaf(q[i], kf[i], dot);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    const float sc = dot * a.scale;
+    const float mn = fmaxf(m, sc);
+    const float c = expf(m - mn), e = expf(sc - mn);
+    l = l * c + e;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o[i] = fmaf(o[i], c, e * vf[i]);
+    m = mn;
+  }
+  if (lane == 0) {
+    wm[w] = m;
+    wl[w] = l;
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) wo[w][lane * PER + i] = o[i];
+  __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kSplitWarps; ++i) M = fmaxf(M, wm[i]);
+  float* out = a.part + (static_cast<int64_t>(h) * a.nsplit + s) * (D + 2);
+  for (int i = t; i < D; i += kSplitWarps * 32) {
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < kSplitWarps; ++j)
+      if (wl[j] > 0.f) acc = fmaf(wo[j][i], expf(wm[j] - M), acc);
+    out[i] = acc;
+  }
+  if (t == 0) {
+    float L = 0.f;
+#pragma unroll
+    for (int j = 0; j < kSplitWarps; ++j)
+      if (wl[j] > 0.f) L = fmaf(wl[j], expf(wm[j] - M), L);
+    out[D] = M;
+    out[D + 1] = L;
+  }
+}
+
+// One block per query head (blockDim = d): the splits' partials rescaled to
+// the largest maximum and added in split order; o = sum / normaliser.
+__global__ void attn_combine_kernel(const float* part, int nsplit, int d, float* o) {
+  const int h = blockIdx.x, t = threadIdx.x;
+  const float* p = part + static_cast<int64_t>(h) * nsplit * (d + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p[s * (d + 2) + d]);
+  float L = 0.f, acc = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float f = expf(p[s * (d + 2) + d] - M);
+    L = fmaf(p[s * (d + 2) + d + 1], f, L);
+    acc = fmaf(p[s * (d + 2) + t], f, acc);
+  }
+  o[static_cast<int64_t>(h) * d + t] = acc / L;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+struct moe_attn {
+  moe_attn_config cfg{};
+  std::vector<int> sliding;
+  std::vector<double> theta;
+  std::vector<int64_t> cap, kv_off, next_pos;
+  int device = 0;
+  int64_t rbD = 0, rbQ = 0, wqkv_bytes = 0, layer_bytes = 0;
+  uint8_t* w = nullptr;   // per layer: q/k/v qrows, then the output projection's qrows
+  __half* kv = nullptr;   // per layer: keys [Hkv][cap][d], then values
+  float* qkv = nullptr;   // [(Hq + 2 Hkv) d]
+  float* qn = nullptr;    // [Hq d]
+  float* part = nullptr;  // [Hq][kMaxSplits][d + 2]
+  float* o = nullptr;     // [Hq d]
+  uint16_t* xa = nullptr; // decode-step temporaries, bf16 [2][D]
+  std::string err;
+};
+
+namespace {
+
+thread_local std::string g_attn_create_error;
+
+moe_status afail(moe_attn* a, moe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (a)
+    a->err = buf;
+  else
+    g_attn_create_error = buf;
+  return s;
+}
+
+void attn_free(moe_attn* a) {
+  if (!a) return;
+  if (a->w || a->kv) cudaDeviceSynchronize();
+  cudaFree(a->w);
+  cudaFree(a->kv);
+  cudaFree(a->qkv);
+  cudaFree(a->qn);
+  cudaFree(a->part);
+  cudaFree(a->o);
+  cudaFree(a->xa);
+}
+
+bool qt_ok(const moe_qtensor& t) { return t.q && t.scale && t.bias; }
+
+int launch_gemv(const GemvArgs& g, cudaStream_t s) {
+  const int grid = (g.R + kGemvRows - 1) / kGemvRows;
+  qgemv_kernel<<<grid, kGemvWarps * 32, 0, s>>>(g);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+#pragma GCC visibility push(default)
+extern "C" {
+
+moe_status moe_attn_create(const moe_attn_config* cfg, const moe_attn_weights* layers, moe_attn** out) {
+  if (!out) return afail(nullptr, MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg || !layers) return afail(nullptr, MOE_ERR_INVALID_ARG, "cfg or layers is NULL");
+  const moe_attn_config& c = *cfg;
+  const int d = c.head_dim;
+  if (c.group != kGroup || c.d_model <= 0 || c.d_model % 256 || c.d_model > kGemvMaxK ||
+      c.n_heads < 1 || c.n_kv_heads < 1 || c.n_heads % c.n_kv_heads || (d != 64 && d != 128 && d != 256) ||
+      c.n_heads * d > kGemvMaxK || (c.n_heads * d) % 256 || c.n_layers < 1 || c.window < 1 ||
+      c.max_seq < 1)
+    return afail(nullptr, MOE_ERR_INVALID_ARG, "unsupported attention configuration");
+  for (int l = 0; l < c.n_layers; ++l) {
+    const moe_attn_weights& w = layers[l];
+    if (!qt_ok(w.wq) || !qt_ok(w.wk) || !qt_ok(w.wv) || !qt_ok(w.wo))
+      return afail(nullptr, MOE_ERR_INVALID_ARG, "layer %d: missing attention weights", l);
+    if (c.rope_theta && !(c.rope_theta[l] > 0.f))
+      return afail(nullptr, MOE_ERR_INVALID_ARG, "layer %d: rope_theta must be positive", l);
+  }
+  std::unique_ptr<moe_attn> a(new moe_attn());
+  a->cfg = c;
+  a->cfg.sliding = nullptr;
+  a->cfg.rope_theta = nullptr;
+  const int L = c.n_layers, D = c.d_model, Hq = c.n_heads, Hkv = c.n_kv_heads;
+  a->sliding.resize(L);
+  a->theta.resize(L);
+  a->cap.resize(L);
+  a->kv_off.resize(L);
+  a->next_pos.assign(L, 0);
+  int64_t kv_total = 0;
+  for (int l = 0; l < L; ++l) {
+    a->sliding[l] = c.sliding ? (c.sliding[l] != 0) : 0;
+    a->theta[l] = c.rope_theta ? c.rope_theta[l] : 10000.0;
+    a->cap[l] = a->sliding[l] ? c.window : c.max_seq;
+    a->kv_off[l] = kv_total;
+    kv_total += 2 * int64_t(Hkv) * a->cap[l] * d;
+  }
+  a->rbD = qrow_bytes(D);
+  a->rbQ = qrow_bytes(int64_t(Hq) * d);
+  const int64_t R = int64_t(Hq + 2 * Hkv) * d;
+  a->wqkv_bytes = R * a->rbD;
+  a->layer_bytes = (a->wqkv_bytes + int64_t(D) * a->rbQ + 255) / 256 * 256;
+#define ATRY(call)                                                                        \
+  do {                                                                                    \
+    const cudaError_t e_ = (call);                                                        \
+    if (e_ != cudaSuccess) {                                                              \
+      const moe_status st_ = afail(nullptr, e_ == cudaErrorMemoryAllocation ? MOE_ERR_OOM \
+                                                                              : MOE_ERR_CUDA, \
+                                   "%s: %s", #call, cudaGetErrorString(e_));              \
+      attn_free(a.get());                                                                 \
+      return st_;                                                                         \
+    }                                                                                     \
+  } while (0)
+  ATRY(cudaGetDevice(&a->device));
+  ATRY(cudaMalloc(&a->w, a->layer_bytes * L));
+  ATRY(cudaMalloc(&a->kv, kv_total * sizeof(__half)));
+  ATRY(cudaMemset(a->kv, 0, kv_total * sizeof(__half)));
+  ATRY(cudaMalloc(&a->qkv, R * sizeof(float)));
+  ATRY(cudaMalloc(&a->qn, int64_t(Hq) * d * sizeof(float)));
+  ATRY(cudaMalloc(&a->part, int64_t(Hq) * kMaxSplits * (d + 2) * sizeof(float)));
+  ATRY(cudaMalloc(&a->o, int64_t(Hq) * d * sizeof(float)));
+  ATRY(cudaMalloc(&a->xa, 2 * int64_t(D) * sizeof(uint16_t)));
+  {
+    std::vector<uint8_t> stage(static_cast<size_t>(a->layer_bytes));
+    for (int l = 0; l < L; ++l) {
+      const moe_attn_weights& w = layers[l];
+      std::fill(stage.begin(), stage.end(), 0);
+      repack_matrix(w.wq, int64_t(Hq) * d, D, stage.data());
+      repack_matrix(w.wk, int64_t(Hkv) * d, D, stage.data() + int64_t(Hq) * d * a->rbD);
+      repack_matrix(w.wv, int64_t(Hkv) * d, D, stage.data() + int64_t(Hq + Hkv) * d * a->rbD);
+      repack_matrix(w.wo, D, int64_t(Hq) * d, stage.data() + a->wqkv_bytes);
+      ATRY(cudaMemcpy(a->w + l * a->layer_bytes, stage.data(), stage.size(), cudaMemcpyHostToDevice));
+    }
+  }
+#undef ATRY
+  *out = a.release();
+  return MOE_OK;
+}
+
+void moe_attn_destroy(moe_attn* a) {
+  if (!a) return;
+  attn_free(a);
+  delete a;
+}
+
+const char* moe_attn_last_error(const moe_attn* a) {
+  return a ? a->err.c_str() : g_attn_create_error.c_str();
+}
+
+moe_status moe_attn_reset(moe_attn* a) {
+  if (!a) return MOE_ERR_INVALID_ARG;
+  std::fill(a->next_pos.begin(), a->next_pos.end(), 0);
+  return MOE_OK;
+}
+
+moe_status moe_attn_forward(moe_attn* a, int layer, const void* x, long long pos, void* y, int flags,
+                            void* stream) {
+  if (!a || !x || !y || x == y) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15)
+    return afail(a, MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+  if (layer < 0 || layer >= a->cfg.n_layers) return afail(a, MOE_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (pos != 0 && pos != a->next_pos[layer])
+    return afail(a, MOE_ERR_STATE, "layer %d expects position %lld (or 0 to restart), got %lld",
+                 layer, static_cast<long long>(a->next_pos[layer]), pos);
+  if (pos < 0 || (!a->sliding[layer] && pos >= a->cfg.max_seq))
+    return afail(a, MOE_ERR_INVALID_ARG, "position %lld beyond max_seq of a full-attention layer", pos);
+  const int D = a->cfg.d_model, Hq = a->cfg.n_heads, Hkv = a->cfg.n_kv_heads, d = a->cfg.head_dim;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* wl = a->w + layer * a->layer_bytes;
+  __half* kc = a->kv + a->kv_off[layer];
+  __half* vc = kc + int64_t(Hkv) * a->cap[layer] * d;
+  // q, k, v projections of the pre-normed input
+  GemvArgs g{};
+  g.w = wl;
+  g.R = (Hq + 2 * Hkv) * d;
+  g.K = D;
+  g.rb = static_cast<int>(a->rbD);
+  g.x_bf16 = static_cast<const uint16_t*>(x);
+  g.prenorm = 1;
+  g.eps = 1e-6f;
+  g.y_f32 = a->qkv;
+  int e = launch_gemv(g, s);
+  // norms, rotation, KV append
+  PrepArgs pa{};
+  pa.qkv = a->qkv;
+  pa.Hq = Hq;
+  pa.Hkv = Hkv;
+  pa.d = d;
+  pa.eps = 1e-6f;
+  pa.pos = pos;
+  pa.cap = a->cap[layer];
+  pa.theta = a->theta[layer];
+  pa.qn = a->qn;
+  pa.kc = kc;
+  pa.vc = vc;
+  if (!e) {
+    attn_prep_kernel<<<Hq + 2 * Hkv, d, 0, s>>>(pa);
+    e = static_cast<int>(cudaGetLastError());
+  }
+  // split-K/V attention over the visible positions, then the merge
+  const long long n = a->sliding[layer] ? (pos + 1 < a->cfg.window ? pos + 1 : a->cfg.window) : pos + 1;
+  SplitArgs sa{};
+  sa.qn = a->qn;
+  sa.kc = kc;
+  sa.vc = vc;
+  sa.Hq = Hq;
+  sa.Hkv = Hkv;
+  sa.d = d;
+  sa.cap = a->cap[layer];
+  sa.first = pos + 1 - n;
+  sa.n = n;
+  sa.nsplit = static_cast<int>(std::min<long long>(kMaxSplits, (n + 63) / 64));
+  sa.scale = 1.f / std::sqrt(static_cast<float>(d));
+  sa.part = a->part;
+  if (!e) {
+    const dim3 grid(Hq, sa.nsplit);
+    if (d == 256) attn_split_kernel<8><<<grid, kSplitWarps * 32, 0, s>>>(sa);
+    else if (d == 128) attn_split_kernel<4><<<grid, kSplitWarps * 32, 0, s>>>(sa);
+    else attn_split_kernel<2><<<grid, kSplitWarps * 32, 0, s>>>(sa);
+    e = static_cast<int>(cudaGetLastError());
+  }
+  if (!e) {
+    attn_combine_kernel<<<Hq, d, 0, s>>>(a->part, sa.nsplit, d, a->o);
+    e = static_cast<int>(cudaGetLastError());
+  }
+  // output projection (+ residual), bf16
+  GemvArgs go{};
+  go.w = wl + a->wqkv_bytes;
+  go.R = D;
+  go.K = Hq * d;
+  go.rb = static_cast<int>(a->rbQ);
+  go.x_f32 = a->o;
+  go.prenorm = 0;
+  go.y_bf16 = static_cast<uint16_t*>(y);
+  go.res = (flags & MOE_FWD_RESIDUAL) ? static_cast<const uint16_t*>(x) : nullptr;
+  if (!e) e = launch_gemv(go, s);
+  if (e) return afail(a, MOE_ERR_CUDA, "attention launch: %s", cudaGetErrorString(cudaError_t(e)));
+  a->next_pos[layer] = pos + 1;
+  return MOE_OK;
+}
+
+moe_status moe_decode_step(moe_attn* a, moe_handle* h, const void* x, long long pos, void* y,
+                           int n_layers, void* stream) {
+  if (!a || !h || !x || !y || x == y) return MOE_ERR_INVALID_ARG;
+  if (n_layers < 1 || n_layers > a->cfg.n_layers)
+    return afail(a, MOE_ERR_INVALID_ARG, "n_layers out of range for the attention handle");
+  const int D = a->cfg.d_model;
+  const void* cur = x;
+  for (int l = 0; l < n_layers; ++l) {
+    // attention (+ residual) into xa[0]; the MoE layer reads it directly
+    // (the router hand-off) and writes x_{l+1} into xa[1] or y
+    uint16_t* t0 = a->xa;
+    uint16_t* t1 = a->xa + D;
+    moe_status st = moe_attn_forward(a, l, cur, pos, t0, MOE_FWD_RESIDUAL, stream);
+    if (st != MOE_OK) return st;
+    void* dst = l + 1 == n_layers ? y : static_cast<void*>(t1);
+    st = moe_layer_forward(h, l, t0, 1, dst, MOE_FWD_RESIDUAL | MOE_FWD_PRENORM, nullptr, stream,
+                           nullptr);
+    if (st != MOE_OK) return afail(a, st, "MoE layer %d: %s", l, moe_last_error(h));
+    cur = t1;
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"
+#pragma GCC visibility pop

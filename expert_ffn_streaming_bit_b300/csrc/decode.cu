@@ -41,6 +41,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "qdot.cuh"
 
 namespace moe {
 
@@ -107,25 +108,6 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 }
 
 __device__ __forceinline__ void csync() { named_sync(1, kConsumers); }
-
-// Integer dot product of one 32-column chunk: the chunk's 16 code bytes
-// (byte i of word j = column 8j+i in the low nibble, column 8j+4+i in the
-// high nibble) against the int16 activation chunk x (x[j] = columns 8j..8j+7
-// as four int16 pairs).  Exact in int32; two chains per nibble half.
-__device__ __forceinline__ int idot_chunk(const uint4& w, const uint4 (&x)[4]) {
-  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-  int lo_acc[2] = {0, 0}, hi_acc[2] = {0, 0};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t lo = words[j] & 0x0F0F0F0Fu;  // codes of columns 8j+0..3
-    const uint32_t hi = words[j] & 0xF0F0F0F0u;  // 16 x codes of columns 8j+4..7
-    lo_acc[j & 1] = dp2a_lo(x[j].x, lo, lo_acc[j & 1]);
-    lo_acc[j & 1] = dp2a_hi(x[j].y, lo, lo_acc[j & 1]);
-    hi_acc[j & 1] = dp2a_lo(x[j].z, hi, hi_acc[j & 1]);
-    hi_acc[j & 1] = dp2a_hi(x[j].w, hi, hi_acc[j & 1]);
-  }
-  return (lo_acc[0] + lo_acc[1]) + ((hi_acc[0] + hi_acc[1]) >> 4);
-}
 
 struct LayerPlan {
   int n_r, n_bs, n_br, n_c;  // stage counts
@@ -379,22 +361,6 @@ __device__ void consumer_max_sum(const Ctx& cx, float& a, float& b) {
     b += rb[i];
   }
   csync();
-}
-
-// Sum of the int16 pairs of a uint4 (8 values, exact).
-__device__ __forceinline__ int sum8_s16(const uint4& q) {
-  int s = dp2a_lo(q.x, 0x01010101u, 0);
-  s = dp2a_lo(q.y, 0x01010101u, s);
-  s = dp2a_lo(q.z, 0x01010101u, s);
-  return dp2a_lo(q.w, 0x01010101u, s);
-}
-
-// int16 quantisation factor for a vector with max |v| = m: X = rint(v * q).
-__device__ __forceinline__ float quant_factor(float m) { return m > 0.f ? 32767.f / m : 0.f; }
-
-__device__ __forceinline__ uint32_t pack_s16x2(float a, float b) {
-  const int ia = __float2int_rn(a), ib = __float2int_rn(b);
-  return (static_cast<uint32_t>(ia) & 0xffffu) | (static_cast<uint32_t>(ib) << 16);
 }
 
 struct VecView {

@@ -38,6 +38,10 @@ static void repack_rows(const moe_qtensor& t, int64_t row0, int64_t nrows, int64
                 dst + (r - row0) * dst_stride);
 }
 
+void repack_matrix(const moe_qtensor& t, int64_t rows, int64_t K, uint8_t* dst) {
+  parallel_for(rows, [&](int64_t r) { repack_rows(t, r, 1, K, dst + r * qrow_bytes(K), qrow_bytes(K)); });
+}
+
 int64_t expert_blob_bytes(const Dims& d) {
   return d.I * 2 * qrow_bytes(d.D) + d.D * qrow_bytes(d.I);
 }

@@ -27,6 +27,8 @@ void repack_layer_fixed(const Dims& d, const moe_layer_weights& w, uint8_t* dst)
 // gate/up interleaved qrows of K=D, then down qrows of K=I
 void repack_expert(const Dims& d, const moe_qtensor& gate, const moe_qtensor& up,
                    const moe_qtensor& down, uint8_t* blob);
+// A whole 4-bit [rows][K] matrix as consecutive qrows of K inputs.
+void repack_matrix(const moe_qtensor& t, int64_t rows, int64_t K, uint8_t* dst);
 void parallel_for(int64_t n, const std::function<void(int64_t)>& fn);
 
 // LFU slot table of one layer (policy stated in moe.h at moe_cache_step).

@@ -405,6 +405,75 @@ moe_status moe_trace_read(moe_handle* h, int64_t* out, int n_layers);
  */
 moe_status moe_prefill_phase_ms(moe_handle* h, float* ms, int* calls);
 
+/* ------------------------------------------------------------------------
+ * Decode attention: the step before the router (shilu.ai
+ * "drumih/turbo-fieldfare", section 推理引擎的工作原理: in every layer the GPU
+ * computes attention and then the router from resident weights; section
+ * 状态和范围: 4-bit MLX affine attention weights, an FP16 KV store that is a
+ * bounded ring for sliding-window layers and linear for full-attention
+ * layers, and exact split-K/V decode attention with distinct normalised K
+ * and V paths).  The pages give no formulas or shapes; the reading used:
+ *   u = x / sqrt(mean(x^2) + 1e-6); q = Wq u, k = Wk u, v = Wv u;
+ *   each head of q, k and v divided by its RMS (eps 1e-6); RoPE on q and k
+ *   (pairs (i, i + d/2) rotated by pos * theta^(-2i/d));
+ *   k, v stored in fp16 in slot pos % capacity; scores q . k / sqrt(d) over
+ *   the visible positions (a sliding layer: the last `window`; a full layer:
+ *   all of 0 .. pos); softmax; o = sum w v; y = Wo o (+ x), bf16.
+ *   Query head h reads key/value head h / (n_heads / n_kv_heads).
+ */
+typedef struct moe_attn moe_attn;
+
+/* Shape of the attention blocks.  Requirements: group == 64; d_model % 256
+ * == 0 and <= 4096; n_heads % n_kv_heads == 0; head_dim in {64, 128, 256};
+ * n_heads * head_dim % 256 == 0 and <= 4096; window >= 1; max_seq >= 1. */
+typedef struct {
+  int d_model, n_heads, n_kv_heads, head_dim, group, n_layers;
+  int window;               /* sliding layers: attended positions (the ring's capacity) */
+  int max_seq;              /* full layers: positions 0 .. max_seq - 1 (linear capacity) */
+  const int32_t* sliding;   /* host [n_layers]: 1 sliding window, 0 full; NULL: all full */
+  const float* rope_theta;  /* host [n_layers] RoPE base; NULL: 10000 for every layer */
+} moe_attn_config;
+
+/* Weights of one attention block, HOST memory, canonical 4-bit form:
+ *   wq [n_heads * head_dim][d_model], wk and wv [n_kv_heads * head_dim][d_model],
+ *   wo [d_model][n_heads * head_dim]. */
+typedef struct {
+  moe_qtensor wq, wk, wv, wo;
+} moe_attn_weights;
+
+/* moe_attn_create — repack the weights into HBM and allocate the FP16 KV
+ * caches (per layer n_kv_heads x capacity x head_dim for keys and for values)
+ * on the current device.  The caller may free `layers` afterwards.  On
+ * failure *out is NULL (message: moe_attn_last_error(NULL)). */
+moe_status moe_attn_create(const moe_attn_config* cfg, const moe_attn_weights* layers,
+                           moe_attn** out);
+void moe_attn_destroy(moe_attn* a); /* NULL-safe; synchronises the device */
+const char* moe_attn_last_error(const moe_attn* a);
+
+/* moe_attn_forward — one token's attention step of layer `layer`.
+ * x: device bf16 [d_model] (the layer input), y: device bf16 [d_model],
+ * y may not alias x; both 16-byte aligned.  pos: the token's position; a
+ * layer takes positions 0, 1, 2, ... in order (pos 0 restarts it, anything
+ * else out of order is MOE_ERR_STATE); a full layer refuses pos >= max_seq.
+ * The token's key and value are appended to the layer's cache, then
+ * y = bf16(attention(x)), or bf16(x + attention(x)) with MOE_FWD_RESIDUAL.
+ * Five kernels on `stream`; nothing synchronises. */
+moe_status moe_attn_forward(moe_attn* a, int layer, const void* x, long long pos, void* y,
+                            int flags, void* stream);
+
+/* moe_attn_reset — forget every layer's positions (the next call of each
+ * layer must use pos 0). */
+moe_status moe_attn_reset(moe_attn* a);
+
+/* moe_decode_step — one decode token through n_layers full layer steps: for
+ * each layer l, x = bf16(x + attention_l(x)) (moe_attn_forward with the
+ * residual), then that bf16 x goes straight to layer l's router and experts
+ * (moe_layer_forward with MOE_FWD_PRENORM | MOE_FWD_RESIDUAL): the router
+ * hand-off stays on the device.  x, y: device bf16 [d_model], y may not
+ * alias x.  `h` must have the same d_model and at least n_layers layers. */
+moe_status moe_decode_step(moe_attn* a, moe_handle* h, const void* x, long long pos, void* y,
+                           int n_layers, void* stream);
+
 const char* moe_status_string(moe_status s);
 /* Last error text of this handle ("" if none); with h == NULL, of the last
  * failed moe_create in this process. */
