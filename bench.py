@@ -261,11 +261,16 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(shape, layers, L, args.cpu_budget)
     del layers
+    if rank == 0 and not args.no_sub_records:
+        # the full decode layer step on the same MoE handle: attention at a
+        # 4096-token context, then the router and experts, for every layer
+        layer_step = compact(measure_layer_step(args, h, L, context=4096, steps=50, warmup=5))
     moe.moe_destroy(h)
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_sub_records:
         # the other workloads, timed in the same run on fewer steps
         line["sub_records"] = {
+            "decode_layer_step_ctx4096": layer_step,
             "prefill_4096": compact(measure_prefill(args, steps=3, warmup=3)),
             "chunked_128": compact(measure_chunked(args, steps=2, warmup=3)),
             "streaming_pinned_4l": compact(measure_streaming(args, 32, 3, 4, None, False)),
@@ -276,6 +281,89 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_layer_step(args, h, L, context, steps, warmup):
+    """Full decode layer steps: for each of the L layers, decode attention
+    (the Gemma-shape reading: 16 query heads over 8 kv heads of 256; every
+    sixth layer full attention, the others a 1024-token window) at a context
+    of `context` earlier tokens, then the router and the experts of the MoE
+    handle h on the attention output (moe_decode_step).  The KV caches are
+    filled first by attention steps over seeded tokens."""
+    import torch
+    import synth
+    import expert_ffn_streaming_bit_b300 as moe
+    ash = synth.GEMMA_ATTN
+    alayers = []
+    for l in range(L):
+        A = synth.make_attn_layer(ash, "decode", l, device="cuda")
+        alayers.append({k: v.to("cpu") for k, v in A.items()})
+        del A
+    torch.cuda.empty_cache()
+    a = moe.moe_attn_create(ash, alayers)
+    del alayers
+    n = context + warmup + steps
+    xs = synth.make_tokens(synth.GEMMA, "decode", 256, index=5000).cuda()
+    y = torch.empty_like(xs[0:1])
+    for p in range(context):                      # fill the caches
+        for l in range(L):
+            moe.moe_attn_forward(a, l, xs[p % 256:p % 256 + 1], p, y)
+    torch.cuda.synchronize()
+    for p in range(context, context + warmup):
+        moe.moe_decode_step(a, h, xs[p % 256:p % 256 + 1], p, y, L)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for p in range(context + warmup, n):
+        moe.moe_decode_step(a, h, xs[p % 256:p % 256 + 1], p, y, L)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / steps
+    hbm, bf16, src = peaks()
+    kv_pos = sum(min(context + warmup + steps // 2, ash.window) if ash.sliding[l]
+                 else context + warmup + steps // 2 for l in range(L))
+    kv_bytes = kv_pos * ash.n_kv_heads * ash.head_dim * 2 * 2
+    moe_bytes = L * synth.GEMMA.decode_layer_bytes()
+    attn_bytes = L * ash.attn_weight_bytes()
+    total = moe_bytes + attn_bytes + kv_bytes
+    gbs = total / (ms / 1e3) / 1e9
+    line = {
+        "value": 1e3 / ms, "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "warmup": warmup,
+        "config": {"workload": "decode layer step: %d layers of attention (16 x 256 query heads, "
+                               "8 kv heads, 1024-token window on 5 of 6 layers, full on every "
+                               "sixth) at a %d-token context, then the MoE layer (128 experts, "
+                               "top-8, shared 2112), T=1" % (L, context),
+                   "layers": L, "context": context, "tokens_per_step": 1},
+        "bytes_per_token": {"moe_weights": moe_bytes, "attention_weights": attn_bytes,
+                            "kv_cache": kv_bytes},
+        "roofline": {"bound": "hbm", "kernel": "whole layer step (attention + MoE)",
+                     "achieved": gbs, "peak": hbm, "peak_source": src, "unit": "GB/s",
+                     "frac": gbs / hbm, "traffic": None},
+        "gpu_launches": 6 * L * steps,
+        "clocks": clk,
+        "dtype": "u4 x s16 -> s32 (dp2a) projections and experts; f16 KV, f32 softmax",
+    }
+    moe.moe_attn_destroy(a)
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_layer_step(args):
+    import synth
+    import expert_ffn_streaming_bit_b300 as moe
+    import torch
+    torch.cuda.set_device(0)
+    L = args.layers or 30
+    layers = make_layers(synth.GEMMA, "decode", L, "cuda")
+    h = moe.moe_create(synth.GEMMA, layers, max_tokens=1)
+    del layers
+    print(json.dumps(measure_layer_step(args, h, L, args.context, args.steps, args.warmup)),
+          flush=True)
 
 
 def gemm_flops_per_layer(shape, T):
@@ -289,7 +377,7 @@ def compact(line: dict) -> dict:
     """A workload's line without the keys the headline line already carries."""
     keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline",
             "whole_layer", "phase_ms_per_layer", "phase_ms_per_chunk_layer",
-            "touched_weight_bytes_per_step", "hit_rate", "misses_per_layer_step",
+            "touched_weight_bytes_per_step", "bytes_per_token", "hit_rate", "misses_per_layer_step",
             "h2d_gbs", "h2d_link_gbs", "store", "e2e", "clocks", "dtype")
     return {k: line[k] for k in keep if k in line}
 
@@ -797,10 +885,12 @@ def main():
                     help="print the decode kernel's per-phase device trace instead of timing")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "chunked_prefill", "streaming_decode",
-                             "batched_decode"],
+                             "batched_decode", "layer_step"],
                     help="decode (default, the headline line), a prefill workload, "
                          "streaming decode with the expert-slot cache, or batched decode")
     ap.add_argument("--batch", type=int, default=32, help="tokens per step of batched_decode")
+    ap.add_argument("--context", type=int, default=4096,
+                    help="layer_step: earlier tokens in the KV caches")
     ap.add_argument("--store", default=None,
                     help="streaming_decode: directory for an expert store file to stream from "
                          "(default: the pinned host pool)")
@@ -809,7 +899,8 @@ def main():
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {"decode": 5000, "prefill": 3, "chunked_prefill": 2,
-                      "streaming_decode": 256, "batched_decode": 200}[args.workload]
+                      "streaming_decode": 256, "batched_decode": 200,
+                      "layer_step": 100}[args.workload]
         if args.impl == "reference":
             args.steps = 20
     if args.warmup < 3:
@@ -829,6 +920,8 @@ def main():
         run_streaming(args)
     elif args.workload == "batched_decode":
         run_batched(args)
+    elif args.workload == "layer_step":
+        run_layer_step(args)
     else:
         run_ours(args)
 

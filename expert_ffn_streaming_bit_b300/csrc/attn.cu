@@ -17,10 +17,10 @@
 // Launches per layer and token:
 //   qgemv_kernel        q, k, v = W u (4-bit integer dot products; the
 //                       pre-norm is a scale applied after the dot product)
-//   attn_prep_kernel    per-head RMS norms, RoPE, the fp16 KV append
-//   attn_split_kernel   (head, split) blocks: scores and an online softmax
-//                       over the split's positions -> (o, max, sum) partials
-//   attn_combine_kernel per head: the partials rescaled to one maximum
+//   attn_decode_kernel  (head, split) blocks: per-head RMS norms and RoPE, the
+//                       fp16 KV append, scores and an online softmax over the
+//                       split's positions; the head's last block merges the
+//                       splits
 //   qgemv_kernel        y = Wo o (+ x), bf16
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -43,7 +43,6 @@ namespace moe {
 namespace {
 
 constexpr int kGemvWarps = 8;
-constexpr int kGemvRows = 2 * kGemvWarps;  // rows per block (two per warp)
 constexpr int kGemvMaxK = 4096;            // input length <= 4096
 constexpr int kGemvXC = kGemvMaxK / 1024;  // activation chunks per lane
 constexpr int kMaxSplits = 64;
@@ -74,15 +73,35 @@ struct GemvArgs {
 
 // y = W x for a 4-bit matrix in qrows.  Every block quantises the whole
 // input to int16 chunks in shared memory (one scale: max|x|), then each warp
-// takes two rows: each lane loads its 32-column chunks of both rows (codes
+// takes RPW rows: each lane loads its 32-column chunks of its rows (codes
 // and scale/bias words, coalesced across the warp) and accumulates
 // s * sum(q X) + b * sum(X) per chunk; a fixed-order warp sum finishes the row.
+// The weight loads are issued before the input is prepared, so their
+// latency overlaps the block's input reduction.
+template <int RPW>  // rows per warp
 __global__ void __launch_bounds__(kGemvWarps * 32) qgemv_kernel(GemvArgs a) {
   __shared__ __align__(16) uint8_t xs[(kGemvMaxK / 32) * 80];
   __shared__ float xsum[kGemvMaxK / 32];
   __shared__ float red[2][kGemvWarps];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int nc = a.K / 32, nv = a.K / 8;
+  // ---- RPW rows per warp: their code and scale/bias words are requested
+  // first, so that they are in flight while the input is prepared
+  const int r0 = (blockIdx.x * kGemvWarps + w) * RPW;
+  uint4 wv[RPW][kGemvXC];
+  uint32_t sbv[RPW][kGemvXC];
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const bool row_ok = r0 + k < a.R;
+    const uint8_t* row = a.w + static_cast<int64_t>(row_ok ? r0 + k : 0) * a.rb;
+#pragma unroll
+    for (int i = 0; i < kGemvXC; ++i) {
+      const int c = lane + 32 * i;
+      const bool ok = row_ok && c < nc;
+      wv[k][i] = ok ? __ldg(reinterpret_cast<const uint4*>(row + c * 16)) : make_uint4(0, 0, 0, 0);
+      sbv[k][i] = ok ? __ldg(reinterpret_cast<const uint32_t*>(row + a.K / 2 + (c >> 1) * 4)) : 0u;
+    }
+  }
   // ---- the input, 8 values per thread and group of 256 threads
   float v[2][8];
   float m = 0.f, ss = 0.f;
@@ -149,23 +168,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32) qgemv_kernel(GemvArgs a) {
     if (idx < nv && (idx & 3) == 0) xsum[idx >> 2] = static_cast<float>(cs);
   }
   __syncthreads();
-  // ---- two rows per warp
-  const int r0 = blockIdx.x * kGemvRows + 2 * w;
-  uint4 wv[2][kGemvXC];
-  uint32_t sbv[2][kGemvXC];
+  float acc[RPW];
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const bool row_ok = r0 + k < a.R;
-    const uint8_t* row = a.w + static_cast<int64_t>(row_ok ? r0 + k : 0) * a.rb;
-#pragma unroll
-    for (int i = 0; i < kGemvXC; ++i) {
-      const int c = lane + 32 * i;
-      const bool ok = row_ok && c < nc;
-      wv[k][i] = ok ? __ldg(reinterpret_cast<const uint4*>(row + c * 16)) : make_uint4(0, 0, 0, 0);
-      sbv[k][i] = ok ? __ldg(reinterpret_cast<const uint32_t*>(row + a.K / 2 + (c >> 1) * 4)) : 0u;
-    }
-  }
-  float acc[2] = {0.f, 0.f};
+  for (int k = 0; k < RPW; ++k) acc[k] = 0.f;
 #pragma unroll
   for (int i = 0; i < kGemvXC; ++i) {
     const int c = lane + 32 * i;
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) qgemv_kernel(GemvArgs a) {
       for (int j = 0; j < 4; ++j) xc[j] = src[j];
       const float sx = xsum[c];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int k = 0; k < RPW; ++k) {
         const int tot = idot_chunk(wv[k][i], xc);
         const __half2 sb = *reinterpret_cast<const __half2*>(&sbv[k][i]);
         acc[k] += fmaf(__low2float(sb), static_cast<float>(tot), __high2float(sb) * sx);
@@ -184,12 +189,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32) qgemv_kernel(GemvArgs a) {
     }
   }
 #pragma unroll
-  for (int k = 0; k < 2; ++k)
+  for (int k = 0; k < RPW; ++k)
 #pragma unroll
     for (int o = 16; o; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
   if (lane == 0) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < RPW; ++k) {
       const int row = r0 + k;
       if (row >= a.R) continue;
       const float out = acc[k] * vs;
@@ -199,69 +204,26 @@ __global__ void __launch_bounds__(kGemvWarps * 32) qgemv_kernel(GemvArgs a) {
   }
 }
 
-struct PrepArgs {
-  const float* qkv;  // raw projections: Hq query heads, then Hkv key heads, then Hkv value heads
+struct AttnArgs {
+  const float* qkv;         // raw projections: Hq query heads, Hkv key heads, Hkv value heads
   int Hq, Hkv, d;
   float eps;
-  long long pos, cap;
-  double theta;
-  float* qn;         // [Hq][d] normalised, rotated queries
-  __half* kc;        // this layer's key cache [Hkv][cap][d]
-  __half* vc;        // this layer's value cache [Hkv][cap][d]
-};
-
-// One block per head (blockDim = d): RMS norm; RoPE for query and key heads;
-// the key and value of this position go to cache slot pos % cap as fp16.
-// The rotation angle is formed in fp64 (positions reach 10^4 and more).
-__global__ void attn_prep_kernel(PrepArgs a) {
-  __shared__ float vals[256];
-  __shared__ float red[8];
-  const int b = blockIdx.x, t = threadIdx.x, d = a.d;
-  float v = a.qkv[static_cast<int64_t>(b) * d + t];
-  float ss = v * v;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((t & 31) == 0) red[t >> 5] = ss;
-  __syncthreads();
-  ss = 0.f;
-  for (int i = 0; i < d / 32; ++i) ss += red[i];
-  v *= rsqrtf(ss / static_cast<float>(d) + a.eps);
-  const bool is_v = b >= a.Hq + a.Hkv;
-  if (!is_v) {  // rotate pairs (i, i + d/2)
-    vals[t] = v;
-    __syncthreads();
-    const int h = d / 2, i = t < h ? t : t - h;
-    const double ang = static_cast<double>(a.pos) * pow(a.theta, -2.0 * i / d);
-    double sn, cs;
-    sincos(ang, &sn, &cs);
-    const float x0 = vals[i], x1 = vals[i + h];
-    v = t < h ? static_cast<float>(x0 * cs - x1 * sn) : static_cast<float>(x0 * sn + x1 * cs);
-  }
-  const long long slot = a.pos % a.cap;
-  if (b < a.Hq) {
-    a.qn[static_cast<int64_t>(b) * d + t] = v;
-  } else if (!is_v) {
-    a.kc[(static_cast<int64_t>(b - a.Hq) * a.cap + slot) * d + t] = __float2half_rn(v);
-  } else {
-    a.vc[(static_cast<int64_t>(b - a.Hq - a.Hkv) * a.cap + slot) * d + t] = __float2half_rn(v);
-  }
-}
-
-struct SplitArgs {
-  const float* qn;
-  const __half* kc;
-  const __half* vc;
-  int Hq, Hkv, d;
-  long long cap, first, n;  // visible positions [first, first + n)
+  long long pos, cap;       // this token's position; the layer cache's capacity
+  long long first, n;       // visible positions [first, first + n), the last one is pos
   int nsplit;
   float scale;              // 1 / sqrt(d)
+  const double* freq_pi;    // [d/2] theta^(-2i/d) / pi of this layer
+  __half* kc;               // this layer's key cache [Hkv][cap][d]
+  __half* vc;               // this layer's value cache [Hkv][cap][d]
   float* part;              // [Hq][nsplit][d + 2]: unnormalised o, then max and sum
+  unsigned int* done;       // [Hq] arrival counters (zero between calls)
+  float* o;                 // [Hq][d] attention output
 };
 
 template <int PER>  // head dims per lane: d = 32 * PER
 __device__ __forceinline__ void load_half(const __half* p, float (&out)[PER]) {
   if constexpr (PER == 8) {
-    const uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
     const uint32_t ww[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -270,47 +232,111 @@ __device__ __forceinline__ void load_half(const __half* p, float (&out)[PER]) {
       out[2 * j + 1] = f.y;
     }
   } else if constexpr (PER == 4) {
-    const uint2 r = __ldg(reinterpret_cast<const uint2*>(p));
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
     out[0] = f0.x; out[1] = f0.y; out[2] = f1.x; out[3] = f1.y;
   } else {
-    const uint32_t r = __ldg(reinterpret_cast<const uint32_t*>(p));
+    const uint32_t r = *reinterpret_cast<const uint32_t*>(p);
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&r));
     out[0] = f.x; out[1] = f.y;
   }
 }
 
-// Block (h, s): the split's positions of query head h (kv head h / (Hq/Hkv)).
-// Warp w takes positions first + lo + w, + 8, ...; lane l holds head dims
-// [l * PER, (l + 1) * PER).  Each warp keeps an online softmax (running max,
-// running sum, rescaled output); the 8 warps are then merged in a fixed order.
+// One head vector (d values, one per thread t < d; the other threads pass 0)
+// divided by its RMS; `rotate`: RoPE at position pos through shared memory.
+// Every thread of the block calls it (two block barriers).
+__device__ float head_norm_rope(float v, const AttnArgs& a, bool rotate, float* buf, float* red) {
+  const int t = threadIdx.x, d = a.d;
+  float ss = v * v;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((t & 31) == 0) red[t >> 5] = ss;
+  __syncthreads();
+  ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kSplitWarps; ++i) ss += red[i];
+  v *= rsqrtf(ss / static_cast<float>(d) + a.eps);
+  if (!rotate) {
+    __syncthreads();  // red is reused by the next call
+    return v;
+  }
+  if (t < d) buf[t] = v;
+  __syncthreads();
+  if (t < d) {
+    // angle in half turns t = pos * theta^(-2i/d) / pi, formed in fp64 and
+    // reduced exactly to [-1, 1]; sine and cosine of the reduced angle in fp32
+    const int h = d / 2, i = t < h ? t : t - h;
+    const double turns = static_cast<double>(a.pos) * a.freq_pi[i];
+    const float r = static_cast<float>(turns - 2.0 * rint(0.5 * turns));
+    float sn, cs;
+    sincospif(r, &sn, &cs);
+    const float x0 = buf[i], x1 = buf[i + h];
+    v = t < h ? x0 * cs - x1 * sn : x0 * sn + x1 * cs;
+  }
+  __syncthreads();
+  return v;
+}
+
+// Decode attention of one layer for one token, block (h, s) = (query head,
+// split of the visible positions); kv head g = h / (Hq / Hkv).
+//  1. q_h = RoPE(q_raw_h / RMS); the split that holds position pos (the last
+//     one) also forms this token's key RoPE(k_raw_g / RMS) and value
+//     v_raw_g / RMS, rounded to fp16 as the cache stores them, and the first
+//     query head of the group writes them to cache slot pos % cap.
+//  2. Warp w takes the split's earlier positions lo + w, + 8, ... in batches
+//     of 4 (their key and value rows loaded together) with an online
+//     softmax; warp 0 then folds in position pos from shared memory.  The 8
+//     warps merge in a fixed order into the split's (o, max, sum).
+//  3. The last block of head h to finish (an arrival counter) merges the
+//     head's splits in split order: o_h = sum o_s e^(m_s - M) / sum l_s e^(m_s - M),
+//     and clears the counter for the next call.
 template <int PER>
-__global__ void __launch_bounds__(kSplitWarps * 32) attn_split_kernel(SplitArgs a) {
+__global__ void __launch_bounds__(kSplitWarps * 32) attn_decode_kernel(AttnArgs a) {
   constexpr int D = 32 * PER;
+  __shared__ float buf[D], red[kSplitWarps];
+  __shared__ float qs[D];
+  __shared__ __align__(16) __half kcur[D], vcur[D];
   __shared__ float wm[kSplitWarps], wl[kSplitWarps];
   __shared__ float wo[kSplitWarps][D];
+  __shared__ unsigned int last;
   const int h = blockIdx.x, s = blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int g = h / (a.Hq / a.Hkv);
+  const int grp = a.Hq / a.Hkv, g = h / grp;
   const long long lo = a.first + a.n * s / a.nsplit, hi = a.first + a.n * (s + 1) / a.nsplit;
+  const bool has_pos = hi == a.pos + 1;  // the last split
+  // ---- 1. this head's query, and (last split) this token's key and value
+  {
+    const float qv = head_norm_rope(t < D ? a.qkv[static_cast<int64_t>(h) * D + t] : 0.f, a, true,
+                                    buf, red);
+    if (t < D) qs[t] = qv;
+    if (has_pos) {
+      const float kv = head_norm_rope(
+          t < D ? a.qkv[static_cast<int64_t>(a.Hq + g) * D + t] : 0.f, a, true, buf, red);
+      const float vv = head_norm_rope(
+          t < D ? a.qkv[static_cast<int64_t>(a.Hq + a.Hkv + g) * D + t] : 0.f, a, false, buf, red);
+      if (t < D) {
+        kcur[t] = __float2half_rn(kv);
+        vcur[t] = __float2half_rn(vv);
+        if (h % grp == 0) {
+          const int64_t at = (static_cast<int64_t>(g) * a.cap + a.pos % a.cap) * D + t;
+          a.kc[at] = kcur[t];
+          a.vc[at] = vcur[t];
+        }
+      }
+    }
+    __syncthreads();
+  }
   float q[PER];
 #pragma unroll
-  for (int i = 0; i < PER; ++i) q[i] = a.qn[static_cast<int64_t>(h) * D + lane * PER + i];
+  for (int i = 0; i < PER; ++i) q[i] = qs[lane * PER + i];
+  // ---- 2. scores and online softmax
   float m = -INFINITY, l = 0.f, o[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) o[i] = 0.f;
   const __half* kbase = a.kc + static_cast<int64_t>(g) * a.cap * D + lane * PER;
   const __half* vbase = a.vc + static_cast<int64_t>(g) * a.cap * D + lane * PER;
-  for (long long p = lo + w; p < hi; p += kSplitWarps) {
-    const long long slot = p % a.cap;
-    float kf[PER], vf[PER];
-    load_half<PER>(kbase + slot * D, kf);
-    load_half<PER>(vbase + slot * D, vf);
-    float dot = 0.f;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) dot = fmaf(q[i], kf[i], dot);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  const long long hc = has_pos ? hi - 1 : hi;  // positions read from the cache
+  auto fold = [&](float dot, const float (&vf)[PER]) {
     const float sc = dot * a.scale;
     const float mn = fmaxf(m, sc);
     const float c = expf(m - mn), e = expf(sc - mn);
@@ -318,6 +344,44 @@ __global__ void __launch_bounds__(kSplitWarps * 32) attn_split_kernel(SplitArgs 
 #pragma unroll
     for (int i = 0; i < PER; ++i) o[i] = fmaf(o[i], c, e * vf[i]);
     m = mn;
+  };
+  constexpr int kBatch = 4;
+  for (long long p0 = lo + w; p0 < hc; p0 += kSplitWarps * kBatch) {
+    float kf[kBatch][PER], vf[kBatch][PER];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const long long p = p0 + static_cast<long long>(b) * kSplitWarps;
+      const long long slot = (p < hc ? p : lo) % a.cap;
+      load_half<PER>(kbase + slot * D, kf[b]);
+      load_half<PER>(vbase + slot * D, vf[b]);
+    }
+    float dot[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      dot[b] = 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) dot[b] = fmaf(q[i], kf[b][i], dot[b]);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1)
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) dot[b] += __shfl_xor_sync(0xffffffffu, dot[b], off);
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (p0 + static_cast<long long>(b) * kSplitWarps >= hc) break;
+      fold(dot[b], vf[b]);
+    }
+  }
+  if (has_pos && w == 0) {  // this token's own key and value
+    float kf[PER], vf[PER];
+    load_half<PER>(kcur + lane * PER, kf);
+    load_half<PER>(vcur + lane * PER, vf);
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) dot = fmaf(q[i], kf[i], dot);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    fold(dot, vf);
   }
   if (lane == 0) {
     wm[w] = m;
@@ -345,22 +409,43 @@ __global__ void __launch_bounds__(kSplitWarps * 32) attn_split_kernel(SplitArgs 
     out[D] = M;
     out[D + 1] = L;
   }
-}
-
-// One block per query head (blockDim = d): the splits' partials rescaled to
-// the largest maximum and added in split order; o = sum / normaliser.
-__global__ void attn_combine_kernel(const float* part, int nsplit, int d, float* o) {
-  const int h = blockIdx.x, t = threadIdx.x;
-  const float* p = part + static_cast<int64_t>(h) * nsplit * (d + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p[s * (d + 2) + d]);
-  float L = 0.f, acc = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float f = expf(p[s * (d + 2) + d] - M);
-    L = fmaf(p[s * (d + 2) + d + 1], f, L);
-    acc = fmaf(p[s * (d + 2) + t], f, acc);
+  // ---- 3. the head's last block merges its splits
+  __threadfence();
+  __syncthreads();
+  if (t == 0) last = atomicAdd(a.done + h, 1u) == static_cast<unsigned int>(a.nsplit - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const float* ph = a.part + static_cast<int64_t>(h) * a.nsplit * (D + 2);
+  // the splits' (max, sum) into shared memory, then each thread's column of
+  // every split in batches of 8 independent loads, added in split order
+  float* fm = buf;                  // reused: [kMaxSplits] <= D floats
+  float* fl = &wo[0][0];            // reused: [kMaxSplits]
+  if (t < a.nsplit) {
+    fm[t] = __ldcg(ph + t * (D + 2) + D);
+    fl[t] = __ldcg(ph + t * (D + 2) + D + 1);
   }
-  o[static_cast<int64_t>(h) * d + t] = acc / L;
+  __syncthreads();
+  float Mh = -INFINITY;
+  for (int j = 0; j < a.nsplit; ++j) Mh = fmaxf(Mh, fm[j]);
+  if (t < D) {
+    float L = 0.f, acc = 0.f;
+    for (int j0 = 0; j0 < a.nsplit; j0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = j0 + k < a.nsplit ? __ldcg(ph + (j0 + k) * (D + 2) + t) : 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (j0 + k < a.nsplit) {
+          const float f = expf(fm[j0 + k] - Mh);
+          L = fmaf(fl[j0 + k], f, L);
+          acc = fmaf(v[k], f, acc);
+        }
+      }
+    }
+    a.o[static_cast<int64_t>(h) * D + t] = acc / L;
+  }
+  if (t == 0) a.done[h] = 0u;
 }
 
 }  // namespace
@@ -382,6 +467,8 @@ struct moe_attn {
   float* part = nullptr;  // [Hq][kMaxSplits][d + 2]
   float* o = nullptr;     // [Hq d]
   uint16_t* xa = nullptr; // decode-step temporaries, bf16 [2][D]
+  double* freq = nullptr; // [L][d/2] theta_l^(-2i/d) / pi
+  unsigned int* done = nullptr;  // [Hq] arrival counters of the attention kernel
   std::string err;
 };
 
@@ -412,13 +499,20 @@ void attn_free(moe_attn* a) {
   cudaFree(a->part);
   cudaFree(a->o);
   cudaFree(a->xa);
+  cudaFree(a->freq);
+  cudaFree(a->done);
 }
 
 bool qt_ok(const moe_qtensor& t) { return t.q && t.scale && t.bias; }
 
+// Rows per warp: 4 for tall matrices (one wave of blocks with their loads
+// in flight), 2 otherwise (enough blocks to cover the SMs).
 int launch_gemv(const GemvArgs& g, cudaStream_t s) {
-  const int grid = (g.R + kGemvRows - 1) / kGemvRows;
-  qgemv_kernel<<<grid, kGemvWarps * 32, 0, s>>>(g);
+  if (g.R >= 6144) {
+    qgemv_kernel<4><<<(g.R + 4 * kGemvWarps - 1) / (4 * kGemvWarps), kGemvWarps * 32, 0, s>>>(g);
+  } else {
+    qgemv_kernel<2><<<(g.R + 2 * kGemvWarps - 1) / (2 * kGemvWarps), kGemvWarps * 32, 0, s>>>(g);
+  }
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -488,6 +582,16 @@ moe_status moe_attn_create(const moe_attn_config* cfg, const moe_attn_weights* l
   ATRY(cudaMalloc(&a->part, int64_t(Hq) * kMaxSplits * (d + 2) * sizeof(float)));
   ATRY(cudaMalloc(&a->o, int64_t(Hq) * d * sizeof(float)));
   ATRY(cudaMalloc(&a->xa, 2 * int64_t(D) * sizeof(uint16_t)));
+  ATRY(cudaMalloc(&a->done, Hq * sizeof(unsigned int)));
+  ATRY(cudaMemset(a->done, 0, Hq * sizeof(unsigned int)));
+  {
+    std::vector<double> fr(static_cast<size_t>(L) * (d / 2));
+    const double pi = 3.14159265358979323846;
+    for (int l = 0; l < L; ++l)
+      for (int i = 0; i < d / 2; ++i) fr[size_t(l) * (d / 2) + i] = std::pow(a->theta[l], -2.0 * i / d) / pi;
+    ATRY(cudaMalloc(&a->freq, fr.size() * sizeof(double)));
+    ATRY(cudaMemcpy(a->freq, fr.data(), fr.size() * sizeof(double), cudaMemcpyHostToDevice));
+  }
   {
     std::vector<uint8_t> stage(static_cast<size_t>(a->layer_bytes));
     for (int l = 0; l < L; ++l) {
@@ -548,47 +652,31 @@ moe_status moe_attn_forward(moe_attn* a, int layer, const void* x, long long pos
   g.eps = 1e-6f;
   g.y_f32 = a->qkv;
   int e = launch_gemv(g, s);
-  // norms, rotation, KV append
-  PrepArgs pa{};
-  pa.qkv = a->qkv;
-  pa.Hq = Hq;
-  pa.Hkv = Hkv;
-  pa.d = d;
-  pa.eps = 1e-6f;
-  pa.pos = pos;
-  pa.cap = a->cap[layer];
-  pa.theta = a->theta[layer];
-  pa.qn = a->qn;
-  pa.kc = kc;
-  pa.vc = vc;
-  if (!e) {
-    attn_prep_kernel<<<Hq + 2 * Hkv, d, 0, s>>>(pa);
-    e = static_cast<int>(cudaGetLastError());
-  }
-  // split-K/V attention over the visible positions, then the merge
+  // norms, rotation, KV append, split-K/V attention and the merge: one launch
   const long long n = a->sliding[layer] ? (pos + 1 < a->cfg.window ? pos + 1 : a->cfg.window) : pos + 1;
-  SplitArgs sa{};
-  sa.qn = a->qn;
-  sa.kc = kc;
-  sa.vc = vc;
-  sa.Hq = Hq;
-  sa.Hkv = Hkv;
-  sa.d = d;
-  sa.cap = a->cap[layer];
-  sa.first = pos + 1 - n;
-  sa.n = n;
-  sa.nsplit = static_cast<int>(std::min<long long>(kMaxSplits, (n + 63) / 64));
-  sa.scale = 1.f / std::sqrt(static_cast<float>(d));
-  sa.part = a->part;
+  AttnArgs aa{};
+  aa.qkv = a->qkv;
+  aa.Hq = Hq;
+  aa.Hkv = Hkv;
+  aa.d = d;
+  aa.eps = 1e-6f;
+  aa.pos = pos;
+  aa.cap = a->cap[layer];
+  aa.first = pos + 1 - n;
+  aa.n = n;
+  aa.nsplit = static_cast<int>(std::min<long long>(kMaxSplits, (n + 63) / 64));
+  aa.scale = 1.f / std::sqrt(static_cast<float>(d));
+  aa.freq_pi = a->freq + int64_t(layer) * (d / 2);
+  aa.kc = kc;
+  aa.vc = vc;
+  aa.part = a->part;
+  aa.done = a->done;
+  aa.o = a->o;
   if (!e) {
-    const dim3 grid(Hq, sa.nsplit);
-    if (d == 256) attn_split_kernel<8><<<grid, kSplitWarps * 32, 0, s>>>(sa);
-    else if (d == 128) attn_split_kernel<4><<<grid, kSplitWarps * 32, 0, s>>>(sa);
-    else attn_split_kernel<2><<<grid, kSplitWarps * 32, 0, s>>>(sa);
-    e = static_cast<int>(cudaGetLastError());
-  }
-  if (!e) {
-    attn_combine_kernel<<<Hq, d, 0, s>>>(a->part, sa.nsplit, d, a->o);
+    const dim3 grid(Hq, aa.nsplit);
+    if (d == 256) attn_decode_kernel<8><<<grid, kSplitWarps * 32, 0, s>>>(aa);
+    else if (d == 128) attn_decode_kernel<4><<<grid, kSplitWarps * 32, 0, s>>>(aa);
+    else attn_decode_kernel<2><<<grid, kSplitWarps * 32, 0, s>>>(aa);
     e = static_cast<int>(cudaGetLastError());
   }
   // output projection (+ residual), bf16
