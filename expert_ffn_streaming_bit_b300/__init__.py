@@ -36,6 +36,7 @@ MOE_PLAN_ONLY = 1
 MOE_INJECT_NONE, MOE_INJECT_H2D_FAIL, MOE_INJECT_SLOW_COPY, MOE_INJECT_PINNED_ALLOC_FAIL = 0, 1, 2, 3
 MOE_INJECT_DEVICE_STALL = 4
 MOE_INJECT_READ_FAIL = 5
+MOE_INJECT_GEMM_STALL = 6
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "MOE_ERR_CUDA",
           -4: "MOE_ERR_TIMEOUT", -5: "MOE_ERR_INJECTED", -6: "MOE_ERR_STATE",
           -7: "MOE_ERR_DEVICE", -8: "MOE_ERR_IO"}

@@ -33,6 +33,7 @@ struct Inject {
   int slow_copy_ms = 0;
   int stall_ms = 0;     // next decode launch: first grid barrier cannot complete, this wait limit
   int read_fail_in = 0; // fail the first read of the n-th next expert-store batch (1 = next)
+  int gemm_stall_ms = 0;// next grouped-GEMM launch: the MMA role stalls, this wait limit
 };
 
 }  // namespace
@@ -804,6 +805,10 @@ moe_status moe_debug_inject(moe_handle* h, int what, int arg) {
       if (!h || arg < 1) return MOE_ERR_INVALID_ARG;
       h->inj.read_fail_in = arg;
       return MOE_OK;
+    case MOE_INJECT_GEMM_STALL:
+      if (!h || arg < 1 || arg > 2000) return MOE_ERR_INVALID_ARG;
+      h->inj.gemm_stall_ms = arg;
+      return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -1009,7 +1014,14 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   gp.hout[1] = h->pf_hs;
   gp.hld[0] = static_cast<int>(d.I);
   gp.hld[1] = static_cast<int>(d.S);
+  if (h->inj.gemm_stall_ms > 0) {  // injected: a wait that nothing completes, a short limit
+    gp.stall = 1;
+    gp.timeout_ns = uint64_t(h->inj.gemm_stall_ms) * 1000000ull;
+    h->inj.gemm_stall_ms = 0;
+  }
   e = gemm_tc_launch(gp, h->num_sms, s);
+  gp.stall = 0;
+  gp.timeout_ns = h->base.timeout_ns;
   if (e) return fail(h, MOE_ERR_CUDA, "gate/up GEMM launch: %s", cudaGetErrorString(cudaError_t(e)));
   if (ev) CUDA_TRY(h, cudaEventRecord(ev[3], s));
   // down: routed output weighted by the routing weight (bf16), shared (fp32)

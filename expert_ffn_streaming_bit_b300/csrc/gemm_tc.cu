@@ -264,7 +264,9 @@ __device__ void role_mma(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
     const int nkb = K / 64;
     const uint32_t idesc = tc_idesc_f16(128, unit_nmma(un.n));
     const uint32_t acc = tmem + (uc & 1) * kAccSet;  // this unit's accumulator set
-    if (!wait_bar(&bars->acc_empty[uc & 1], ((uc >> 1) & 1) ^ 1, p, bars)) return;
+    // (an injected stall waits for the phase before, which never completes)
+    const uint32_t par = ((uc >> 1) & 1) ^ (p.stall ? 0u : 1u);
+    if (!wait_bar(&bars->acc_empty[uc & 1], par, p, bars)) return;
     tc_fence_after();
     for (int kb = 0; kb < nkb; ++kb, ++ac, ++bc) {
       const int as = ac % kNA, bs = bc % kNB;

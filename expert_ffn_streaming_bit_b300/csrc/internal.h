@@ -202,6 +202,8 @@ struct GemmParams {
   int D;
   uint32_t* status;
   unsigned long long timeout_ns;
+  int stall;               // test injection: the MMA role waits for an accumulator phase
+                           // that never completes (every role then leaves through abort)
 };
 int gemm_tc_smem_bytes();
 int gemm_tc_launch(const GemmParams& p, int grid, void* stream);

@@ -362,6 +362,14 @@ moe_status moe_get_info(const moe_handle* h, moe_info* out);
  *   MOE_INJECT_READ_FAIL: in the `arg`-th next expert-store read batch the
  *     first 1 MiB read fails (as if the device returned an error): that
  *     expert's slot is left empty and moe_cache_step returns MOE_ERR_IO.
+ *   MOE_INJECT_GEMM_STALL: in the next multi-token (prefill) call of h, the
+ *     gate/up grouped GEMM's MMA issuer waits for an accumulator phase that
+ *     never completes, with a device-side wait limit of `arg` ms (1..2000).
+ *     The wait runs out, the status word records it and every role of the
+ *     kernel (loaders, dequantisers, epilogue) leaves through the CTA's abort
+ *     flag after its copies in flight have landed; the tensor memory is
+ *     freed.  The next synchronising call returns MOE_ERR_TIMEOUT and the
+ *     handle stays usable.
  *   MOE_INJECT_NONE: clear everything. */
 #define MOE_INJECT_NONE 0
 #define MOE_INJECT_H2D_FAIL 1
@@ -369,6 +377,7 @@ moe_status moe_get_info(const moe_handle* h, moe_info* out);
 #define MOE_INJECT_PINNED_ALLOC_FAIL 3
 #define MOE_INJECT_DEVICE_STALL 4
 #define MOE_INJECT_READ_FAIL 5
+#define MOE_INJECT_GEMM_STALL 6
 moe_status moe_debug_inject(moe_handle* h, int what, int arg);
 
 /* Host waits on device work poll with this deadline (default 10000 ms) and

@@ -341,3 +341,38 @@ def test_gemma_multi_token_stack_teacher_forced(moe, gemma_decode_layers4):
         st = moe.moe_layer_forward(h, l, xl, yl, flags=moe.MOE_FWD_PRENORM, want_ids=True)
         assert np.array_equal(st["ids"], ids[l])
         check_output(yl.cpu(), ref["y"])
+
+
+def test_prefill_gemm_wait_runs_out_and_the_handle_recovers(moe, gemma_layer):
+    """Failure detection in the tensor-core GEMM without a fault: the injected
+    gate/up launch's MMA issuer waits for an accumulator phase that never
+    completes, its 50 ms device-side limit runs out and every role leaves
+    through the abort flag.  The status check reports MOE_ERR_TIMEOUT; the
+    next multi-token calls on the same handle match the oracle (a tiny layer,
+    then the full-size 4096-token layer on sampled tokens)."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 0)
+    T = 333
+    h = moe.moe_create(sh, [L], max_tokens=T)
+    x = synth.make_tokens(sh, "tiny", T, index=55)
+    moe.moe_debug_inject(h, moe.MOE_INJECT_GEMM_STALL, 50)
+    with pytest.raises(moe.MoEError) as ei:
+        _forward(moe, h, x)
+    assert ei.value.status == -4
+    y, st = _forward(moe, h, x)
+    ref = oracle.moe_layer(oracle.LayerView(sh, L), x)
+    assert check_ids(st["ids"], ref, sh.top_k) <= 1
+    check_output(y, ref["y"])
+    moe.moe_destroy(h)
+
+    gs = synth.GEMMA
+    T = 4096
+    hg = moe.moe_create(gs, [gemma_layer], max_tokens=T)
+    xg = synth.make_tokens(gs, "prefill", T, index=1)
+    moe.moe_debug_inject(hg, moe.MOE_INJECT_GEMM_STALL, 50)
+    with pytest.raises(moe.MoEError) as ei:
+        _forward(moe, hg, xg, flags=moe.MOE_FWD_PRENORM)
+    assert ei.value.status == -4
+    y, st = _forward(moe, hg, xg, flags=moe.MOE_FWD_PRENORM)
+    sample = np.sort(np.random.default_rng(2).choice(T, 32, replace=False))
+    _sample_check(moe, gs, gemma_layer, xg, y, st, sample, prenorm=True)
