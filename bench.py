@@ -109,6 +109,29 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# DRAM traffic (read + write) of one 4-layer decode_kernel launch from the
+# `--set full` capture summarised in profiles/decode_kernel_gemma30.md, and
+# a hash of the kernel's sources when it was taken.  Reported, scaled to the
+# launch's layers by the algorithmic bytes, only while the sources match.
+DECODE_CAPTURE = {"sources_sha16": "d0924444c32ef448", "traffic_bytes": 149356544 + 3791104,
+                  "algo_bytes": 148729856}
+DECODE_SOURCES = ["decode.cu", "qdot.cuh", "ptx.cuh", "internal.h"]
+
+
+def decode_traffic(algo_bytes: int):
+    import hashlib
+    h = hashlib.sha256()
+    try:
+        for f in DECODE_SOURCES:
+            with open(os.path.join(ROOT, "expert_ffn_streaming_bit_b300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    if h.hexdigest()[:16] != DECODE_CAPTURE["sources_sha16"]:
+        return None
+    return DECODE_CAPTURE["traffic_bytes"] * algo_bytes / DECODE_CAPTURE["algo_bytes"]
+
+
 def decode_bytes_per_token(shape) -> int:
     """Algorithmic weight bytes one token reads through all layers (canonical sizes)."""
     return shape.n_layers * shape.decode_layer_bytes()
@@ -251,7 +274,10 @@ def run_ours(args):
         "hbm_frac_of_8tbs": algo * value / world / 1e9 / 8000.0,
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
                      "peak": hbm, "peak_source": src, "unit": "GB/s", "frac": achieved / hbm,
-                     "bytes_per_launch": algo, "avg_launch_ms": launch_ms, "traffic": None},
+                     "bytes_per_launch": algo, "avg_launch_ms": launch_ms,
+                     "traffic": decode_traffic(algo),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of a "
+                                       "4-layer launch, scaled by the algorithmic bytes"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * shape.d_model,
                 "d2h_bytes_per_step": 2 * shape.d_model, "api": "moe_forward_stack_host"},
         "gpu_launches": args.steps,
