@@ -212,7 +212,9 @@ def run_ours(args):
     shape = synth.GEMMA
     L = args.layers or shape.n_layers
     layers = make_layers(shape, "decode", L, "cuda")
-    h = moe.moe_create(shape, layers, max_tokens=1)
+    # room for a 32-token batch (the batched-decode sub-record); single tokens
+    # run the same decode kernel either way
+    h = moe.moe_create(shape, layers, max_tokens=32)
     info = moe.moe_get_info(h)
     P = 64
     xs = synth.make_tokens(shape, "decode", P, index=1000 + rank).cuda()
@@ -291,12 +293,14 @@ def run_ours(args):
         # the full decode layer step on the same MoE handle: attention at a
         # 4096-token context, then the router and experts, for every layer
         layer_step = compact(measure_layer_step(args, h, L, context=4096, steps=50, warmup=5))
+        batched = compact(measure_batched(args, h, L, 32, steps=20, warmup=3))
     moe.moe_destroy(h)
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_sub_records:
         # the other workloads, timed in the same run on fewer steps
         line["sub_records"] = {
             "decode_layer_step_ctx4096": layer_step,
+            "batched_decode_32": batched,
             "prefill_4096": compact(measure_prefill(args, steps=3, warmup=3)),
             "chunked_128": compact(measure_chunked(args, steps=2, warmup=3)),
             "streaming_pinned_4l": compact(measure_streaming(args, 32, 3, 4, None, False)),
@@ -404,7 +408,7 @@ def compact(line: dict) -> dict:
     keep = ("value", "unit", "ms_per_step", "steps", "warmup", "config", "roofline",
             "whole_layer", "phase_ms_per_layer", "phase_ms_per_chunk_layer",
             "touched_weight_bytes_per_step", "bytes_per_token", "hit_rate", "misses_per_layer_step",
-            "h2d_gbs", "h2d_link_gbs", "store", "e2e", "clocks", "dtype")
+            "h2d_gbs", "h2d_link_gbs", "store", "overlap", "path", "e2e", "clocks", "dtype")
     return {k: line[k] for k in keep if k in line}
 
 
@@ -593,7 +597,20 @@ def h2d_link_gbs(device_index: int) -> float:
 
 
 def run_batched(args):
-    """Batched decode: a batch of B tokens (default 32) through the 30-layer
+    import torch
+    import synth
+    import expert_ffn_streaming_bit_b300 as moe
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    L = args.layers or synth.GEMMA.n_layers
+    layers = make_layers(synth.GEMMA, "decode", L, "cuda")
+    h = moe.moe_create(synth.GEMMA, layers, max_tokens=args.batch)
+    del layers
+    print(json.dumps(measure_batched(args, h, L, args.batch, args.steps, args.warmup)), flush=True)
+
+
+def measure_batched(args, h, L, B, steps, warmup):
+    """Batched decode: a batch of B tokens (default 32) through the L-layer
     decode stack per step, on the same weights as the decode workload.  From
     10 tokens on, each layer takes the multi-token path (router GEMM,
     bucketing, grouped tensor-core GEMMs, combine), so each chosen expert's
@@ -603,19 +620,14 @@ def run_batched(args):
     import synth
     import expert_ffn_streaming_bit_b300 as moe
     rank, world, local = dist_env()
-    torch.cuda.set_device(local)
     shape = synth.GEMMA
-    L = args.layers or shape.n_layers
-    B = args.batch
-    layers = make_layers(shape, "decode", L, "cuda")
-    h = moe.moe_create(shape, layers, max_tokens=B)
     x = synth.make_tokens(shape, "decode", B, index=3000 + rank).cuda()
     y = torch.empty_like(x)
 
     def step():
         moe.moe_forward_stack(h, x, y, L)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     # touched expert bytes: distinct experts per layer from the ids
@@ -635,12 +647,12 @@ def run_batched(args):
     time.sleep(0.3)
     torch.cuda.synchronize()
     t0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
+    ms = t0.elapsed_time(t1) / steps
     value = B / (ms / 1e3)
     hbm, bf16, src = peaks()
     gbs = touched / (ms / 1e3) / 1e9
@@ -648,7 +660,7 @@ def run_batched(args):
     per_layer = 8 if B * shape.top_k <= 2048 else 10
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 x f16 -> f32 (tcgen05 kind::f16), 4-bit weights",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 tokens, router-driven ids)",
@@ -665,10 +677,10 @@ def run_batched(args):
         "roofline": {"bound": "hbm", "kernel": "whole step (touched weight bytes)",
                      "achieved": gbs, "peak": hbm, "peak_source": src, "unit": "GB/s",
                      "frac": gbs / hbm, "traffic": None},
-        "gpu_launches": (per_layer * L if multi else B) * args.steps,
+        "gpu_launches": (per_layer * L if multi else B) * steps,
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_streaming(args):
@@ -744,6 +756,25 @@ def measure_streaming(args, steps, warmup, L, store_dir=None, cpu_baseline=True)
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1) / K
+    # compute alone: the same launches with every id resident (the step-0
+    # ids of each layer repeated: all hits after the first step)
+    def step_hits(x):
+        src = x
+        for l in range(L):
+            moe.moe_layer_forward(h, l, src, bufs[l & 1], flags=flags, forced_ids=traces[l][0:1])
+            src = bufs[l & 1]
+
+    moe.moe_cache_reset(h)
+    step_hits(xs_dev[0:1])
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for i in range(K):
+        step_hits(xs_dev[i:i + 1])
+    c1.record(stream)
+    torch.cuda.synchronize()
+    ms_compute = c0.elapsed_time(c1) / K
+    moe.moe_cache_reset(h)
     # end to end: x from pinned host memory, y back to the host, every step
     xs_pin = xs.pin_memory()
     y_host = torch.empty((1, shape.d_model), dtype=torch.bfloat16, pin_memory=True)
@@ -778,7 +809,14 @@ def measure_streaming(args, steps, warmup, L, store_dir=None, cpu_baseline=True)
                      "achieved": h2d / (ms / 1e3) / 1e9, "peak": link,
                      "peak_source": "measured here: pinned 1 GiB cudaMemcpyAsync, best of 10",
                      "unit": "GB/s", "frac": h2d / (ms / 1e3) / 1e9 / link, "traffic": None},
-        "overlap_efficiency": (h2d / (link * 1e9)) / (ms / 1e3),
+        # copies alone (the step's miss bytes at the measured link rate), compute
+        # alone (all hits) and the step: 1 = the fetches are fully hidden under
+        # the compute (or the compute under them), 0 = they run one after the other
+        "overlap": {"fetch_ms": (h2d / (link * 1e9) * 1e3 if not store_path else None),
+                    "compute_ms": ms_compute, "step_ms": ms,
+                    "efficiency": (max(0.0, min(1.0, (h2d / (link * 1e9) * 1e3 + ms_compute - ms)
+                                                / min(h2d / (link * 1e9) * 1e3, ms_compute)))
+                                   if not store_path and h2d > 0 else None)},
         "e2e": {"value": 1.0 / te, "unit": "tokens/s", "h2d_bytes_per_step": 2 * shape.d_model,
                 "d2h_bytes_per_step": 2 * shape.d_model, "api": "moe_layer_forward x 30"},
         "gpu_launches": 2 * L * K,
