@@ -220,72 +220,52 @@ struct AttnArgs {
   float* o;                 // [Hq][d] attention output
 };
 
-template <int PER>  // head dims per lane: d = 32 * PER
-__device__ __forceinline__ void load_half(const __half* p, float (&out)[PER]) {
-  if constexpr (PER == 8) {
-    const uint4 r = *reinterpret_cast<const uint4*>(p);
-    const uint32_t ww[4] = {r.x, r.y, r.z, r.w};
+// A lane's PER fp16 values of one cache row, as loaded (8 values: 16 bytes).
+template <int PER> struct Raw;
+template <> struct Raw<8> { using T = uint4; };
+template <> struct Raw<4> { using T = uint2; };
+template <> struct Raw<2> { using T = uint32_t; };
+
+template <int PER>
+__device__ __forceinline__ typename Raw<PER>::T load_raw(const __half* p) {
+  return *reinterpret_cast<const typename Raw<PER>::T*>(p);
+}
+
+template <int PER>
+__device__ __forceinline__ void to_float(const typename Raw<PER>::T& r, float (&out)[PER]) {
+  const uint32_t* ww = reinterpret_cast<const uint32_t*>(&r);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[j]));
-      out[2 * j] = f.x;
-      out[2 * j + 1] = f.y;
-    }
-  } else if constexpr (PER == 4) {
-    const uint2 r = *reinterpret_cast<const uint2*>(p);
-    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
-    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
-    out[0] = f0.x; out[1] = f0.y; out[2] = f1.x; out[3] = f1.y;
-  } else {
-    const uint32_t r = *reinterpret_cast<const uint32_t*>(p);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&r));
-    out[0] = f.x; out[1] = f.y;
+  for (int j = 0; j < PER / 2; ++j) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[j]));
+    out[2 * j] = f.x;
+    out[2 * j + 1] = f.y;
   }
 }
 
-// One head vector (d values, one per thread t < d; the other threads pass 0)
-// divided by its RMS; `rotate`: RoPE at position pos through shared memory.
-// Every thread of the block calls it (two block barriers).
-__device__ float head_norm_rope(float v, const AttnArgs& a, bool rotate, float* buf, float* red) {
-  const int t = threadIdx.x, d = a.d;
-  float ss = v * v;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((t & 31) == 0) red[t >> 5] = ss;
-  __syncthreads();
-  ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < kSplitWarps; ++i) ss += red[i];
-  v *= rsqrtf(ss / static_cast<float>(d) + a.eps);
-  if (!rotate) {
-    __syncthreads();  // red is reused by the next call
-    return v;
-  }
-  if (t < d) buf[t] = v;
-  __syncthreads();
-  if (t < d) {
-    // angle in half turns t = pos * theta^(-2i/d) / pi, formed in fp64 and
-    // reduced exactly to [-1, 1]; sine and cosine of the reduced angle in fp32
-    const int h = d / 2, i = t < h ? t : t - h;
-    const double turns = static_cast<double>(a.pos) * a.freq_pi[i];
-    const float r = static_cast<float>(turns - 2.0 * rint(0.5 * turns));
-    float sn, cs;
-    sincospif(r, &sn, &cs);
-    const float x0 = buf[i], x1 = buf[i + h];
-    v = t < h ? x0 * cs - x1 * sn : x0 * sn + x1 * cs;
-  }
-  __syncthreads();
-  return v;
+// RoPE of one head vector held one value per thread (t < d) through shared
+// memory: the pairs (i, i + d/2) rotate by the angle, in half turns,
+// pos * theta^(-2i/d) / pi; formed in fp64 and reduced exactly to [-1, 1],
+// then sine and cosine in fp32.
+__device__ __forceinline__ float rope_value(float x0, float x1, int t, const AttnArgs& a) {
+  const int h = a.d / 2, i = t < h ? t : t - h;
+  const double turns = static_cast<double>(a.pos) * a.freq_pi[i];
+  const float r = static_cast<float>(turns - 2.0 * rint(0.5 * turns));
+  float sn, cs;
+  sincospif(r, &sn, &cs);
+  return t < h ? x0 * cs - x1 * sn : x0 * sn + x1 * cs;
 }
 
 // Decode attention of one layer for one token, block (h, s) = (query head,
 // split of the visible positions); kv head g = h / (Hq / Hkv).
+//  0. Each warp requests the cache rows of its first kBatch positions before
+//     anything else, so their latency overlaps step 1.
 //  1. q_h = RoPE(q_raw_h / RMS); the split that holds position pos (the last
 //     one) also forms this token's key RoPE(k_raw_g / RMS) and value
 //     v_raw_g / RMS, rounded to fp16 as the cache stores them, and the first
-//     query head of the group writes them to cache slot pos % cap.
+//     query head of the group writes them to cache slot pos % cap.  The three
+//     norms share one block reduction and the two rotations one exchange.
 //  2. Warp w takes the split's earlier positions lo + w, + 8, ... in batches
-//     of 4 (their key and value rows loaded together) with an online
+//     of kBatch (their key and value rows loaded together) with an online
 //     softmax; warp 0 then folds in position pos from shared memory.  The 8
 //     warps merge in a fixed order into the split's (o, max, sum).
 //  3. The last block of head h to finish (an arrival counter) merges the
@@ -294,7 +274,10 @@ __device__ float head_norm_rope(float v, const AttnArgs& a, bool rotate, float* 
 template <int PER>
 __global__ void __launch_bounds__(kSplitWarps * 32) attn_decode_kernel(AttnArgs a) {
   constexpr int D = 32 * PER;
-  __shared__ float buf[D], red[kSplitWarps];
+  constexpr int kBatch = 8;
+  using RawT = typename Raw<PER>::T;
+  __shared__ float bq[D], bk[D];
+  __shared__ float red[3][kSplitWarps];
   __shared__ float qs[D];
   __shared__ __align__(16) __half kcur[D], vcur[D];
   __shared__ float wm[kSplitWarps], wl[kSplitWarps];
@@ -304,19 +287,60 @@ __global__ void __launch_bounds__(kSplitWarps * 32) attn_decode_kernel(AttnArgs 
   const int grp = a.Hq / a.Hkv, g = h / grp;
   const long long lo = a.first + a.n * s / a.nsplit, hi = a.first + a.n * (s + 1) / a.nsplit;
   const bool has_pos = hi == a.pos + 1;  // the last split
+  const long long hc = has_pos ? hi - 1 : hi;  // positions read from the cache
+  const __half* kbase = a.kc + static_cast<int64_t>(g) * a.cap * D + lane * PER;
+  const __half* vbase = a.vc + static_cast<int64_t>(g) * a.cap * D + lane * PER;
+  // ---- 0. the first batch of cache rows
+  RawT kr[kBatch], vr[kBatch];
+  auto fetch = [&](long long p0) {
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const long long p = p0 + static_cast<long long>(b) * kSplitWarps;
+      const long long slot = (p < hc ? p : lo) % a.cap;
+      kr[b] = load_raw<PER>(kbase + slot * D);
+      vr[b] = load_raw<PER>(vbase + slot * D);
+    }
+  };
+  if (lo + w < hc) fetch(lo + w);
   // ---- 1. this head's query, and (last split) this token's key and value
   {
-    const float qv = head_norm_rope(t < D ? a.qkv[static_cast<int64_t>(h) * D + t] : 0.f, a, true,
-                                    buf, red);
-    if (t < D) qs[t] = qv;
-    if (has_pos) {
-      const float kv = head_norm_rope(
-          t < D ? a.qkv[static_cast<int64_t>(a.Hq + g) * D + t] : 0.f, a, true, buf, red);
-      const float vv = head_norm_rope(
-          t < D ? a.qkv[static_cast<int64_t>(a.Hq + a.Hkv + g) * D + t] : 0.f, a, false, buf, red);
-      if (t < D) {
-        kcur[t] = __float2half_rn(kv);
-        vcur[t] = __float2half_rn(vv);
+    const float qv = t < D ? a.qkv[static_cast<int64_t>(h) * D + t] : 0.f;
+    const float kv = has_pos && t < D ? a.qkv[static_cast<int64_t>(a.Hq + g) * D + t] : 0.f;
+    const float vv = has_pos && t < D ? a.qkv[static_cast<int64_t>(a.Hq + a.Hkv + g) * D + t] : 0.f;
+    float sq = qv * qv, sk = kv * kv, sv = vv * vv;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      sv += __shfl_xor_sync(0xffffffffu, sv, o);
+    }
+    if (lane == 0) {
+      red[0][w] = sq;
+      red[1][w] = sk;
+      red[2][w] = sv;
+    }
+    __syncthreads();
+    sq = sk = sv = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSplitWarps; ++i) {
+      sq += red[0][i];
+      sk += red[1][i];
+      sv += red[2][i];
+    }
+    const float inv_d = 1.f / static_cast<float>(D);
+    const float qn = qv * rsqrtf(sq * inv_d + a.eps), kn = kv * rsqrtf(sk * inv_d + a.eps);
+    const float vn = vv * rsqrtf(sv * inv_d + a.eps);
+    if (t < D) {
+      bq[t] = qn;
+      bk[t] = kn;
+    }
+    __syncthreads();
+    if (t < D) {
+      const int hh = D / 2, i = t < hh ? t : t - hh;
+      qs[t] = rope_value(bq[i], bq[i + hh], t, a);
+      if (has_pos) {
+        kcur[t] = __float2half_rn(rope_value(bk[i], bk[i + hh], t, a));
+        vcur[t] = __float2half_rn(vn);
         if (h % grp == 0) {
           const int64_t at = (static_cast<int64_t>(g) * a.cap + a.pos % a.cap) * D + t;
           a.kc[at] = kcur[t];
@@ -333,9 +357,6 @@ __global__ void __launch_bounds__(kSplitWarps * 32) attn_decode_kernel(AttnArgs 
   float m = -INFINITY, l = 0.f, o[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) o[i] = 0.f;
-  const __half* kbase = a.kc + static_cast<int64_t>(g) * a.cap * D + lane * PER;
-  const __half* vbase = a.vc + static_cast<int64_t>(g) * a.cap * D + lane * PER;
-  const long long hc = has_pos ? hi - 1 : hi;  // positions read from the cache
   auto fold = [&](float dot, const float (&vf)[PER]) {
     const float sc = dot * a.scale;
     const float mn = fmaxf(m, sc);
@@ -345,22 +366,16 @@ __global__ void __launch_bounds__(kSplitWarps * 32) attn_decode_kernel(AttnArgs 
     for (int i = 0; i < PER; ++i) o[i] = fmaf(o[i], c, e * vf[i]);
     m = mn;
   };
-  constexpr int kBatch = 4;
   for (long long p0 = lo + w; p0 < hc; p0 += kSplitWarps * kBatch) {
-    float kf[kBatch][PER], vf[kBatch][PER];
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const long long p = p0 + static_cast<long long>(b) * kSplitWarps;
-      const long long slot = (p < hc ? p : lo) % a.cap;
-      load_half<PER>(kbase + slot * D, kf[b]);
-      load_half<PER>(vbase + slot * D, vf[b]);
-    }
+    if (p0 != lo + w) fetch(p0);
     float dot[kBatch];
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
+      float kf[PER];
+      to_float<PER>(kr[b], kf);
       dot[b] = 0.f;
 #pragma unroll
-      for (int i = 0; i < PER; ++i) dot[b] = fmaf(q[i], kf[b][i], dot[b]);
+      for (int i = 0; i < PER; ++i) dot[b] = fmaf(q[i], kf[i], dot[b]);
     }
 #pragma unroll
     for (int off = 16; off; off >>= 1)
@@ -369,13 +384,15 @@ __global__ void __launch_bounds__(kSplitWarps * 32) attn_decode_kernel(AttnArgs 
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       if (p0 + static_cast<long long>(b) * kSplitWarps >= hc) break;
-      fold(dot[b], vf[b]);
+      float vf[PER];
+      to_float<PER>(vr[b], vf);
+      fold(dot[b], vf);
     }
   }
   if (has_pos && w == 0) {  // this token's own key and value
     float kf[PER], vf[PER];
-    load_half<PER>(kcur + lane * PER, kf);
-    load_half<PER>(vcur + lane * PER, vf);
+    to_float<PER>(load_raw<PER>(kcur + lane * PER), kf);
+    to_float<PER>(load_raw<PER>(vcur + lane * PER), vf);
     float dot = 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) dot = fmaf(q[i], kf[i], dot);
@@ -419,7 +436,7 @@ __global__ void __launch_bounds__(kSplitWarps * 32) attn_decode_kernel(AttnArgs 
   const float* ph = a.part + static_cast<int64_t>(h) * a.nsplit * (D + 2);
   // the splits' (max, sum) into shared memory, then each thread's column of
   // every split in batches of 8 independent loads, added in split order
-  float* fm = buf;                  // reused: [kMaxSplits] <= D floats
+  float* fm = bq;                   // reused: [kMaxSplits] <= D floats
   float* fl = &wo[0][0];            // reused: [kMaxSplits]
   if (t < a.nsplit) {
     fm[t] = __ldcg(ph + t * (D + 2) + D);
