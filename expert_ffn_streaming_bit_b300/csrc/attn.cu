@@ -102,6 +102,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32) qgemv_kernel(GemvArgs a) {
       sbv[k][i] = ok ? __ldg(reinterpret_cast<const uint32_t*>(row + a.K / 2 + (c >> 1) * 4)) : 0u;
     }
   }
+  // the input comes from the kernel before on the stream.  The next kernel
+  // may start only once this one has passed its wait, so a kernel's early
+  // reads (weights here, older cache rows in the attention kernel) overlap
+  // at most the kernel right before it, which never writes them.
+  grid_dep_wait();
+  grid_dep_launch();
   // ---- the input, 8 values per thread and group of 256 threads
   float v[2][8];
   float m = 0.f, ss = 0.f;
@@ -302,6 +308,10 @@ __global__ void __launch_bounds__(kSplitWarps * 32) attn_decode_kernel(AttnArgs 
     }
   };
   if (lo + w < hc) fetch(lo + w);
+  // the projections come from the kernel before on the stream (the cache
+  // rows fetched above were written two or more launches earlier)
+  grid_dep_wait();
+  grid_dep_launch();
   // ---- 1. this head's query, and (last split) this token's key and value
   {
     const float qv = t < D ? a.qkv[static_cast<int64_t>(h) * D + t] : 0.f;
@@ -522,15 +532,31 @@ void attn_free(moe_attn* a) {
 
 bool qt_ok(const moe_qtensor& t) { return t.q && t.scale && t.bias; }
 
+// A launch that may overlap the end of the kernel before it on the stream
+// (programmatic dependent launch); the kernels wait for their inputs with
+// grid_dep_wait after requesting the data that does not depend on them.
+template <typename Args>
+int launch_pdl(void (*kernel)(Args), dim3 grid, int threads, cudaStream_t s, const Args& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return static_cast<int>(cudaLaunchKernelEx(&cfg, kernel, args));
+}
+
 // Rows per warp: 4 for tall matrices (one wave of blocks with their loads
 // in flight), 2 otherwise (enough blocks to cover the SMs).
 int launch_gemv(const GemvArgs& g, cudaStream_t s) {
-  if (g.R >= 6144) {
-    qgemv_kernel<4><<<(g.R + 4 * kGemvWarps - 1) / (4 * kGemvWarps), kGemvWarps * 32, 0, s>>>(g);
-  } else {
-    qgemv_kernel<2><<<(g.R + 2 * kGemvWarps - 1) / (2 * kGemvWarps), kGemvWarps * 32, 0, s>>>(g);
-  }
-  return static_cast<int>(cudaGetLastError());
+  if (g.R >= 6144)
+    return launch_pdl(qgemv_kernel<4>, dim3((g.R + 4 * kGemvWarps - 1) / (4 * kGemvWarps)),
+                      kGemvWarps * 32, s, g);
+  return launch_pdl(qgemv_kernel<2>, dim3((g.R + 2 * kGemvWarps - 1) / (2 * kGemvWarps)),
+                    kGemvWarps * 32, s, g);
 }
 
 }  // namespace
@@ -691,10 +717,9 @@ moe_status moe_attn_forward(moe_attn* a, int layer, const void* x, long long pos
   aa.o = a->o;
   if (!e) {
     const dim3 grid(Hq, aa.nsplit);
-    if (d == 256) attn_decode_kernel<8><<<grid, kSplitWarps * 32, 0, s>>>(aa);
-    else if (d == 128) attn_decode_kernel<4><<<grid, kSplitWarps * 32, 0, s>>>(aa);
-    else attn_decode_kernel<2><<<grid, kSplitWarps * 32, 0, s>>>(aa);
-    e = static_cast<int>(cudaGetLastError());
+    if (d == 256) e = launch_pdl(attn_decode_kernel<8>, grid, kSplitWarps * 32, s, aa);
+    else if (d == 128) e = launch_pdl(attn_decode_kernel<4>, grid, kSplitWarps * 32, s, aa);
+    else e = launch_pdl(attn_decode_kernel<2>, grid, kSplitWarps * 32, s, aa);
   }
   // output projection (+ residual), bf16
   GemvArgs go{};

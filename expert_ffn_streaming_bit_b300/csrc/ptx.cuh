@@ -182,6 +182,16 @@ __device__ __forceinline__ int ld_cg_s32(const int* p) {
   return v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the kernel before it on the stream finishes.
+// grid_dep_launch lets the next kernel start early; grid_dep_wait blocks until
+// the kernel before has completed and its memory is visible (immediately if
+// the launch was an ordinary one).
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
