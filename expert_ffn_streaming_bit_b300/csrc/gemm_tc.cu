@@ -88,9 +88,28 @@ constexpr int kStageBytes = 2048;                // per epilogue warp: output tr
 constexpr int kSmemBytes = kNP * kPBytes + kNB * kBBytes + kMetaBytes + kEpiWarps * kStageBytes +
                            1024 /*Bars*/ + 1024 /*alignment slack*/;
 
+// The tanh form of GELU, 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3),
+// evaluated through the identity 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)): one
+// exponential and one division, and no cancellation for large negative u
+// (exp overflows to inf and the quotient goes to 0, the function's limit).
 __device__ __forceinline__ float gelu_tanh(float x) {
-  const float c = 0.7978845608028654f;  // sqrt(2/pi)
-  return 0.5f * x * (1.f + tanhf(c * (x + 0.044715f * x * x * x)));
+  const float c2 = 1.5957691216057308f;  // 2 sqrt(2/pi)
+  const float u2 = c2 * fmaf(0.044715f * x, x * x, x);
+  return __fdividef(x, 1.f + __expf(-u2));
+}
+
+// 16 consecutive per-column factors of the unit from shared memory into
+// registers (broadcast vector loads), ahead of the chunk's stores to the
+// staging tile, so that no factor load waits behind a store.
+__device__ __forceinline__ void load16(const float* src, float (&d)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 v = reinterpret_cast<const float4*>(src)[i];
+    d[4 * i] = v.x;
+    d[4 * i + 1] = v.y;
+    d[4 * i + 2] = v.z;
+    d[4 * i + 3] = v.w;
+  }
 }
 
 // Bounded mbarrier wait shared by all roles: on expiry record a timeout and
@@ -106,6 +125,20 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const G
 __device__ __forceinline__ int unit_nmma(int n) { return (n + 15) & ~15; }
 
 // ---------------------------------------------------------------- roles
+
+// Position in an mbarrier-pipelined ring of N stages: the stage and the
+// parity of its current fill.
+struct RingPos {
+  int s = 0;
+  uint32_t ph = 0;  // parity of the stage's current fill
+  template <int N>
+  __device__ __forceinline__ void next() {
+    if (++s == N) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
 
 // Two loader threads, so that neither ring waits for the other: the weight
 // slices (P ring, one stage per 256 columns) and the activation tiles (B
@@ -159,76 +192,95 @@ __device__ void role_tma_b(const GemmParams& p, uint8_t* B, Bars* bars, int nU) 
     mbar_wait(&bars->b_full[q % kNB], (q / kNB) & 1, p.timeout_ns, nullptr);
 }
 
-// Dequantisation.  With two tiles per unit warp w takes tile (w-2)/4 and
-// whole rows (64 values per 64-column block); with one tile the two warps of
-// a lane quarter take the two 32-column halves of each row.
+// Dequantisation (8 warps): the two warps of tensor-memory lane quarter w%4
+// take the two 32-column halves of its 32 rows.  Per 64-column block each
+// thread turns its row's 32 codes into fp16 w = fp16(s q + b) (one rounding)
+// and stores them into the block's A stage.  Blocks go two at a time while
+// the weight slice holds two more: the warps are bound by latency (barrier
+// waits, shared-memory loads, the tensor-memory store and its completion),
+// and a pair overlaps those of two blocks and halves the synchronisation per
+// block.
+__device__ __forceinline__ void dequant32(const uint8_t* codes, const uint32_t* sbw, int row,
+                                          int half, int sb, __half2 k1024, uint32_t (&o)[16]) {
+  const uint32_t word = sbw[row * 4 + sb];
+  const __half2 s2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word & 0xffffu)));
+  const __half2 b2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word >> 16)));
+  // packed chunk c (32 columns) of this row, stored at chunk c ^ (row & 7)
+  const int c = 2 * sb + half;
+  const uint4 wq = *reinterpret_cast<const uint4*>(codes + row * 128 + ((c ^ (row & 7)) << 4));
+  const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    // word j: columns 8j..8j+7 of the chunk; byte i = col i (low) | col 4+i (high)
+    const uint32_t lo = ws[j] & 0x0F0F0F0Fu;
+    const uint32_t hi = (ws[j] >> 4) & 0x0F0F0F0Fu;
+    // fp16 1024 + q pairs: bytes (q, 0x64) per half
+    const uint32_t mm[4] = {__byte_perm(lo, 0x64646464u, 0x5140), __byte_perm(lo, 0x64646464u, 0x7362),
+                            __byte_perm(hi, 0x64646464u, 0x5140), __byte_perm(hi, 0x64646464u, 0x7362)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&mm[i]), k1024);
+      const __half2 v = __hfma2(q, s2, b2);
+      o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+  }
+}
+
 __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, int nU) {
+  static_assert(kTU == 1, "the dequantisation warps fill one weight tile per unit");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = (w - 2) >> 2;        // tile (two tiles) or half of the row (one tile)
-  const int m = kTU == 2 ? grp : 0;    // weight tile
+  const int half = (w - 2) >> 2;       // 32-column half of the row
   const int qd = w & 3;                // tensor-memory lane quarter
   const int row = 32 * qd + lane;      // row of the weight tile
-  const uint32_t tbase = bars->tmem_base + (static_cast<uint32_t>(32 * qd) << 16);
-  uint32_t pc = 0, ac = 0;
+  const uint32_t tbase =
+      bars->tmem_base + (static_cast<uint32_t>(32 * qd) << 16) + kACol0 + half * 16;
   const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+  RingPos ra;
+  uint32_t pc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x) {
     const GemmUnit un = p.units[u];
     const int K = p.K[un.kind];
     const int nkb = K / 64;
     const int np = (K + 255) / 256;
-    const bool active = m < un.nmt;  // warp-uniform
     for (int sp = 0; sp < np; ++sp, ++pc) {
       const int st = pc % kNP;
       if (!wait_bar(&bars->p_full[st], (pc / kNP) & 1, p, bars)) return;
       const int nsub = min(4, nkb - 4 * sp);
-      const uint8_t* codes = P + st * kPBytes + m * kPTile;
+      const uint8_t* codes = P + st * kPBytes;
       const uint32_t* sbw = reinterpret_cast<const uint32_t*>(codes + kPCodeBytes);
-      for (int sb = 0; sb < nsub; ++sb, ++ac) {
-        const int as = ac % kNA;
-        if (!wait_bar(&bars->a_empty[as], ((ac / kNA) & 1) ^ 1, p, bars)) return;
-        if (active) {
-          const uint32_t word = sbw[row * 4 + sb];
-          const __half2 s2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word & 0xffffu)));
-          const __half2 b2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word >> 16)));
-          constexpr int kHalves = kTU == 2 ? 2 : 1;
-          uint32_t o[16 * kHalves];
-#pragma unroll
-          for (int hh = 0; hh < kHalves; ++hh) {
-            const int half = kTU == 2 ? hh : grp;
-            // packed chunk c (32 columns) of this row, stored at chunk c ^ (row & 7)
-            const int c = 2 * sb + half;
-            const uint4 wq = *reinterpret_cast<const uint4*>(codes + row * 128 + ((c ^ (row & 7)) << 4));
-            const uint32_t ws[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              // word j: columns 8j..8j+7 of the chunk; byte i = col i (low) | col 4+i (high)
-              const uint32_t lo = ws[j] & 0x0F0F0F0Fu;
-              const uint32_t hi = (ws[j] >> 4) & 0x0F0F0F0Fu;
-              // fp16 1024 + q pairs: bytes (q, 0x64) per half
-              const uint32_t mm[4] = {__byte_perm(lo, 0x64646464u, 0x5140),
-                                      __byte_perm(lo, 0x64646464u, 0x7362),
-                                      __byte_perm(hi, 0x64646464u, 0x5140),
-                                      __byte_perm(hi, 0x64646464u, 0x7362)};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&mm[i]), k1024);
-                const __half2 v = __hfma2(q, s2, b2);
-                o[16 * hh + 4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
-              }
-            }
-          }
-          if constexpr (kTU == 2) {
-            tmem_st32(tbase + kACol0 + as * kAStage + m * 32,
-                      *reinterpret_cast<const uint32_t(*)[32]>(o));
-          } else {
-            tmem_st16(tbase + kACol0 + as * kAStage + grp * 16,
-                      *reinterpret_cast<const uint32_t(*)[16]>(o));
-          }
+      for (int sb = 0; sb < nsub;) {
+        if (sb + 1 < nsub) {
+          RingPos r1 = ra;
+          r1.next<kNA>();
+          if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
+          if (!wait_bar(&bars->a_empty[r1.s], r1.ph ^ 1u, p, bars)) return;
+          uint32_t o0[16], o1[16];
+          dequant32(codes, sbw, row, half, sb, k1024, o0);
+          dequant32(codes, sbw, row, half, sb + 1, k1024, o1);
+          tmem_st16(tbase + ra.s * kAStage, o0);
+          tmem_st16(tbase + r1.s * kAStage, o1);
           tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->a_full[ra.s]);
+            mbar_arrive(&bars->a_full[r1.s]);
+          }
+          ra = r1;
+          ra.next<kNA>();
+          sb += 2;
+        } else {
+          if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
+          uint32_t o0[16];
+          dequant32(codes, sbw, row, half, sb, k1024, o0);
+          tmem_st16(tbase + ra.s * kAStage, o0);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->a_full[ra.s]);
+          ra.next<kNA>();
+          sb += 1;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->a_full[as]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_empty[st]);
@@ -236,49 +288,76 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
   }
 }
 
-// The issue loop is kept to a few instructions per MMA: descriptors are
-// precomputed (a B stage is the stage-0 descriptor plus its offset in 16-byte
-// units, a k-step adds 32 bytes), the k-steps and tiles are unrolled.
-__device__ __forceinline__ void mma_kblock(uint32_t acc, uint32_t a0, uint64_t bd, uint32_t idesc,
-                                           int nmt, uint32_t first) {
-  if (kTU == 2 && nmt == 2) {
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint32_t f = kk == 0 ? first : 1u;
-      tc_mma_f16_ts(acc, a0 + 8 * kk, bd + 2 * kk, idesc, f);
-      tc_mma_f16_ts(acc + kAccCols, a0 + 32 + 8 * kk, bd + 2 * kk, idesc, f);
-    }
-  } else {
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) tc_mma_f16_ts(acc, a0 + 8 * kk, bd + 2 * kk, idesc, kk == 0 ? first : 1u);
+// The MMA role runs on a whole warp: every lane waits, the warp stays
+// converged, and one elected lane issues each K block's four MMAs and its two
+// commits from a single instruction sequence.  A unit's K blocks run in a
+// loop instantiated for its token count (the MMA's N, a multiple of 16), so
+// the instruction descriptor is a constant, and the ring positions advance
+// by increment: the warp shares its issue slots with dequantisation and
+// epilogue warps, so every instruction it saves per K block keeps the tensor
+// pipe fed.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
+                                          Bars* bars) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, p, bars));
+}
+
+
+template <int NMMA>
+__device__ __forceinline__ bool mma_unit(const GemmParams& p, Bars* bars, uint32_t acc,
+                                         uint32_t a_base, uint64_t bdesc0, int nkb, RingPos& ra,
+                                         RingPos& rb) {
+  constexpr uint32_t idesc = tc_idesc_f16(128, NMMA);
+  for (int kb = 0; kb < nkb; ++kb) {
+    if (!warp_wait(&bars->a_full[ra.s], ra.ph, p, bars)) return false;
+    if (!warp_wait(&bars->b_full[rb.s], rb.ph, p, bars)) return false;
+    tc_fence_after();
+    tc_kblock_ts_warp(acc, a_base + ra.s * kAStage,
+                      bdesc0 + static_cast<uint64_t>(rb.s * (kBBytes >> 4)), idesc, kb != 0,
+                      &bars->a_empty[ra.s], &bars->b_empty[rb.s]);
+    ra.next<kNA>();
+    rb.next<kNB>();
   }
+  return true;
 }
 
 __device__ void role_mma(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
+  static_assert(kUnitTokens % 16 == 0 && kUnitTokens <= 256, "unit token count");
+  static_assert(kTU == 1, "the MMA loop issues one weight tile per unit");
   const uint32_t tmem = bars->tmem_base;
   const uint64_t bdesc0 = tc_desc_sw128(smem_u32(B));
-  uint32_t ac = 0, bc = 0, uc = 0;
+  RingPos ra, rb;
+  uint32_t uc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x, ++uc) {
     const GemmUnit un = p.units[u];
-    const int K = p.K[un.kind];
-    const int nkb = K / 64;
-    const uint32_t idesc = tc_idesc_f16(128, unit_nmma(un.n));
+    const int nkb = p.K[un.kind] / 64;
     const uint32_t acc = tmem + (uc & 1) * kAccSet;  // this unit's accumulator set
     // (an injected stall waits for the phase before, which never completes)
     const uint32_t par = ((uc >> 1) & 1) ^ (p.stall ? 0u : 1u);
-    if (!wait_bar(&bars->acc_empty[uc & 1], par, p, bars)) return;
+    if (!warp_wait(&bars->acc_empty[uc & 1], par, p, bars)) return;
     tc_fence_after();
-    for (int kb = 0; kb < nkb; ++kb, ++ac, ++bc) {
-      const int as = ac % kNA, bs = bc % kNB;
-      if (!wait_bar(&bars->a_full[as], (ac / kNA) & 1, p, bars)) return;
-      if (!wait_bar(&bars->b_full[bs], (bc / kNB) & 1, p, bars)) return;
-      tc_fence_after();
-      mma_kblock(acc, tmem + kACol0 + as * kAStage,
-                 bdesc0 + static_cast<uint64_t>(bs * (kBBytes >> 4)), idesc, un.nmt, kb != 0);
-      tc_commit(&bars->a_empty[as]);
-      tc_commit(&bars->b_empty[bs]);
+    const uint32_t a_base = tmem + kACol0;
+    const int n16 = unit_nmma(un.n) >> 4;
+    if (n16 < 1 || 16 * n16 > kUnitTokens) {  // never emitted by the bucketing
+      if (!bars->abort) atomicCAS(p.status, DEV_OK, DEV_BAD_ID);
+      bars->abort = 1;
+      return;
     }
-    tc_commit(&bars->acc_full[uc & 1]);
+    bool ok = false;
+    switch (n16) {
+#define MOE_MMA_CASE(c)                                                                   \
+  case c:                                                                                 \
+    if constexpr (16 * (c) <= kUnitTokens)                                                \
+      ok = mma_unit<16 * (c)>(p, bars, acc, a_base, bdesc0, nkb, ra, rb);                \
+    break;
+      MOE_MMA_CASE(1) MOE_MMA_CASE(2) MOE_MMA_CASE(3) MOE_MMA_CASE(4) MOE_MMA_CASE(5)
+      MOE_MMA_CASE(6) MOE_MMA_CASE(7) MOE_MMA_CASE(8) MOE_MMA_CASE(9) MOE_MMA_CASE(10)
+      MOE_MMA_CASE(11) MOE_MMA_CASE(12) MOE_MMA_CASE(13) MOE_MMA_CASE(14) MOE_MMA_CASE(15)
+      MOE_MMA_CASE(16)
+#undef MOE_MMA_CASE
+      default: break;
+    }
+    if (!ok) return;  // a wait ran out
+    tc_commit_warp(&bars->acc_full[uc & 1]);
   }
   // the last commits must complete before the CTA exits
   if (uc > 0) mbar_wait(&bars->acc_full[(uc - 1) & 1], ((uc - 1) >> 1) & 1, p.timeout_ns, nullptr);
@@ -338,6 +417,9 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
           const int jj = lane >> 1;
           const bool odd = lane & 1;
           __half* sh = reinterpret_cast<__half*>(stg);
+          float sgv[16], hsv[16];
+          load16(meta + c0 + (odd ? 16 : 0), sgv);
+          load16(meta + kUnitTokens + c0 + (odd ? 16 : 0), hsv);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float mine_lo = __uint_as_float(r[i]), mine_hi = __uint_as_float(r[16 + i]);
@@ -347,10 +429,7 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
             const int tc = (odd ? 16 : 0) + i;  // token within the chunk
             const int col = c0 + tc;
             float h = 0.f;
-            if (col < un.n) {
-              const float sg = meta[col];
-              h = gelu_tanh(g * sg) * (v * sg) * meta[kUnitTokens + col];
-            }
+            if (col < un.n) h = gelu_tanh(g * sgv[i]) * (v * sgv[i]) * hsv[i];
             sh[tc * 16 + jj] = __float2half_rn(fminf(fmaxf(h, -65504.f), 65504.f));
           }
           __syncwarp();
@@ -371,10 +450,13 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
           // routed down: bf16 [32 tokens][32 features] (64-byte rows)
           const int d0 = mt * 128 + 32 * q;
           __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg);
+          float mv[2][16];
+          load16(meta + c0, mv[0]);
+          load16(meta + c0 + 16, mv[1]);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int col = c0 + i;
-            const float v = col < un.n ? __uint_as_float(r[i]) * meta[col] : 0.f;
+            const float v = col < un.n ? __uint_as_float(r[i]) * mv[i >> 4][i & 15] : 0.f;
             sb[i * 32 + lane] = __float2bfloat16_rn(v);
           }
           __syncwarp();
@@ -394,12 +476,15 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
           // shared down: fp32 [16 tokens][32 features] (128-byte rows), twice
           const int d0 = mt * 128 + 32 * q;
           float* sf = reinterpret_cast<float*>(stg);
+          float mv[2][16];
+          load16(meta + c0, mv[0]);
+          load16(meta + c0 + 16, mv[1]);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int col = c0 + 16 * hh + i;
-              sf[i * 32 + lane] = col < un.n ? __uint_as_float(r[16 * hh + i]) * meta[col] : 0.f;
+              sf[i * 32 + lane] = col < un.n ? __uint_as_float(r[16 * hh + i]) * mv[hh][i] : 0.f;
             }
             __syncwarp();
 #pragma unroll
@@ -467,7 +552,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   } else if (w == kBLoadWarp) {
     if ((threadIdx.x & 31) == 0) role_tma_b(p, B, bars, nU);
   } else if (w == 1) {
-    if ((threadIdx.x & 31) == 0) role_mma(p, B, bars, nU);
+    role_mma(p, B, bars, nU);
   } else if (w < kEpiWarp0) {
     role_dequant(p, P, bars, nU);
   } else {

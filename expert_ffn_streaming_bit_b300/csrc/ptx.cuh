@@ -330,6 +330,65 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// Warp-collective forms of the two calls above: the whole (converged) warp
+// executes them and one lane, chosen by elect.sync, issues the instruction.
+// The operands must be the same in every lane.  Issuing this way, with the
+// instruction descriptor a compile-time constant, lets consecutive MMAs
+// reach the tensor core's rate; a single diverged thread issuing them cannot
+// go below a few dozen cycles per MMA.
+__device__ __forceinline__ void tc_mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// One 64-column K block of a GEMM with A in tensor memory: four MMAs of
+// K = 16 (A columns a_tmem + 8 j, B descriptor b_desc + 2 j, i.e. 32 bytes
+// further along the 128-byte swizzled rows), then a commit to each of two
+// mbarriers, all issued by one lane elected from the converged warp.  The
+// first MMA overwrites D when accumulate == 0.
+__device__ __forceinline__ void tc_kblock_ts_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate, uint64_t* bar0,
+                                                  uint64_t* bar1) {
+  asm volatile(
+      "{\n"
+      " .reg .pred e, p, t;\n"
+      " .reg .b32 l, a1, a2, a3;\n"
+      " .reg .b64 b1, b2, b3;\n"
+      " elect.sync l|e, 0xffffffff;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " setp.eq.b32 t, %4, %4;\n"
+      " add.u32 a1, %1, 8;\n"
+      " add.u32 a2, %1, 16;\n"
+      " add.u32 a3, %1, 24;\n"
+      " add.u64 b1, %2, 2;\n"
+      " add.u64 b2, %2, 4;\n"
+      " add.u64 b3, %2, 6;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(smem_u32(bar0)),
+      "r"(smem_u32(bar1))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n .reg .b32 l;\n elect.sync l|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
 // 32 TMEM lanes x 32 consecutive 32-bit columns from registers; thread i of
 // the warp writes lane (lane field of taddr) + i.  Follow with
 // tmem_st_wait() before signalling that the data is in place.
