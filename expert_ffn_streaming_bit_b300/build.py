@@ -11,7 +11,8 @@ LIB = os.path.join(HERE, "libmoe_b300.so")
 SOURCES = ["csrc/api.cu", "csrc/decode.cu", "csrc/noalloc.cu", "csrc/prefill.cu",
            "csrc/gemm_tc.cu", "csrc/repack.cpp", "csrc/slot_table.cpp", "csrc/store.cpp",
            "csrc/attn.cu"]
-HEADERS = ["csrc/internal.h", "csrc/ptx.cuh", "csrc/qdot.cuh", "csrc/repack.h", "csrc/store.h"]
+HEADERS = ["csrc/internal.h", "csrc/launch.cuh", "csrc/ptx.cuh", "csrc/qdot.cuh", "csrc/repack.h",
+           "csrc/store.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -35,6 +35,7 @@
 
 #include "../../include/moe.h"
 #include "internal.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 #include "qdot.cuh"
 #include "repack.h"
@@ -532,31 +533,15 @@ void attn_free(moe_attn* a) {
 
 bool qt_ok(const moe_qtensor& t) { return t.q && t.scale && t.bias; }
 
-// A launch that may overlap the end of the kernel before it on the stream
-// (programmatic dependent launch); the kernels wait for their inputs with
-// grid_dep_wait after requesting the data that does not depend on them.
-template <typename Args>
-int launch_pdl(void (*kernel)(Args), dim3 grid, int threads, cudaStream_t s, const Args& args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(threads);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return static_cast<int>(cudaLaunchKernelEx(&cfg, kernel, args));
-}
 
 // Rows per warp: 4 for tall matrices (one wave of blocks with their loads
 // in flight), 2 otherwise (enough blocks to cover the SMs).
 int launch_gemv(const GemvArgs& g, cudaStream_t s) {
   if (g.R >= 6144)
     return launch_pdl(qgemv_kernel<4>, dim3((g.R + 4 * kGemvWarps - 1) / (4 * kGemvWarps)),
-                      kGemvWarps * 32, s, g);
+                      dim3(kGemvWarps * 32), 0, s, g);
   return launch_pdl(qgemv_kernel<2>, dim3((g.R + 2 * kGemvWarps - 1) / (2 * kGemvWarps)),
-                    kGemvWarps * 32, s, g);
+                    dim3(kGemvWarps * 32), 0, s, g);
 }
 
 }  // namespace
@@ -717,9 +702,9 @@ moe_status moe_attn_forward(moe_attn* a, int layer, const void* x, long long pos
   aa.o = a->o;
   if (!e) {
     const dim3 grid(Hq, aa.nsplit);
-    if (d == 256) e = launch_pdl(attn_decode_kernel<8>, grid, kSplitWarps * 32, s, aa);
-    else if (d == 128) e = launch_pdl(attn_decode_kernel<4>, grid, kSplitWarps * 32, s, aa);
-    else e = launch_pdl(attn_decode_kernel<2>, grid, kSplitWarps * 32, s, aa);
+    if (d == 256) e = launch_pdl(attn_decode_kernel<8>, grid, dim3(kSplitWarps * 32), 0, s, aa);
+    else if (d == 128) e = launch_pdl(attn_decode_kernel<4>, grid, dim3(kSplitWarps * 32), 0, s, aa);
+    else e = launch_pdl(attn_decode_kernel<2>, grid, dim3(kSplitWarps * 32), 0, s, aa);
   }
   // output projection (+ residual), bf16
   GemvArgs go{};

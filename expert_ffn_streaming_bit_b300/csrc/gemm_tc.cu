@@ -49,6 +49,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -546,6 +547,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_wait();  // the units, activations and factors come from the kernels before
+  grid_dep_launch();
   const int nU = *p.n_units;
   if (w == 0) {
     if ((threadIdx.x & 31) == 0) role_tma_p(p, P, bars, nU);
@@ -624,16 +627,33 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t acc = bars->tmem;
   if (w == 0 && lane == 0) {
+    // the weight tiles of the first stages depend on no earlier kernel: they
+    // are requested before the wait for the token tiles
+    const int npre = min(kRtStages, kb1 - kb0);
+    for (int i = 0; i < npre; ++i) {
+      uint8_t* dst = smem + i * kRtStage;
+      mbar_arrive_expect_tx(&bars->full[i], kRtStage);
+      tma_load_2d(dst, &wmap, (kb0 + i) * 64, mt * 128, &bars->full[i]);
+      tma_load_2d(dst + kRtTile, &wmap, (kb0 + i) * 64, Epad + mt * 128, &bars->full[i]);
+    }
+    grid_dep_wait();
+    grid_dep_launch();
     for (int kb = kb0; kb < kb1; ++kb) {
       const int i = kb - kb0, st = i % kRtStages;
-      if (!rt_wait(&bars->empty[st], ((i / kRtStages) & 1) ^ 1, timeout_ns, bars, status)) break;
       uint8_t* dst = smem + st * kRtStage;
-      mbar_arrive_expect_tx(&bars->full[st], kRtStage);
-      tma_load_2d(dst, &wmap, kb * 64, mt * 128, &bars->full[st]);
-      tma_load_2d(dst + kRtTile, &wmap, kb * 64, Epad + mt * 128, &bars->full[st]);
+      if (i >= npre) {
+        if (!rt_wait(&bars->empty[st], ((i / kRtStages) & 1) ^ 1, timeout_ns, bars, status)) break;
+        mbar_arrive_expect_tx(&bars->full[st], kRtStage);
+        tma_load_2d(dst, &wmap, kb * 64, mt * 128, &bars->full[st]);
+        tma_load_2d(dst + kRtTile, &wmap, kb * 64, Epad + mt * 128, &bars->full[st]);
+      }
       tma_load_2d(dst + 2 * kRtTile, &xmap, kb * 64, t0, &bars->full[st]);
     }
-  } else if (w == 1 && lane == 0) {
+  } else {
+    grid_dep_wait();
+    grid_dep_launch();
+  }
+  if (w == 1 && lane == 0) {
     const uint32_t idesc = tc_idesc_f16(128, 128);
     const uint64_t d0 = tc_desc_sw128(smem_u32(smem));
     bool ok = true;
@@ -686,6 +706,8 @@ __global__ void __launch_bounds__(128, 1)
 __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restrict__ x16, int D8,
                                                           const int32_t* __restrict__ perm, int topk,
                                                           uint4* __restrict__ out) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int pos = blockIdx.x;
   const int tok = perm[pos] / topk;
   const uint4* src = x16 + static_cast<int64_t>(tok) * D8;
@@ -700,8 +722,8 @@ int gemm_tc_smem_bytes() { return kSmemBytes; }
 int gemm_tc_launch(const GemmParams& p, int grid, void* stream) {
   const int e = set_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel), kSmemBytes);
   if (e != 0) return e;
-  gemm_tc_kernel<<<grid, kGemmThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(p);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(gemm_tc_kernel, dim3(grid), dim3(kGemmThreads), kSmemBytes,
+                    static_cast<cudaStream_t>(stream), p);
 }
 
 int router_tc_splits(int T, int E, int D, int num_sms) {
@@ -723,17 +745,15 @@ int router_tc_launch(const CUtensorMap& wmap, const CUtensorMap& xmap, int T, in
   const int kbs = (nkb + nsplit - 1) / nsplit;
   const int Epad = (E + 127) / 128 * 128;
   dim3 grid((T + 127) / 128, Epad / 128, nsplit);
-  router_tc_kernel<<<grid, 128, kRtSmem, static_cast<cudaStream_t>(stream)>>>(
-      wmap, xmap, T, E, Epad, nkb, kbs, partials, status, timeout_ns);
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(router_tc_kernel, grid, dim3(128), kRtSmem, static_cast<cudaStream_t>(stream),
+                    wmap, xmap, T, E, Epad, nkb, kbs, partials, status, timeout_ns);
 }
 
 int gather_rows_launch(const void* x16, int D, const int32_t* perm, int topk, int rows, void* out,
                        void* stream) {
   if (rows <= 0) return 0;
-  gather_rows_kernel<<<rows, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(x16), D / 8, perm, topk, static_cast<uint4*>(out));
-  return static_cast<int>(cudaGetLastError());
+  return launch_pdl(gather_rows_kernel, dim3(rows), dim3(128), 0, static_cast<cudaStream_t>(stream),
+                    static_cast<const uint4*>(x16), D / 8, perm, topk, static_cast<uint4*>(out));
 }
 
 }  // namespace moe

@@ -14,6 +14,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -70,6 +71,8 @@ __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restric
                                                        float* __restrict__ sigma,
                                                        float* __restrict__ rscale,
                                                        float* __restrict__ hscale) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -148,6 +151,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           const int32_t* __restrict__ forced,
                                                           int32_t* __restrict__ ids,
                                                           float* __restrict__ wts) {
+  grid_dep_wait();
+  grid_dep_launch();
   constexpr int kB = 48 / EPL;  // splits per batch of loads
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
@@ -260,6 +265,8 @@ constexpr int kBkWarpSeg = 32 * kBkPerLane;       // 256 per warp
 constexpr int kBkBlockSeg = kBkWarps * kBkWarpSeg;  // 2048 per block
 
 __global__ void __launch_bounds__(kBkThreads) bk_hist_kernel(BucketArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int h[kBkWarps][kMaxPrefillExperts];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, n = a.T * a.K;
@@ -369,6 +376,8 @@ __device__ void emit_units(const BucketArgs& a, const int* cnt, const int* off, 
 }
 
 __global__ void __launch_bounds__(kScanThreads) bk_scan_kernel(BucketArgs a, int nb) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int part[kScanThreads];
   __shared__ int cnt[kMaxPrefillExperts];
   __shared__ int off[kMaxPrefillExperts + 1];
@@ -450,6 +459,8 @@ __device__ __forceinline__ void place_segment(const BucketArgs& a, int* base,
 }
 
 __global__ void __launch_bounds__(kBkThreads) bk_place_kernel(BucketArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int base[kBkWarps][kMaxPrefillExperts];
   __shared__ int cnt[kMaxPrefillExperts];
   __shared__ int off[kMaxPrefillExperts + 1];
@@ -486,6 +497,8 @@ constexpr int kSmallN = kScanThreads * kSmallPerLane;
 constexpr int kSmallBlocks = 8;
 
 __global__ void __launch_bounds__(kScanThreads) bk_small_kernel(BucketArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ int h[kSmallWarps][kMaxPrefillExperts];
   __shared__ int cnt[kMaxPrefillExperts];
   __shared__ int off[kMaxPrefillExperts + 1];
@@ -540,6 +553,8 @@ __global__ void __launch_bounds__(kScanThreads) bk_small_kernel(BucketArgs a) {
 // y[t] = bf16([x[t]] + s[t] + sum_j e[inv[t*K + j]]), summed in that order in
 // fp32.  Each thread handles 8 consecutive columns.
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int t = blockIdx.y;
   const int c8 = blockIdx.x * 128 + threadIdx.x;
   if (c8 * 8 >= a.D) return;
@@ -592,21 +607,19 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
 
 int prefill_route(const RouteArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  tok_prep_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a.x, a.T, a.D, a.prenorm, a.rms_eps,
-                                                reinterpret_cast<__half*>(a.x16), a.sigma, a.rscale,
-                                                a.hscale);
-  int e = static_cast<int>(cudaGetLastError());
+  int e = launch_pdl(tok_prep_kernel, dim3((a.T + 7) / 8), dim3(256), 0, s, a.x, a.T, a.D,
+                     a.prenorm, a.rms_eps, reinterpret_cast<__half*>(a.x16), a.sigma, a.rscale,
+                     a.hscale);
   if (e) return e;
   e = router_tc_launch(*a.wmap, *a.xmap, a.T, a.E, a.D, a.nsplit, a.partials, a.status,
                        a.timeout_ns, stream);
   if (e) return e;
+  const dim3 grid((a.T + 7) / 8);
   if (a.E <= 128)
-    router_topk_kernel<4><<<(a.T + 7) / 8, 256, 0, s>>>(a.partials, a.nsplit, a.T, a.E, a.K, a.sigma,
-                                                        a.logit_bias, a.forced, a.ids, a.wts);
-  else
-    router_topk_kernel<kMaxPrefillExperts / 32><<<(a.T + 7) / 8, 256, 0, s>>>(
-        a.partials, a.nsplit, a.T, a.E, a.K, a.sigma, a.logit_bias, a.forced, a.ids, a.wts);
-  return static_cast<int>(cudaGetLastError());
+    return launch_pdl(router_topk_kernel<4>, grid, dim3(256), 0, s, a.partials, a.nsplit, a.T, a.E,
+                      a.K, a.sigma, a.logit_bias, a.forced, a.ids, a.wts);
+  return launch_pdl(router_topk_kernel<kMaxPrefillExperts / 32>, grid, dim3(256), 0, s, a.partials,
+                    a.nsplit, a.T, a.E, a.K, a.sigma, a.logit_bias, a.forced, a.ids, a.wts);
 }
 
 int bucket_blocks(int n) { return (n + kBkBlockSeg - 1) / kBkBlockSeg; }
@@ -614,21 +627,18 @@ int bucket_blocks(int n) { return (n + kBkBlockSeg - 1) / kBkBlockSeg; }
 int prefill_bucket(const BucketArgs& a, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n = a.T * a.K;
-  if (n <= kSmallN) {
-    bk_small_kernel<<<kSmallBlocks, kScanThreads, 0, s>>>(a);
-    return static_cast<int>(cudaGetLastError());
-  }
+  if (n <= kSmallN)
+    return launch_pdl(bk_small_kernel, dim3(kSmallBlocks), dim3(kScanThreads), 0, s, a);
   const int nb = bucket_blocks(n);
-  bk_hist_kernel<<<nb, kBkThreads, 0, s>>>(a);
-  bk_scan_kernel<<<1, kScanThreads, 0, s>>>(a, nb);
-  bk_place_kernel<<<nb, kBkThreads, 0, s>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  int e = launch_pdl(bk_hist_kernel, dim3(nb), dim3(kBkThreads), 0, s, a);
+  if (!e) e = launch_pdl(bk_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, a, nb);
+  if (!e) e = launch_pdl(bk_place_kernel, dim3(nb), dim3(kBkThreads), 0, s, a);
+  return e;
 }
 
 int prefill_combine(const CombineArgs& a, void* stream) {
-  dim3 grid((a.D / 8 + 127) / 128, a.T);
-  combine_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  const dim3 grid((a.D / 8 + 127) / 128, a.T);
+  return launch_pdl(combine_kernel, grid, dim3(128), 0, static_cast<cudaStream_t>(stream), a);
 }
 
 }  // namespace moe
