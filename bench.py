@@ -612,7 +612,7 @@ def run_batched(args):
 def measure_batched(args, h, L, B, steps, warmup):
     """Batched decode: a batch of B tokens (default 32) through the L-layer
     decode stack per step, on the same weights as the decode workload.  From
-    10 tokens on, each layer takes the multi-token path (router GEMM,
+    5 tokens on, each layer takes the multi-token path (router GEMM,
     bucketing, grouped tensor-core GEMMs, combine), so each chosen expert's
     weights are read once for all the batch's rows routed to it; fewer tokens
     run as one single-token decode launch each (moe_forward_stack decides)."""
@@ -656,7 +656,7 @@ def measure_batched(args, h, L, B, steps, warmup):
     value = B / (ms / 1e3)
     hbm, bf16, src = peaks()
     gbs = touched / (ms / 1e3) / 1e9
-    multi = B >= 10  # moe_forward_stack's split between the two paths
+    multi = B >= 5  # moe_forward_stack's split between the two paths
     per_layer = 8 if B * shape.top_k <= 2048 else 10
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,

@@ -88,7 +88,8 @@ struct moe_handle {
     CUtensorMap rt;  // router weight as two fp16 parts, [2 Epad][D]
   };
   std::vector<LayerMaps> maps;
-  CUtensorMap bmap_gu[2], bmap_dn[2];  // activation operands: [0] routed, [1] shared
+  CUtensorMap bmap_gu[2][kNBox], bmap_dn[2][kNBox];  // activation operands: [0] routed,
+                                                    // [1] shared; one per tile height
   uint16_t* pf_xperm = nullptr;        // x16 rows in bucket order (routed gate/up operand)
   uint16_t* pf_rw = nullptr;           // router weights as fp16 parts, [L][2 Epad][D]
   int32_t* pf_hist = nullptr;          // bucketing counts / write bases
@@ -313,14 +314,14 @@ EncodeTiledFn encode_tiled() {
 
 // A byte tensor of `rank` 2 or 3: rows of `row_bytes` (pitch `row_bytes`),
 // `rows` rows, and for rank 3 `planes` planes `plane_bytes` apart.
-// fp16 rows [rows][cols] (pitch cols): box 64 columns x 256 rows, 128-byte
-// swizzle (the UMMA K-major operand layout).
+// fp16 rows [rows][cols] (pitch `pitch` columns, default cols): box 64
+// columns x box_rows rows, 128-byte swizzle (the UMMA K-major operand layout).
 bool make_act_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
-                  uint32_t box_rows = kUnitTokens) {
+                  uint32_t box_rows = kUnitTokens, uint64_t pitch = 0) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {(pitch ? pitch : cols) * 2};
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
@@ -672,12 +673,13 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     auto groups = [](int64_t tiles) { return (tiles + kTilesPerUnit - 1) / kTilesPerUnit; };
     const int64_t ngu = nt * groups(h->mt_gu_r) + stl * groups(h->mt_gu_s),
                   ndn = (nt + stl) * groups(h->mt_dn);
-    int64_t sizes[] = {Tm * d.D * 2,      Tm * 4,          Tm * 4,        Tm * 4,        part * 4,
+    const int64_t Dx = d.D + kGsumCols;  // x16 pitch: D columns, then the group sums
+    int64_t sizes[] = {Tm * Dx * 2,        Tm * 4,          Tm * 4,        Tm * 4,        part * 4,
                        L * Tm * K * 4,    L * Tm * K * 4,  Tm * K * 4,    E * 4,
                        (E + 1) * 4,       Tm * K * 4,      Tm * K * 4,    ngu * int64_t(sizeof(GemmUnit)),
                        ndn * int64_t(sizeof(GemmUnit)), 16, Tm * K * d.I * 2, Tm * d.S * 2,
                        Tm * K * d.D * 2,  Tm * d.D * 4,    Tm * d.D * 2,  Tm * d.D * 2,
-                       Tm * K * d.D * 2,  int64_t(bucket_blocks(int(Tm * K))) * 8 * E * 4};
+                       Tm * K * Dx * 2,   int64_t(bucket_blocks(int(Tm * K))) * 8 * E * 4};
     const int ns = sizeof(sizes) / sizeof(sizes[0]);
     int64_t offs[32];
     int64_t tot = 0;
@@ -712,12 +714,15 @@ moe_status moe_create(const moe_config* cfg, const moe_layer_weights* layers, mo
     h->pf_xs[1] = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
     h->pf_xperm = reinterpret_cast<uint16_t*>(h->pf + offs[i++]);
     h->pf_hist = reinterpret_cast<int32_t*>(h->pf + offs[i++]);
-    if (!make_act_map(&h->bmap_gu[0], h->pf_xperm, d.D, Tm * K) ||
-        !make_act_map(&h->bmap_gu[1], h->pf_x16, d.D, Tm) ||
-        !make_act_map(&h->bmap_dn[0], h->pf_hr, d.I, Tm * K) ||
-        !make_act_map(&h->bmap_dn[1], h->pf_hs, d.S, Tm) ||
-        !make_act_map(&h->bmap_rt, h->pf_x16, d.D, Tm, 128))
-      CREATE_FAIL(MOE_ERR_CUDA, "could not encode the prefill activation tensor maps");
+    bool mok = make_act_map(&h->bmap_rt, h->pf_x16, d.D, Tm, 128, Dx);
+    for (int b = 0; b < kNBox && mok; ++b) {
+      const uint32_t r = box_rows(b);
+      mok = make_act_map(&h->bmap_gu[0][b], h->pf_xperm, Dx, Tm * K, r) &&
+            make_act_map(&h->bmap_gu[1][b], h->pf_x16, Dx, Tm, r) &&
+            make_act_map(&h->bmap_dn[0][b], h->pf_hr, d.I, Tm * K, r) &&
+            make_act_map(&h->bmap_dn[1][b], h->pf_hs, d.S, Tm, r);
+    }
+    if (!mok) CREATE_FAIL(MOE_ERR_CUDA, "could not encode the prefill activation tensor maps");
     // Router weights for the tensor-core router GEMM: w = s q + b (fp32, one
     // rounding) split into fp16(w) and fp16(w - fp16(w)); rows E..Epad-1 zero.
     {
@@ -1002,14 +1007,15 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   gp.tm_code[1] = mp.gu_code[1];
   gp.tm_sb[0] = mp.gu_sb[0];
   gp.tm_sb[1] = mp.gu_sb[1];
-  e = gather_rows_launch(h->pf_x16, static_cast<int>(d.D), h->pf_perm, K, T * K, h->pf_xperm, s);
+  e = gather_rows_launch(h->pf_x16, static_cast<int>(d.D) + kGsumCols, h->pf_perm, K, T * K,
+                         h->pf_xperm, s);
   if (e) return fail(h, MOE_ERR_CUDA, "row gather: %s", cudaGetErrorString(cudaError_t(e)));
   gp.units = h->pf_units_gu;
   gp.n_units = h->pf_nunits;
   gp.mode = 0;
+  gp.gsum = 1;
   gp.K[0] = gp.K[1] = static_cast<int>(d.D);
-  gp.tm_b[0] = h->bmap_gu[0];
-  gp.tm_b[1] = h->bmap_gu[1];
+  std::memcpy(gp.tm_b, h->bmap_gu, sizeof gp.tm_b);
   gp.hout[0] = h->pf_hr;
   gp.hout[1] = h->pf_hs;
   gp.hld[0] = static_cast<int>(d.I);
@@ -1032,10 +1038,10 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   gp.units = h->pf_units_dn;
   gp.n_units = h->pf_nunits + 1;
   gp.mode = 1;
+  gp.gsum = 0;
   gp.K[0] = static_cast<int>(d.I);
   gp.K[1] = static_cast<int>(d.S);
-  gp.tm_b[0] = h->bmap_dn[0];
-  gp.tm_b[1] = h->bmap_dn[1];
+  std::memcpy(gp.tm_b, h->bmap_dn, sizeof gp.tm_b);
   gp.eout = h->pf_e;
   gp.sout = h->pf_s;
   e = gemm_tc_launch(gp, h->num_sms, s);
@@ -1188,10 +1194,12 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
 }
 
 // Fewer tokens than this run the stack as one single-token decode launch per
-// token: on the 30-layer stack at 8 tokens that is 4.8 ms against 5.4 ms for
-// the multi-token path, whose per-layer fixed cost (eight launches, MMAs at
-// their narrowest width) only pays from about 10 tokens on.
-constexpr int kStackBatchMin = 10;
+// token.  Measured on the 30-layer Gemma-shape stack (single-token launches
+// at 0.60 ms a token against the multi-token path): 4 tokens 2.40 against
+// 2.60 ms, 5 tokens 3.00 against 2.78 ms, 8 tokens 4.81 against 3.57 ms.
+// Below 5 tokens the multi-token path's per-layer fixed cost (eight
+// launches) outweighs reading each chosen expert once for all its rows.
+constexpr int kStackBatchMin = 5;
 
 moe_status moe_forward_stack(moe_handle* h, const void* x, int T, void* y, int n_layers,
                              void* stream) {

@@ -68,7 +68,7 @@ constexpr int kAccSet = kTU * kAccCols;            // one unit's accumulators
 constexpr int kACol0 = 2 * kAccSet;                // A stages after the two sets
 constexpr int kAStage = kTU * 32;                  // per tile 32 columns (64 fp16 of K)
 constexpr int kNA = (kTmemCols - kACol0) / kAStage;
-constexpr int kNP = kTU == 1 ? 3 : 4, kNB = kTU == 1 ? 6 : 4;
+constexpr int kNP = kTU == 1 ? 3 : 4, kNB = kTU == 1 ? 5 : 4;
 static_assert(kNA >= 2 && kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
 constexpr int kDqWarps = 8, kEpiWarps = 8;
 constexpr int kGemmThreads = (3 + kDqWarps + kEpiWarps) * 32;  // + the activation loader warp
@@ -86,7 +86,14 @@ struct Bars {
 
 constexpr int kMetaBytes = 2 * kUnitTokens * 4;  // per-column factors
 constexpr int kStageBytes = 2048;                // per epilogue warp: output transpose
+// 64 b per row and group of the gate/up unit in flight, kept by the
+// dequantisation threads for the group-sum K block (144-byte rows: the
+// 16-byte loads stay aligned and the 2-byte stores of a warp's 32 rows spread
+// over 8 banks).
+constexpr int kGsumPitch = 144;
+constexpr int kGsumBytes = 128 * kGsumPitch;
 constexpr int kSmemBytes = kNP * kPBytes + kNB * kBBytes + kMetaBytes + kEpiWarps * kStageBytes +
+                           kGsumBytes +
                            1024 /*Bars*/ + 1024 /*alignment slack*/;
 
 // The tanh form of GELU, 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3),
@@ -180,12 +187,15 @@ __device__ void role_tma_b(const GemmParams& p, uint8_t* B, Bars* bars, int nU) 
   uint32_t bc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x) {
     const GemmUnit un = p.units[u];
-    const int nkb = p.K[un.kind] / 64;
-    const void* tb = &p.tm_b[un.kind];
+    const int nkb = p.K[un.kind] / 64 + p.gsum;  // the group sums follow the K columns
+    int box = 0;  // the lowest tile that holds the MMA's rows
+    while (box + 1 < kNBox && box_rows(box) < unit_nmma(un.n)) ++box;
+    const void* tb = &p.tm_b[un.kind][box];
+    const uint32_t bytes = box_rows(box) * 128;
     for (int kb = 0; kb < nkb; ++kb, ++bc) {
       const int bs = bc % kNB;
       if (!wait_bar(&bars->b_empty[bs], ((bc / kNB) & 1) ^ 1, p, bars)) return;
-      mbar_arrive_expect_tx(&bars->b_full[bs], kBBytes);
+      mbar_arrive_expect_tx(&bars->b_full[bs], bytes);
       tma_load_2d(B + bs * kBBytes, tb, kb * 64, un.row0, &bars->b_full[bs]);
     }
   }
@@ -201,11 +211,18 @@ __device__ void role_tma_b(const GemmParams& p, uint8_t* B, Bars* bars, int nU) 
 // waits, shared-memory loads, the tensor-memory store and its completion),
 // and a pair overlaps those of two blocks and halves the synchronisation per
 // block.
+// One half K block (32 columns) of this thread's row as fp16 A values, from its
+// packed codes and the group's scale/bias word.  kGsum: A = fp16(s q), as
+// fp16((1024 + q) s - 1024 s) in one fused multiply-add (exact before its one
+// rounding); otherwise A = fp16(s q + b) (q = (1024 + q) - 1024 exactly, then
+// one fused multiply-add).
+template <bool kGsum>
 __device__ __forceinline__ void dequant32(const uint8_t* codes, const uint32_t* sbw, int row,
                                           int half, int sb, __half2 k1024, uint32_t (&o)[16]) {
   const uint32_t word = sbw[row * 4 + sb];
   const __half2 s2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word & 0xffffu)));
-  const __half2 b2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word >> 16)));
+  const __half2 b2 = kGsum ? __hmul2(s2, __hneg2(k1024))  // -1024 s, exact
+                           : __half2half2(__ushort_as_half(static_cast<unsigned short>(word >> 16)));
   // packed chunk c (32 columns) of this row, stored at chunk c ^ (row & 7)
   const int c = 2 * sb + half;
   const uint4 wq = *reinterpret_cast<const uint4*>(codes + row * 128 + ((c ^ (row & 7)) << 4));
@@ -220,14 +237,29 @@ __device__ __forceinline__ void dequant32(const uint8_t* codes, const uint32_t* 
                             __byte_perm(hi, 0x64646464u, 0x5140), __byte_perm(hi, 0x64646464u, 0x7362)};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&mm[i]), k1024);
-      const __half2 v = __hfma2(q, s2, b2);
+      const __half2 m = *reinterpret_cast<const __half2*>(&mm[i]);
+      const __half2 v = kGsum ? __hfma2(m, s2, b2) : __hfma2(__hsub2(m, k1024), s2, b2);
       o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
     }
   }
 }
 
-__device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, int nU) {
+// 64 b of group g (K block g) into this thread's row of the group-sum
+// scratch, if g is in this thread's half of the K range.
+__device__ __forceinline__ void keep_bias(const uint32_t* sbw, uint8_t* gsb, int row, int half,
+                                          int g, int sb) {
+  if ((g >> 5) != half) return;
+  const __half b = __ushort_as_half(static_cast<unsigned short>(sbw[row * 4 + sb] >> 16));
+  *reinterpret_cast<__half*>(gsb + row * kGsumPitch + 2 * g) = __hmul(b, __float2half(64.f));
+}
+
+// With kGsum (gate/up) each thread also keeps 64 b of the groups of its half
+// of the K range (groups 32 half .. 32 half + 31) in its row of `gsb`, and after
+// the unit's K blocks stores them as the group-sum block's A columns (zero
+// past the last group); the activations' group sums form that block's B.
+template <bool kGsum>
+__device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, int nU,
+                             uint8_t* gsb) {
   static_assert(kTU == 1, "the dequantisation warps fill one weight tile per unit");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = (w - 2) >> 2;       // 32-column half of the row
@@ -256,8 +288,10 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
           if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
           if (!wait_bar(&bars->a_empty[r1.s], r1.ph ^ 1u, p, bars)) return;
           uint32_t o0[16], o1[16];
-          dequant32(codes, sbw, row, half, sb, k1024, o0);
-          dequant32(codes, sbw, row, half, sb + 1, k1024, o1);
+          dequant32<kGsum>(codes, sbw, row, half, sb, k1024, o0);
+          dequant32<kGsum>(codes, sbw, row, half, sb + 1, k1024, o1);
+          if (kGsum) keep_bias(sbw, gsb, row, half, 4 * sp + sb, sb);
+          if (kGsum) keep_bias(sbw, gsb, row, half, 4 * sp + sb + 1, sb + 1);
           tmem_st16(tbase + ra.s * kAStage, o0);
           tmem_st16(tbase + r1.s * kAStage, o1);
           tmem_st_wait();
@@ -273,7 +307,8 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
         } else {
           if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
           uint32_t o0[16];
-          dequant32(codes, sbw, row, half, sb, k1024, o0);
+          dequant32<kGsum>(codes, sbw, row, half, sb, k1024, o0);
+          if (kGsum) keep_bias(sbw, gsb, row, half, 4 * sp + sb, sb);
           tmem_st16(tbase + ra.s * kAStage, o0);
           tmem_st_wait();
           tc_fence_before();
@@ -285,6 +320,32 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_empty[st]);
+    }
+    if (kGsum) {  // the group-sum block: A columns 64 b_g of this half's groups
+      const int ng = K / 64;
+      if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
+      const uint4* src = reinterpret_cast<const uint4*>(gsb + row * kGsumPitch + half * 64);
+      uint32_t o[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = src[i];
+        o[4 * i] = v.x;
+        o[4 * i + 1] = v.y;
+        o[4 * i + 2] = v.z;
+        o[4 * i + 3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {  // column pair i holds groups 32 half + 2i, + 2i + 1
+        const int g = 32 * half + 2 * i;
+        if (g >= ng) o[i] = 0u;
+        else if (g + 1 >= ng) o[i] &= 0xffffu;
+      }
+      tmem_st16(tbase + ra.s * kAStage, o);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->a_full[ra.s]);
+      ra.next<kNA>();
     }
   }
 }
@@ -330,7 +391,7 @@ __device__ void role_mma(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
   uint32_t uc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x, ++uc) {
     const GemmUnit un = p.units[u];
-    const int nkb = p.K[un.kind] / 64;
+    const int nkb = p.K[un.kind] / 64 + p.gsum;  // + the group-sum block
     const uint32_t acc = tmem + (uc & 1) * kAccSet;  // this unit's accumulator set
     // (an injected stall waits for the phase before, which never completes)
     const uint32_t par = ((uc >> 1) & 1) ^ (p.stall ? 0u : 1u);
@@ -518,7 +579,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   uint8_t* B = P + kNP * kPBytes;
   float* meta = reinterpret_cast<float*>(B + kNB * kBBytes);
   uint8_t* stage = B + kNB * kBBytes + kMetaBytes;
-  Bars* bars = reinterpret_cast<Bars*>(stage + kEpiWarps * kStageBytes);
+  uint8_t* gsb = stage + kEpiWarps * kStageBytes;
+  Bars* bars = reinterpret_cast<Bars*>(gsb + kGsumBytes);
   const int w = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNP; ++i) {
@@ -557,7 +619,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   } else if (w == 1) {
     role_mma(p, B, bars, nU);
   } else if (w < kEpiWarp0) {
-    role_dequant(p, P, bars, nU);
+    if (p.gsum) role_dequant<true>(p, P, bars, nU, gsb);
+    else role_dequant<false>(p, P, bars, nU, gsb);
   } else {
     role_epilogue(p, bars, meta, stage, nU);
   }

@@ -105,6 +105,15 @@ struct DecodeParams {
 // GELU epilogue, then down), and a gather combine.
 
 constexpr int kUnitTokens = 192;   // max B rows (tokens) of one GEMM work unit
+// Heights of the activation tiles the GEMM loads (one tensor map each): a unit
+// of n rows loads the smallest that holds its MMA width (n rounded up to 16),
+// so a unit of a few tokens does not fill shared memory with 192 rows.
+constexpr int kNBox = 7;
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int box_rows(int i) { return i == 0 ? 16 : 32 * i; }  // 16, 32 .. 192
+static_assert(box_rows(kNBox - 1) == kUnitTokens, "the highest tile holds a whole unit");
 constexpr int kTilesPerUnit = 1;   // 128-row weight tiles per GEMM work unit
 constexpr int kMaxPrefillExperts = 256;
 
@@ -131,6 +140,14 @@ int router_tc_splits(int T, int E, int D, int num_sms);
 int router_tc_launch(const CUtensorMap& wmap, const CUtensorMap& xmap, int T, int E, int D,
                      int nsplit, float* partials, uint32_t* status, uint64_t timeout_ns, void* stream);
 
+// x16, the fp16 token rows of the multi-token path, has a row pitch of
+// D + kGsumCols: D columns of f_t x, then the token's 64-column group sums
+// X_g = sum of the group's fp16 values, held as fp16(X_g / 64) (exact
+// scaling; the sum of 64 values of up to 2^15 stays in range), for
+// g < D / 64, and zeros after them.  The gate/up GEMM applies the weights'
+// per-group biases b_g through these sums: sum_g (64 b_g) (X_g / 64).
+constexpr int kGsumCols = 64;
+
 struct RouteArgs {
   const uint16_t* x;  // bf16 [T][D]
   int T, D, E, K;
@@ -138,10 +155,10 @@ struct RouteArgs {
   float rms_eps;
   const CUtensorMap* wmap;    // router weight as fp16 parts: rows [0, Epad) = fp16(w),
                               // rows [Epad, 2 Epad) = fp16(w - fp16(w)), [2 Epad][D]
-  const CUtensorMap* xmap;    // x16 [T][D], 64 x 128 boxes
+  const CUtensorMap* xmap;    // x16 [T][D] (pitch D + kGsumCols), 64 x 128 boxes
   const float* logit_bias;    // [E] or nullptr
   const int32_t* forced;      // device [T][K] or nullptr
-  uint16_t* x16;              // fp16 [T][D] out: x * f_t
+  uint16_t* x16;              // fp16 [T][D + kGsumCols] out: x * f_t, then the group sums
   float* sigma;               // [T] out: (r_t / f_t), the scale of dot products with x16
   float* rscale;              // [T] out: r_t (pre-norm factor, 1 without)
   float* hscale;              // [T] out: power-of-two scale of the fp16 intermediate h
@@ -185,11 +202,14 @@ int prefill_combine(const CombineArgs& a, void* stream);
 struct GemmParams {
   CUtensorMap tm_code[2];  // 4-bit codes: box 128 B x 128 rows, 128-byte swizzle
   CUtensorMap tm_sb[2];    // scale/bias words: box 16 B x 128 rows
-  CUtensorMap tm_b[2];     // activation rows (fp16): box 64 x 256, 128-byte swizzle
+  CUtensorMap tm_b[2][kNBox];  // activation rows (fp16): box 64 x box_rows(i), 128-byte swizzle
   const GemmUnit* units;
   const int32_t* n_units;  // device: number of units
   int mode;                // 0: gate/up (+ GELU epilogue), 1: down
   int K[2];                // reduction length (D for gate/up; I or S for down)
+  int gsum;                // 1: the weights' biases enter through the activations' group
+                           // sums, one more K block after the K columns (gate/up; the A
+                           // operand is then fp16(s q)), 0: A = fp16(s q + b)
   const int32_t* perm;     // bucket position -> assignment
   int topk;
   const float* sigma;      // per-token scale of dot products with x16 (gate/up)
@@ -207,7 +227,7 @@ struct GemmParams {
 };
 int gemm_tc_smem_bytes();
 int gemm_tc_launch(const GemmParams& p, int grid, void* stream);
-// out[pos] = x16[perm[pos] / topk] for pos < rows (fp16 rows of D).
+// out[pos] = x16[perm[pos] / topk] for pos < rows (fp16 rows of `D` columns).
 int gather_rows_launch(const void* x16, int D, const int32_t* perm, int topk, int rows, void* out,
                        void* stream);
 

@@ -62,7 +62,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 // hscale = 2^(-2e), e = ceil(log2(max|u|)): the gated intermediate h grows
 // like |u|^2, so it is held as fp16(h * hscale), inside fp16's normal range
 // for tiny and huge inputs alike, and the down output is divided by hscale
-// again (exact powers of two).
+// again (exact powers of two).  The row of x16 ends with its group sums
+// (internal.h, kGsumCols): the sums of the fp16 values actually stored, in a
+// fixed order.
 constexpr int kPrepV = 12;  // D <= 8 * 32 * kPrepV
 
 __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restrict__ x, int T, int D,
@@ -96,8 +98,10 @@ __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restric
   int e = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xffu) - 127 : 14;
   e = max(-100, min(100, e));
   const float f = ldexpf(1.f, 14 - e);
-  uint4* out = reinterpret_cast<uint4*>(x16 + static_cast<size_t>(t) * D);
+  const size_t pitch = static_cast<size_t>(D) + kGsumCols;
+  uint4* out = reinterpret_cast<uint4*>(x16 + static_cast<size_t>(t) * pitch);
   float ss = 0.f;
+  float part[kPrepV] = {};  // sum of the lane's 8 stored values per load
 #pragma unroll
   for (int k = 0; k < kPrepV; ++k) {
     const int i = lane + 32 * k;
@@ -110,9 +114,22 @@ __global__ void __launch_bounds__(256) tok_prep_kernel(const uint16_t* __restric
       ss = fmaf(a, a, fmaf(b, b, ss));
       const __half2 h = __floats2half2_rn(a, b);
       o[j] = *reinterpret_cast<const uint32_t*>(&h);
+      part[k] += __low2float(h) + __high2float(h);
     }
     out[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  // group g (64 columns) = loads 8g .. 8g+7 = lanes 8j .. 8j+7 of load k,
+  // g = 4k + j; D is a multiple of 128, so a group is wholly in or out
+  __half* gs = x16 + static_cast<size_t>(t) * pitch + D;
+#pragma unroll
+  for (int k = 0; k < kPrepV; ++k) {
+    float v = (lane + 32 * k < nv) ? part[k] : 0.f;
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    if ((lane & 7) == 0 && lane + 32 * k < nv) gs[4 * k + (lane >> 3)] = __float2half_rn(v * 0.015625f);
+  }
+  for (int g = D / 64 + lane; g < kGsumCols; g += 32) gs[g] = __float2half_rn(0.f);
   ss = warp_sum(ss);
   if (lane == 0) {
     // fp32 arithmetic: B300's fp64 pipe is narrow, and eight warps of a block

@@ -213,17 +213,18 @@ moe_status moe_layer_forward(moe_handle* h, int layer, const void* x, int T, voi
                              const int32_t* forced_ids, void* stream, moe_layer_stats* stats);
 
 /*
- * moe_forward_stack — layers [0, n_layers) back to back (T < 10: one
- * persistent kernel per token for the whole stack; T >= 10: the multi-token
+ * moe_forward_stack — layers [0, n_layers) back to back (T < 5: one
+ * persistent kernel per token for the whole stack; T >= 5: the multi-token
  * path layer by layer over all T tokens, which reads each chosen expert once
  * for all its rows), each reading the
  * RMS-normalised residual stream and adding its output to it:
  * x_{l+1} = bf16(x_l + moe_l(x_l / sqrt(mean(x_l^2) + 1e-6))); y = x_{n_layers}
  * (the flags MOE_FWD_RESIDUAL | MOE_FWD_PRENORM on every layer).
  * Resident mode only.  x, y: device [T][D] bf16, y may not alias x.
- * The split at 10 tokens is measured: on the 30-layer Gemma-shape stack, 8
- * tokens take 4.8 ms as 8 single-token launches and 5.4 ms through the
- * multi-token path, and 32 tokens 19 ms against 8.1 ms.
+ * The split at 5 tokens is measured: on the 30-layer Gemma-shape stack, 4
+ * tokens take 2.40 ms as 4 single-token launches and 2.60 ms through the
+ * multi-token path, 5 tokens 3.00 against 2.78 ms, 8 tokens 4.81 against
+ * 3.57 ms and 32 tokens 19 ms against 5.9 ms.
  */
 moe_status moe_forward_stack(moe_handle* h, const void* x, int T, void* y, int n_layers,
                              void* stream);

@@ -200,30 +200,30 @@ def test_tiny_prefill_stack_matches_decode_stack(moe):
 
 
 def test_tiny_stack_small_batches_run_as_single_token_launches(moe):
-    """moe_forward_stack runs fewer than 10 tokens as one single-token decode
+    """moe_forward_stack runs fewer than 5 tokens as one single-token decode
     launch each: the batch's outputs, ids and weights are bit-identical to
-    running each token alone.  From 10 tokens on the multi-token path runs
+    running each token alone.  From 5 tokens on the multi-token path runs
     (its buckets exist afterwards)."""
     sh = synth.MoEShape("tiny4", 256, 16, 128, 2, 256, 64, 4)
     layers = [synth.make_layer(sh, "tiny", l) for l in range(4)]
-    h = moe.moe_create(sh, layers, max_tokens=10)
-    x = synth.make_tokens(sh, "tiny", 10, index=9).cuda()
-    yb = torch.empty_like(x[:8])
-    moe.moe_forward_stack(h, x[:8], yb, 4)
-    ids_b, w_b = moe.moe_stack_ids(h, 4, 8)
+    h = moe.moe_create(sh, layers, max_tokens=5)
+    x = synth.make_tokens(sh, "tiny", 5, index=9).cuda()
+    yb = torch.empty_like(x[:4])
+    moe.moe_forward_stack(h, x[:4], yb, 4)
+    ids_b, w_b = moe.moe_stack_ids(h, 4, 4)
     with pytest.raises(moe.MoEError) as ei:
-        moe.moe_last_buckets(h, 8)
+        moe.moe_last_buckets(h, 4)
     assert ei.value.status == -6
-    for t in range(8):
+    for t in range(4):
         yt = torch.empty_like(x[:1])
         moe.moe_forward_stack(h, x[t:t + 1], yt, 4)
         ids_t, w_t = moe.moe_stack_ids(h, 4, 1)
         assert torch.equal(yt, yb[t:t + 1])
         assert np.array_equal(ids_t[:, 0], ids_b[:, t]) and np.array_equal(w_t[:, 0], w_b[:, t])
-    y10 = torch.empty_like(x)
-    moe.moe_forward_stack(h, x, y10, 4)
-    counts, _, _ = moe.moe_last_buckets(h, 10)
-    assert counts.sum() == 10 * sh.top_k
+    y5 = torch.empty_like(x)
+    moe.moe_forward_stack(h, x, y5, 4)
+    counts, _, _ = moe.moe_last_buckets(h, 5)
+    assert counts.sum() == 5 * sh.top_k
 
 
 # ---------------------------------------------------------------- full shape
