@@ -1025,7 +1025,7 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
     gp.timeout_ns = uint64_t(h->inj.gemm_stall_ms) * 1000000ull;
     h->inj.gemm_stall_ms = 0;
   }
-  e = gemm_tc_launch(gp, h->num_sms, s);
+  e = gemm_tc_launch(gp, h->num_sms, T, s);
   gp.stall = 0;
   gp.timeout_ns = h->base.timeout_ns;
   if (e) return fail(h, MOE_ERR_CUDA, "gate/up GEMM launch: %s", cudaGetErrorString(cudaError_t(e)));
@@ -1044,7 +1044,7 @@ static moe_status prefill_layer(moe_handle* h, int layer, const void* x, int T, 
   std::memcpy(gp.tm_b, h->bmap_dn, sizeof gp.tm_b);
   gp.eout = h->pf_e;
   gp.sout = h->pf_s;
-  e = gemm_tc_launch(gp, h->num_sms, s);
+  e = gemm_tc_launch(gp, h->num_sms, T, s);
   if (e) return fail(h, MOE_ERR_CUDA, "down GEMM launch: %s", cudaGetErrorString(cudaError_t(e)));
   if (ev) CUDA_TRY(h, cudaEventRecord(ev[4], s));
   CombineArgs ca{};

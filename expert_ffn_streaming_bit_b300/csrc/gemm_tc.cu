@@ -56,50 +56,62 @@ namespace moe {
 
 namespace {
 
-constexpr int kTU = kTilesPerUnit;                 // weight tiles per unit (1 or 2)
+constexpr int kTU = kTilesPerUnit;                 // weight tiles per unit
 constexpr int kPCodeBytes = 128 * 128;             // 128 rows x 256 columns of 4-bit codes
 constexpr int kPSbBytes = 128 * 16;                // 128 rows x 4 scale/bias words
 constexpr int kPTile = kPCodeBytes + kPSbBytes;    // 18 KB per weight tile
 constexpr int kPBytes = kTU * kPTile;              // the unit's weight tiles per P stage
-constexpr int kBBytes = kUnitTokens * 128;         // tokens x 64 fp16
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = kUnitTokens;              // per tile
-constexpr int kAccSet = kTU * kAccCols;            // one unit's accumulators
-constexpr int kACol0 = 2 * kAccSet;                // A stages after the two sets
 constexpr int kAStage = kTU * 32;                  // per tile 32 columns (64 fp16 of K)
-constexpr int kNA = (kTmemCols - kACol0) / kAStage;
-constexpr int kNP = kTU == 1 ? 3 : 4, kNB = kTU == 1 ? 5 : 4;
-static_assert(kNA >= 2 && kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
 constexpr int kDqWarps = 8, kEpiWarps = 8;
 constexpr int kGemmThreads = (3 + kDqWarps + kEpiWarps) * 32;  // + the activation loader warp
 constexpr int kBLoadWarp = 2 + kDqWarps + kEpiWarps;
 constexpr int kEpiWarp0 = 2 + kDqWarps;
-
-struct Bars {
-  uint64_t p_full[kNP], p_empty[kNP];
-  uint64_t a_full[kNA], a_empty[kNA];
-  uint64_t b_full[kNB], b_empty[kNB];
-  uint64_t acc_full[2], acc_empty[2];
-  uint32_t tmem_base;
-  int abort;
-};
-
-constexpr int kMetaBytes = 2 * kUnitTokens * 4;  // per-column factors
-constexpr int kStageBytes = 2048;                // per epilogue warp: output transpose
+constexpr int kStageBytes = 2048;                  // per epilogue warp: output transpose
 // 64 b per row and group of the gate/up unit in flight, kept by the
 // dequantisation threads for the group-sum K block (144-byte rows: the
 // 16-byte loads stay aligned and the 2-byte stores of a warp's 32 rows spread
 // over 8 banks).
 constexpr int kGsumPitch = 144;
 constexpr int kGsumBytes = 128 * kGsumPitch;
-constexpr int kSmemBytes = kNP * kPBytes + kNB * kBBytes + kMetaBytes + kEpiWarps * kStageBytes +
-                           kGsumBytes +
-                           1024 /*Bars*/ + 1024 /*alignment slack*/;
 
-// The tanh form of GELU, 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3),
-// evaluated through the identity 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)): one
-// exponential and one division, and no cancellation for large negative u
-// (exp overflows to inf and the quotient goes to 0, the function's limit).
+// The kernel's plan for units of up to kUT activation rows.  Tensor memory
+// holds two accumulator sets of kUT columns and A stages in the rest; shared
+// memory holds the P (weight), B (activation) and epilogue buffers.  The wide
+// plan (kUT = 192) serves batches of more than 32 tokens; the narrow one
+// (kUT = 32), for at most 32 tokens, turns the columns and bytes that wide
+// units need into deeper rings, which hide the latency of the per-block
+// hand-offs when a block carries little MMA work.
+template <int kUT>
+struct Tile {
+  static constexpr int kUnit = kUT;
+  static constexpr int kBBytes = kUT * 128;          // tokens x 64 fp16
+  static constexpr int kAccCols = kUT;               // per tile
+  static constexpr int kAccSet = kTU * kAccCols;     // one unit's accumulators
+  static constexpr int kACol0 = 2 * kAccSet;         // A stages after the two sets
+  static constexpr int kNA = (kTmemCols - kACol0) / kAStage > 14 ? 14 : (kTmemCols - kACol0) / kAStage;
+  static constexpr int kNP = kUT > 64 ? 3 : 6;
+  static constexpr int kNB = kUT > 64 ? 5 : 16;
+  static_assert(kNA >= 2 && kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
+  struct Bars {
+    uint64_t p_full[kNP], p_empty[kNP];
+    uint64_t a_full[kNA], a_empty[kNA];
+    uint64_t b_full[kNB], b_empty[kNB];
+    uint64_t acc_full[2], acc_empty[2];
+    uint32_t tmem_base;
+    int abort;
+  };
+  static constexpr int kMetaBytes = 2 * kUT * 4;     // per-column factors
+  static constexpr int kSmemBytes = kNP * kPBytes + kNB * kBBytes + kMetaBytes +
+                                    kEpiWarps * kStageBytes + kGsumBytes +
+                                    1024 /*Bars*/ + 1024 /*alignment slack*/;
+  static_assert(sizeof(Bars) <= 1024, "barrier block");
+};
+using WideTile = Tile<kUnitTokens>;
+using NarrowTile = Tile<32>;
+static_assert(WideTile::kSmemBytes <= 227 * 1024 && NarrowTile::kSmemBytes <= 227 * 1024,
+              "shared memory plan");
+
 __device__ __forceinline__ float gelu_tanh(float x) {
   const float c2 = 1.5957691216057308f;  // 2 sqrt(2/pi)
   const float u2 = c2 * fmaf(0.044715f * x, x * x, x);
@@ -122,8 +134,9 @@ __device__ __forceinline__ void load16(const float* src, float (&d)[16]) {
 
 // Bounded mbarrier wait shared by all roles: on expiry record a timeout and
 // make every role stop.
+template <class BarsT>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const GemmParams& p,
-                                         Bars* bars) {
+                                         BarsT* bars) {
   if (mbar_wait(bar, parity, p.timeout_ns, &bars->abort)) return true;
   if (!bars->abort) atomicCAS(p.status, DEV_OK, DEV_TIMEOUT);
   bars->abort = 1;
@@ -152,7 +165,8 @@ struct RingPos {
 // slices (P ring, one stage per 256 columns) and the activation tiles (B
 // ring, one stage per 64-column block) are issued independently, each as far
 // ahead as its ring allows.
-__device__ void role_tma_p(const GemmParams& p, uint8_t* P, Bars* bars, int nU) {
+template <class T>
+__device__ void role_tma_p(const GemmParams& p, uint8_t* P, typename T::Bars* bars, int nU) {
   uint32_t pc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x) {
     const GemmUnit un = p.units[u];
@@ -161,8 +175,8 @@ __device__ void role_tma_p(const GemmParams& p, uint8_t* P, Bars* bars, int nU) 
     const void* tc = &p.tm_code[un.kind];
     const void* ts = &p.tm_sb[un.kind];
     for (int sp = 0; sp < np; ++sp, ++pc) {
-      const int st = pc % kNP;
-      if (!wait_bar(&bars->p_empty[st], ((pc / kNP) & 1) ^ 1, p, bars)) return;
+      const int st = pc % T::kNP;
+      if (!wait_bar(&bars->p_empty[st], ((pc / T::kNP) & 1) ^ 1, p, bars)) return;
       uint8_t* dst = P + st * kPBytes;
       mbar_arrive_expect_tx(&bars->p_full[st], un.nmt * kPTile);
       const int xc = sp * 128, xs = K / 2 + sp * 16;
@@ -179,28 +193,34 @@ __device__ void role_tma_p(const GemmParams& p, uint8_t* P, Bars* bars, int nU) 
     }
   }
   // drain: copies still in flight must land before the CTA exits
-  for (uint32_t q = pc > kNP ? pc - kNP : 0; q < pc; ++q)
-    mbar_wait(&bars->p_full[q % kNP], (q / kNP) & 1, p.timeout_ns, nullptr);
+  for (uint32_t q = pc > T::kNP ? pc - T::kNP : 0; q < pc; ++q)
+    mbar_wait(&bars->p_full[q % T::kNP], (q / T::kNP) & 1, p.timeout_ns, nullptr);
 }
 
-__device__ void role_tma_b(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
+template <class T>
+__device__ void role_tma_b(const GemmParams& p, uint8_t* B, typename T::Bars* bars, int nU) {
   uint32_t bc = 0;
   for (int u = blockIdx.x; u < nU; u += gridDim.x) {
     const GemmUnit un = p.units[u];
     const int nkb = p.K[un.kind] / 64 + p.gsum;  // the group sums follow the K columns
+    if (unit_nmma(un.n) > T::kUnit) {  // wider than this plan's stages (never launched so)
+      if (!bars->abort) atomicCAS(p.status, DEV_OK, DEV_BAD_ID);
+      bars->abort = 1;
+      break;
+    }
     int box = 0;  // the lowest tile that holds the MMA's rows
     while (box + 1 < kNBox && box_rows(box) < unit_nmma(un.n)) ++box;
     const void* tb = &p.tm_b[un.kind][box];
     const uint32_t bytes = box_rows(box) * 128;
     for (int kb = 0; kb < nkb; ++kb, ++bc) {
-      const int bs = bc % kNB;
-      if (!wait_bar(&bars->b_empty[bs], ((bc / kNB) & 1) ^ 1, p, bars)) return;
+      const int bs = bc % T::kNB;
+      if (!wait_bar(&bars->b_empty[bs], ((bc / T::kNB) & 1) ^ 1, p, bars)) return;
       mbar_arrive_expect_tx(&bars->b_full[bs], bytes);
-      tma_load_2d(B + bs * kBBytes, tb, kb * 64, un.row0, &bars->b_full[bs]);
+      tma_load_2d(B + bs * T::kBBytes, tb, kb * 64, un.row0, &bars->b_full[bs]);
     }
   }
-  for (uint32_t q = bc > kNB ? bc - kNB : 0; q < bc; ++q)
-    mbar_wait(&bars->b_full[q % kNB], (q / kNB) & 1, p.timeout_ns, nullptr);
+  for (uint32_t q = bc > T::kNB ? bc - T::kNB : 0; q < bc; ++q)
+    mbar_wait(&bars->b_full[q % T::kNB], (q / T::kNB) & 1, p.timeout_ns, nullptr);
 }
 
 // Dequantisation (8 warps): the two warps of tensor-memory lane quarter w%4
@@ -257,8 +277,8 @@ __device__ __forceinline__ void keep_bias(const uint32_t* sbw, uint8_t* gsb, int
 // of the K range (groups 32 half .. 32 half + 31) in its row of `gsb`, and after
 // the unit's K blocks stores them as the group-sum block's A columns (zero
 // past the last group); the activations' group sums form that block's B.
-template <bool kGsum>
-__device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, int nU,
+template <class T, bool kGsum>
+__device__ void role_dequant(const GemmParams& p, const uint8_t* P, typename T::Bars* bars, int nU,
                              uint8_t* gsb) {
   static_assert(kTU == 1, "the dequantisation warps fill one weight tile per unit");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -266,7 +286,7 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
   const int qd = w & 3;                // tensor-memory lane quarter
   const int row = 32 * qd + lane;      // row of the weight tile
   const uint32_t tbase =
-      bars->tmem_base + (static_cast<uint32_t>(32 * qd) << 16) + kACol0 + half * 16;
+      bars->tmem_base + (static_cast<uint32_t>(32 * qd) << 16) + T::kACol0 + half * 16;
   const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
   RingPos ra;
   uint32_t pc = 0;
@@ -276,15 +296,15 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
     const int nkb = K / 64;
     const int np = (K + 255) / 256;
     for (int sp = 0; sp < np; ++sp, ++pc) {
-      const int st = pc % kNP;
-      if (!wait_bar(&bars->p_full[st], (pc / kNP) & 1, p, bars)) return;
+      const int st = pc % T::kNP;
+      if (!wait_bar(&bars->p_full[st], (pc / T::kNP) & 1, p, bars)) return;
       const int nsub = min(4, nkb - 4 * sp);
       const uint8_t* codes = P + st * kPBytes;
       const uint32_t* sbw = reinterpret_cast<const uint32_t*>(codes + kPCodeBytes);
       for (int sb = 0; sb < nsub;) {
         if (sb + 1 < nsub) {
           RingPos r1 = ra;
-          r1.next<kNA>();
+          r1.next<T::kNA>();
           if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
           if (!wait_bar(&bars->a_empty[r1.s], r1.ph ^ 1u, p, bars)) return;
           uint32_t o0[16], o1[16];
@@ -302,7 +322,7 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
             mbar_arrive(&bars->a_full[r1.s]);
           }
           ra = r1;
-          ra.next<kNA>();
+          ra.next<T::kNA>();
           sb += 2;
         } else {
           if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
@@ -314,7 +334,7 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->a_full[ra.s]);
-          ra.next<kNA>();
+          ra.next<T::kNA>();
           sb += 1;
         }
       }
@@ -345,7 +365,7 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->a_full[ra.s]);
-      ra.next<kNA>();
+      ra.next<T::kNA>();
     }
   }
 }
@@ -358,32 +378,39 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, Bars* bars, 
 // by increment: the warp shares its issue slots with dequantisation and
 // epilogue warps, so every instruction it saves per K block keeps the tensor
 // pipe fed.
+template <class BarsT>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
-                                          Bars* bars) {
+                                          BarsT* bars) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, p, bars));
 }
 
 
-template <int NMMA>
-__device__ __forceinline__ bool mma_unit(const GemmParams& p, Bars* bars, uint32_t acc,
+template <class T, int NMMA>
+__device__ __forceinline__ bool mma_unit(const GemmParams& p, typename T::Bars* bars, uint32_t acc,
                                          uint32_t a_base, uint64_t bdesc0, int nkb, RingPos& ra,
                                          RingPos& rb) {
   constexpr uint32_t idesc = tc_idesc_f16(128, NMMA);
   for (int kb = 0; kb < nkb; ++kb) {
-    if (!warp_wait(&bars->a_full[ra.s], ra.ph, p, bars)) return false;
-    if (!warp_wait(&bars->b_full[rb.s], rb.ph, p, bars)) return false;
+    // both stages are usually ready: probe them together, and take the
+    // bounded waits only when one is not
+    if (!__all_sync(0xffffffffu,
+                    mbar_test_wait2(&bars->a_full[ra.s], ra.ph, &bars->b_full[rb.s], rb.ph))) {
+      if (!warp_wait(&bars->a_full[ra.s], ra.ph, p, bars)) return false;
+      if (!warp_wait(&bars->b_full[rb.s], rb.ph, p, bars)) return false;
+    }
     tc_fence_after();
     tc_kblock_ts_warp(acc, a_base + ra.s * kAStage,
-                      bdesc0 + static_cast<uint64_t>(rb.s * (kBBytes >> 4)), idesc, kb != 0,
+                      bdesc0 + static_cast<uint64_t>(rb.s * (T::kBBytes >> 4)), idesc, kb != 0,
                       &bars->a_empty[ra.s], &bars->b_empty[rb.s]);
-    ra.next<kNA>();
-    rb.next<kNB>();
+    ra.next<T::kNA>();
+    rb.next<T::kNB>();
   }
   return true;
 }
 
-__device__ void role_mma(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
-  static_assert(kUnitTokens % 16 == 0 && kUnitTokens <= 256, "unit token count");
+template <class T>
+__device__ void role_mma(const GemmParams& p, uint8_t* B, typename T::Bars* bars, int nU) {
+  static_assert(T::kUnit % 16 == 0 && T::kUnit <= 256, "unit token count");
   static_assert(kTU == 1, "the MMA loop issues one weight tile per unit");
   const uint32_t tmem = bars->tmem_base;
   const uint64_t bdesc0 = tc_desc_sw128(smem_u32(B));
@@ -392,14 +419,14 @@ __device__ void role_mma(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
   for (int u = blockIdx.x; u < nU; u += gridDim.x, ++uc) {
     const GemmUnit un = p.units[u];
     const int nkb = p.K[un.kind] / 64 + p.gsum;  // + the group-sum block
-    const uint32_t acc = tmem + (uc & 1) * kAccSet;  // this unit's accumulator set
+    const uint32_t acc = tmem + (uc & 1) * T::kAccSet;  // this unit's accumulator set
     // (an injected stall waits for the phase before, which never completes)
     const uint32_t par = ((uc >> 1) & 1) ^ (p.stall ? 0u : 1u);
     if (!warp_wait(&bars->acc_empty[uc & 1], par, p, bars)) return;
     tc_fence_after();
-    const uint32_t a_base = tmem + kACol0;
+    const uint32_t a_base = tmem + T::kACol0;
     const int n16 = unit_nmma(un.n) >> 4;
-    if (n16 < 1 || 16 * n16 > kUnitTokens) {  // never emitted by the bucketing
+    if (n16 < 1 || 16 * n16 > T::kUnit) {  // never emitted by the bucketing
       if (!bars->abort) atomicCAS(p.status, DEV_OK, DEV_BAD_ID);
       bars->abort = 1;
       return;
@@ -408,8 +435,8 @@ __device__ void role_mma(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
     switch (n16) {
 #define MOE_MMA_CASE(c)                                                                   \
   case c:                                                                                 \
-    if constexpr (16 * (c) <= kUnitTokens)                                                \
-      ok = mma_unit<16 * (c)>(p, bars, acc, a_base, bdesc0, nkb, ra, rb);                \
+    if constexpr (16 * (c) <= T::kUnit)                                                \
+      ok = mma_unit<T, 16 * (c)>(p, bars, acc, a_base, bdesc0, nkb, ra, rb);             \
     break;
       MOE_MMA_CASE(1) MOE_MMA_CASE(2) MOE_MMA_CASE(3) MOE_MMA_CASE(4) MOE_MMA_CASE(5)
       MOE_MMA_CASE(6) MOE_MMA_CASE(7) MOE_MMA_CASE(8) MOE_MMA_CASE(9) MOE_MMA_CASE(10)
@@ -433,7 +460,8 @@ __device__ void role_mma(const GemmParams& p, uint8_t* B, Bars* bars, int nU) {
 // covering whole output row segments (one token row per group of lanes).
 __device__ __forceinline__ void epi_sync() { named_sync(1, kEpiWarps * 32); }
 
-__device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint8_t* stage,
+template <class T>
+__device__ void role_epilogue(const GemmParams& p, typename T::Bars* bars, float* meta, uint8_t* stage,
                               int nU) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = w & 3;
@@ -449,7 +477,7 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
       if (p.mode == 0) {
         const int tok = un.kind == 0 ? p.perm[brow] / p.topk : brow;
         meta[col] = p.sigma[tok];
-        meta[kUnitTokens + col] = p.hscale[tok];
+        meta[T::kUnit + col] = p.hscale[tok];
       } else if (un.kind == 0) {
         const int a = p.perm[brow];
         meta[col] = p.wts[a] / p.hscale[a / p.topk];
@@ -460,17 +488,17 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
     if (!wait_bar(&bars->acc_full[uc & 1], (uc >> 1) & 1, p, bars)) return;
     tc_fence_after();
     epi_sync();
-    const uint32_t acc = tmem + (uc & 1) * kAccSet;
+    const uint32_t acc = tmem + (uc & 1) * T::kAccSet;
     // the unit's 32-column chunks (3 per tile), alternating between the two
     // warps of this lane quarter
-    constexpr int kChunks = kAccCols / 32;
+    constexpr int kChunks = T::kAccCols / 32;
     for (int idx = chalf; idx < un.nmt * kChunks; idx += 2) {
       const int m = idx / kChunks, c0 = (idx % kChunks) * 32;
       if (c0 >= un.n) continue;
       const int mt = un.mt + m;
       {
         uint32_t r[32];
-        tmem_ld32(acc + (static_cast<uint32_t>(32 * q) << 16) + m * kAccCols + c0, r);
+        tmem_ld32(acc + (static_cast<uint32_t>(32 * q) << 16) + m * T::kAccCols + c0, r);
         tmem_ld_wait();
         if (p.mode == 0) {
           // rows 2j / 2j+1 of the tile are gate / up of output column j:
@@ -481,7 +509,7 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
           __half* sh = reinterpret_cast<__half*>(stg);
           float sgv[16], hsv[16];
           load16(meta + c0 + (odd ? 16 : 0), sgv);
-          load16(meta + kUnitTokens + c0 + (odd ? 16 : 0), hsv);
+          load16(meta + T::kUnit + c0 + (odd ? 16 : 0), hsv);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float mine_lo = __uint_as_float(r[i]), mine_hi = __uint_as_float(r[16 + i]);
@@ -570,28 +598,29 @@ __device__ void role_epilogue(const GemmParams& p, Bars* bars, float* meta, uint
   }
 }
 
+template <class T>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   const uint32_t base = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (base & 1023u)) & 1023u);
   uint8_t* P = smem;
-  uint8_t* B = P + kNP * kPBytes;
-  float* meta = reinterpret_cast<float*>(B + kNB * kBBytes);
-  uint8_t* stage = B + kNB * kBBytes + kMetaBytes;
+  uint8_t* B = P + T::kNP * kPBytes;
+  float* meta = reinterpret_cast<float*>(B + T::kNB * T::kBBytes);
+  uint8_t* stage = B + T::kNB * T::kBBytes + T::kMetaBytes;
   uint8_t* gsb = stage + kEpiWarps * kStageBytes;
-  Bars* bars = reinterpret_cast<Bars*>(gsb + kGsumBytes);
+  typename T::Bars* bars = reinterpret_cast<typename T::Bars*>(gsb + kGsumBytes);
   const int w = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNP; ++i) {
+    for (int i = 0; i < T::kNP; ++i) {
       mbar_init(&bars->p_full[i], 1);
       mbar_init(&bars->p_empty[i], kDqWarps);
     }
-    for (int i = 0; i < kNA; ++i) {
+    for (int i = 0; i < T::kNA; ++i) {
       mbar_init(&bars->a_full[i], kDqWarps);
       mbar_init(&bars->a_empty[i], 1);
     }
-    for (int i = 0; i < kNB; ++i) {
+    for (int i = 0; i < T::kNB; ++i) {
       mbar_init(&bars->b_full[i], 1);
       mbar_init(&bars->b_empty[i], 1);
     }
@@ -613,16 +642,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   grid_dep_launch();
   const int nU = *p.n_units;
   if (w == 0) {
-    if ((threadIdx.x & 31) == 0) role_tma_p(p, P, bars, nU);
+    if ((threadIdx.x & 31) == 0) role_tma_p<T>(p, P, bars, nU);
   } else if (w == kBLoadWarp) {
-    if ((threadIdx.x & 31) == 0) role_tma_b(p, B, bars, nU);
+    if ((threadIdx.x & 31) == 0) role_tma_b<T>(p, B, bars, nU);
   } else if (w == 1) {
-    role_mma(p, B, bars, nU);
+    role_mma<T>(p, B, bars, nU);
   } else if (w < kEpiWarp0) {
-    if (p.gsum) role_dequant<true>(p, P, bars, nU, gsb);
-    else role_dequant<false>(p, P, bars, nU, gsb);
+    if (p.gsum) role_dequant<T, true>(p, P, bars, nU, gsb);
+    else role_dequant<T, false>(p, P, bars, nU, gsb);
   } else {
-    role_epilogue(p, bars, meta, stage, nU);
+    role_epilogue<T>(p, bars, meta, stage, nU);
   }
   tc_fence_before();
   __syncthreads();
@@ -778,15 +807,23 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restric
   for (int i = threadIdx.x; i < D8; i += 128) dst[i] = __ldg(src + i);
 }
 
+template <class T>
+int launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
+  const int e = set_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<T>), T::kSmemBytes);
+  if (e != 0) return e;
+  return launch_pdl(gemm_tc_kernel<T>, dim3(grid), dim3(kGemmThreads), T::kSmemBytes, s, p);
+}
+
 }  // namespace
 
-int gemm_tc_smem_bytes() { return kSmemBytes; }
+int gemm_tc_smem_bytes() {
+  return WideTile::kSmemBytes > NarrowTile::kSmemBytes ? WideTile::kSmemBytes : NarrowTile::kSmemBytes;
+}
 
-int gemm_tc_launch(const GemmParams& p, int grid, void* stream) {
-  const int e = set_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel), kSmemBytes);
-  if (e != 0) return e;
-  return launch_pdl(gemm_tc_kernel, dim3(grid), dim3(kGemmThreads), kSmemBytes,
-                    static_cast<cudaStream_t>(stream), p);
+int gemm_tc_launch(const GemmParams& p, int grid, int max_rows, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return max_rows <= NarrowTile::kUnit ? launch_gemm<NarrowTile>(p, grid, s)
+                                       : launch_gemm<WideTile>(p, grid, s);
 }
 
 int router_tc_splits(int T, int E, int D, int num_sms) {

@@ -226,7 +226,9 @@ struct GemmParams {
                            // that never completes (every role then leaves through abort)
 };
 int gemm_tc_smem_bytes();
-int gemm_tc_launch(const GemmParams& p, int grid, void* stream);
+// max_rows: an upper bound on the activation rows of any unit (the batch's
+// token count); at most 32 selects the kernel's narrow plan.
+int gemm_tc_launch(const GemmParams& p, int grid, int max_rows, void* stream);
 // out[pos] = x16[perm[pos] / topk] for pos < rows (fp16 rows of `D` columns).
 int gather_rows_launch(const void* x16, int D, const int32_t* perm, int topk, int rows, void* out,
                        void* stream);

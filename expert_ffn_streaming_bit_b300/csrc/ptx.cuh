@@ -69,6 +69,22 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// Non-blocking test of two mbarrier phases at once (both probes in flight
+// together): true when both are complete.
+__device__ __forceinline__ bool mbar_test_wait2(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p, q;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n"
+      " and.pred p, p, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(a)), "r"(pa), "r"(smem_u32(b)), "r"(pb)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait on a phase of an mbarrier for at most `timeout_ns` (checked between
 // suspensions of at most 20 us), giving up early when *abort becomes
 // non-zero.  Returns false if the phase did not complete.
