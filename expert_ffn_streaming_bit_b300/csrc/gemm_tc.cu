@@ -62,7 +62,11 @@ constexpr int kPSbBytes = 128 * 16;                // 128 rows x 4 scale/bias wo
 constexpr int kPTile = kPCodeBytes + kPSbBytes;    // 18 KB per weight tile
 constexpr int kPBytes = kTU * kPTile;              // the unit's weight tiles per P stage
 constexpr int kTmemCols = 512;
-constexpr int kAStage = kTU * 32;                  // per tile 32 columns (64 fp16 of K)
+constexpr int kAStage = kTU * 32;                  // per K block and tile: 32 columns (64 fp16)
+// A and B rings advance by stages of kStageKB 64-column K blocks, so that one
+// wait, one pair of commits and one arrival per role cover them all; a unit
+// with an odd number of K blocks ends with a stage of one.
+constexpr int kStageKB = 2;
 constexpr int kDqWarps = 8, kEpiWarps = 8;
 constexpr int kGemmThreads = (3 + kDqWarps + kEpiWarps) * 32;  // + the activation loader warp
 constexpr int kBLoadWarp = 2 + kDqWarps + kEpiWarps;
@@ -85,14 +89,16 @@ constexpr int kGsumBytes = 128 * kGsumPitch;
 template <int kUT>
 struct Tile {
   static constexpr int kUnit = kUT;
-  static constexpr int kBBytes = kUT * 128;          // tokens x 64 fp16
+  static constexpr int kBBytes = kUT * 128;          // one K block's tile: tokens x 64 fp16
+  static constexpr int kBStage = kStageKB * kBBytes;
   static constexpr int kAccCols = kUT;               // per tile
   static constexpr int kAccSet = kTU * kAccCols;     // one unit's accumulators
   static constexpr int kACol0 = 2 * kAccSet;         // A stages after the two sets
-  static constexpr int kNA = (kTmemCols - kACol0) / kAStage > 14 ? 14 : (kTmemCols - kACol0) / kAStage;
-  static constexpr int kNP = kUT > 64 ? 3 : 6;
-  static constexpr int kNB = kUT > 64 ? 5 : 16;
-  static_assert(kNA >= 2 && kACol0 + kNA * kAStage <= kTmemCols, "tensor memory plan");
+  static constexpr int kAStageCols = kStageKB * kAStage;
+  static constexpr int kNA = (kTmemCols - kACol0) / kAStageCols;
+  static constexpr int kNP = kUT > 64 ? 2 : 6;
+  static constexpr int kNB = kUT > 64 ? 3 : 8;
+  static_assert(kNA >= 2 && kACol0 + kNA * kAStageCols <= kTmemCols, "tensor memory plan");
   struct Bars {
     uint64_t p_full[kNP], p_empty[kNP];
     uint64_t a_full[kNA], a_empty[kNA];
@@ -102,7 +108,7 @@ struct Tile {
     int abort;
   };
   static constexpr int kMetaBytes = 2 * kUT * 4;     // per-column factors
-  static constexpr int kSmemBytes = kNP * kPBytes + kNB * kBBytes + kMetaBytes +
+  static constexpr int kSmemBytes = kNP * kPBytes + kNB * kBStage + kMetaBytes +
                                     kEpiWarps * kStageBytes + kGsumBytes +
                                     1024 /*Bars*/ + 1024 /*alignment slack*/;
   static_assert(sizeof(Bars) <= 1024, "barrier block");
@@ -161,6 +167,16 @@ struct RingPos {
   }
 };
 
+// K blocks in the A/B stage that starts at K block kb of unit `un`: two, or
+// one at the end of the weight columns when their count is odd, and one for
+// the group-sum block.  The dequantisation forms the same stages (pairs
+// inside each 4-block weight slice, which is odd only at the unit's end).
+__device__ __forceinline__ int stage_blocks(const GemmUnit& un, const GemmParams& p, int kb) {
+  const int nmain = p.K[un.kind] / 64;
+  if (kb >= nmain) return 1;  // the group-sum block
+  return kb + 1 < nmain ? kStageKB : 1;
+}
+
 // Two loader threads, so that neither ring waits for the other: the weight
 // slices (P ring, one stage per 256 columns) and the activation tiles (B
 // ring, one stage per 64-column block) are issued independently, each as far
@@ -212,11 +228,15 @@ __device__ void role_tma_b(const GemmParams& p, uint8_t* B, typename T::Bars* ba
     while (box + 1 < kNBox && box_rows(box) < unit_nmma(un.n)) ++box;
     const void* tb = &p.tm_b[un.kind][box];
     const uint32_t bytes = box_rows(box) * 128;
-    for (int kb = 0; kb < nkb; ++kb, ++bc) {
+    for (int kb = 0; kb < nkb; ++bc) {
+      const int nb = stage_blocks(un, p, kb);
       const int bs = bc % T::kNB;
       if (!wait_bar(&bars->b_empty[bs], ((bc / T::kNB) & 1) ^ 1, p, bars)) return;
-      mbar_arrive_expect_tx(&bars->b_full[bs], bytes);
-      tma_load_2d(B + bs * T::kBBytes, tb, kb * 64, un.row0, &bars->b_full[bs]);
+      mbar_arrive_expect_tx(&bars->b_full[bs], nb * bytes);
+      for (int i = 0; i < nb; ++i)
+        tma_load_2d(B + bs * T::kBStage + i * T::kBBytes, tb, (kb + i) * 64, un.row0,
+                    &bars->b_full[bs]);
+      kb += nb;
     }
   }
   for (uint32_t q = bc > T::kNB ? bc - T::kNB : 0; q < bc; ++q)
@@ -287,6 +307,7 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, typename T::
   const int row = 32 * qd + lane;      // row of the weight tile
   const uint32_t tbase =
       bars->tmem_base + (static_cast<uint32_t>(32 * qd) << 16) + T::kACol0 + half * 16;
+  static_assert(kStageKB == 2, "a pass fills one stage of two K blocks");
   const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
   RingPos ra;
   uint32_t pc = 0;
@@ -302,34 +323,27 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, typename T::
       const uint8_t* codes = P + st * kPBytes;
       const uint32_t* sbw = reinterpret_cast<const uint32_t*>(codes + kPCodeBytes);
       for (int sb = 0; sb < nsub;) {
-        if (sb + 1 < nsub) {
-          RingPos r1 = ra;
-          r1.next<T::kNA>();
+        if (sb + 1 < nsub) {  // a stage of two blocks
           if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
-          if (!wait_bar(&bars->a_empty[r1.s], r1.ph ^ 1u, p, bars)) return;
           uint32_t o0[16], o1[16];
           dequant32<kGsum>(codes, sbw, row, half, sb, k1024, o0);
           dequant32<kGsum>(codes, sbw, row, half, sb + 1, k1024, o1);
           if (kGsum) keep_bias(sbw, gsb, row, half, 4 * sp + sb, sb);
           if (kGsum) keep_bias(sbw, gsb, row, half, 4 * sp + sb + 1, sb + 1);
-          tmem_st16(tbase + ra.s * kAStage, o0);
-          tmem_st16(tbase + r1.s * kAStage, o1);
+          tmem_st16(tbase + ra.s * T::kAStageCols, o0);
+          tmem_st16(tbase + ra.s * T::kAStageCols + kAStage, o1);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars->a_full[ra.s]);
-            mbar_arrive(&bars->a_full[r1.s]);
-          }
-          ra = r1;
+          if (lane == 0) mbar_arrive(&bars->a_full[ra.s]);
           ra.next<T::kNA>();
           sb += 2;
-        } else {
+        } else {  // the unit's last block, alone in its stage
           if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
           uint32_t o0[16];
           dequant32<kGsum>(codes, sbw, row, half, sb, k1024, o0);
           if (kGsum) keep_bias(sbw, gsb, row, half, 4 * sp + sb, sb);
-          tmem_st16(tbase + ra.s * kAStage, o0);
+          tmem_st16(tbase + ra.s * T::kAStageCols, o0);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
@@ -360,7 +374,7 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, typename T::
         if (g >= ng) o[i] = 0u;
         else if (g + 1 >= ng) o[i] &= 0xffffu;
       }
-      tmem_st16(tbase + ra.s * kAStage, o);
+      tmem_st16(tbase + ra.s * T::kAStageCols, o);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -386,11 +400,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 
 template <class T, int NMMA>
-__device__ __forceinline__ bool mma_unit(const GemmParams& p, typename T::Bars* bars, uint32_t acc,
-                                         uint32_t a_base, uint64_t bdesc0, int nkb, RingPos& ra,
-                                         RingPos& rb) {
+__device__ __forceinline__ bool mma_unit(const GemmParams& p, const GemmUnit& un,
+                                         typename T::Bars* bars, uint32_t acc, uint32_t a_base,
+                                         uint64_t bdesc0, int nkb, RingPos& ra, RingPos& rb) {
   constexpr uint32_t idesc = tc_idesc_f16(128, NMMA);
-  for (int kb = 0; kb < nkb; ++kb) {
+  for (int kb = 0; kb < nkb;) {
+    const int nb = stage_blocks(un, p, kb);
     // both stages are usually ready: probe them together, and take the
     // bounded waits only when one is not
     if (!__all_sync(0xffffffffu,
@@ -399,11 +414,12 @@ __device__ __forceinline__ bool mma_unit(const GemmParams& p, typename T::Bars* 
       if (!warp_wait(&bars->b_full[rb.s], rb.ph, p, bars)) return false;
     }
     tc_fence_after();
-    tc_kblock_ts_warp(acc, a_base + ra.s * kAStage,
-                      bdesc0 + static_cast<uint64_t>(rb.s * (T::kBBytes >> 4)), idesc, kb != 0,
-                      &bars->a_empty[ra.s], &bars->b_empty[rb.s]);
+    tc_stage_ts_warp(acc, a_base + ra.s * T::kAStageCols,
+                     bdesc0 + static_cast<uint64_t>(rb.s * (T::kBStage >> 4)), T::kBBytes >> 4,
+                     idesc, kb != 0, nb == 2, &bars->a_empty[ra.s], &bars->b_empty[rb.s]);
     ra.next<T::kNA>();
     rb.next<T::kNB>();
+    kb += nb;
   }
   return true;
 }
@@ -436,7 +452,7 @@ __device__ void role_mma(const GemmParams& p, uint8_t* B, typename T::Bars* bars
 #define MOE_MMA_CASE(c)                                                                   \
   case c:                                                                                 \
     if constexpr (16 * (c) <= T::kUnit)                                                \
-      ok = mma_unit<T, 16 * (c)>(p, bars, acc, a_base, bdesc0, nkb, ra, rb);             \
+      ok = mma_unit<T, 16 * (c)>(p, un, bars, acc, a_base, bdesc0, nkb, ra, rb);         \
     break;
       MOE_MMA_CASE(1) MOE_MMA_CASE(2) MOE_MMA_CASE(3) MOE_MMA_CASE(4) MOE_MMA_CASE(5)
       MOE_MMA_CASE(6) MOE_MMA_CASE(7) MOE_MMA_CASE(8) MOE_MMA_CASE(9) MOE_MMA_CASE(10)
@@ -606,8 +622,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_tc_kernel(const __grid_c
   uint8_t* smem = smem_raw + ((1024u - (base & 1023u)) & 1023u);
   uint8_t* P = smem;
   uint8_t* B = P + T::kNP * kPBytes;
-  float* meta = reinterpret_cast<float*>(B + T::kNB * T::kBBytes);
-  uint8_t* stage = B + T::kNB * T::kBBytes + T::kMetaBytes;
+  float* meta = reinterpret_cast<float*>(B + T::kNB * T::kBStage);
+  uint8_t* stage = B + T::kNB * T::kBStage + T::kMetaBytes;
   uint8_t* gsb = stage + kEpiWarps * kStageBytes;
   typename T::Bars* bars = reinterpret_cast<typename T::Bars*>(gsb + kGsumBytes);
   const int w = threadIdx.x >> 5;
