@@ -63,10 +63,10 @@ constexpr int kPTile = kPCodeBytes + kPSbBytes;    // 18 KB per weight tile
 constexpr int kPBytes = kTU * kPTile;              // the unit's weight tiles per P stage
 constexpr int kTmemCols = 512;
 constexpr int kAStage = kTU * 32;                  // per K block and tile: 32 columns (64 fp16)
-// A and B rings advance by stages of kStageKB 64-column K blocks, so that one
-// wait, one pair of commits and one arrival per role cover them all; a unit
-// with an odd number of K blocks ends with a stage of one.
-constexpr int kStageKB = 2;
+// A and B rings advance by stages of several 64-column K blocks (the plan's
+// kStageKB: two, or four = a whole weight slice), so that one wait, one pair
+// of commits and one arrival per role cover them all; a unit's last stage of
+// weight columns may hold fewer.
 constexpr int kDqWarps = 8, kEpiWarps = 8;
 constexpr int kGemmThreads = (3 + kDqWarps + kEpiWarps) * 32;  // + the activation loader warp
 constexpr int kBLoadWarp = 2 + kDqWarps + kEpiWarps;
@@ -89,6 +89,7 @@ constexpr int kGsumBytes = 128 * kGsumPitch;
 template <int kUT>
 struct Tile {
   static constexpr int kUnit = kUT;
+  static constexpr int kStageKB = kUT > 64 ? 2 : 4;  // K blocks per A/B stage
   static constexpr int kBBytes = kUT * 128;          // one K block's tile: tokens x 64 fp16
   static constexpr int kBStage = kStageKB * kBBytes;
   static constexpr int kAccCols = kUT;               // per tile
@@ -96,8 +97,8 @@ struct Tile {
   static constexpr int kACol0 = 2 * kAccSet;         // A stages after the two sets
   static constexpr int kAStageCols = kStageKB * kAStage;
   static constexpr int kNA = (kTmemCols - kACol0) / kAStageCols;
-  static constexpr int kNP = kUT > 64 ? 2 : 6;
-  static constexpr int kNB = kUT > 64 ? 3 : 8;
+  static constexpr int kNP = kUT > 64 ? 2 : 4;
+  static constexpr int kNB = kUT > 64 ? 3 : 6;
   static_assert(kNA >= 2 && kACol0 + kNA * kAStageCols <= kTmemCols, "tensor memory plan");
   struct Bars {
     uint64_t p_full[kNP], p_empty[kNP];
@@ -167,14 +168,15 @@ struct RingPos {
   }
 };
 
-// K blocks in the A/B stage that starts at K block kb of unit `un`: two, or
-// one at the end of the weight columns when their count is odd, and one for
-// the group-sum block.  The dequantisation forms the same stages (pairs
-// inside each 4-block weight slice, which is odd only at the unit's end).
+// K blocks in the A/B stage that starts at K block kb of unit `un`: the
+// plan's kStageKB, fewer at the end of the weight columns, and one for the
+// group-sum block.  The dequantisation forms the same stages inside each
+// 4-block weight slice (only a unit's last slice holds fewer than four).
+template <class T>
 __device__ __forceinline__ int stage_blocks(const GemmUnit& un, const GemmParams& p, int kb) {
   const int nmain = p.K[un.kind] / 64;
   if (kb >= nmain) return 1;  // the group-sum block
-  return kb + 1 < nmain ? kStageKB : 1;
+  return min(T::kStageKB, nmain - kb);
 }
 
 // Two loader threads, so that neither ring waits for the other: the weight
@@ -229,7 +231,7 @@ __device__ void role_tma_b(const GemmParams& p, uint8_t* B, typename T::Bars* ba
     const void* tb = &p.tm_b[un.kind][box];
     const uint32_t bytes = box_rows(box) * 128;
     for (int kb = 0; kb < nkb; ++bc) {
-      const int nb = stage_blocks(un, p, kb);
+      const int nb = stage_blocks<T>(un, p, kb);
       const int bs = bc % T::kNB;
       if (!wait_bar(&bars->b_empty[bs], ((bc / T::kNB) & 1) ^ 1, p, bars)) return;
       mbar_arrive_expect_tx(&bars->b_full[bs], nb * bytes);
@@ -307,7 +309,7 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, typename T::
   const int row = 32 * qd + lane;      // row of the weight tile
   const uint32_t tbase =
       bars->tmem_base + (static_cast<uint32_t>(32 * qd) << 16) + T::kACol0 + half * 16;
-  static_assert(kStageKB == 2, "a pass fills one stage of two K blocks");
+  static_assert(T::kStageKB == 2 || T::kStageKB == 4, "a stage is a pair or a weight slice");
   const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
   RingPos ra;
   uint32_t pc = 0;
@@ -322,7 +324,27 @@ __device__ void role_dequant(const GemmParams& p, const uint8_t* P, typename T::
       const int nsub = min(4, nkb - 4 * sp);
       const uint8_t* codes = P + st * kPBytes;
       const uint32_t* sbw = reinterpret_cast<const uint32_t*>(codes + kPCodeBytes);
-      for (int sb = 0; sb < nsub;) {
+      if constexpr (T::kStageKB == 4) {  // the slice is one stage: one wait, one arrival
+        if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
+        const uint32_t ta = tbase + ra.s * T::kAStageCols;
+        for (int sb = 0; sb < nsub; sb += 2) {
+          uint32_t o0[16], o1[16];
+          dequant32<kGsum>(codes, sbw, row, half, sb, k1024, o0);
+          if (kGsum) keep_bias(sbw, gsb, row, half, 4 * sp + sb, sb);
+          tmem_st16(ta + sb * kAStage, o0);
+          if (sb + 1 < nsub) {
+            dequant32<kGsum>(codes, sbw, row, half, sb + 1, k1024, o1);
+            if (kGsum) keep_bias(sbw, gsb, row, half, 4 * sp + sb + 1, sb + 1);
+            tmem_st16(ta + (sb + 1) * kAStage, o1);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->a_full[ra.s]);
+        ra.next<T::kNA>();
+      }
+      for (int sb = 0; T::kStageKB == 2 && sb < nsub;) {
         if (sb + 1 < nsub) {  // a stage of two blocks
           if (!wait_bar(&bars->a_empty[ra.s], ra.ph ^ 1u, p, bars)) return;
           uint32_t o0[16], o1[16];
@@ -405,7 +427,7 @@ __device__ __forceinline__ bool mma_unit(const GemmParams& p, const GemmUnit& un
                                          uint64_t bdesc0, int nkb, RingPos& ra, RingPos& rb) {
   constexpr uint32_t idesc = tc_idesc_f16(128, NMMA);
   for (int kb = 0; kb < nkb;) {
-    const int nb = stage_blocks(un, p, kb);
+    const int nb = stage_blocks<T>(un, p, kb);
     // both stages are usually ready: probe them together, and take the
     // bounded waits only when one is not
     if (!__all_sync(0xffffffffu,
@@ -414,9 +436,15 @@ __device__ __forceinline__ bool mma_unit(const GemmParams& p, const GemmUnit& un
       if (!warp_wait(&bars->b_full[rb.s], rb.ph, p, bars)) return false;
     }
     tc_fence_after();
-    tc_stage_ts_warp(acc, a_base + ra.s * T::kAStageCols,
-                     bdesc0 + static_cast<uint64_t>(rb.s * (T::kBStage >> 4)), T::kBBytes >> 4,
-                     idesc, kb != 0, nb == 2, &bars->a_empty[ra.s], &bars->b_empty[rb.s]);
+    const uint32_t a0 = a_base + ra.s * T::kAStageCols;
+    const uint64_t b0 = bdesc0 + static_cast<uint64_t>(rb.s * (T::kBStage >> 4));
+    if (T::kStageKB == 4 && nb > 2)  // blocks 0 and 1 first, without the commits
+      tc_stage_ts_warp(acc, a0, b0, T::kBBytes >> 4, idesc, kb != 0, 1u, 0u, &bars->a_empty[ra.s],
+                       &bars->b_empty[rb.s]);
+    const int j0 = (T::kStageKB == 4 && nb > 2) ? 2 : 0;  // blocks j0, j0 + 1 (if any), commits
+    tc_stage_ts_warp(acc, a0 + j0 * kAStage, b0 + static_cast<uint64_t>(j0 * (T::kBBytes >> 4)),
+                     T::kBBytes >> 4, idesc, (kb + j0) != 0, nb - j0 == 2, 1u,
+                     &bars->a_empty[ra.s], &bars->b_empty[rb.s]);
     ra.next<T::kNA>();
     rb.next<T::kNB>();
     kb += nb;

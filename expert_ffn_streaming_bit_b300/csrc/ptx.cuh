@@ -400,22 +400,24 @@ __device__ __forceinline__ void tc_kblock_ts_warp(uint32_t d_tmem, uint32_t a_tm
 // One ring stage of up to two 64-column K blocks with A in tensor memory: the
 // first block's four MMAs (A columns a_tmem + 8 j, B descriptor b_desc + 2 j),
 // when `two` is set the second block's four (A columns a_tmem + 32 + 8 j, B
-// descriptor b_desc + b_step + 2 j, b_step in 16-byte units), then a commit
-// to each of two mbarriers; one lane elected from the converged warp issues
-// them all.  The first MMA overwrites D when accumulate == 0.
+// descriptor b_desc + b_step + 2 j, b_step in 16-byte units), then, when
+// `commit` is set, a commit to each of two mbarriers; one lane elected from
+// the converged warp issues them all.  The first MMA overwrites D when
+// accumulate == 0.
 __device__ __forceinline__ void tc_stage_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                  uint32_t b_step, uint32_t idesc,
                                                  uint32_t accumulate, uint32_t two,
-                                                 uint64_t* bar0, uint64_t* bar1) {
+                                                 uint32_t commit, uint64_t* bar0, uint64_t* bar1) {
   asm volatile(
       "{\n"
-      " .reg .pred e, e2, p, t;\n"
+      " .reg .pred e, e2, ec, p, t;\n"
       " .reg .b32 l, a1, a2, a3, a4, a5, a6, a7;\n"
       " .reg .b64 bs, b1, b2, b3, b4, b5, b6, b7;\n"
       " elect.sync l|e, 0xffffffff;\n"
       " setp.ne.b32 p, %5, 0;\n"
       " setp.eq.b32 t, %5, %5;\n"
       " setp.ne.and.b32 e2, %6, 0, e;\n"
+      " setp.ne.and.b32 ec, %7, 0, e;\n"
       " add.u32 a1, %1, 8;\n add.u32 a2, %1, 16;\n add.u32 a3, %1, 24;\n"
       " add.u32 a4, %1, 32;\n add.u32 a5, %1, 40;\n add.u32 a6, %1, 48;\n add.u32 a7, %1, 56;\n"
       " add.u64 b1, %2, 2;\n add.u64 b2, %2, 4;\n add.u64 b3, %2, 6;\n"
@@ -429,11 +431,11 @@ __device__ __forceinline__ void tc_stage_ts_warp(uint32_t d_tmem, uint32_t a_tme
       " @e2 tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %4, t;\n"
       " @e2 tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %4, t;\n"
       " @e2 tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %4, t;\n"
-      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n"
-      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n"
+      " @ec tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n"
+      " @ec tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n"
       "}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(b_step), "r"(idesc), "r"(accumulate), "r"(two),
-      "r"(smem_u32(bar0)), "r"(smem_u32(bar1))
+      "r"(commit), "r"(smem_u32(bar0)), "r"(smem_u32(bar1))
       : "memory");
 }
 
