@@ -81,15 +81,16 @@ constexpr int kGsumBytes = 128 * kGsumPitch;
 
 // The kernel's plan for units of up to kUT activation rows.  Tensor memory
 // holds two accumulator sets of kUT columns and A stages in the rest; shared
-// memory holds the P (weight), B (activation) and epilogue buffers.  The wide
-// plan (kUT = 192) serves batches of more than 32 tokens; the narrow one
-// (kUT = 32), for at most 32 tokens, turns the columns and bytes that wide
-// units need into deeper rings, which hide the latency of the per-block
-// hand-offs when a block carries little MMA work.
+// memory holds the P (weight), B (activation) and epilogue buffers.  Three
+// plans: wide (kUT = 192, stages of two K blocks) for more than 128 tokens,
+// medium (128) and narrow (32, for at most 32 tokens), both with stages of a
+// whole 4-block weight slice.  A narrower plan turns the columns and bytes
+// that wide units need into longer stages and deeper rings, which cut the
+// per-block hand-offs that bound a unit of few tokens.
 template <int kUT>
 struct Tile {
   static constexpr int kUnit = kUT;
-  static constexpr int kStageKB = kUT > 64 ? 2 : 4;  // K blocks per A/B stage
+  static constexpr int kStageKB = kUT > 128 ? 2 : 4;  // K blocks per A/B stage
   static constexpr int kBBytes = kUT * 128;          // one K block's tile: tokens x 64 fp16
   static constexpr int kBStage = kStageKB * kBBytes;
   static constexpr int kAccCols = kUT;               // per tile
@@ -97,8 +98,8 @@ struct Tile {
   static constexpr int kACol0 = 2 * kAccSet;         // A stages after the two sets
   static constexpr int kAStageCols = kStageKB * kAStage;
   static constexpr int kNA = (kTmemCols - kACol0) / kAStageCols;
-  static constexpr int kNP = kUT > 64 ? 2 : 4;
-  static constexpr int kNB = kUT > 64 ? 3 : 6;
+  static constexpr int kNP = kUT > 32 ? 2 : 4;
+  static constexpr int kNB = kUT > 128 ? 3 : (kUT > 32 ? 2 : 6);
   static_assert(kNA >= 2 && kACol0 + kNA * kAStageCols <= kTmemCols, "tensor memory plan");
   struct Bars {
     uint64_t p_full[kNP], p_empty[kNP];
@@ -115,8 +116,10 @@ struct Tile {
   static_assert(sizeof(Bars) <= 1024, "barrier block");
 };
 using WideTile = Tile<kUnitTokens>;
+using MediumTile = Tile<128>;
 using NarrowTile = Tile<32>;
-static_assert(WideTile::kSmemBytes <= 227 * 1024 && NarrowTile::kSmemBytes <= 227 * 1024,
+static_assert(WideTile::kSmemBytes <= 227 * 1024 && MediumTile::kSmemBytes <= 227 * 1024 &&
+                  NarrowTile::kSmemBytes <= 227 * 1024,
               "shared memory plan");
 
 __device__ __forceinline__ float gelu_tanh(float x) {
@@ -861,13 +864,17 @@ int launch_gemm(const GemmParams& p, int grid, cudaStream_t s) {
 }  // namespace
 
 int gemm_tc_smem_bytes() {
-  return WideTile::kSmemBytes > NarrowTile::kSmemBytes ? WideTile::kSmemBytes : NarrowTile::kSmemBytes;
+  int m = WideTile::kSmemBytes;
+  if (MediumTile::kSmemBytes > m) m = MediumTile::kSmemBytes;
+  if (NarrowTile::kSmemBytes > m) m = NarrowTile::kSmemBytes;
+  return m;
 }
 
 int gemm_tc_launch(const GemmParams& p, int grid, int max_rows, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return max_rows <= NarrowTile::kUnit ? launch_gemm<NarrowTile>(p, grid, s)
-                                       : launch_gemm<WideTile>(p, grid, s);
+  if (max_rows <= NarrowTile::kUnit) return launch_gemm<NarrowTile>(p, grid, s);
+  if (max_rows <= MediumTile::kUnit) return launch_gemm<MediumTile>(p, grid, s);
+  return launch_gemm<WideTile>(p, grid, s);
 }
 
 int router_tc_splits(int T, int E, int D, int num_sms) {

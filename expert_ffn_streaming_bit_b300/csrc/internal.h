@@ -227,7 +227,8 @@ struct GemmParams {
 };
 int gemm_tc_smem_bytes();
 // max_rows: an upper bound on the activation rows of any unit (the batch's
-// token count); at most 32 selects the kernel's narrow plan.
+// token count); it picks the kernel's plan: narrow up to 32, medium up to 128,
+// wide above.
 int gemm_tc_launch(const GemmParams& p, int grid, int max_rows, void* stream);
 // out[pos] = x16[perm[pos] / topk] for pos < rows (fp16 rows of `D` columns).
 int gather_rows_launch(const void* x16, int D, const int32_t* perm, int topk, int rows, void* out,
