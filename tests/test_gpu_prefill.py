@@ -71,6 +71,29 @@ def test_tiny_prefill_bucketing_paths_at_the_boundary(moe, T):
     check_output(y, ref["y"])
 
 
+@pytest.mark.parametrize("T", [31, 32, 33, 127, 128, 129, 193])
+def test_tiny_prefill_gemm_plans_at_their_widths(moe, T):
+    """The grouped GEMM runs a narrow plan for batches of at most 32 tokens, a
+    medium one up to 128 and a wide one above.  Every token is sent to expert
+    0 (and one other), so expert 0's unit is as wide as the batch: the widest
+    unit each plan takes (32, 128), one past it (33, 129), and a batch that
+    the wide plan cuts into two token tiles (193).  Output, weights and
+    buckets are checked against the oracle."""
+    sh = synth.TINY
+    L = synth.make_layer(sh, "tiny", 5)
+    h = moe.moe_create(sh, [L], max_tokens=T)
+    x = synth.make_tokens(sh, "tiny", T, index=700 + T)
+    forced = np.stack([np.zeros(T, np.int32), 1 + np.arange(T, dtype=np.int32) % (sh.n_experts - 1)],
+                      axis=1)
+    y, st = _forward(moe, h, x, forced=forced)
+    ref = oracle.moe_layer(oracle.LayerView(sh, L), x, forced)
+    assert np.array_equal(st["ids"], forced)
+    check_weights(st["weights"], ref, st["ids"])
+    counts = _check_buckets(moe, h, st["ids"], sh.n_experts)
+    assert counts[0] == T
+    check_output(y, ref["y"])
+
+
 def test_tiny_prefill_rejects_bad_forced_ids(moe):
     """Out-of-range or repeated forced ids are refused on the host before any
     launch, and the handle stays usable."""
