@@ -842,16 +842,26 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // Token rows of x16 into bucket order (the routed gate/up activation operand).
-__global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restrict__ x16, int D8,
-                                                          const int32_t* __restrict__ perm, int topk,
-                                                          uint4* __restrict__ out) {
+// One warp per output row: a lane's 16-byte pieces of the row are all loaded
+// before any is stored, so a row's reads are in flight together.
+constexpr int kGatherWarps = 8, kGatherV = 13;  // rows of up to 32 * 13 uint4 (3,328 fp16)
+__global__ void __launch_bounds__(kGatherWarps * 32) gather_rows_kernel(
+    const uint4* __restrict__ x16, int D8, const int32_t* __restrict__ perm, int topk, int rows,
+    uint4* __restrict__ out) {
   grid_dep_wait();
   grid_dep_launch();
-  const int pos = blockIdx.x;
+  const int pos = blockIdx.x * kGatherWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (pos >= rows) return;
   const int tok = perm[pos] / topk;
   const uint4* src = x16 + static_cast<int64_t>(tok) * D8;
   uint4* dst = out + static_cast<int64_t>(pos) * D8;
-  for (int i = threadIdx.x; i < D8; i += 128) dst[i] = __ldg(src + i);
+  uint4 v[kGatherV];
+#pragma unroll
+  for (int j = 0; j < kGatherV; ++j)
+    if (lane + 32 * j < D8) v[j] = __ldg(src + lane + 32 * j);
+#pragma unroll
+  for (int j = 0; j < kGatherV; ++j)
+    if (lane + 32 * j < D8) dst[lane + 32 * j] = v[j];
 }
 
 template <class T>
@@ -903,8 +913,10 @@ int router_tc_launch(const CUtensorMap& wmap, const CUtensorMap& xmap, int T, in
 int gather_rows_launch(const void* x16, int D, const int32_t* perm, int topk, int rows, void* out,
                        void* stream) {
   if (rows <= 0) return 0;
-  return launch_pdl(gather_rows_kernel, dim3(rows), dim3(128), 0, static_cast<cudaStream_t>(stream),
-                    static_cast<const uint4*>(x16), D / 8, perm, topk, static_cast<uint4*>(out));
+  if (D / 8 > 32 * kGatherV || D % 8) return static_cast<int>(cudaErrorInvalidValue);
+  return launch_pdl(gather_rows_kernel, dim3((rows + kGatherWarps - 1) / kGatherWarps),
+                    dim3(kGatherWarps * 32), 0, static_cast<cudaStream_t>(stream),
+                    static_cast<const uint4*>(x16), D / 8, perm, topk, rows, static_cast<uint4*>(out));
 }
 
 }  // namespace moe
