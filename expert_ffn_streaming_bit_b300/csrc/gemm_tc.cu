@@ -1,40 +1,40 @@
 // Grouped GEMM of the multi-token layer step on the 5th-generation tensor
 // cores (tcgen05, accumulators in tensor memory).
 //
-// One work unit = kTilesPerUnit (here 1) 128-row tiles of one 4-bit weight
-// matrix (an expert's interleaved gate/up rows, its down rows, or the shared
-// expert's) against up to 192 activation rows (the tokens routed to that
-// expert, in bucket order, or a tile of all tokens for the shared expert).
-// The weight tile is the MMA's M side (128), the tokens its N side (16..192
-// in steps of 16), so the tile shape follows the ragged per-expert token
-// counts without padding M.  An MMA of M = 128, K = 16 costs a roughly fixed
-// number of cycles up to N = 128, so one wide token tile per weight tile
-// beats two weight tiles sharing a narrower one.
+// One work unit = one 128-row tile of one 4-bit weight matrix (an expert's
+// interleaved gate/up rows, its down rows, or the shared expert's) against the
+// unit's activation rows: the tokens routed to that expert, in bucket order,
+// or a tile of all tokens for the shared expert.  The weight tile is the MMA's
+// M side (128) and the tokens its N side (16 up to the plan's width in steps
+// of 16), so the tile shape follows the ragged per-expert token counts without
+// padding M.  The kernel is a template over that width (Tile below: 160, 128
+// or 32 tokens), chosen by the host from the batch size.
 //
 // The dequantised weights never touch shared memory: the dequantisation
 // warps write them straight into tensor memory, and the MMA reads its A
-// operand from there (only the activations come from shared memory).  That
-// keeps the shared-memory traffic per FLOP under its bandwidth, which A tiles
-// written to and read back from shared memory would exceed.
-// Tensor memory (512 columns): two accumulator sets of 192 columns (the
-// epilogue drains one unit while the MMA fills the next) and four A stages
-// of 32 columns (64 fp16 of K per row).
+// operand from there (only the activations come from shared memory).
+// Tensor memory (512 columns): two accumulator sets (the epilogue drains one
+// unit while the MMA fills the next) and the A stages.  The A and B rings
+// advance in stages of two or four 64-column K blocks, so that each role
+// synchronises once per stage.
 //
 // Per CTA (persistent, one per SM, 19 warps):
 //   warp 0       weight loader: packed 4-bit codes (128 B x 128 rows, 128-byte
 //                swizzle) and scale/bias words (16 B x 128 rows) of a
-//                256-column slice of the weight tile -> P ring (3 stages)
-//   warp 18      activation loader: the tile (64 fp16 columns x 192 rows,
-//                128-byte swizzle, the UMMA K-major layout) -> B ring (6
-//                stages), independent of the P ring
-//   warp 1       MMA: one thread issues tcgen05.mma kind::f16 (M=128,
-//                N=tokens, K=16, A in tensor memory), 4 k-steps per 64-column
-//                block, fp32 accumulators in tensor memory
+//                256-column slice of the weight tile -> P ring
+//   warp 18      activation loader: the stage's tiles (64 fp16 columns x the
+//                unit's rows, 128-byte swizzle, the UMMA K-major layout) -> B
+//                ring, independent of the P ring
+//   warp 1       MMA: the whole warp waits, one elected lane issues the
+//                stage's tcgen05.mma kind::f16 (M=128, N=tokens, K=16, A in
+//                tensor memory) and its commits; fp32 accumulators in tensor
+//                memory
 //   warps 2-9    dequantisation: the two warps of tensor-memory lane quarter
 //                w%4 take the two 32-column halves of its 32 rows; per
-//                64-column block each thread turns its codes into fp16
-//                w = fp16(s q + b) (one rounding) and stores them into the A
-//                stage
+//                64-column block each thread turns its codes into fp16 A
+//                values (gate/up: fp16(s q), the biases entering through one
+//                more K block of the tokens' group sums; down: fp16(s q + b))
+//                and stores them into the A stage
 //   warps 10-17  epilogue: tensor memory -> registers; gate/up units write
 //                h = gelu(g) * u (fp16, times a per-token power of two that
 //                keeps it in range), down units undo that factor and write the
@@ -82,7 +82,7 @@ constexpr int kGsumBytes = 128 * kGsumPitch;
 // The kernel's plan for units of up to kUT activation rows.  Tensor memory
 // holds two accumulator sets of kUT columns and A stages in the rest; shared
 // memory holds the P (weight), B (activation) and epilogue buffers.  Three
-// plans: wide (kUT = 192, stages of two K blocks) for more than 128 tokens,
+// plans: wide (kUT = 160, stages of two K blocks) for more than 128 tokens,
 // medium (128) and narrow (32, for at most 32 tokens), both with stages of a
 // whole 4-block weight slice.  A narrower plan turns the columns and bytes
 // that wide units need into longer stages and deeper rings, which cut the
@@ -98,7 +98,7 @@ struct Tile {
   static constexpr int kACol0 = 2 * kAccSet;         // A stages after the two sets
   static constexpr int kAStageCols = kStageKB * kAStage;
   static constexpr int kNA = (kTmemCols - kACol0) / kAStageCols;
-  static constexpr int kNP = kUT > 32 ? 2 : 4;
+  static constexpr int kNP = kUT > 128 ? 3 : (kUT > 32 ? 2 : 4);
   static constexpr int kNB = kUT > 128 ? 3 : (kUT > 32 ? 2 : 6);
   static_assert(kNA >= 2 && kACol0 + kNA * kAStageCols <= kTmemCols, "tensor memory plan");
   struct Bars {

@@ -104,15 +104,15 @@ struct DecodeParams {
 // GEMM's work units), two grouped GEMMs on the tensor cores (gate/up with the
 // GELU epilogue, then down), and a gather combine.
 
-constexpr int kUnitTokens = 192;   // max B rows (tokens) of one GEMM work unit
+constexpr int kUnitTokens = 160;   // max B rows (tokens) of one GEMM work unit
 // Heights of the activation tiles the GEMM loads (one tensor map each): a unit
 // of n rows loads the smallest that holds its MMA width (n rounded up to 16),
-// so a unit of a few tokens does not fill shared memory with 192 rows.
-constexpr int kNBox = 7;
+// so a unit of a few tokens does not fill shared memory with 160 rows.
+constexpr int kNBox = 6;
 #ifdef __CUDACC__
 __host__ __device__
 #endif
-constexpr int box_rows(int i) { return i == 0 ? 16 : 32 * i; }  // 16, 32 .. 192
+constexpr int box_rows(int i) { return i == 0 ? 16 : 32 * i; }  // 16, 32 .. 160
 static_assert(box_rows(kNBox - 1) == kUnitTokens, "the highest tile holds a whole unit");
 constexpr int kTilesPerUnit = 1;   // 128-row weight tiles per GEMM work unit
 constexpr int kMaxPrefillExperts = 256;
