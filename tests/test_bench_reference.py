@@ -17,10 +17,10 @@ def test_reference_arm_prints_one_json_line():
     lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
-    with open(os.path.join(ROOT, "BASELINE.json")) as f:
-        metric = json.load(f)["metric"]
+    sys.path.insert(0, ROOT)
+    import bench
     assert d["impl"] == "reference"
-    assert d["metric"] == metric
+    assert d["metric"] == bench.METRIC  # the same metric as the GPU arm's line
     assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["steps"] == 1 and d["warmup"] == 3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
