@@ -358,6 +358,9 @@ __device__ void emit_units(const BucketArgs& a, const int* cnt, const int* off, 
     a.n_units[0] = routed_tiles * pgu_r + st * pgu_s;
     a.n_units[1] = (routed_tiles + st) * pdn;
   }
+  // The shared expert's units come first: the CTAs take units in grid-stride
+  // order, and its down units (K = d_shared) are the longest, so last they
+  // would set the launch's tail.
   // routed: one thread per (token tile, weight group); the tile's expert is
   // found by a binary search over toff
   for (int idx = tid; idx < routed_tiles * (pgu_r + pdn); idx += nthreads) {
@@ -376,8 +379,8 @@ __device__ void emit_units(const BucketArgs& a, const int* cnt, const int* off, 
     const int r0t = c * tt / nt, r1t = c * (tt + 1) / nt;
     const int mt_all = gu ? a.mt_gu_r : a.mt_dn;
     GemmUnit u{0, kTU * m, ex, off[ex] + r0t, r1t - r0t, min(kTU, mt_all - kTU * m), {0, 0}};
-    if (gu) a.units_gu[tile * pgu_r + m] = u;
-    else a.units_dn[tile * pdn + m] = u;
+    if (gu) a.units_gu[st * pgu_s + tile * pgu_r + m] = u;
+    else a.units_dn[(st + tile) * pdn + m] = u;
   }
   for (int idx = tid; idx < st * (pgu_s + pdn); idx += nthreads) {
     const bool gu = idx < st * pgu_s;
@@ -387,8 +390,8 @@ __device__ void emit_units(const BucketArgs& a, const int* cnt, const int* off, 
     const int r0t = a.T * tt / st, r1t = a.T * (tt + 1) / st;
     const int mt_all = gu ? a.mt_gu_s : a.mt_dn;
     GemmUnit u{1, kTU * m, 0, r0t, r1t - r0t, min(kTU, mt_all - kTU * m), {0, 0}};
-    if (gu) a.units_gu[routed_tiles * pgu_r + tt * pgu_s + m] = u;
-    else a.units_dn[(routed_tiles + tt) * pdn + m] = u;
+    if (gu) a.units_gu[tt * pgu_s + m] = u;
+    else a.units_dn[tt * pdn + m] = u;
   }
 }
 
