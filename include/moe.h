@@ -191,8 +191,9 @@ typedef struct {
  * Resident mode: T == 1 runs the persistent decode kernel; T >= 2 runs the
  *   prefill path: router GEMM + top-k, token-to-expert bucketing, grouped
  *   GEMMs on the tensor cores (fp16 operands: weights dequantised to fp16 in
- *   shared memory, activations scaled by a per-token power of two; fp32
- *   accumulation), and a gather combine.  The prefill path holds the gated
+ *   tensor memory, activations scaled by a per-token power of two; fp32
+ *   accumulation; in the gate/up GEMM the weights' per-group biases enter
+ *   through the tokens' 64-column group sums), and a gather combine.  The prefill path holds the gated
  *   intermediate h in fp16 scaled per token by a power of two chosen from
  *   the token's input range, and the routed expert outputs in bf16 before
  *   the combine.
